@@ -1,0 +1,278 @@
+/*
+ * forkkv.h -- C ABI of libforkkv: residual attention over a copy-on-write,
+ * disaggregated KV cache, for one GB300 (sm_103a) GPU.
+ *
+ * Model (ForkKV guide, "Mathematical Decomposition of LoRA KV Activations"
+ * and "The Disaggregated Memory Layout"; LRAgent summary, section 2
+ * "BaseShared"):
+ *   - many LoRA agents share one paged base cache (bCache) holding the
+ *     post-RoPE keys Kb and values Vb computed with the frozen weights W0;
+ *   - agent a keeps a rank-r_a residual cache (rCache) Lk_a = X A_k,a and
+ *     Lv_a = X A_v,a ([T, r_a] per layer, shared by all kv heads) and its
+ *     up-projections Bk_a, Bv_a ([r_a, H_kv*d] per layer);
+ *   - for kv head h, agent a attends over
+ *       K_a[t] = Kb[t] + s_a * RoPE_t(Lk_a[t] Bk_a[:, h*d:(h+1)*d])
+ *       V_a[t] = Vb[t] + s_a * Lv_a[t] Bv_a[:, h*d:(h+1)*d]
+ *     with rotate-half RoPE, theta_i = rope_base^(-2i/d), t the 0-based
+ *     position in the agent's own sequence; query head hq reads kv head
+ *     hq / (H_q/H_kv).
+ *
+ * Conventions shared by every call:
+ *   - All tensors are row-major.  "bf16" is IEEE bfloat16 stored as uint16_t.
+ *   - Device pointers ("dev") are CUDA global-memory addresses of the
+ *     current device; host pointers ("host") are ordinary memory.  The
+ *     caller owns every buffer it passes; the library keeps no pointer to a
+ *     caller buffer after a call returns, except the pool carve-out given to
+ *     fk_pool_create, which it uses until fk_pool_destroy.
+ *   - Calls that take a stream enqueue work on it and return without
+ *     synchronising; their device effects are ordered by that stream only.
+ *     Calls on one pool must not run concurrently from several host threads,
+ *     and kernels of two fk_residual_attention calls on one pool must not
+ *     overlap on the GPU (they share the pool's workspace).
+ *   - Every call returns an fk_status.  FK_OK is 0.  On failure nothing was
+ *     enqueued, the pool's host state is unchanged, and fk_last_error()
+ *     returns a message (thread-local, valid until the next call on that
+ *     thread).  No call aborts, exits, or throws.
+ */
+#ifndef FORKKV_H
+#define FORKKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int fk_status;
+enum {
+  FK_OK = 0,
+  FK_ERR_INVALID_ARG = 1,   /* bad pointer, size, index, or state */
+  FK_ERR_OUT_OF_PAGES = 2,  /* the page free list cannot satisfy the call */
+  FK_ERR_OOM = 3,           /* a pool arena (rCache, workspace) is full */
+  FK_ERR_UNSUPPORTED = 4,   /* shape the kernels do not implement */
+  FK_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+  FK_ERR_DEVICE_CHECK = 6,  /* a kernel's own bounds check fired */
+  FK_ERR_TIMEOUT = 7        /* a bounded device wait gave up */
+};
+
+/* Pool geometry.  All sizes are per layer unless stated. */
+typedef struct fk_pool_config {
+  int32_t n_layers;        /* >= 1 */
+  int32_t n_q_heads;       /* H_q, a multiple of n_kv_heads */
+  int32_t n_kv_heads;      /* H_kv */
+  int32_t head_dim;        /* d: 64 or 128 */
+  int32_t page_size;       /* P: must be 16 */
+  int32_t num_pages;       /* physical bCache pages (page ids 0..num_pages-1,
+                              the same ids name a page in every layer) */
+  int32_t max_agents;      /* agent ids 0..max_agents-1 */
+  int32_t max_rank;        /* largest r_a: a multiple of 8, <= 64 */
+  int32_t max_tokens;      /* rCache capacity per agent (tokens) */
+  int64_t rcache_rank_budget; /* sum of ranks of live agents the rCache
+                              arena holds; 0 = max_agents * max_rank */
+  int64_t workspace_bytes; /* device workspace for the cached work list and
+                              split-K partials; 0 = 64 MiB */
+  float   rope_base;       /* RoPE base (10000 for Llama-style layers) */
+  int32_t compressed;      /* 1: also hold a compressed copy of the bCache
+                              (int8 K, 3-bit V) for fk_pool_compress */
+} fk_pool_config;
+
+typedef struct fk_pool fk_pool;
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* fk_last_error(void);
+
+/* Library version string. */
+const char* fk_version(void);
+
+/* Bytes of device memory the pool needs for `cfg` (0 and FK_ERR_* message
+ * via fk_last_error if cfg is invalid).  The caller allocates them (e.g.
+ * with torch) and hands them to fk_pool_create. */
+size_t fk_pool_bytes(const fk_pool_config* cfg);
+
+/* Create a pool over the caller's device carve-out `dev_buf` (dev, 256-byte
+ * aligned, >= fk_pool_bytes(cfg) bytes).  The buffer's contents need not be
+ * initialised.  Host metadata (page free list and reference counts, agent
+ * table) lives in the returned handle.  Uses the current CUDA device. */
+fk_status fk_pool_create(const fk_pool_config* cfg, void* dev_buf,
+                         size_t bytes, fk_pool** out);
+fk_status fk_pool_destroy(fk_pool* pool);
+
+/* Byte offset and size of a region of the pool carve-out, for reading the
+ * pool back in tests and tools.  Regions and their element layouts:
+ *   0 FK_REGION_KB   bf16 base keys:  [L][num_pages][H_kv][2][d/8][8][8]
+ *                    (token-group of 8, d-chunk of 8, token, d: the
+ *                    core-matrix order tensor cores read directly)
+ *   1 FK_REGION_VB   bf16 base values: [L][num_pages][H_kv][2][d/8][8][8]
+ *                    (token-chunk of 8, d-group of 8, d, token: values are
+ *                    stored transposed inside each 8x8 core)
+ *   2 FK_REGION_RC   rCache arena.  Per agent and layer: Lk as
+ *                    [T_cap/8][rp/8][8][8] (token-group, r-chunk, token,
+ *                    r), then Lv as [T_cap/8][rp/8][8][8] (token-chunk,
+ *                    r-group, r, token); rp = rank rounded up to 16 (the
+ *                    padding columns hold zeros), T_cap = max_tokens
+ *                    rounded up to 128.  Rows never appended hold zeros.
+ *   3 FK_REGION_KQ   int8 keys [L][num_pages][H_kv][16][d]
+ *   4 FK_REGION_VC   3-bit value codes [L][num_pages][H_kv][16][3*d/8]
+ *                    (three bit planes; code i at bit i%8 of byte i/8)
+ *   5 FK_REGION_VN   fp32 value norms [L][num_pages][H_kv][16]
+ *   6 FK_REGION_KS   fp32 key scale per layer [L]
+ */
+enum { FK_REGION_KB = 0, FK_REGION_VB = 1, FK_REGION_RC = 2,
+       FK_REGION_KQ = 3, FK_REGION_VC = 4, FK_REGION_VN = 5,
+       FK_REGION_KS = 6 };
+fk_status fk_pool_region(const fk_pool* pool, int region, size_t* offset,
+                         size_t* bytes);
+
+/* ---- pages: reference-counted, copy-on-write (ForkKV guide, "The
+ * Copy-on-Write Paradigm" and "Reference Counting and Eviction") ---- */
+
+/* Take `n` free pages; their ids go to page_ids (host, n entries) with
+ * reference count 1 and no tokens.  FK_ERR_OUT_OF_PAGES if fewer than n are
+ * free (then none is taken). */
+fk_status fk_pages_alloc(fk_pool* pool, int n, int32_t* page_ids);
+
+/* Drop one reference to each page (host ids, n entries; -1 entries are
+ * skipped).  A page whose count reaches 0 returns to the free list.
+ * FK_ERR_INVALID_ARG (and no change) if any id is out of range or already
+ * free. */
+fk_status fk_pages_release(fk_pool* pool, int n, const int32_t* page_ids);
+
+/* Fork: child_row[i] = parent_row[i] for i < n_pages and one more reference
+ * to each named page (host arrays; -1 entries are copied as -1). */
+fk_status fk_fork(fk_pool* pool, const int32_t* parent_row, int n_pages,
+                  int32_t* child_row);
+
+/* Current reference count of a page (0 = free), or -1 if out of range. */
+int fk_page_refcount(const fk_pool* pool, int32_t page_id);
+
+/* ---- agents ---- */
+
+/* Register agent `agent` with rank `rank` (multiple of 8, <= max_rank) and
+ * residual scale `s` (alpha/r of the adapter), copying its up-projections
+ * Bk, Bv (dev bf16 [n_layers][rank][H_kv*d]) into the pool and reserving
+ * its rCache (n_layers x max_tokens x rank for Lk and for Lv).
+ * FK_ERR_INVALID_ARG if the id is taken; FK_ERR_OOM if the rCache arena is
+ * full.  Ranks that are not a multiple of 8 must be zero-padded by the
+ * caller (padding columns of Lk/Lv and rows of Bk/Bv set to 0). */
+fk_status fk_agent_register(fk_pool* pool, int agent, int rank, float s,
+                            const uint16_t* Bk, const uint16_t* Bv,
+                            void* stream);
+fk_status fk_agent_release(fk_pool* pool, int agent);
+
+/* ---- appends ---- */
+
+/* Write base keys/values of tokens pos..pos+n-1 of one sequence into layer
+ * `layer` of the pages named by `block_table_row` (host, max_pages
+ * entries, logical page -> page id, -1 = none).  Kb, Vb: dev bf16
+ * [n][H_kv][d], post-RoPE.  Missing pages (-1) are allocated and written
+ * into the row.  A named page whose reference count is above 1 is shared:
+ * it is copied to a fresh page (all layers), the row entry is rewritten to
+ * the copy and the shared page loses one reference (copy-on-write), so
+ * shared pages are never written.  FK_ERR_OUT_OF_PAGES if pages run out
+ * (the row may then hold pages allocated before the failure; they stay
+ * valid). */
+fk_status fk_base_append(fk_pool* pool, int layer, int32_t* block_table_row,
+                         int max_pages, int pos, int n, const uint16_t* Kb,
+                         const uint16_t* Vb, void* stream);
+
+/* Write residual rows of tokens pos..pos+n-1 of agent `agent`, layer
+ * `layer`: Lk, Lv dev bf16 [n][rank] (Lk = X A_k, Lv = X A_v of those
+ * tokens).  pos + n <= max_tokens. */
+fk_status fk_residual_append(fk_pool* pool, int layer, int agent, int pos,
+                             int n, const uint16_t* Lk, const uint16_t* Lv,
+                             void* stream);
+
+/* ---- compressed shared pool (PolyKV summary, section 2B) ---- */
+
+/* Encode layer `layer` of every live page (reference count > 0, rows that
+ * hold tokens) into the compressed copy: keys as int8 with one fp32 scale
+ * for the whole layer (scale = max|K|/127, codes = round-half-even(K/scale)
+ * clamped to +-127); each value vector v (per token and kv head) as its
+ * fp32 norm n and the 3-bit index of the nearest 8-level Lloyd-Max level
+ * (unit normal) of each coordinate of z = H v / n, H the unnormalised
+ * Sylvester Hadamard matrix (ties go to the upper level).  Needs
+ * cfg.compressed = 1. */
+fk_status fk_pool_compress(fk_pool* pool, int layer, void* stream);
+
+/* Load an already-encoded layer: for the n_pages pages in page_ids (host),
+ * kq (dev int8 [n_pages][16][H_kv][d]), vcodes (dev uint8
+ * [n_pages][16][H_kv][3*d/8], bit planes as in FK_REGION_VC) and vnorm (dev
+ * fp32 [n_pages][16][H_kv]) are copied into the compressed copy, and the
+ * layer's key scale is set to k_scale. */
+fk_status fk_pool_load_compressed(fk_pool* pool, int layer,
+                                  const int32_t* page_ids, int n_pages,
+                                  const int8_t* kq, const uint8_t* vcodes,
+                                  const float* vnorm, float k_scale,
+                                  void* stream);
+
+/* ---- the hot path ---- */
+
+/* Residual attention of A agents, C query rows each, at layer `layer`.
+ *   q        dev bf16 [A][C][H_q][d], post-RoPE; row c of agent i sits at
+ *            position seq_lens[i] - C + c.
+ *   agents   host int32 [A], registered agent ids (distinct).
+ *   block_table host int32 [A][max_pages], logical page -> page id.
+ *   seq_lens host int32 [A], keys per agent (C <= seq_lens[i]); the agent's
+ *            residual rows 0..seq_lens[i]-1 must have been appended.
+ *   causal   1: row c sees keys t <= seq_lens[i] - C + c; 0: all keys.
+ *   compressed 1: read the compressed copy of the bCache (keys dequantised
+ *            in the kernel, values accumulated in the rotated domain and
+ *            rotated back once per output row); 0: the bf16 bCache.
+ *   out      dev bf16 [A][C][H_q][d], written with round-to-nearest-even.
+ * Pages that several agents name at the same logical index are streamed
+ * from HBM once per kv head for all of them.  The work list built from
+ * (agents, block_table, seq_lens, A, C, causal) is cached in the pool and
+ * reused while those inputs are unchanged.  Per-token residual keys are
+ * rebuilt on chip (Lk Bk then RoPE) and the value residual is applied
+ * factored as (P Lv) Bv after the split-K combine (LRAgent summary,
+ * section 3 "Flash-LoRA-Attention"). */
+fk_status fk_residual_attention(fk_pool* pool, int layer, const uint16_t* q,
+                                const int32_t* agents,
+                                const int32_t* block_table, int max_pages,
+                                const int32_t* seq_lens, int A, int C,
+                                int causal, int compressed, uint16_t* out,
+                                void* stream);
+
+/* Number of kernel launches the last fk_residual_attention enqueued. */
+int fk_last_launch_count(const fk_pool* pool);
+
+/* Synchronise `stream` and read the pool's device error word: FK_OK, or
+ * FK_ERR_DEVICE_CHECK if a kernel's bounds check fired since the last
+ * fk_check (the word is then cleared). */
+fk_status fk_check(fk_pool* pool, void* stream);
+
+/* ---- work list (host only; exposed for inspection and tests) ---- */
+
+/* One unit of GPU work: kv head `head`, rows [row_begin, row_begin+n_rows)
+ * of the row table, consecutive logical pages lp_begin.. of page list
+ * entries [page_begin, page_begin+n_pages), agents [agent_begin,
+ * agent_begin+n_agents) of the tile agent list. */
+typedef struct fk_work_item {
+  int32_t head, row_begin, n_rows, page_begin, n_pages, lp_begin,
+          agent_begin, n_agents, partial_begin, sum_rank;
+} fk_work_item;
+
+/* Build the work list for a call shape without a pool or GPU.  Outputs are
+ * host arrays of the given capacities; counts go to *n_*.  row_agent[i] is
+ * the call-local agent index of row i, row_cg[i] = c * G + g.  tile_agents
+ * holds call-local agent indices.  page_ids holds physical page ids.
+ * ranks: host int32 [A] ranks of the call's agents.  max_rows_per_tile,
+ * max_rank_sum_per_tile: tile limits; target_items: desired work items
+ * (e.g. 2 x SM count). */
+fk_status fk_plan_host(int A, int C, int H_q, int H_kv, int page_size,
+                       const int32_t* block_table, int max_pages,
+                       const int32_t* seq_lens, const int32_t* ranks,
+                       int max_rows_per_tile, int max_rank_sum_per_tile,
+                       int target_items,
+                       fk_work_item* items, int cap_items, int* n_items,
+                       int32_t* row_agent, int32_t* row_cg, int cap_rows,
+                       int* n_rows,
+                       int32_t* page_ids, int cap_pages, int* n_pages,
+                       int32_t* tile_agents, int cap_tile_agents,
+                       int* n_tile_agents);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FORKKV_H */

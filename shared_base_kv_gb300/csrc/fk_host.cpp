@@ -1,0 +1,804 @@
+// Host side of libforkkv: pool metadata (page reference counts and free
+// list, copy-on-write appends, agent registry, rCache arena), the work-list
+// planner, and the C ABI.  Kernels live in fk_kernels.cu.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "fk_internal.h"
+
+using namespace fk;
+
+namespace {
+
+thread_local std::string g_err;
+
+fk_status fail(fk_status code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+
+fk_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(FK_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+struct HostPlan {
+  std::vector<fk_work_item> items;
+  std::vector<int32_t> row_agent, row_cg, pages, tile_agents;
+  std::vector<int32_t> csr_ptr, csr_slots;
+  int n_partials = 0;
+};
+
+// Pinned host staging buffer for small host->device uploads.  A new upload
+// waits for the previous one to have been consumed.
+struct Staging {
+  void* host = nullptr;
+  size_t cap = 0;
+  cudaEvent_t done = nullptr;
+  bool pending = false;
+};
+
+}  // namespace
+
+struct fk_pool {
+  fk_pool_config cfg;
+  PoolGeom g;
+  int device = 0;
+  int num_sms = 0;
+  std::vector<int32_t> refcount;             // per page
+  std::vector<int32_t> free_list;            // stack of free page ids
+  std::vector<uint8_t> fill;                 // [L][num_pages] tokens held
+  struct Agent {
+    bool live = false;
+    int rank = 0, rp = 0;
+    float s = 0.f;
+    int64_t rc_off = 0, rc_bytes = 0;
+  };
+  std::vector<Agent> agents;
+  std::map<int64_t, int64_t> rc_free;        // offset -> bytes
+  Staging stage;
+  // cached work list
+  bool plan_valid = false;
+  std::vector<int32_t> key;                  // call inputs the plan is for
+  HostPlan plan;
+  PlanDev plan_dev{};
+  int last_launches = 0;
+};
+
+namespace {
+
+fk_status validate_config(const fk_pool_config* c) {
+  if (!c) return fail(FK_ERR_INVALID_ARG, "config is NULL");
+  if (c->n_layers < 1) return fail(FK_ERR_INVALID_ARG, "n_layers must be >= 1");
+  if (c->n_kv_heads < 1 || c->n_q_heads < 1 || c->n_q_heads % c->n_kv_heads)
+    return fail(FK_ERR_INVALID_ARG, "n_q_heads must be a positive multiple of n_kv_heads");
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(FK_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (c->page_size != kPage) return fail(FK_ERR_UNSUPPORTED, "page_size must be 16");
+  if (c->num_pages < 1) return fail(FK_ERR_INVALID_ARG, "num_pages must be >= 1");
+  if (c->max_agents < 1) return fail(FK_ERR_INVALID_ARG, "max_agents must be >= 1");
+  if (c->max_rank < 8 || c->max_rank > kMaxRankPad || c->max_rank % 8)
+    return fail(FK_ERR_UNSUPPORTED, "max_rank must be a multiple of 8 in [8, 64]");
+  if (c->max_tokens < 1) return fail(FK_ERR_INVALID_ARG, "max_tokens must be >= 1");
+  if (c->rcache_rank_budget < 0 || c->workspace_bytes < 0)
+    return fail(FK_ERR_INVALID_ARG, "negative arena size");
+  if (!(c->rope_base > 1.0f)) return fail(FK_ERR_INVALID_ARG, "rope_base must be > 1");
+  return FK_OK;
+}
+
+PoolGeom make_geom(const fk_pool_config* c) {
+  PoolGeom g{};
+  g.L = c->n_layers;
+  g.H_q = c->n_q_heads;
+  g.H_kv = c->n_kv_heads;
+  g.d = c->head_dim;
+  g.G = c->n_q_heads / c->n_kv_heads;
+  g.num_pages = c->num_pages;
+  g.max_agents = c->max_agents;
+  g.rmax_pad = rank_pad(c->max_rank);
+  g.tcap = (int32_t)align_up(c->max_tokens, kTileTok);
+  g.rope_base = c->rope_base;
+  g.compressed = c->compressed ? 1 : 0;
+  g.page_bytes = (int64_t)kPage * g.d * 2;
+  g.kb_layer_bytes = (int64_t)g.num_pages * g.H_kv * g.page_bytes;
+  int64_t off = 0;
+  auto take = [&](int64_t bytes) {
+    int64_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  g.off_kb = take(g.kb_layer_bytes * g.L);
+  g.off_vb = take(g.kb_layer_bytes * g.L);
+  int64_t budget = c->rcache_rank_budget ? c->rcache_rank_budget
+                                         : (int64_t)c->max_agents * c->max_rank;
+  // rank budget in padded-rank units: every agent may round up to 16
+  int64_t budget_pad = align_up(budget, 16) + 16LL * c->max_agents;
+  budget_pad = std::min<int64_t>(budget_pad, (int64_t)c->max_agents * g.rmax_pad);
+  int64_t rc_bytes = budget_pad * g.L * 2LL * g.tcap * 2;
+  int64_t off_rc = take(rc_bytes);
+  (void)off_rc;  // arena starts here; recorded below via off_bk - rc_bytes
+  g.bk_agent_bytes = (int64_t)g.L * g.H_kv * g.d * g.rmax_pad * 2;
+  g.bv_agent_bytes = (int64_t)g.L * g.rmax_pad * g.H_kv * g.d * 2;
+  g.off_bk = take(g.bk_agent_bytes * g.max_agents);
+  g.off_bv = take(g.bv_agent_bytes * g.max_agents);
+  g.off_agents = take((int64_t)sizeof(AgentDev) * g.max_agents);
+  g.off_rope = take(4LL * 4 * 64);
+  g.off_err = take(64);
+  if (g.compressed) {
+    int64_t tok = (int64_t)g.L * g.num_pages * g.H_kv * kPage;
+    g.off_kq = take(tok * g.d);
+    g.off_vc = take(tok * (3 * g.d / 8));
+    g.off_vn = take(tok * 4);
+    g.off_ks = take(4LL * g.L);
+    g.off_kmax = take(4LL * g.L);
+  } else {
+    g.off_kq = g.off_vc = g.off_vn = g.off_ks = g.off_kmax = -1;
+  }
+  g.meta_bytes = align_up(8LL * g.num_pages + 4096, 256);
+  g.off_meta = take(g.meta_bytes);
+  g.ws_bytes = c->workspace_bytes ? c->workspace_bytes : (64LL << 20);
+  g.off_ws = take(g.ws_bytes);
+  return g;
+}
+
+int64_t total_bytes(const PoolGeom& g) { return g.off_ws + g.ws_bytes; }
+
+int64_t rc_arena_offset(const PoolGeom& g) {
+  // the rCache arena sits right after the value pages
+  return align_up(g.off_vb + g.kb_layer_bytes * g.L, 256);
+}
+int64_t rc_arena_bytes(const PoolGeom& g) { return g.off_bk - rc_arena_offset(g); }
+
+fk_status stage_upload(fk_pool* p, const void* src, size_t bytes, void* dst,
+                       cudaStream_t st) {
+  Staging& s = p->stage;
+  if (s.pending) {
+    cudaError_t e = cudaEventSynchronize(s.done);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    s.pending = false;
+  }
+  if (bytes > s.cap) {
+    if (s.host) cudaFreeHost(s.host);
+    s.host = nullptr;
+    size_t cap = std::max<size_t>(bytes, 1 << 20);
+    cudaError_t e = cudaMallocHost(&s.host, cap);
+    if (e != cudaSuccess) { s.cap = 0; return cuda_fail(e, "cudaMallocHost"); }
+    s.cap = cap;
+  }
+  std::memcpy(s.host, src, bytes);
+  cudaError_t e = cudaMemcpyAsync(dst, s.host, bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+  e = cudaEventRecord(s.done, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  s.pending = true;
+  return FK_OK;
+}
+
+fk_status upload_agent(fk_pool* p, int a, cudaStream_t st) {
+  const auto& A = p->agents[a];
+  AgentDev dv{};
+  dv.rp = A.live ? A.rp : 0;
+  dv.s = A.s;
+  dv.rc_off = A.rc_off;
+  return stage_upload(p, &dv, sizeof(dv),
+                      p->g.base + p->g.off_agents + (int64_t)a * sizeof(AgentDev), st);
+}
+
+// ----------------------------------------------------------- planner --
+
+fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
+                     int max_pages, const int32_t* seq, const int32_t* rpad,
+                     int max_rows, int max_rank_sum, int target_items,
+                     HostPlan& out) {
+  if (A < 1 || C < 1) return fail(FK_ERR_INVALID_ARG, "A and C must be >= 1");
+  if (H_kv < 1 || H_q % H_kv) return fail(FK_ERR_INVALID_ARG, "bad head counts");
+  if (!bt || !seq || !rpad) return fail(FK_ERR_INVALID_ARG, "NULL table");
+  if (max_rows < 1 || max_rows > kMaxRows || max_rank_sum < 16)
+    return fail(FK_ERR_INVALID_ARG, "bad tile limits");
+  const int G = H_q / H_kv;
+  for (int i = 0; i < A; ++i) {
+    if (seq[i] < C) return fail(FK_ERR_INVALID_ARG, "seq_lens[i] must be >= C >= 1");
+    int np = (seq[i] + P - 1) / P;
+    if (np > max_pages) return fail(FK_ERR_INVALID_ARG, "seq_len exceeds max_pages");
+    for (int lp = 0; lp < np; ++lp)
+      if (bt[(int64_t)i * max_pages + lp] < 0)
+        return fail(FK_ERR_INVALID_ARG, "block table names no page for a live token");
+    if (rpad[i] < 16 || rpad[i] % 16 || rpad[i] > kMaxRankPad)
+      return fail(FK_ERR_INVALID_ARG, "bad padded rank");
+  }
+  // 1. sharing classes: (logical page, physical page) -> agents
+  std::map<std::pair<int32_t, int32_t>, std::vector<int32_t>> cls;
+  for (int i = 0; i < A; ++i) {
+    int np = (seq[i] + P - 1) / P;
+    for (int lp = 0; lp < np; ++lp)
+      cls[{lp, bt[(int64_t)i * max_pages + lp]}].push_back(i);
+  }
+  // 2. group by agent set; pages of a set in logical order
+  std::map<std::vector<int32_t>, std::vector<std::pair<int32_t, int32_t>>> sets;
+  for (auto& kv : cls) sets[kv.second].push_back(kv.first);
+  // 3. tiles of every set, and page runs
+  struct Tile { std::vector<int32_t> agents; std::vector<std::pair<int32_t,int32_t>> rows; int rank_sum; };
+  struct SetWork { std::vector<Tile> tiles; std::vector<std::vector<std::pair<int32_t,int32_t>>> runs; };
+  std::vector<SetWork> work;
+  int64_t total_units = 0;
+  const int rpa = G * C;
+  for (auto& kv : sets) {
+    SetWork sw;
+    Tile cur{{}, {}, 0};
+    auto flush = [&]() { if (!cur.rows.empty()) sw.tiles.push_back(cur); cur = Tile{{}, {}, 0}; };
+    // 16-row groups touched by the agents of a tile, each agent counted once
+    auto groups_with = [&](int n_agents) {
+      int tot = 0;
+      for (int k = 0; k < n_agents; ++k) tot += (k * rpa + rpa - 1) / 16 - (k * rpa) / 16 + 1;
+      return tot;
+    };
+    for (int32_t a : kv.first) {
+      if (rpa <= max_rows) {
+        if ((int)cur.rows.size() + rpa > max_rows || cur.rank_sum + rpad[a] > max_rank_sum ||
+            (int)cur.agents.size() >= kMaxAgentsPerTile ||
+            groups_with((int)cur.agents.size() + 1) > kMaxRowGroups)
+          flush();
+        cur.agents.push_back(a);
+        cur.rank_sum += rpad[a];
+        for (int cg = 0; cg < rpa; ++cg) cur.rows.push_back({a, cg});
+      } else {
+        flush();
+        for (int c0 = 0; c0 < rpa; c0 += max_rows) {
+          Tile t{{a}, {}, rpad[a]};
+          for (int cg = c0; cg < std::min(rpa, c0 + max_rows); ++cg) t.rows.push_back({a, cg});
+          sw.tiles.push_back(t);
+        }
+      }
+    }
+    flush();
+    const auto& pg = kv.second;   // sorted by logical page
+    size_t s0 = 0;
+    for (size_t k = 1; k <= pg.size(); ++k) {
+      if (k == pg.size() || pg[k].first != pg[k - 1].first + 1) {
+        sw.runs.emplace_back(pg.begin() + s0, pg.begin() + k);
+        total_units += (int64_t)(k - s0) * sw.tiles.size() * H_kv;
+        s0 = k;
+      }
+    }
+    work.push_back(std::move(sw));
+  }
+  int64_t ppi = std::max<int64_t>(1, (total_units + target_items - 1) / std::max(1, target_items));
+  // 4. emit items
+  HostPlan pl;
+  for (auto& sw : work) {
+    std::vector<int> tile_row0, tile_ag0;
+    for (auto& t : sw.tiles) {
+      tile_row0.push_back((int)pl.row_agent.size());
+      for (auto& r : t.rows) { pl.row_agent.push_back(r.first); pl.row_cg.push_back(r.second); }
+      tile_ag0.push_back((int)pl.tile_agents.size());
+      for (int32_t a : t.agents) pl.tile_agents.push_back(a);
+    }
+    for (auto& run : sw.runs) {
+      int64_t len = (int64_t)run.size();
+      int64_t nch = (len + ppi - 1) / ppi;
+      for (int64_t ch = 0; ch < nch; ++ch) {
+        int64_t b = len * ch / nch, e = len * (ch + 1) / nch;
+        int page_begin = (int)pl.pages.size();
+        for (int64_t k = b; k < e; ++k) pl.pages.push_back(run[k].second);
+        for (size_t ti = 0; ti < sw.tiles.size(); ++ti) {
+          for (int h = 0; h < H_kv; ++h) {
+            fk_work_item it{};
+            it.head = h;
+            it.row_begin = tile_row0[ti];
+            it.n_rows = (int)sw.tiles[ti].rows.size();
+            it.page_begin = page_begin;
+            it.n_pages = (int)(e - b);
+            it.lp_begin = run[b].first;
+            it.agent_begin = tile_ag0[ti];
+            it.n_agents = (int)sw.tiles[ti].agents.size();
+            it.partial_begin = pl.n_partials;
+            it.sum_rank = sw.tiles[ti].rank_sum;
+            pl.n_partials += it.n_rows;
+            pl.items.push_back(it);
+          }
+        }
+      }
+    }
+  }
+  // 5. combine lists: output row (i, c, hq) -> partial slots
+  const int n_out = A * C * H_q;
+  std::vector<int32_t> cnt(n_out + 1, 0);
+  auto out_row = [&](const fk_work_item& it, int j) {
+    int a = pl.row_agent[it.row_begin + j], cg = pl.row_cg[it.row_begin + j];
+    int c = cg / G, g = cg % G;
+    return (a * C + c) * H_q + it.head * G + g;
+  };
+  for (auto& it : pl.items)
+    for (int j = 0; j < it.n_rows; ++j) cnt[out_row(it, j) + 1]++;
+  for (int r = 0; r < n_out; ++r) {
+    if (cnt[r + 1] == 0) return fail(FK_ERR_INVALID_ARG, "an output row has no keys");
+    cnt[r + 1] += cnt[r];
+  }
+  pl.csr_ptr = cnt;
+  pl.csr_slots.assign(cnt[n_out], 0);
+  std::vector<int32_t> pos(cnt.begin(), cnt.end() - 1);
+  for (auto& it : pl.items)
+    for (int j = 0; j < it.n_rows; ++j) pl.csr_slots[pos[out_row(it, j)]++] = it.partial_begin + j;
+  out = std::move(pl);
+  return FK_OK;
+}
+
+}  // namespace
+
+// ================================================================= ABI ==
+
+extern "C" {
+
+const char* fk_last_error(void) { return g_err.c_str(); }
+
+const char* fk_version(void) { return "forkkv-gb300 0.1 (sm_103a)"; }
+
+size_t fk_pool_bytes(const fk_pool_config* cfg) {
+  if (validate_config(cfg) != FK_OK) return 0;
+  return (size_t)total_bytes(make_geom(cfg));
+}
+
+fk_status fk_pool_create(const fk_pool_config* cfg, void* dev_buf, size_t bytes,
+                         fk_pool** out) {
+  fk_status st = validate_config(cfg);
+  if (st != FK_OK) return st;
+  if (!out) return fail(FK_ERR_INVALID_ARG, "out is NULL");
+  if (!dev_buf || ((uintptr_t)dev_buf % 256))
+    return fail(FK_ERR_INVALID_ARG, "dev_buf must be a 256-byte aligned device pointer");
+  PoolGeom g = make_geom(cfg);
+  if ((int64_t)bytes < total_bytes(g))
+    return fail(FK_ERR_INVALID_ARG, "dev_buf smaller than fk_pool_bytes(cfg)");
+  cudaPointerAttributes attr{};
+  cudaError_t e = cudaPointerGetAttributes(&attr, dev_buf);
+  if (e != cudaSuccess || attr.type != cudaMemoryTypeDevice) {
+    cudaGetLastError();
+    return fail(FK_ERR_INVALID_ARG, "dev_buf is not device memory");
+  }
+  fk_pool* p = new fk_pool();
+  p->cfg = *cfg;
+  p->g = g;
+  p->g.base = (uint8_t*)dev_buf;
+  cudaGetDevice(&p->device);
+  cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+  p->refcount.assign(g.num_pages, 0);
+  p->free_list.reserve(g.num_pages);
+  for (int i = g.num_pages - 1; i >= 0; --i) p->free_list.push_back(i);
+  p->fill.assign((size_t)g.L * g.num_pages, 0);
+  p->agents.assign(g.max_agents, {});
+  p->rc_free[rc_arena_offset(g)] = rc_arena_bytes(g);
+  e = cudaEventCreateWithFlags(&p->stage.done, cudaEventDisableTiming);
+  if (e != cudaSuccess) { delete p; return cuda_fail(e, "cudaEventCreate"); }
+  // zero the small tables (agents, error word); write the RoPE table:
+  // theta_i in fp32 plus its fp32 residual, and the exact rotation by one
+  // 128-token tile, all computed in double.
+  // zero the page stores (rows never appended must read as finite zeros),
+  // the small tables and the compressed copy
+  e = cudaMemset(p->g.base + g.off_kb, 0, 2 * g.kb_layer_bytes * g.L);
+  if (e == cudaSuccess) e = cudaMemset(p->g.base + g.off_agents, 0, g.off_err + 64 - g.off_agents);
+  if (e == cudaSuccess && g.compressed)
+    e = cudaMemset(p->g.base + g.off_kq, 0, g.off_kmax + 4LL * g.L - g.off_kq);
+  if (e != cudaSuccess) { cudaEventDestroy(p->stage.done); delete p; return cuda_fail(e, "cudaMemset"); }
+  std::vector<float> rope(4 * 64, 0.f);
+  for (int i = 0; i < g.d / 2; ++i) {
+    double th = std::pow((double)g.rope_base, -2.0 * i / g.d);
+    float hi = (float)th;
+    rope[i] = hi;
+    rope[64 + i] = (float)(th - (double)hi);
+    rope[128 + i] = (float)std::cos(kTileTok * th);
+    rope[192 + i] = (float)std::sin(kTileTok * th);
+  }
+  e = cudaMemcpy(p->g.base + g.off_rope, rope.data(), rope.size() * 4, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) { cudaEventDestroy(p->stage.done); delete p; return cuda_fail(e, "cudaMemcpy"); }
+  *out = p;
+  return FK_OK;
+}
+
+fk_status fk_pool_destroy(fk_pool* p) {
+  if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
+  if (p->stage.pending) cudaEventSynchronize(p->stage.done);
+  if (p->stage.host) cudaFreeHost(p->stage.host);
+  if (p->stage.done) cudaEventDestroy(p->stage.done);
+  delete p;
+  return FK_OK;
+}
+
+fk_status fk_pool_region(const fk_pool* p, int region, size_t* offset, size_t* bytes) {
+  if (!p || !offset || !bytes) return fail(FK_ERR_INVALID_ARG, "NULL argument");
+  const PoolGeom& g = p->g;
+  int64_t tok = (int64_t)g.L * g.num_pages * g.H_kv * kPage;
+  int64_t o = -1, b = 0;
+  switch (region) {
+    case FK_REGION_KB: o = g.off_kb; b = g.kb_layer_bytes * g.L; break;
+    case FK_REGION_VB: o = g.off_vb; b = g.kb_layer_bytes * g.L; break;
+    case FK_REGION_RC: o = rc_arena_offset(g); b = rc_arena_bytes(g); break;
+    case FK_REGION_KQ: o = g.off_kq; b = tok * g.d; break;
+    case FK_REGION_VC: o = g.off_vc; b = tok * (3 * g.d / 8); break;
+    case FK_REGION_VN: o = g.off_vn; b = tok * 4; break;
+    case FK_REGION_KS: o = g.off_ks; b = 4LL * g.L; break;
+    default: return fail(FK_ERR_INVALID_ARG, "unknown region");
+  }
+  if (o < 0) return fail(FK_ERR_INVALID_ARG, "region absent (pool not compressed)");
+  *offset = (size_t)o;
+  *bytes = (size_t)b;
+  return FK_OK;
+}
+
+fk_status fk_pages_alloc(fk_pool* p, int n, int32_t* ids) {
+  if (!p || n < 0 || (n > 0 && !ids)) return fail(FK_ERR_INVALID_ARG, "bad arguments");
+  if ((size_t)n > p->free_list.size())
+    return fail(FK_ERR_OUT_OF_PAGES, "not enough free pages");
+  for (int i = 0; i < n; ++i) {
+    int32_t id = p->free_list.back();
+    p->free_list.pop_back();
+    p->refcount[id] = 1;
+    for (int l = 0; l < p->g.L; ++l) p->fill[(size_t)l * p->g.num_pages + id] = 0;
+    ids[i] = id;
+  }
+  return FK_OK;
+}
+
+fk_status fk_pages_release(fk_pool* p, int n, const int32_t* ids) {
+  if (!p || n < 0 || (n > 0 && !ids)) return fail(FK_ERR_INVALID_ARG, "bad arguments");
+  std::map<int32_t, int> drops;
+  for (int i = 0; i < n; ++i) {
+    if (ids[i] == -1) continue;
+    if (ids[i] < 0 || ids[i] >= p->g.num_pages) return fail(FK_ERR_INVALID_ARG, "page id out of range");
+    drops[ids[i]]++;
+  }
+  for (auto& kv : drops)
+    if (p->refcount[kv.first] < kv.second)
+      return fail(FK_ERR_INVALID_ARG, "releasing a page that is already free");
+  for (auto& kv : drops) {
+    p->refcount[kv.first] -= kv.second;
+    if (p->refcount[kv.first] == 0) p->free_list.push_back(kv.first);
+  }
+  p->plan_valid = false;
+  return FK_OK;
+}
+
+fk_status fk_fork(fk_pool* p, const int32_t* parent, int n, int32_t* child) {
+  if (!p || n < 0 || (n > 0 && (!parent || !child))) return fail(FK_ERR_INVALID_ARG, "bad arguments");
+  for (int i = 0; i < n; ++i) {
+    if (parent[i] == -1) continue;
+    if (parent[i] < 0 || parent[i] >= p->g.num_pages || p->refcount[parent[i]] <= 0)
+      return fail(FK_ERR_INVALID_ARG, "parent row names a free or invalid page");
+  }
+  for (int i = 0; i < n; ++i) {
+    child[i] = parent[i];
+    if (parent[i] >= 0) p->refcount[parent[i]]++;
+  }
+  return FK_OK;
+}
+
+int fk_page_refcount(const fk_pool* p, int32_t id) {
+  if (!p || id < 0 || id >= p->g.num_pages) return -1;
+  return p->refcount[id];
+}
+
+fk_status fk_agent_register(fk_pool* p, int agent, int rank, float s,
+                            const uint16_t* Bk, const uint16_t* Bv, void* stream) {
+  if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
+  if (agent < 0 || agent >= p->g.max_agents) return fail(FK_ERR_INVALID_ARG, "agent id out of range");
+  if (p->agents[agent].live) return fail(FK_ERR_INVALID_ARG, "agent id already registered");
+  if (rank < 8 || rank % 8 || rank > p->cfg.max_rank)
+    return fail(FK_ERR_INVALID_ARG, "rank must be a multiple of 8 and <= max_rank");
+  if (!Bk || !Bv) return fail(FK_ERR_INVALID_ARG, "Bk/Bv are NULL");
+  if (!std::isfinite(s)) return fail(FK_ERR_INVALID_ARG, "s must be finite");
+  int rp = rank_pad(rank);
+  int64_t need = (int64_t)p->g.L * rc_layer_bytes(p->g, rp);
+  auto it = p->rc_free.begin();
+  for (; it != p->rc_free.end(); ++it)
+    if (it->second >= need) break;
+  if (it == p->rc_free.end()) return fail(FK_ERR_OOM, "rCache arena full");
+  int64_t off = it->first, len = it->second;
+  p->rc_free.erase(it);
+  if (len > need) p->rc_free[off + need] = len - need;
+  auto& A = p->agents[agent];
+  A.live = true; A.rank = rank; A.rp = rp; A.s = s; A.rc_off = off; A.rc_bytes = need;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemsetAsync(p->g.base + off, 0, need, st);
+  AgentDev dv{rp, s, off};
+  if (e == cudaSuccess)
+    e = (cudaError_t)launch_agent_register(p->g, agent, rank, rp, dv, Bk, Bv, stream);
+  fk_status r2 = (e == cudaSuccess) ? upload_agent(p, agent, st) : cuda_fail(e, "agent register");
+  if (r2 != FK_OK) {
+    A = fk_pool::Agent{};
+    p->rc_free[off] = need;
+    return r2;
+  }
+  p->plan_valid = false;
+  return FK_OK;
+}
+
+fk_status fk_agent_release(fk_pool* p, int agent) {
+  if (!p || agent < 0 || agent >= p->g.max_agents || !p->agents[agent].live)
+    return fail(FK_ERR_INVALID_ARG, "agent not registered");
+  auto& A = p->agents[agent];
+  // return the range and merge neighbours
+  int64_t off = A.rc_off, len = A.rc_bytes;
+  auto nx = p->rc_free.lower_bound(off);
+  if (nx != p->rc_free.end() && nx->first == off + len) { len += nx->second; p->rc_free.erase(nx); }
+  auto pv = p->rc_free.lower_bound(off);
+  if (pv != p->rc_free.begin()) {
+    --pv;
+    if (pv->first + pv->second == off) { off = pv->first; len += pv->second; p->rc_free.erase(pv); }
+  }
+  p->rc_free[off] = len;
+  A = fk_pool::Agent{};
+  p->plan_valid = false;
+  return upload_agent(p, agent, nullptr);
+}
+
+fk_status fk_base_append(fk_pool* p, int layer, int32_t* row, int max_pages, int pos,
+                         int n, const uint16_t* Kb, const uint16_t* Vb, void* stream) {
+  if (!p || !row) return fail(FK_ERR_INVALID_ARG, "NULL argument");
+  if (layer < 0 || layer >= p->g.L) return fail(FK_ERR_INVALID_ARG, "layer out of range");
+  if (pos < 0 || n < 0) return fail(FK_ERR_INVALID_ARG, "negative position or count");
+  if (n == 0) return FK_OK;
+  if (!Kb || !Vb) return fail(FK_ERR_INVALID_ARG, "Kb/Vb are NULL");
+  int lp0 = pos / kPage, lp1 = (pos + n - 1) / kPage;
+  if (lp1 >= max_pages) return fail(FK_ERR_INVALID_ARG, "append runs past max_pages");
+  for (int lp = lp0; lp <= lp1; ++lp)
+    if (row[lp] < -1 || row[lp] >= p->g.num_pages || (row[lp] >= 0 && p->refcount[row[lp]] <= 0))
+      return fail(FK_ERR_INVALID_ARG, "block table row names a free or invalid page");
+  int need_new = 0;
+  for (int lp = lp0; lp <= lp1; ++lp)
+    if (row[lp] < 0 || p->refcount[row[lp]] > 1) need_new++;
+  if ((size_t)need_new > p->free_list.size())
+    return fail(FK_ERR_OUT_OF_PAGES, "not enough free pages for append / copy-on-write");
+  cudaStream_t st = (cudaStream_t)stream;
+  const PoolGeom& g = p->g;
+  for (int lp = lp0; lp <= lp1; ++lp) {
+    if (row[lp] < 0) {
+      int32_t id;
+      fk_pages_alloc(p, 1, &id);
+      row[lp] = id;
+    } else if (p->refcount[row[lp]] > 1) {
+      // copy-on-write: never write a page other rows still name
+      int32_t old = row[lp], id;
+      fk_pages_alloc(p, 1, &id);
+      int64_t blk = (int64_t)g.H_kv * g.page_bytes;
+      for (int64_t region : {g.off_kb, g.off_vb}) {
+        cudaError_t e = cudaMemcpy2DAsync(g.base + region + id * blk, g.kb_layer_bytes,
+                                          g.base + region + old * blk, g.kb_layer_bytes,
+                                          blk, g.L, cudaMemcpyDeviceToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(e, "copy-on-write copy");
+      }
+      if (g.compressed) {
+        int64_t tokb = (int64_t)g.H_kv * kPage;
+        struct R { int64_t off, per_tok; } regs[3] = {{g.off_kq, g.d}, {g.off_vc, 3 * g.d / 8}, {g.off_vn, 4}};
+        for (auto& r : regs) {
+          int64_t b = tokb * r.per_tok;
+          cudaError_t e = cudaMemcpy2DAsync(g.base + r.off + id * b, b * g.num_pages,
+                                            g.base + r.off + old * b, b * g.num_pages, b, g.L,
+                                            cudaMemcpyDeviceToDevice, st);
+          if (e != cudaSuccess) return cuda_fail(e, "copy-on-write copy");
+        }
+      }
+      for (int l = 0; l < g.L; ++l)
+        p->fill[(size_t)l * g.num_pages + id] = p->fill[(size_t)l * g.num_pages + old];
+      p->refcount[old]--;
+      row[lp] = id;
+    }
+  }
+  // write in launches of at most 64 pages
+  for (int c0 = lp0; c0 <= lp1; c0 += 64) {
+    int c1 = std::min(lp1, c0 + 63);
+    int t0 = std::max(pos, c0 * kPage), t1 = std::min(pos + n, (c1 + 1) * kPage);
+    int e = launch_base_append(g, layer, row + c0, c1 - c0 + 1, t0, t1 - t0,
+                               Kb + (int64_t)(t0 - pos) * g.H_kv * g.d,
+                               Vb + (int64_t)(t0 - pos) * g.H_kv * g.d, stream);
+    if (e != 0) return cuda_fail((cudaError_t)e, "base append kernel");
+  }
+  for (int lp = lp0; lp <= lp1; ++lp) {
+    int end = std::min(pos + n - lp * kPage, kPage);
+    uint8_t& f = p->fill[(size_t)layer * g.num_pages + row[lp]];
+    f = (uint8_t)std::max<int>(f, end);
+  }
+  p->plan_valid = false;
+  return FK_OK;
+}
+
+fk_status fk_residual_append(fk_pool* p, int layer, int agent, int pos, int n,
+                             const uint16_t* Lk, const uint16_t* Lv, void* stream) {
+  if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
+  if (layer < 0 || layer >= p->g.L) return fail(FK_ERR_INVALID_ARG, "layer out of range");
+  if (agent < 0 || agent >= p->g.max_agents || !p->agents[agent].live)
+    return fail(FK_ERR_INVALID_ARG, "agent not registered");
+  if (pos < 0 || n < 0 || (int64_t)pos + n > p->cfg.max_tokens)
+    return fail(FK_ERR_INVALID_ARG, "rows out of the rCache capacity");
+  if (n == 0) return FK_OK;
+  if (!Lk || !Lv) return fail(FK_ERR_INVALID_ARG, "Lk/Lv are NULL");
+  const auto& A = p->agents[agent];
+  AgentDev dv{A.rp, A.s, A.rc_off};
+  int e = launch_residual_append(p->g, layer, dv, A.rank, pos, n, Lk, Lv, stream);
+  if (e != 0) return cuda_fail((cudaError_t)e, "residual append kernel");
+  return FK_OK;
+}
+
+fk_status fk_pool_compress(fk_pool* p, int layer, void* stream) {
+  if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
+  if (!p->g.compressed) return fail(FK_ERR_INVALID_ARG, "pool has no compressed copy");
+  if (layer < 0 || layer >= p->g.L) return fail(FK_ERR_INVALID_ARG, "layer out of range");
+  std::vector<int32_t> buf;
+  for (int id = 0; id < p->g.num_pages; ++id) {
+    int f = p->fill[(size_t)layer * p->g.num_pages + id];
+    if (p->refcount[id] > 0 && f > 0) { buf.push_back(id); }
+  }
+  int n = (int)buf.size();
+  std::vector<int32_t> fills(n);
+  for (int i = 0; i < n; ++i) fills[i] = p->fill[(size_t)layer * p->g.num_pages + buf[i]];
+  buf.insert(buf.end(), fills.begin(), fills.end());
+  if ((int64_t)buf.size() * 4 > p->g.meta_bytes) return fail(FK_ERR_OOM, "meta region too small");
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t* d = (int32_t*)(p->g.base + p->g.off_meta);
+  if (n > 0) {
+    fk_status s = stage_upload(p, buf.data(), buf.size() * 4, d, st);
+    if (s != FK_OK) return s;
+  }
+  int e = launch_compress(p->g, layer, d, d + n, n, stream);
+  if (e != 0) return cuda_fail((cudaError_t)e, "compress kernels");
+  return FK_OK;
+}
+
+fk_status fk_pool_load_compressed(fk_pool* p, int layer, const int32_t* ids, int n,
+                                  const int8_t* kq, const uint8_t* vc, const float* vn,
+                                  float k_scale, void* stream) {
+  if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
+  if (!p->g.compressed) return fail(FK_ERR_INVALID_ARG, "pool has no compressed copy");
+  if (layer < 0 || layer >= p->g.L) return fail(FK_ERR_INVALID_ARG, "layer out of range");
+  if (n < 0 || (n > 0 && (!ids || !kq || !vc || !vn))) return fail(FK_ERR_INVALID_ARG, "bad arguments");
+  if (!(k_scale > 0.f) || !std::isfinite(k_scale)) return fail(FK_ERR_INVALID_ARG, "k_scale must be > 0");
+  for (int i = 0; i < n; ++i)
+    if (ids[i] < 0 || ids[i] >= p->g.num_pages) return fail(FK_ERR_INVALID_ARG, "page id out of range");
+  if ((int64_t)n * 4 > p->g.meta_bytes) return fail(FK_ERR_OOM, "meta region too small");
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t* d = (int32_t*)(p->g.base + p->g.off_meta);
+  if (n > 0) {
+    fk_status s = stage_upload(p, ids, (size_t)n * 4, d, st);
+    if (s != FK_OK) return s;
+  }
+  int e = launch_load_compressed(p->g, layer, d, n, kq, vc, vn, k_scale, stream);
+  if (e != 0) return cuda_fail((cudaError_t)e, "load compressed kernel");
+  return FK_OK;
+}
+
+fk_status fk_plan_host(int A, int C, int H_q, int H_kv, int page_size,
+                       const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                       const int32_t* ranks, int max_rows, int max_rank_sum, int target_items,
+                       fk_work_item* items, int cap_items, int* n_items,
+                       int32_t* row_agent, int32_t* row_cg, int cap_rows, int* n_rows,
+                       int32_t* page_ids, int cap_pages, int* n_pages,
+                       int32_t* tile_agents, int cap_tile_agents, int* n_tile_agents) {
+  if (page_size != kPage) return fail(FK_ERR_UNSUPPORTED, "page_size must be 16");
+  if (!ranks) return fail(FK_ERR_INVALID_ARG, "ranks is NULL");
+  std::vector<int32_t> rp(A > 0 ? A : 0);
+  for (int i = 0; i < A; ++i) rp[i] = rank_pad(ranks[i]);
+  HostPlan pl;
+  fk_status s = plan_build(A, C, H_q, H_kv, page_size, block_table, max_pages, seq_lens,
+                           rp.data(), max_rows, max_rank_sum, target_items, pl);
+  if (s != FK_OK) return s;
+  if (n_items) *n_items = (int)pl.items.size();
+  if (n_rows) *n_rows = (int)pl.row_agent.size();
+  if (n_pages) *n_pages = (int)pl.pages.size();
+  if (n_tile_agents) *n_tile_agents = (int)pl.tile_agents.size();
+  if ((int)pl.items.size() > cap_items || (int)pl.row_agent.size() > cap_rows ||
+      (int)pl.pages.size() > cap_pages || (int)pl.tile_agents.size() > cap_tile_agents)
+    return fail(FK_ERR_OOM, "output capacity too small");
+  if (items) std::copy(pl.items.begin(), pl.items.end(), items);
+  if (row_agent) std::copy(pl.row_agent.begin(), pl.row_agent.end(), row_agent);
+  if (row_cg) std::copy(pl.row_cg.begin(), pl.row_cg.end(), row_cg);
+  if (page_ids) std::copy(pl.pages.begin(), pl.pages.end(), page_ids);
+  if (tile_agents) std::copy(pl.tile_agents.begin(), pl.tile_agents.end(), tile_agents);
+  return FK_OK;
+}
+
+fk_status fk_residual_attention(fk_pool* p, int layer, const uint16_t* q, const int32_t* agents,
+                                const int32_t* bt, int max_pages, const int32_t* seq, int A,
+                                int C, int causal, int compressed, uint16_t* out, void* stream) {
+  if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
+  const PoolGeom& g = p->g;
+  if (layer < 0 || layer >= g.L) return fail(FK_ERR_INVALID_ARG, "layer out of range");
+  if (!q || !out || !agents || !bt || !seq) return fail(FK_ERR_INVALID_ARG, "NULL argument");
+  if (A < 1 || C < 1 || max_pages < 1) return fail(FK_ERR_INVALID_ARG, "A, C, max_pages must be >= 1");
+  if (compressed && !g.compressed) return fail(FK_ERR_INVALID_ARG, "pool has no compressed copy");
+  cudaStream_t st = (cudaStream_t)stream;
+  // cache key: everything the work list depends on
+  std::vector<int32_t> key;
+  key.reserve(8 + 2 * A + (size_t)A * max_pages);
+  key.insert(key.end(), {A, C, causal ? 1 : 0, max_pages});
+  key.insert(key.end(), agents, agents + A);
+  key.insert(key.end(), seq, seq + A);
+  key.insert(key.end(), bt, bt + (int64_t)A * max_pages);
+  if (!p->plan_valid || key != p->key) {
+    p->plan_valid = false;
+    std::vector<int32_t> rp(A), seen(g.max_agents, 0);
+    for (int i = 0; i < A; ++i) {
+      int a = agents[i];
+      if (a < 0 || a >= g.max_agents || !p->agents[a].live)
+        return fail(FK_ERR_INVALID_ARG, "agents[] names an unregistered agent");
+      if (seen[a]++) return fail(FK_ERR_INVALID_ARG, "agents[] repeats an agent");
+      if (seq[i] > p->cfg.max_tokens) return fail(FK_ERR_INVALID_ARG, "seq_len beyond rCache capacity");
+      rp[i] = p->agents[a].rp;
+      int np = (seq[i] + kPage - 1) / kPage;
+      for (int lp = 0; lp < std::min(np, max_pages); ++lp) {
+        int32_t id = bt[(int64_t)i * max_pages + lp];
+        if (id >= g.num_pages || (id >= 0 && p->refcount[id] <= 0))
+          return fail(FK_ERR_INVALID_ARG, "block table names a free or invalid page");
+      }
+    }
+    HostPlan pl;
+    fk_status s = plan_build(A, C, g.H_q, g.H_kv, kPage, bt, max_pages, seq, rp.data(),
+                             kMaxRows, kMaxRankSum, p->num_sms, pl);
+    if (s != FK_OK) return s;
+    // pack into the workspace
+    PlanDev pd{};
+    pd.n_items = (int)pl.items.size();
+    pd.n_rows = (int)pl.row_agent.size();
+    pd.n_pages = (int)pl.pages.size();
+    pd.n_tile_agents = (int)pl.tile_agents.size();
+    pd.A = A; pd.C = C; pd.causal = causal ? 1 : 0;
+    pd.n_out_rows = A * C * g.H_q;
+    pd.n_partials = pl.n_partials;
+    pd.partial_stride = g.d + g.rmax_pad + 4;
+    std::vector<uint8_t> blob;
+    auto put = [&](const void* src, size_t bytes) {
+      int64_t o = align_up((int64_t)blob.size(), 256);
+      blob.resize(o + bytes);
+      if (bytes) std::memcpy(blob.data() + o, src, bytes);
+      return o;
+    };
+    std::vector<CallAgent> ca(A);
+    for (int i = 0; i < A; ++i) ca[i] = CallAgent{agents[i], seq[i]};
+    pd.off_items = put(pl.items.data(), pl.items.size() * sizeof(fk_work_item));
+    pd.off_row_agent = put(pl.row_agent.data(), pl.row_agent.size() * 4);
+    pd.off_row_cg = put(pl.row_cg.data(), pl.row_cg.size() * 4);
+    pd.off_pages = put(pl.pages.data(), pl.pages.size() * 4);
+    pd.off_tile_agents = put(pl.tile_agents.data(), pl.tile_agents.size() * 4);
+    pd.off_call_agents = put(ca.data(), ca.size() * sizeof(CallAgent));
+    pd.off_csr_ptr = put(pl.csr_ptr.data(), pl.csr_ptr.size() * 4);
+    pd.off_csr_slots = put(pl.csr_slots.data(), pl.csr_slots.size() * 4);
+    pd.off_partials = align_up((int64_t)blob.size(), 256);
+    int64_t need = pd.off_partials + (int64_t)pd.n_partials * pd.partial_stride * 4;
+    if (need > g.ws_bytes) return fail(FK_ERR_OOM, "workspace too small for this call");
+    fk_status s2 = stage_upload(p, blob.data(), blob.size(), g.base + g.off_ws, st);
+    if (s2 != FK_OK) return s2;
+    p->plan = std::move(pl);
+    p->plan_dev = pd;
+    p->key = std::move(key);
+    p->plan_valid = true;
+  }
+  int launches = 0;
+  int e = launch_attention(g, p->plan_dev, layer, q, out, compressed ? 1 : 0, p->num_sms,
+                           stream, &launches);
+  if (e != 0) return cuda_fail((cudaError_t)e, "attention kernels");
+  p->last_launches = launches;
+  return FK_OK;
+}
+
+int fk_last_launch_count(const fk_pool* p) { return p ? p->last_launches : 0; }
+
+fk_status fk_check(fk_pool* p, void* stream) {
+  if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t word[2] = {0, 0};
+  cudaError_t e = cudaMemcpyAsync(word, p->g.base + p->g.off_err, 8, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "fk_check");
+  if (word[0] || word[1]) {
+    cudaMemsetAsync(p->g.base + p->g.off_err, 0, 8, st);
+    cudaStreamSynchronize(st);
+    char msg[128];
+    std::snprintf(msg, sizeof msg, "device check fired: bounds 0x%x, waits %u", word[0], word[1]);
+    return fail(word[1] ? FK_ERR_TIMEOUT : FK_ERR_DEVICE_CHECK, msg);
+  }
+  return FK_OK;
+}
+
+}  // extern "C"

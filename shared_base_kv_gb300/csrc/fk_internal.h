@@ -1,0 +1,93 @@
+// Internal declarations shared by the host side (fk_host.cpp) and the
+// kernels (fk_kernels.cu).  Not part of the C ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include "forkkv.h"
+
+#if defined(__CUDACC__)
+#define FK_HD __host__ __device__
+#else
+#define FK_HD
+#endif
+
+namespace fk {
+
+constexpr int kPage = 16;          // tokens per page
+constexpr int kTileTok = 128;      // tokens per attention tile (8 pages)
+constexpr int kTilePages = kTileTok / kPage;
+constexpr int kMaxRows = 64;       // query rows of one work tile
+constexpr int kMaxRankSum = 64;    // sum of padded ranks of one work tile
+constexpr int kMaxAgentsPerTile = 4;
+constexpr int kMaxRowGroups = 4;   // 16-row query groups the agents of a tile touch
+constexpr int kMaxRankPad = 64;
+
+FK_HD inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+FK_HD inline int rank_pad(int r) { return (r + 15) / 16 * 16; }
+
+// Per registered agent; mirrored on the device.
+struct AgentDev {
+  int32_t rp;              // rank rounded up to 16 (0: not registered)
+  float s;                 // residual scale alpha / r
+  int64_t rc_off;          // byte offset of layer 0's Lk in the carve-out
+};
+
+// Geometry and region offsets of a pool, passed to kernels by value.
+struct PoolGeom {
+  uint8_t* base;           // device carve-out
+  int32_t L, H_q, H_kv, d, G, num_pages, max_agents, rmax_pad;
+  int32_t tcap;            // rCache tokens per agent (multiple of 128)
+  float rope_base;
+  int64_t off_kb, off_vb, off_bk, off_bv, off_agents, off_rope, off_err;
+  int64_t off_kq, off_vc, off_vn, off_ks, off_kmax, off_meta, off_ws;
+  int64_t ws_bytes, meta_bytes;
+  int64_t page_bytes;      // bytes of one (page, head) bf16 block: 16*d*2
+  int64_t kb_layer_bytes;  // num_pages * H_kv * page_bytes
+  int64_t bk_agent_bytes;  // one agent's BkT for all layers
+  int64_t bv_agent_bytes;
+  int32_t compressed;
+};
+
+// rCache bytes of one layer of one agent (Lk + Lv).
+FK_HD inline int64_t rc_layer_bytes(const PoolGeom& g, int rp) {
+  return 2LL * g.tcap * rp * 2;
+}
+
+// ---------------------------------------------------------------- plans --
+// Device-side plan, packed in the workspace.  All offsets are in elements
+// of the named array, counted from the workspace start.
+struct CallAgent {
+  int32_t pool_agent;      // pool agent id
+  int32_t seq_len;         // keys of this agent
+};
+
+struct PlanDev {
+  int32_t n_items, n_rows, n_pages, n_tile_agents, A, C, causal;
+  int32_t n_out_rows;      // A * C * H_q
+  int32_t n_partials;      // partial slots
+  int32_t partial_stride;  // floats per partial slot: d + rmax_pad + 4
+  int64_t off_items, off_row_agent, off_row_cg, off_pages, off_tile_agents,
+          off_call_agents, off_csr_ptr, off_csr_slots, off_partials;
+};
+
+// Host launchers (fk_kernels.cu).  All return a cudaError_t as int.
+int launch_base_append(const PoolGeom& g, int layer, const int32_t* page_of_chunk,
+                       int n_chunks, int pos, int n, const uint16_t* Kb,
+                       const uint16_t* Vb, void* stream);
+int launch_residual_append(const PoolGeom& g, int layer, const AgentDev& ag,
+                           int r, int pos, int n, const uint16_t* Lk,
+                           const uint16_t* Lv, void* stream);
+int launch_agent_register(const PoolGeom& g, int agent, int r, int rp,
+                          const AgentDev& ag, const uint16_t* Bk,
+                          const uint16_t* Bv, void* stream);
+int launch_compress(const PoolGeom& g, int layer, const int32_t* d_pages,
+                    const int32_t* d_fill, int n_pages, void* stream);
+int launch_load_compressed(const PoolGeom& g, int layer, const int32_t* d_pages,
+                           int n_pages, const int8_t* kq, const uint8_t* vcodes,
+                           const float* vnorm, float k_scale, void* stream);
+int launch_attention(const PoolGeom& g, const PlanDev& p, int layer,
+                     const uint16_t* q, uint16_t* out, int compressed,
+                     int num_sms, void* stream, int* n_launches);
+
+}  // namespace fk

@@ -1,0 +1,1103 @@
+// Kernels of libforkkv for sm_103a (GB300).
+//
+//  * base / residual appends into the pool's tensor-core-native layouts;
+//  * agent registration (B matrices laid out for the MMA);
+//  * the compressed pool codec (int8 keys, 3-bit FWHT + Lloyd-Max values);
+//  * the residual attention kernel (warp-specialised, tcgen05 + TMEM, bulk
+//    copies into shared memory) and its split-K combine.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fk_device.cuh"
+#include "fk_internal.h"
+
+namespace fk {
+
+__device__ __forceinline__ uint32_t* err_word(const PoolGeom& g) {
+  return (uint32_t*)(g.base + g.off_err);
+}
+__device__ __forceinline__ void flag_bounds(const PoolGeom& g, uint32_t bit) {
+  atomicOr(err_word(g), bit);
+}
+
+// ============================================================= appends ==
+
+struct PageList {
+  int32_t id[64];
+};
+
+// Tokens t in [pos, pos+n) are written; rows of the touched pages past
+// pos+n are zeroed (a page is only ever appended to at its end).  One
+// thread per (token slot, head, 8-element chunk of d).
+__global__ void base_append_kernel(PoolGeom g, int layer, PageList pages, int lp0, int pos, int n,
+                                   const uint4* __restrict__ Kb, const uint4* __restrict__ Vb) {
+  const int D = g.d, H = g.H_kv, CH = D / 8;
+  const int end = ((pos + n + kPage - 1) / kPage) * kPage;
+  const int64_t total = (int64_t)(end - pos) * H * CH;
+  for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total;
+       u += (int64_t)gridDim.x * blockDim.x) {
+    int ch = (int)(u % CH);
+    int h = (int)((u / CH) % H);
+    int t = pos + (int)(u / ((int64_t)CH * H));
+    int lp = t / kPage, row = t % kPage;
+    int32_t page = pages.id[lp - lp0];
+    if (page < 0 || page >= g.num_pages) { flag_bounds(g, 1u); continue; }
+    uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+    if (t < pos + n) {
+      int64_t src = ((int64_t)(t - pos) * H + h) * CH + ch;
+      kv = Kb[src];
+      vv = Vb[src];
+    }
+    int64_t blk = (int64_t)layer * g.kb_layer_bytes + ((int64_t)page * H + h) * g.page_bytes;
+    // keys: [token-group][d-chunk][token][8 d]
+    uint8_t* kp = g.base + g.off_kb + blk + (((row / 8) * CH + ch) * 128 + (row % 8) * 16);
+    *(uint4*)kp = kv;
+    // values: [token-chunk][d-group][d][8 tokens]
+    uint16_t* vp = (uint16_t*)(g.base + g.off_vb + blk + ((row / 8) * CH + ch) * 128) + (row % 8);
+    const uint16_t* ve = (const uint16_t*)&vv;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vp[e * 8] = ve[e];
+  }
+}
+
+// Residual rows: Lk as [token-group][r-chunk][token][8 r], Lv as
+// [token-chunk][r-group][r][8 tokens]; padding columns r..rp stay zero.
+__global__ void residual_append_kernel(PoolGeom g, uint8_t* lk_base, uint8_t* lv_base, int r,
+                                       int rp, int pos, int n, const uint16_t* __restrict__ Lk,
+                                       const uint16_t* __restrict__ Lv) {
+  const int RC = rp / 8;
+  const int64_t total = (int64_t)n * RC;
+  for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total;
+       u += (int64_t)gridDim.x * blockDim.x) {
+    int ch = (int)(u % RC);
+    int t = pos + (int)(u / RC);
+    uint16_t kv[8], vv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      int c = ch * 8 + e;
+      kv[e] = c < r ? Lk[(int64_t)(t - pos) * r + c] : (uint16_t)0;
+      vv[e] = c < r ? Lv[(int64_t)(t - pos) * r + c] : (uint16_t)0;
+    }
+    uint8_t* kp = lk_base + ((int64_t)(t / 8) * RC + ch) * 128 + (t % 8) * 16;
+    *(uint4*)kp = *(uint4*)kv;
+    uint16_t* vp = (uint16_t*)(lv_base + ((int64_t)(t / 8) * RC + ch) * 128) + (t % 8);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vp[e * 8] = vv[e];
+  }
+}
+
+// B matrices: BkT per (layer, head) as [d-group][r-chunk][d][8 r] (the MMA
+// operand of Lk Bk), Bv row-major [layer][rmax_pad][H_kv*d]; rows past the
+// rank are zero.
+__global__ void agent_register_kernel(PoolGeom g, int agent, int r, int rp,
+                                      const uint16_t* __restrict__ Bk,
+                                      const uint16_t* __restrict__ Bv) {
+  const int D = g.d, H = g.H_kv, HD = H * D, RC = rp / 8;
+  const int64_t total = (int64_t)g.L * g.rmax_pad * HD;
+  uint16_t* bkt = (uint16_t*)(g.base + g.off_bk + (int64_t)agent * g.bk_agent_bytes);
+  uint16_t* bv = (uint16_t*)(g.base + g.off_bv + (int64_t)agent * g.bv_agent_bytes);
+  for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total;
+       u += (int64_t)gridDim.x * blockDim.x) {
+    int col = (int)(u % HD);
+    int k = (int)((u / HD) % g.rmax_pad);
+    int l = (int)(u / ((int64_t)HD * g.rmax_pad));
+    uint16_t bkv = 0, bvv = 0;
+    if (k < r) {
+      int64_t src = ((int64_t)l * r + k) * HD + col;
+      bkv = Bk[src];
+      bvv = Bv[src];
+    }
+    bv[((int64_t)l * g.rmax_pad + k) * HD + col] = bvv;
+    if (k < rp) {
+      int h = col / D, dd = col % D;
+      int64_t blk = ((int64_t)l * H + h) * (int64_t)D * g.rmax_pad;
+      bkt[blk + ((dd / 8) * RC + k / 8) * 64 + (dd % 8) * 8 + (k % 8)] = bkv;
+    }
+  }
+}
+
+// ============================================================ codec =====
+
+__constant__ float c_lloyd[8] = {-2.1520f, -1.3439f, -0.7560f, -0.2451f,
+                                 0.2451f,  0.7560f,  1.3439f,  2.1520f};
+
+__device__ __forceinline__ float bf16_at(const uint8_t* p) {
+  return __bfloat162float(*(const __nv_bfloat16*)p);
+}
+
+// Address of key element (row, dd) of a (layer, page, head) block.
+__device__ __forceinline__ const uint8_t* key_at(const PoolGeom& g, int layer, int page, int h,
+                                                 int row, int dd) {
+  const int CH = g.d / 8;
+  int64_t blk = (int64_t)layer * g.kb_layer_bytes + ((int64_t)page * g.H_kv + h) * g.page_bytes;
+  return g.base + g.off_kb + blk + ((row / 8) * CH + dd / 8) * 128 + (row % 8) * 16 + (dd % 8) * 2;
+}
+__device__ __forceinline__ const uint8_t* val_at(const PoolGeom& g, int layer, int page, int h,
+                                                 int row, int dd) {
+  const int CH = g.d / 8;
+  int64_t blk = (int64_t)layer * g.kb_layer_bytes + ((int64_t)page * g.H_kv + h) * g.page_bytes;
+  return g.base + g.off_vb + blk + ((row / 8) * CH + dd / 8) * 128 + (dd % 8) * 16 + (row % 8) * 2;
+}
+
+// max |K| over the live rows of the listed pages (float bits of |x| order
+// like unsigned integers).
+__global__ void kmax_kernel(PoolGeom g, int layer, const int32_t* __restrict__ pages,
+                            const int32_t* __restrict__ fill, int n_pages) {
+  const int D = g.d, H = g.H_kv;
+  float m = 0.f;
+  const int64_t total = (int64_t)n_pages * kPage * H * D;
+  for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total;
+       u += (int64_t)gridDim.x * blockDim.x) {
+    int dd = (int)(u % D);
+    int h = (int)((u / D) % H);
+    int row = (int)((u / ((int64_t)D * H)) % kPage);
+    int pi = (int)(u / ((int64_t)D * H * kPage));
+    if (row >= fill[pi]) continue;
+    m = fmaxf(m, fabsf(bf16_at(key_at(g, layer, pages[pi], h, row, dd))));
+  }
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) atomicMax((unsigned int*)(g.base + g.off_kmax) + layer, __float_as_uint(m));
+}
+
+// One warp per (page, row, head): int8 keys with the layer scale, and the
+// value vector's norm and 3-bit codes of z = H v / n.
+__global__ void encode_kernel(PoolGeom g, int layer, const int32_t* __restrict__ pages,
+                              const int32_t* __restrict__ fill, int n_pages) {
+  const int D = g.d, H = g.H_kv, PER = D / 32, NB = D / 8;
+  const int lane = threadIdx.x & 31;
+  const float kmax = __uint_as_float(((const unsigned int*)(g.base + g.off_kmax))[layer]);
+  const float scale = kmax > 0.f ? __fdiv_rn(kmax, 127.f) : 1.f;
+  if (blockIdx.x == 0 && threadIdx.x == 0) ((float*)(g.base + g.off_ks))[layer] = scale;
+  const int64_t units = (int64_t)n_pages * kPage * H;
+  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; w < units;
+       w += (int64_t)gridDim.x * blockDim.x / 32) {
+    int h = (int)(w % H);
+    int row = (int)((w / H) % kPage);
+    int pi = (int)(w / ((int64_t)H * kPage));
+    int page = pages[pi];
+    int64_t tok = (((int64_t)layer * g.num_pages + page) * H + h) * kPage + row;
+    // tokens are laid out [L][num_pages][H][16]; keys [..][d], codes [..][3d/8]
+    int8_t* kq = (int8_t*)(g.base + g.off_kq) + tok * D;
+    uint8_t* vc = g.base + g.off_vc + tok * (3 * D / 8);
+    float* vn = (float*)(g.base + g.off_vn) + tok;
+    bool live = row < fill[pi];
+    float v[4];
+    for (int e = 0; e < PER; ++e) {
+      int dd = lane * PER + e;
+      float k = live ? bf16_at(key_at(g, layer, page, h, row, dd)) : 0.f;
+      float qv = fminf(fmaxf(rintf(__fdiv_rn(k, scale)), -127.f), 127.f);
+      kq[dd] = (int8_t)qv;
+      v[e] = live ? bf16_at(val_at(g, layer, page, h, row, dd)) : 0.f;
+    }
+    float ss = 0.f;
+    for (int e = 0; e < PER; ++e) ss = fmaf(v[e], v[e], ss);
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    float nrm = sqrtf(ss);
+    // unnormalised FWHT, natural order: in-thread stages, then across lanes
+    for (int hh = 1; hh < PER; hh <<= 1)
+      for (int e = 0; e < PER; ++e)
+        if (!(e & hh)) { float a = v[e], b = v[e + hh]; v[e] = a + b; v[e + hh] = a - b; }
+    for (int hl = 1; hl < 32; hl <<= 1) {
+      for (int e = 0; e < PER; ++e) {
+        float o = __shfl_xor_sync(0xffffffffu, v[e], hl);
+        v[e] = (lane & hl) ? (o - v[e]) : (v[e] + o);
+      }
+    }
+    uint32_t code[4];
+    for (int e = 0; e < PER; ++e) {
+      float z = nrm > 0.f ? __fdiv_rn(v[e], nrm) : 0.f;
+      uint32_t c = 0;
+#pragma unroll
+      for (int j = 0; j < 7; ++j) c += (z >= 0.5f * (c_lloyd[j] + c_lloyd[j + 1])) ? 1u : 0u;
+      code[e] = c;
+    }
+    // bit planes: plane b, code i at bit i%8 of byte i/8
+    for (int b = 0; b < 3; ++b) {
+      uint32_t bits = 0;
+      for (int e = 0; e < PER; ++e) bits |= ((code[e] >> b) & 1u) << e;   // PER bits of this lane
+      // byte j collects codes 8j..8j+7 = lanes (8j/PER) .. ; gather via shuffles
+      uint32_t byte = 0;
+      const int lanes_per_byte = 8 / PER;
+      for (int q = 0; q < lanes_per_byte; ++q) {
+        uint32_t other = __shfl_sync(0xffffffffu, bits, (lane / lanes_per_byte) * lanes_per_byte + q);
+        byte |= other << (q * PER);
+      }
+      if (lane % lanes_per_byte == 0) vc[b * NB + lane / lanes_per_byte] = (uint8_t)byte;
+    }
+    if (lane == 0) *vn = live ? nrm : 0.f;
+  }
+}
+
+__global__ void load_compressed_kernel(PoolGeom g, int layer, const int32_t* __restrict__ pages,
+                                       int n_pages, const int8_t* __restrict__ kq,
+                                       const uint8_t* __restrict__ vc,
+                                       const float* __restrict__ vn, float k_scale) {
+  const int D = g.d, H = g.H_kv, VB = 3 * D / 8;
+  if (blockIdx.x == 0 && threadIdx.x == 0) ((float*)(g.base + g.off_ks))[layer] = k_scale;
+  const int64_t units = (int64_t)n_pages * kPage * H;   // (page, row, head)
+  for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < units;
+       u += (int64_t)gridDim.x * blockDim.x) {
+    int h = (int)(u % H);
+    int row = (int)((u / H) % kPage);
+    int pi = (int)(u / ((int64_t)H * kPage));
+    int page = pages[pi];
+    if (page < 0 || page >= g.num_pages) { flag_bounds(g, 4u); continue; }
+    int64_t dst = (((int64_t)layer * g.num_pages + page) * H + h) * kPage + row;
+    int64_t src = ((int64_t)pi * kPage + row) * H + h;
+    for (int e = 0; e < D; e += 16)
+      *(uint4*)((int8_t*)(g.base + g.off_kq) + dst * D + e) = *(const uint4*)(kq + src * D + e);
+    for (int e = 0; e < VB; e += 16)
+      *(uint4*)(g.base + g.off_vc + dst * VB + e) = *(const uint4*)(vc + src * VB + e);
+    ((float*)(g.base + g.off_vn))[dst] = vn[src];
+  }
+}
+
+// ========================================================= attention =====
+//
+// One persistent CTA per SM walks the work items.  Each item is one kv head,
+// up to 64 query rows of up to 4 agents (sum of padded ranks <= 64) that
+// name the same physical pages over a run of logical pages.  The run is cut
+// into 128-token tiles; per tile:
+//   producer warp : bulk-copies the tile's Kb pages, each agent's Lk rows,
+//                   and (one tile ahead) the Vb pages and Lv rows to smem;
+//   MMA warp      : S  = Kb Q^T                     (TMEM, tokens x rows)
+//                   U_a = Lk_a Bk_a^T  per agent    (TMEM, tokens x d, fp32)
+//                   S += R_a (Q s_a)^T per agent    (A operand from TMEM)
+//                   O^T += Vb^T P^T, OL_a += P Lv_a, L += P 1
+//   compute WG    : R_a = RoPE_t(U_a) in f16, written back over U_a; masked
+//                   online softmax of S (rescaling O, OL, L only when a
+//                   row's running max grows by more than 2^8); P in bf16.
+// Per item the compute warpgroup writes the split partial (m, l, O, OL)
+// of every row; the combine kernel merges splits and applies Bv once.
+
+namespace attn {
+
+constexpr int kThreads = 256;
+constexpr int kPRowGroup = 2304;        // P: 16 token-chunks x 144 B
+constexpr int kPChunk = 144;
+// TMEM columns
+constexpr uint32_t kTmS = 0, kTmU0 = 64, kTmU1 = 192, kTmOT = 320, kTmOL = 384, kTmL = 448;
+
+template <int D, bool COMP>
+struct Layout {
+  static constexpr int PAGE_B = kPage * D * 2;
+  static constexpr int P_B = 8 * kPRowGroup;
+  static constexpr int KB_B = kTilePages * PAGE_B;
+  static constexpr int LK_B = kMaxRankSum * kTileTok * 2;
+  static constexpr int VB_B = KB_B;
+  static constexpr int LV_B = LK_B;
+  static constexpr int BK_B = kMaxRankSum * D * 2;
+  static constexpr int Q_B = kMaxRows * D * 2;
+  static constexpr int QM_B = 4 * 16 * D * 2;
+  static constexpr int ONES_B = 16 * kTileTok * 2;
+  static constexpr int KQ_B = COMP ? kTilePages * kPage * D : 0;
+  static constexpr int VC_B = COMP ? kTilePages * kPage * (3 * D / 8) : 0;
+  static constexpr int VN_B = COMP ? kTilePages * kPage * 4 : 0;
+  static constexpr int oP = 0;
+  static constexpr int oKB = oP + P_B;              // the OL MMA reads 16 row-groups of P:
+  static constexpr int oLK0 = oKB + KB_B;           // the 8 past P_B fall in KB/LK (finite)
+  static constexpr int oLK1 = oLK0 + LK_B;
+  static constexpr int oVB = oLK1 + LK_B;
+  static constexpr int oLV = oVB + VB_B;            // d=64 reads 1 KB past VB: lands in LV
+  static constexpr int oBK = oLV + LV_B;
+  static constexpr int oQ = oBK + BK_B;
+  static constexpr int oQM = oQ + Q_B;
+  static constexpr int oONES = oQM + QM_B;
+  static constexpr int oKQ = oONES + ONES_B;
+  static constexpr int oVC = oKQ + KQ_B;
+  static constexpr int oVN = oVC + VC_B;
+  static constexpr int oMISC = (oVN + VN_B + 127) / 128 * 128;
+  static constexpr int MISC_B = 4096;
+  static constexpr int TOTAL = oMISC + MISC_B;
+};
+
+// barrier indices
+enum {
+  B_KB_FULL, B_KB_EMPTY, B_LK_FULL0, B_LK_FULL1, B_LK_EMPTY0, B_LK_EMPTY1, B_VL_FULL,
+  B_VL_EMPTY, B_BK_FULL, B_BK_EMPTY, B_Q_FULL, B_Q_EMPTY, B_U_FULL0, B_U_FULL1, B_R_FULL0,
+  B_R_FULL1, B_UFREE0, B_UFREE1, B_S_FULL, B_S_EMPTY, B_P_FULL, B_PV_DONE, B_ACC_EMPTY,
+  B_KQ_FULL, B_KQ_EMPTY, B_VC_FULL, B_VC_EMPTY, B_FINAL, B_COUNT
+};
+
+struct Misc {
+  uint64_t bar[B_COUNT];
+  uint32_t tmem_base;
+  int abort_flag;
+  float m_used[kMaxRows];
+  float alpha[kMaxRows];
+  float red[4][kMaxRows];
+  int32_t row_T[kMaxRows];
+  int32_t row_pos[kMaxRows];
+  int32_t row_tagent[kMaxRows];
+  uint32_t rot0[64];       // per tile: f16x2 (cos) pairs then (sin) pairs
+};
+
+// What every role derives from a work item.
+struct ItemInfo {
+  int head, n_rows, nrp, n_pages, lp_begin, n_ag, partial_begin, row_begin, n_tiles;
+  int rp[4], ol_col[4], lk_off[4], bk_off[4], qm_off[4], g0[4], ng[4], ra0[4], ra1[4];
+  int call_agent[4], pool_agent[4];
+  float s[4];
+  int64_t rc_off[4];
+};
+
+__device__ __forceinline__ void load_item(const PoolGeom& g, const PlanDev& p, const uint8_t* ws,
+                                          int it, ItemInfo& I) {
+  const fk_work_item& w = ((const fk_work_item*)(ws + p.off_items))[it];
+  const int32_t* tile_agents = (const int32_t*)(ws + p.off_tile_agents);
+  const CallAgent* ca = (const CallAgent*)(ws + p.off_call_agents);
+  const AgentDev* ag = (const AgentDev*)(g.base + g.off_agents);
+  I.head = w.head;
+  I.n_rows = w.n_rows;
+  I.nrp = (w.n_rows + 15) / 16 * 16;
+  I.n_pages = w.n_pages;
+  I.lp_begin = w.lp_begin;
+  I.n_ag = w.n_agents;
+  I.partial_begin = w.partial_begin;
+  I.row_begin = w.row_begin;
+  I.n_tiles = (w.n_pages + kTilePages - 1) / kTilePages;
+  const int rpa = g.G * p.C;
+  int col = 0, qm = 0;
+  for (int a = 0; a < 4; ++a) {
+    if (a < I.n_ag) {
+      int ci = tile_agents[w.agent_begin + a];
+      int pa = ca[ci].pool_agent;
+      AgentDev dv = ag[pa];
+      I.call_agent[a] = ci;
+      I.pool_agent[a] = pa;
+      I.rp[a] = dv.rp;
+      I.s[a] = dv.s;
+      I.rc_off[a] = dv.rc_off;
+      I.ol_col[a] = col;
+      I.lk_off[a] = col * kTileTok * 2;     // Lk/Lv stage blocks: rp x 128 tokens
+      I.bk_off[a] = 0;                      // byte offsets: item_offsets<D>
+      col += dv.rp;
+      if (I.n_ag == 1) { I.ra0[a] = 0; I.ra1[a] = w.n_rows; }
+      else { I.ra0[a] = a * rpa; I.ra1[a] = (a + 1) * rpa; }
+      I.g0[a] = I.ra0[a] / 16;
+      I.ng[a] = (I.ra1[a] - 1) / 16 - I.g0[a] + 1;
+      I.qm_off[a] = qm;
+      qm += I.ng[a];
+    } else {
+      I.rp[a] = 0; I.ng[a] = 0; I.call_agent[a] = 0; I.pool_agent[a] = 0;
+    }
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void item_offsets(ItemInfo& I) {
+  int col = 0, qm = 0;
+  for (int a = 0; a < I.n_ag; ++a) {
+    I.bk_off[a] = col * D * 2;
+    I.qm_off[a] = qm * 16 * D * 2;
+    col += I.rp[a];
+    qm += I.ng[a];
+  }
+}
+
+__device__ __forceinline__ const uint8_t* rc_lk(const PoolGeom& g, const ItemInfo& I, int a,
+                                                int layer) {
+  return g.base + I.rc_off[a] + (int64_t)layer * rc_layer_bytes(g, I.rp[a]);
+}
+__device__ __forceinline__ const uint8_t* rc_lv(const PoolGeom& g, const ItemInfo& I, int a,
+                                                int layer) {
+  return rc_lk(g, I, a, layer) + (int64_t)g.tcap * I.rp[a] * 2;
+}
+
+}  // namespace attn
+
+template <int D, bool COMP>
+__global__ void __launch_bounds__(attn::kThreads, 1)
+    attention_kernel(PoolGeom g, PlanDev p, int layer, const uint16_t* __restrict__ q) {
+  using namespace attn;
+  using LY = Layout<D, COMP>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Misc& M = *reinterpret_cast<Misc*>(smem + LY::oMISC);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint8_t* ws = g.base + g.off_ws;
+  uint32_t* errw = err_word(g);
+  volatile int* abort_flag = &M.abort_flag;
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) { return smem_u32(&M.bar[i]); };
+
+  // ---- set-up: zero smem (junk rows read by padded MMAs stay finite),
+  // ones block, barriers, TMEM.
+  for (int i = tid * 16; i < LY::TOTAL; i += kThreads * 16) *(uint4*)(smem + i) = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  for (int i = tid; i < LY::ONES_B / 2; i += kThreads) ((uint16_t*)(smem + LY::oONES))[i] = 0x3F80;
+  if (tid == 0) {
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), (i == B_VL_FULL && COMP) ? 2u : 1u);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&M.tmem_base), 512);
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = M.tmem_base;
+
+  if (warp == 0 && lane == 0) {
+    // ================================================== producer ====
+    uint32_t ph_kb_empty = 1, ph_lk_empty[2] = {1, 1}, ph_vl_empty = 1, ph_bk_empty = 1;
+    uint32_t ph_kq_empty = 1, ph_vc_empty = 1;
+    int tile_ctr = 0;
+    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      ItemInfo I;
+      load_item(g, p, ws, it, I);
+      item_offsets<D>(I);
+      const int32_t* pages = (const int32_t*)(ws + p.off_pages) + ((const fk_work_item*)(ws + p.off_items))[it].page_begin;
+      // B_k^T of the item's agents, for this head
+      mbar_wait(bar(B_BK_EMPTY), ph_bk_empty, abort_flag, errw);
+      {
+        uint32_t bytes = 0;
+        for (int a = 0; a < I.n_ag; ++a) bytes += D * I.rp[a] * 2;
+        mbar_expect_tx(bar(B_BK_FULL), bytes);
+        for (int a = 0; a < I.n_ag; ++a) {
+          const uint8_t* src = g.base + g.off_bk + (int64_t)I.pool_agent[a] * g.bk_agent_bytes +
+                               ((int64_t)layer * g.H_kv + I.head) * (int64_t)D * g.rmax_pad * 2;
+          bulk_g2s(sbase + LY::oBK + I.bk_off[a], src, D * I.rp[a] * 2, bar(B_BK_FULL));
+        }
+      }
+      for (int k = 0; k < I.n_tiles; ++k, ++tile_ctr) {
+        const int p0 = k * kTilePages;
+        const int np = min(kTilePages, I.n_pages - p0);
+        const int t0 = (I.lp_begin + p0) * kPage;
+        // keys
+        if (!COMP) {
+          mbar_wait(bar(B_KB_EMPTY), ph_kb_empty, abort_flag, errw);
+          mbar_expect_tx(bar(B_KB_FULL), np * LY::PAGE_B);
+          for (int j = 0; j < np; ++j) {
+            int pg = pages[p0 + j];
+            const uint8_t* src = g.base + g.off_kb + (int64_t)layer * g.kb_layer_bytes +
+                                 ((int64_t)pg * g.H_kv + I.head) * LY::PAGE_B;
+            bulk_g2s(sbase + LY::oKB + j * LY::PAGE_B, src, LY::PAGE_B, bar(B_KB_FULL));
+          }
+        } else {
+          mbar_wait(bar(B_KQ_EMPTY), ph_kq_empty, abort_flag, errw);
+          mbar_expect_tx(bar(B_KQ_FULL), np * kPage * D);
+          for (int j = 0; j < np; ++j) {
+            int pg = pages[p0 + j];
+            const uint8_t* src = g.base + g.off_kq +
+                                 ((((int64_t)layer * g.num_pages + pg) * g.H_kv + I.head) * kPage) * D;
+            bulk_g2s(sbase + LY::oKQ + j * kPage * D, src, kPage * D, bar(B_KQ_FULL));
+          }
+        }
+        // residual keys of every agent (128 tokens, clamped to the capacity)
+        {
+          const int b = tile_ctr & 1;
+          mbar_wait(bar(B_LK_EMPTY0 + b), ph_lk_empty[b], abort_flag, errw);
+          const int ntok = min(kTileTok, g.tcap - t0);
+          uint32_t bytes = 0;
+          for (int a = 0; a < I.n_ag; ++a) bytes += ntok * I.rp[a] * 2;
+          mbar_expect_tx(bar(B_LK_FULL0 + b), bytes);
+          for (int a = 0; a < I.n_ag; ++a)
+            bulk_g2s(sbase + (b ? LY::oLK1 : LY::oLK0) + I.lk_off[a],
+                     rc_lk(g, I, a, layer) + (int64_t)t0 * I.rp[a] * 2, ntok * I.rp[a] * 2,
+                     bar(B_LK_FULL0 + b));
+        }
+        // values (consumed at the end of the tile)
+        if (COMP) {
+          mbar_wait(bar(B_VC_EMPTY), ph_vc_empty, abort_flag, errw);
+          mbar_expect_tx(bar(B_VC_FULL), np * kPage * (3 * D / 8 + 4));
+          for (int j = 0; j < np; ++j) {
+            int pg = pages[p0 + j];
+            int64_t tok = (((int64_t)layer * g.num_pages + pg) * g.H_kv + I.head) * kPage;
+            bulk_g2s(sbase + LY::oVC + j * kPage * (3 * D / 8), g.base + g.off_vc + tok * (3 * D / 8),
+                     kPage * (3 * D / 8), bar(B_VC_FULL));
+            bulk_g2s(sbase + LY::oVN + j * kPage * 4, g.base + g.off_vn + tok * 4, kPage * 4,
+                     bar(B_VC_FULL));
+          }
+        }
+        mbar_wait(bar(B_VL_EMPTY), ph_vl_empty, abort_flag, errw);
+        {
+          const int ntok = min(kTileTok, g.tcap - t0);
+          uint32_t bytes = COMP ? 0 : np * LY::PAGE_B;
+          for (int a = 0; a < I.n_ag; ++a) bytes += ntok * I.rp[a] * 2;
+          mbar_expect_tx(bar(B_VL_FULL), bytes);
+          if (!COMP)
+            for (int j = 0; j < np; ++j) {
+              int pg = pages[p0 + j];
+              const uint8_t* src = g.base + g.off_vb + (int64_t)layer * g.kb_layer_bytes +
+                                   ((int64_t)pg * g.H_kv + I.head) * LY::PAGE_B;
+              bulk_g2s(sbase + LY::oVB + j * LY::PAGE_B, src, LY::PAGE_B, bar(B_VL_FULL));
+            }
+          for (int a = 0; a < I.n_ag; ++a)
+            bulk_g2s(sbase + LY::oLV + I.lk_off[a], rc_lv(g, I, a, layer) + (int64_t)t0 * I.rp[a] * 2,
+                     ntok * I.rp[a] * 2, bar(B_VL_FULL));
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ===================================================== MMA issuer ====
+    uint32_t ph_kb_full = 0, ph_lk_full[2] = {0, 0}, ph_vl_full = 0, ph_bk_full = 0, ph_q_full = 0;
+    uint32_t ph_r_full[2] = {0, 0}, ph_ufree[2] = {1, 1}, ph_s_empty = 1, ph_p_full = 0;
+    uint32_t ph_acc_empty = 1;
+    int tile_ctr = 0;
+    const uint32_t t_S = tmem + kTmS, t_OT = tmem + kTmOT, t_OL = tmem + kTmOL, t_L = tmem + kTmL;
+    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      ItemInfo I;
+      load_item(g, p, ws, it, I);
+      item_offsets<D>(I);
+      mbar_wait(bar(B_BK_FULL), ph_bk_full, abort_flag, errw);
+      mbar_wait(bar(B_Q_FULL), ph_q_full, abort_flag, errw);
+      tc_fence_after();
+      const uint32_t id_S = idesc_f16(128, I.nrp, 1);
+      const uint32_t id_U = idesc_f16(128, D, 1);
+      const uint32_t id_PV = idesc_f16(128, I.nrp, 1);
+      const uint32_t id_L = idesc_f16(128, 16, 1);
+      auto residual = [&](int a) {
+        const int b = a & 1;
+        mbar_wait(bar(B_R_FULL0 + b), ph_r_full[b], abort_flag, errw);
+        tc_fence_after();
+        const uint32_t id_R = idesc_f16(128, 16 * I.ng[a], 0);
+        const uint32_t t_R = tmem + (b ? kTmU1 : kTmU0);
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ts(t_S + 16 * I.g0[a], t_R + 8 * ks,
+                 sdesc(sbase + LY::oQM + I.qm_off[a] + ks * 128, (D / 16) * 128, (D / 8) * 128),
+                 id_R, 1);
+        mma_commit(bar(B_UFREE0 + b));
+      };
+      auto pv = [&](int j) {
+        mbar_wait(bar(B_P_FULL), ph_p_full, abort_flag, errw);
+        mbar_wait(bar(B_VL_FULL), ph_vl_full, abort_flag, errw);
+        if (j == 0) mbar_wait(bar(B_ACC_EMPTY), ph_acc_empty, abort_flag, errw);
+        tc_fence_after();
+        for (int ks = 0; ks < kTileTok / 16; ++ks) {
+          const uint32_t acc = (j == 0 && ks == 0) ? 0u : 1u;
+          const uint64_t dP = sdesc(sbase + LY::oP + ks * 2 * kPChunk, kPChunk, kPRowGroup);
+          mma_ss(t_OT, sdesc(sbase + LY::oVB + ks * LY::PAGE_B, (D / 8) * 128, 128), dP, id_PV, acc);
+          for (int a = 0; a < I.n_ag; ++a) {
+            const int rc = I.rp[a] / 8;
+            mma_ss(t_OL + I.ol_col[a], dP,
+                   sdesc(sbase + LY::oLV + I.lk_off[a] + ks * 2 * rc * 128, rc * 128, 128),
+                   idesc_f16(128, I.rp[a], 1), acc);
+          }
+          mma_ss(t_L, dP, sdesc(sbase + LY::oONES + ks * 256, 128, 2048), id_L, acc);
+        }
+        mma_commit(bar(B_VL_EMPTY));
+        mma_commit(bar(B_PV_DONE));
+      };
+      for (int k = 0; k < I.n_tiles; ++k, ++tile_ctr) {
+        // S = Kb Q^T
+        mbar_wait(bar(B_S_EMPTY), ph_s_empty, abort_flag, errw);
+        mbar_wait(bar(B_KB_FULL), ph_kb_full, abort_flag, errw);
+        tc_fence_after();
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(t_S, sdesc(sbase + LY::oKB + ks * 256, 128, (D / 8) * 128),
+                 sdesc(sbase + LY::oQ + ks * 256, 128, (D / 8) * 128), id_S, ks > 0 ? 1u : 0u);
+        mma_commit(bar(B_KB_EMPTY));
+        // per agent: U_a = Lk_a Bk_a^T, then (one agent behind) S += R Qm^T
+        const int lb = tile_ctr & 1;
+        mbar_wait(bar(B_LK_FULL0 + lb), ph_lk_full[lb], abort_flag, errw);
+        tc_fence_after();
+        for (int a = 0; a < I.n_ag; ++a) {
+          const int b = a & 1;
+          mbar_wait(bar(B_UFREE0 + b), ph_ufree[b], abort_flag, errw);
+          tc_fence_after();
+          const int rc = I.rp[a] / 8;
+          const uint32_t t_U = tmem + (b ? kTmU1 : kTmU0);
+          for (int ks = 0; ks < I.rp[a] / 16; ++ks)
+            mma_ss(t_U, sdesc(sbase + (lb ? LY::oLK1 : LY::oLK0) + I.lk_off[a] + ks * 256, 128, rc * 128),
+                   sdesc(sbase + LY::oBK + I.bk_off[a] + ks * 256, 128, rc * 128), id_U,
+                   ks > 0 ? 1u : 0u);
+          mma_commit(bar(B_U_FULL0 + b));
+          if (a > 0) residual(a - 1);
+        }
+        mma_commit(bar(B_LK_EMPTY0 + lb));
+        residual(I.n_ag - 1);
+        mma_commit(bar(B_S_FULL));
+        if (k > 0) pv(k - 1);
+      }
+      pv(I.n_tiles - 1);
+      mma_commit(bar(B_Q_EMPTY));
+      mma_commit(bar(B_BK_EMPTY));
+    }
+    // every MMA this CTA issued has completed before TMEM is released
+    uint32_t ph_final = 0;
+    mma_commit(bar(B_FINAL));
+    mbar_wait(bar(B_FINAL), ph_final, abort_flag, errw);
+  } else if (COMP && (warp == 2 || warp == 3)) {
+    // ================================== dequantiser (compressed pool) ====
+    const int ct = tid - 64;   // 0..63
+    uint32_t ph_kq_full = 0, ph_kb_empty = 1, ph_vc_full = 0, ph_vl_empty = 1;
+    const float kscale = ((const float*)(g.base + g.off_ks))[layer];
+    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      ItemInfo I;
+      load_item(g, p, ws, it, I);
+      for (int k = 0; k < I.n_tiles; ++k) {
+        const int np = min(kTilePages, I.n_pages - k * kTilePages);
+        // keys: int8 [page][16][D] -> bf16 (value * scale) in the key layout
+        mbar_wait(bar(B_KQ_FULL), ph_kq_full, abort_flag, errw);
+        mbar_wait(bar(B_KB_EMPTY), ph_kb_empty, abort_flag, errw);
+        for (int u = ct; u < np * kPage * (D / 8); u += 64) {
+          int ch = u % (D / 8), row = (u / (D / 8)) % kPage, pj = u / (kPage * (D / 8));
+          const int8_t* src = (const int8_t*)(smem + LY::oKQ) + (pj * kPage + row) * D + ch * 8;
+          uint32_t w[4];
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf2((float)src[2 * e] * kscale, (float)src[2 * e + 1] * kscale);
+          *(uint4*)(smem + LY::oKB + pj * LY::PAGE_B + ((row / 8) * (D / 8) + ch) * 128 + (row % 8) * 16) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async();
+        named_bar(3, 64);
+        if (ct == 0) { mbar_arrive(bar(B_KB_FULL)); mbar_arrive(bar(B_KQ_EMPTY)); }
+        // values: codes -> level * n / D in the value layout (rotated domain)
+        mbar_wait(bar(B_VC_FULL), ph_vc_full, abort_flag, errw);
+        mbar_wait(bar(B_VL_EMPTY), ph_vl_empty, abort_flag, errw);
+        for (int u = ct; u < np * 2 * (D / 8); u += 64) {
+          int dg = u % (D / 8), tc = (u / (D / 8)) % 2, pj = u / (2 * (D / 8));
+          float w8[8];
+          uint32_t c8[8];
+          for (int tt = 0; tt < 8; ++tt) {
+            int row = tc * 8 + tt;
+            const uint8_t* cb = smem + LY::oVC + (pj * kPage + row) * (3 * D / 8);
+            uint32_t b0 = cb[dg], b1 = cb[D / 8 + dg], b2 = cb[2 * (D / 8) + dg];
+            c8[tt] = b0 | (b1 << 8) | (b2 << 16);
+            w8[tt] = ((const float*)(smem + LY::oVN))[pj * kPage + row] * (1.0f / D);
+          }
+          uint8_t* dst = smem + LY::oVB + pj * LY::PAGE_B + (tc * (D / 8) + dg) * 128;
+          for (int e = 0; e < 8; ++e) {   // d = 8 dg + e
+            uint32_t w[4];
+            for (int h2 = 0; h2 < 4; ++h2) {
+              float v2[2];
+              for (int z = 0; z < 2; ++z) {
+                uint32_t cc = c8[2 * h2 + z];
+                uint32_t code = ((cc >> e) & 1u) | (((cc >> (8 + e)) & 1u) << 1) | (((cc >> (16 + e)) & 1u) << 2);
+                v2[z] = c_lloyd[code] * w8[2 * h2 + z];
+              }
+              w[h2] = pack_bf2(v2[0], v2[1]);
+            }
+            *(uint4*)(dst + e * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        fence_proxy_async();
+        named_bar(3, 64);
+        if (ct == 0) { mbar_arrive(bar(B_VL_FULL)); mbar_arrive(bar(B_VC_EMPTY)); }
+      }
+    }
+  } else if (warp >= 4) {
+    // ================================================= compute WG ====
+    const int ln = tid - 128;                          // TMEM lane = token / d / row
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    uint32_t ph_u_full[2] = {0, 0}, ph_s_full = 0, ph_pv_done = 0, ph_q_empty = 1;
+    const float* rope_tab = (const float*)(g.base + g.off_rope);
+    // per-thread rotation by its offset tau = ln inside a tile (f16 pairs)
+    uint32_t ctau[D / 4], stau[D / 4];
+    for (int j = 0; j < D / 4; ++j) {
+      float c0, s0, c1, s1;
+      sincosf((float)ln * rope_tab[2 * j], &s0, &c0);
+      sincosf((float)ln * rope_tab[2 * j + 1], &s1, &c1);
+      ctau[j] = pack_h2(c0, c1);
+      stau[j] = pack_h2(s0, s1);
+    }
+    const float scale_log2 = 1.4426950408889634f * rsqrtf((float)D);
+    int tile_ctr = 0;
+    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+      ItemInfo I;
+      load_item(g, p, ws, it, I);
+      item_offsets<D>(I);
+      const int32_t* row_agent = (const int32_t*)(ws + p.off_row_agent) + I.row_begin;
+      const int32_t* row_cg = (const int32_t*)(ws + p.off_row_cg) + I.row_begin;
+      const CallAgent* ca = (const CallAgent*)(ws + p.off_call_agents);
+      // ---- stage Q (bf16) and per-agent s_a * Q (f16, other agents' rows 0)
+      mbar_wait(bar(B_Q_EMPTY), ph_q_empty, abort_flag, errw);
+      if (ln < kMaxRows) {
+        M.m_used[ln] = -INFINITY;
+        if (ln < I.n_rows) {
+          int ci = row_agent[ln];
+          int T = ca[ci].seq_len;
+          int c = row_cg[ln] / g.G;
+          M.row_T[ln] = T;
+          M.row_pos[ln] = p.causal ? (T - p.C + c) : 0x7fffffff;
+          int ta = 0;
+          for (int a = 0; a < I.n_ag; ++a) if (I.call_agent[a] == ci) ta = a;
+          M.row_tagent[ln] = ta;
+        }
+      }
+      for (int u = ln; u < I.nrp * (D / 8); u += 128) {
+        int row = u / (D / 8), ch = u % (D / 8);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < I.n_rows) {
+          int ci = row_agent[row], cg = row_cg[row];
+          int c = cg / g.G, gg = cg % g.G;
+          int64_t qrow = ((int64_t)ci * p.C + c) * g.H_q + I.head * g.G + gg;
+          v = *(const uint4*)(q + qrow * D + ch * 8);
+        }
+        *(uint4*)(smem + LY::oQ + ((row / 8) * (D / 8) + ch) * 128 + (row % 8) * 16) = v;
+      }
+      for (int a = 0; a < I.n_ag; ++a) {
+        for (int u = ln; u < I.ng[a] * 16 * (D / 8); u += 128) {
+          int lr = u / (D / 8), ch = u % (D / 8);
+          int row = I.g0[a] * 16 + lr;
+          uint32_t w[4] = {0, 0, 0, 0};
+          if (row >= I.ra0[a] && row < I.ra1[a] && row < I.n_rows) {
+            int ci = row_agent[row], cg = row_cg[row];
+            int c = cg / g.G, gg = cg % g.G;
+            int64_t qrow = ((int64_t)ci * p.C + c) * g.H_q + I.head * g.G + gg;
+            const __nv_bfloat16* src = (const __nv_bfloat16*)(q + qrow * D + ch * 8);
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_h2(__bfloat162float(src[2 * e]) * I.s[a], __bfloat162float(src[2 * e + 1]) * I.s[a]);
+          }
+          *(uint4*)(smem + LY::oQM + I.qm_off[a] + ((lr / 8) * (D / 8) + ch) * 128 + (lr % 8) * 16) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async();
+      named_bar(1, 128);
+      if (ln == 0) mbar_arrive(bar(B_Q_FULL));
+
+      for (int k = 0; k < I.n_tiles; ++k, ++tile_ctr) {
+        const int t0 = (I.lp_begin + k * kTilePages) * kPage;
+        const int ntok = min(kTileTok, (I.n_pages - k * kTilePages) * kPage);
+        // ---- rotation of the tile start, exact (fp64 angle, reduced)
+        if (ln < D / 4) {
+          float cc[2], ssn[2];
+          for (int z = 0; z < 2; ++z) {
+            int i = 2 * ln + z;
+            double th = (double)rope_tab[i] + (double)rope_tab[64 + i];
+            double ang = (double)t0 * th;
+            double red = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
+            sincosf((float)red, &ssn[z], &cc[z]);
+          }
+          M.rot0[ln] = pack_h2(cc[0], cc[1]);
+          M.rot0[32 + ln] = pack_h2(ssn[0], ssn[1]);
+        }
+        named_bar(1, 128);
+        uint32_t Cp[D / 4], Sp[D / 4];
+        for (int j = 0; j < D / 4; ++j) {
+          __half2 c0 = as_h2(M.rot0[j]), s0 = as_h2(M.rot0[32 + j]);
+          __half2 ct = as_h2(ctau[j]), st = as_h2(stau[j]);
+          Cp[j] = as_u32(__hfma2(c0, ct, __hneg2(__hmul2(s0, st))));
+          Sp[j] = as_u32(__hfma2(s0, ct, __hmul2(c0, st)));
+        }
+        // ---- RoPE of each agent's residual keys, written back as f16 pairs
+        for (int a = 0; a < I.n_ag; ++a) {
+          const int b = a & 1;
+          const uint32_t t_U = tmem + (b ? kTmU1 : kTmU0) + lane_off;
+          mbar_wait(bar(B_U_FULL0 + b), ph_u_full[b], abort_flag, errw);
+          tc_fence_after();
+#pragma unroll
+          for (int ci = 0; ci < D / 16; ++ci) {
+            uint32_t lo[8], hi[8], r8[8];
+            tmem_ld8(t_U + 8 * ci, lo);
+            tmem_ld8(t_U + D / 2 + 8 * ci, hi);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              __half2 xl = __floats2half2_rn(__uint_as_float(lo[2 * j]), __uint_as_float(lo[2 * j + 1]));
+              __half2 xh = __floats2half2_rn(__uint_as_float(hi[2 * j]), __uint_as_float(hi[2 * j + 1]));
+              __half2 C = as_h2(Cp[4 * ci + j]), S = as_h2(Sp[4 * ci + j]);
+              r8[j] = as_u32(__hfma2(xl, C, __hneg2(__hmul2(xh, S))));
+              r8[4 + j] = as_u32(__hfma2(xh, C, __hmul2(xl, S)));
+            }
+            tmem_st8(t_U + 8 * ci, r8);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          named_bar(1, 128);
+          if (ln == 0) mbar_arrive(bar(B_R_FULL0 + b));
+        }
+        // ---- masked online softmax over this tile's 128 tokens
+        mbar_wait(bar(B_S_FULL), ph_s_full, abort_flag, errw);
+        tc_fence_after();
+        float sv[kMaxRows];
+        {
+          uint32_t raw[16];
+#pragma unroll
+          for (int c0 = 0; c0 < kMaxRows; c0 += 16) {
+            if (c0 < I.nrp) {
+              tmem_ld16(tmem + kTmS + c0 + lane_off, raw);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) sv[c0 + e] = __uint_as_float(raw[e]);
+            }
+          }
+        }
+        tc_fence_before();
+        named_bar(1, 128);
+        if (ln == 0) mbar_arrive(bar(B_S_EMPTY));
+        const int tabs = t0 + ln;
+        bool need = false;
+#pragma unroll
+        for (int j = 0; j < kMaxRows; ++j) {
+          if (j < I.n_rows) {
+            bool ok = ln < ntok && tabs < M.row_T[j] && tabs <= M.row_pos[j];
+            float s = ok ? sv[j] * scale_log2 : -INFINITY;
+            sv[j] = s;
+            need |= s > M.m_used[j] + 8.f;
+          }
+        }
+        int any;
+        asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 2, 128, p; selp.u32 %0, 1, 0, q; }"
+                     : "=r"(any) : "r"((int)need));
+        if (k > 0) mbar_wait(bar(B_PV_DONE), ph_pv_done, abort_flag, errw);
+        if (any) {
+          // column max over the tile, new running max, rescale accumulators
+#pragma unroll
+          for (int j = 0; j < kMaxRows; ++j) {
+            if (j < I.n_rows) {
+              float v = sv[j];
+              for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+              if (lane == 0) M.red[warp - 4][j] = v;
+            }
+          }
+          named_bar(1, 128);
+          if (ln < kMaxRows) {
+            float al = 1.f;
+            if (ln < I.n_rows) {
+              float cm = fmaxf(fmaxf(M.red[0][ln], M.red[1][ln]), fmaxf(M.red[2][ln], M.red[3][ln]));
+              float mo = M.m_used[ln];
+              float mn = fmaxf(mo, cm);
+              if (mn > mo) { al = (mo == -INFINITY) ? 0.f : exp2f(mo - mn); M.m_used[ln] = mn; }
+            }
+            M.alpha[ln] = al;
+          }
+          named_bar(1, 128);
+          if (k > 0) {
+            tc_fence_after();
+            // O^T: lane = d, columns = rows
+            uint32_t raw[16];
+            for (int c0 = 0; c0 < I.nrp; c0 += 16) {
+              tmem_ld16(tmem + kTmOT + c0 + lane_off, raw);
+              tmem_wait_ld();
+              for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * M.alpha[c0 + e]);
+              tmem_st16(tmem + kTmOT + c0 + lane_off, raw);
+            }
+            // OL and L: lane = row
+            const float al = ln < kMaxRows ? M.alpha[ln] : 1.f;
+            for (int c0 = 0; c0 < 80; c0 += 16) {
+              tmem_ld16(tmem + kTmOL + c0 + lane_off, raw);
+              tmem_wait_ld();
+              for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * al);
+              tmem_st16(tmem + kTmOL + c0 + lane_off, raw);
+            }
+            tmem_wait_st();
+          }
+        }
+        // ---- P (bf16) -> smem, K-major for the PV / OL / L MMAs
+        {
+          const int tc = ln / 8, tr = ln % 8;
+#pragma unroll
+          for (int j = 0; j < kMaxRows; ++j) {
+            if (j < I.n_rows) {
+              float m = M.m_used[j];
+              float pv = (sv[j] == -INFINITY || m == -INFINITY) ? 0.f : exp2f(sv[j] - m);
+              *(__nv_bfloat16*)(smem + LY::oP + (j / 8) * kPRowGroup + tc * kPChunk + (j % 8) * 16 + tr * 2) =
+                  __float2bfloat16_rn(pv);
+            }
+          }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        named_bar(1, 128);
+        if (ln == 0) mbar_arrive(bar(B_P_FULL));
+      }
+      // ---- epilogue: write this item's split partials
+      mbar_wait(bar(B_PV_DONE), ph_pv_done, abort_flag, errw);
+      tc_fence_after();
+      float* part = (float*)(ws + p.off_partials);
+      const int PS = p.partial_stride;
+      {
+        uint32_t raw[16];
+        for (int c0 = 0; c0 < I.nrp; c0 += 16) {
+          tmem_ld16(tmem + kTmOT + c0 + lane_off, raw);
+          tmem_wait_ld();
+          if (ln < D)
+            for (int e = 0; e < 16; ++e)
+              if (c0 + e < I.n_rows) part[(int64_t)(I.partial_begin + c0 + e) * PS + 4 + ln] = __uint_as_float(raw[e]);
+        }
+        uint32_t ol[80];
+        for (int c0 = 0; c0 < 80; c0 += 16) {
+          tmem_ld16(tmem + kTmOL + c0 + lane_off, raw);
+          tmem_wait_ld();
+          for (int e = 0; e < 16; ++e) ol[c0 + e] = raw[e];
+        }
+        if (ln < I.n_rows) {
+          float* dst = part + (int64_t)(I.partial_begin + ln) * PS;
+          const int ta = M.row_tagent[ln];
+          dst[0] = M.m_used[ln];
+          dst[1] = __uint_as_float(ol[kTmL - kTmOL]);
+          int col0 = 0;
+          for (int a = 0; a < I.n_ag; ++a) if (a < ta) col0 += I.rp[a];
+          for (int kk = 0; kk < 64; ++kk)
+            if (kk < I.rp[ta]) dst[4 + D + kk] = __uint_as_float(ol[col0 + kk]);
+        }
+      }
+      tc_fence_before();
+      named_bar(1, 128);
+      if (ln == 0) mbar_arrive(bar(B_ACC_EMPTY));
+    }
+  }
+  // ---- tear-down.  After a timed-out wait, give bulk copies still in
+  // flight a bounded grace period before the CTA's smem is released.
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (*abort_flag) {
+    long long t0 = clock64();
+    while (clock64() - t0 < 20000000LL) { }
+  }
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ============================================================ combine ====
+// One warp per output row: merge the row's split partials (log-sum-exp in
+// base 2), apply Bv once to the merged P Lv (LRAgent summary, section 3),
+// rotate back the value sum of a compressed pool (inverse FWHT), normalise.
+template <int D, bool COMP>
+__global__ void combine_kernel(PoolGeom g, PlanDev p, int layer, uint16_t* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  if (row >= p.n_out_rows) return;
+  const uint8_t* ws = g.base + g.off_ws;
+  const int32_t* ptr = (const int32_t*)(ws + p.off_csr_ptr);
+  const int32_t* slots = (const int32_t*)(ws + p.off_csr_slots);
+  const float* part = (const float*)(ws + p.off_partials);
+  const CallAgent* ca = (const CallAgent*)(ws + p.off_call_agents);
+  const AgentDev* ag = (const AgentDev*)(g.base + g.off_agents);
+  const int PS = p.partial_stride;
+  const int hq = row % g.H_q;
+  const int i = row / (g.H_q * p.C);
+  const int h = hq / g.G;
+  const int pa = ca[i].pool_agent;
+  const AgentDev dv = ag[pa];
+  constexpr int PER = D / 32;
+  const int b = ptr[row], e = ptr[row + 1];
+  float Mx = -INFINITY;
+  for (int k = b; k < e; ++k) Mx = fmaxf(Mx, part[(int64_t)slots[k] * PS]);
+  float L = 0.f, o[PER], ol[2] = {0.f, 0.f};
+  for (int x = 0; x < PER; ++x) o[x] = 0.f;
+  for (int k = b; k < e; ++k) {
+    const float* s = part + (int64_t)slots[k] * PS;
+    float m = s[0];
+    float w = (m == -INFINITY) ? 0.f : exp2f(m - Mx);
+    L += w * s[1];
+    for (int x = 0; x < PER; ++x) o[x] += w * s[4 + lane * PER + x];
+    for (int x = 0; x < 2; ++x)
+      if (2 * lane + x < dv.rp) ol[x] += w * s[4 + D + 2 * lane + x];
+  }
+  if (COMP) {
+    for (int hh = 1; hh < PER; hh <<= 1)
+      for (int x = 0; x < PER; ++x)
+        if (!(x & hh)) { float a0 = o[x], a1 = o[x + hh]; o[x] = a0 + a1; o[x + hh] = a0 - a1; }
+    for (int hl = 1; hl < 32; hl <<= 1)
+      for (int x = 0; x < PER; ++x) {
+        float ot = __shfl_xor_sync(0xffffffffu, o[x], hl);
+        o[x] = (lane & hl) ? (ot - o[x]) : (o[x] + ot);
+      }
+  }
+  // up-projection of the merged low-rank value sum: (sum_t p_t Lv_t) Bv
+  const uint16_t* bv = (const uint16_t*)(g.base + g.off_bv + (int64_t)pa * g.bv_agent_bytes) +
+                       (int64_t)layer * g.rmax_pad * g.H_kv * D + h * D;
+  float up[PER];
+  for (int x = 0; x < PER; ++x) up[x] = 0.f;
+  for (int kk = 0; kk < dv.rp; ++kk) {
+    float olk = __shfl_sync(0xffffffffu, ol[kk & 1], kk >> 1);
+    const uint16_t* br = bv + (int64_t)kk * g.H_kv * D + lane * PER;
+    for (int x = 0; x < PER; ++x) {
+      uint16_t u = br[x];
+      up[x] = fmaf(olk, __bfloat162float(*(const __nv_bfloat16*)&u), up[x]);
+    }
+  }
+  const float inv = 1.f / L;
+  uint16_t* dst = out + (int64_t)row * D + lane * PER;
+  for (int x = 0; x < PER; ++x) {
+    __nv_bfloat16 r = __float2bfloat16_rn((o[x] + dv.s * up[x]) * inv);
+    dst[x] = *(uint16_t*)&r;
+  }
+}
+
+// ============================================================ launchers ==
+
+static int grid_for(int64_t work, int per_block) {
+  int64_t b = (work + per_block - 1) / per_block;
+  return (int)(b < 1 ? 1 : (b > 65535 ? 65535 : b));
+}
+
+int launch_base_append(const PoolGeom& g, int layer, const int32_t* page_of_chunk, int n_chunks,
+                       int pos, int n, const uint16_t* Kb, const uint16_t* Vb, void* stream) {
+  PageList pl;
+  for (int i = 0; i < 64; ++i) pl.id[i] = i < n_chunks ? page_of_chunk[i] : -1;
+  int lp0 = pos / kPage;
+  int end = ((pos + n + kPage - 1) / kPage) * kPage;
+  int64_t work = (int64_t)(end - pos) * g.H_kv * (g.d / 8);
+  base_append_kernel<<<grid_for(work, 256), 256, 0, (cudaStream_t)stream>>>(
+      g, layer, pl, lp0, pos, n, (const uint4*)Kb, (const uint4*)Vb);
+  return (int)cudaGetLastError();
+}
+
+int launch_residual_append(const PoolGeom& g, int layer, const AgentDev& ag, int r, int pos, int n,
+                           const uint16_t* Lk, const uint16_t* Lv, void* stream) {
+  uint8_t* lk = g.base + ag.rc_off + (int64_t)layer * rc_layer_bytes(g, ag.rp);
+  uint8_t* lv = lk + (int64_t)g.tcap * ag.rp * 2;
+  int64_t work = (int64_t)n * (ag.rp / 8);
+  residual_append_kernel<<<grid_for(work, 256), 256, 0, (cudaStream_t)stream>>>(g, lk, lv, r, ag.rp,
+                                                                                 pos, n, Lk, Lv);
+  return (int)cudaGetLastError();
+}
+
+int launch_agent_register(const PoolGeom& g, int agent, int r, int rp, const AgentDev&,
+                          const uint16_t* Bk, const uint16_t* Bv, void* stream) {
+  int64_t work = (int64_t)g.L * g.rmax_pad * g.H_kv * g.d;
+  agent_register_kernel<<<grid_for(work, 256), 256, 0, (cudaStream_t)stream>>>(g, agent, r, rp, Bk, Bv);
+  return (int)cudaGetLastError();
+}
+
+int launch_compress(const PoolGeom& g, int layer, const int32_t* d_pages, const int32_t* d_fill,
+                    int n_pages, void* stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemsetAsync(g.base + g.off_kmax + 4LL * layer, 0, 4, st);
+  if (e != cudaSuccess) return (int)e;
+  if (n_pages > 0) {
+    int64_t work = (int64_t)n_pages * kPage * g.H_kv * g.d;
+    kmax_kernel<<<grid_for(work, 256 * 8), 256, 0, st>>>(g, layer, d_pages, d_fill, n_pages);
+    int64_t units = (int64_t)n_pages * kPage * g.H_kv;
+    encode_kernel<<<grid_for(units * 32, 256), 256, 0, st>>>(g, layer, d_pages, d_fill, n_pages);
+  } else {
+    encode_kernel<<<1, 32, 0, st>>>(g, layer, d_pages, d_fill, 0);
+  }
+  return (int)cudaGetLastError();
+}
+
+int launch_load_compressed(const PoolGeom& g, int layer, const int32_t* d_pages, int n_pages,
+                           const int8_t* kq, const uint8_t* vc, const float* vn, float k_scale,
+                           void* stream) {
+  int64_t units = (int64_t)n_pages * kPage * g.H_kv;
+  load_compressed_kernel<<<grid_for(units, 256), 256, 0, (cudaStream_t)stream>>>(
+      g, layer, d_pages, n_pages, kq, vc, vn, k_scale);
+  return (int)cudaGetLastError();
+}
+
+template <int D, bool COMP>
+static int launch_attn_t(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q,
+                         uint16_t* out, int num_sms, cudaStream_t st) {
+  using LY = attn::Layout<D, COMP>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(attention_kernel<D, COMP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL);
+    if (e != cudaSuccess) return (int)e;
+    attr_done = true;
+  }
+  int grid = p.n_items < num_sms ? p.n_items : num_sms;
+  attention_kernel<D, COMP><<<grid, attn::kThreads, LY::TOTAL, st>>>(g, p, layer, q);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return (int)e;
+  combine_kernel<D, COMP><<<(p.n_out_rows + 3) / 4, 128, 0, st>>>(g, p, layer, out);
+  return (int)cudaGetLastError();
+}
+
+int launch_attention(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q,
+                     uint16_t* out, int compressed, int num_sms, void* stream, int* n_launches) {
+  cudaStream_t st = (cudaStream_t)stream;
+  *n_launches = 2;
+  if (g.d == 128) {
+    return compressed ? launch_attn_t<128, true>(g, p, layer, q, out, num_sms, st)
+                      : launch_attn_t<128, false>(g, p, layer, q, out, num_sms, st);
+  }
+  return compressed ? launch_attn_t<64, true>(g, p, layer, q, out, num_sms, st)
+                    : launch_attn_t<64, false>(g, p, layer, q, out, num_sms, st);
+}
+
+}  // namespace fk
