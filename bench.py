@@ -1,0 +1,384 @@
+#!/usr/bin/env python
+"""Benchmark of one residual-attention decode step.
+
+Workload: one Llama-3-8B-shaped layer, 8 LoRA agents sharing a 32,768-token
+bf16 base cache in 16-token pages (H_q=32, H_kv=8, d=128, rank 16), one
+decode query per agent.  A step is one ``fk_residual_attention`` call: the
+attention kernel plus the split-K combine.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+N > 1 runs one independent replica per GPU (the path has no data exchange);
+launch it with torch.distributed.run.  ``--impl reference`` times the CPU
+oracle on the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "agent decode tokens/sec and achieved HBM GB/s, 8 agents × 32K shared ctx"
+UNIT = "agent-tokens/s"
+WORKLOAD = "llama8b_32k"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("shared_base_kv_gb300/csrc/fk_kernels.cu",
+                  "shared_base_kv_gb300/csrc/fk_device.cuh",
+                  "shared_base_kv_gb300/csrc/fk_internal.h")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_kernel_llama8b_32k.txt")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def workload_desc(w) -> str:
+    return (f"{w.name}: {w.n_layers} layer, {w.A} agents x {w.prefix} shared tokens "
+            f"(+private 0), H_q={w.H_q}, H_kv={w.H_kv}, d={w.d}, r={int(w.ranks[0])}, "
+            f"C={w.C}, page 16, bf16 pages and rCache")
+
+
+def algorithmic_bytes(w) -> dict:
+    """Bytes the step must move at least once: every live base page token
+    (K and V) read once, all residual rows, q read and out written."""
+    import numpy as np
+    base = int(np.sum(w.slot_fill)) * w.H_kv * w.d * 2 * 2
+    rc = int(np.sum(w.seq_lens.astype(np.int64) * w.ranks)) * 2 * 2
+    qo = w.A * w.C * w.H_q * w.d * 2
+    return {"bcache": base, "rcache": rc, "q": qo, "out": qo,
+            "kernel": base + rc + qo, "step": base + rc + 2 * qo}
+
+
+def measured_peak_hbm():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_per_launch():
+    """dram read+write bytes per launch from the committed ncu summary, if it
+    was taken on the current kernel sources."""
+    try:
+        vals = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    vals[k.strip()] = v.strip()
+        if vals.get("kernel_source_sha256") != kernel_source_hash():
+            return None
+        return int(float(vals["dram_bytes_per_launch"]))
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def oracle_rate(w, budget_s: float, n_pairs_max: int = 10 ** 9, keys: int = 0):
+    """Time the CPU oracle on (agent, kv-head) pairs of the workload.
+
+    Each pair is 1/H_kv of an agent's decode token.  With ``keys`` > 0 the
+    agents' contexts are cut to their first ``keys`` tokens and the units
+    scaled by keys / T (cost is linear in the keys).  Returns
+    (agent-tokens per second, pairs done, seconds)."""
+    import numpy as np
+    import oracle
+    ld = w.layer(0)
+    pk = ld.pages_k.to(dtype=__import__("torch").float64).numpy()
+    pv = ld.pages_v.to(dtype=__import__("torch").float64).numpy()
+    seq = w.seq_lens.copy()
+    lk, lv = ld.lk, ld.lv
+    scale = 1.0
+    if keys:
+        seq = np.minimum(seq, keys).astype(np.int32)
+        lk = [x[:keys] for x in lk]
+        lv = [x[:keys] for x in lv]
+        scale = float(keys) / float(w.seq_lens.max())
+    pairs = [(a, h) for a in range(w.A) for h in range(w.H_kv)]
+    done, t0 = 0, time.perf_counter()
+    while done < n_pairs_max and (time.perf_counter() - t0) < budget_s:
+        a, h = pairs[done % len(pairs)]
+        oracle.residual_attention(pk, pv, w.block_table, seq, lk, lv, ld.bk, ld.bv, ld.q,
+                                  w.s, w.rope_base, w.causal, w.P, pairs=[(a, h)])
+        done += 1
+    dt = time.perf_counter() - t0
+    return done * scale / w.H_kv / dt, done, dt
+
+
+def cpu_baseline_child(budget_s: float):
+    import workloads
+    w = workloads.make_workload(WORKLOAD)
+    rate, done, dt = oracle_rate(w, budget_s)
+    print(json.dumps({"value": rate, "pairs": done, "seconds": dt}))
+
+
+def run_cpu_baseline(budget_s: float = 15.0) -> dict:
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child",
+                        str(budget_s)], capture_output=True, text=True, env=env, timeout=600)
+    try:
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"failed: {r.stderr[-300:]}"}
+    return {"value": d["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{d['pairs']} (agent, kv-head) pairs of the full workload at 32,768 keys "
+                      f"in {d['seconds']:.1f} s, fp64 NumPy, 1 thread; a pair is 1/8 agent-token"}
+
+
+# -------------------------------------------------------------- GPU arm --
+
+def run_gb300(args, rank: int, world: int, local_rank: int):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import workloads
+    from shared_base_kv_gb300 import (fk_last_launch_count, fk_pool_set_profile_event,
+                                      fk_residual_attention, harness)
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = workloads.make_workload(WORKLOAD)
+    dw = harness.DeviceWorkload(w, device=f"cuda:{local_rank}")
+    w.drop()
+    q = dw.queries(0)
+    out = torch.empty_like(q)
+    agents = np.arange(w.A, dtype=np.int32)
+    bt = np.ascontiguousarray(dw.block_table, dtype=np.int32)
+    seq = np.ascontiguousarray(w.seq_lens, dtype=np.int32)
+    stream = torch.cuda.current_stream(dev)
+    h = dw.pool.h
+    props = torch.cuda.get_device_properties(dev)
+    flush = torch.empty(int(2 * getattr(props, "L2_cache_size", 128 << 20)), dtype=torch.uint8,
+                        device=dev)
+
+    def step():
+        fk_residual_attention(h, 0, q, agents, bt, seq, False, False, out, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_m = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in ev_m:
+        e.record(stream)     # creates the event; the library re-records it after the main kernel
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches = 0
+    for k in range(K):
+        flush.zero_()                       # L2 flush between steps, outside the events
+        fk_pool_set_profile_event(h, ev_m[k])
+        ev_s[k].record(stream)
+        step()
+        ev_e[k].record(stream)
+        launches += fk_last_launch_count(h)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    fk_pool_set_profile_event(h, None)
+    step_ms = [ev_s[k].elapsed_time(ev_e[k]) for k in range(K)]
+    main_ms = [ev_s[k].elapsed_time(ev_m[k]) for k in range(K)]
+    total_ms = sum(step_ms)
+    # end to end through the public call, host buffers: H2D q, call, D2H out
+    q_host = q.cpu().pin_memory()
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_dev = torch.empty_like(q)
+    KE = max(1, min(K, args.e2e_steps))
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+    for k in range(KE):
+        flush.zero_()
+        e_s[k].record(stream)
+        q_dev.copy_(q_host, non_blocking=True)
+        fk_residual_attention(h, 0, q_dev, agents, bt, seq, False, False, out, stream)
+        out_host.copy_(out, non_blocking=True)
+        e_e[k].record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(e_s[k].elapsed_time(e_e[k]) for k in range(KE))
+    ok = bool(torch.isfinite(out.float()).all().item())
+    dw.check()
+    tot = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = float(tot[0]), float(tot[1])
+    units = w.A * K * world
+    value = units / (total_ms / 1e3)
+    e2e_value = (w.A * KE * world) / (e2e_ms / 1e3)
+    ab = algorithmic_bytes(w)
+    main_avg_s = statistics.mean(main_ms) / 1e3
+    peak, peak_kind = measured_peak_hbm()
+    achieved = ab["kernel"] / main_avg_s / 1e9
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(w),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed between steps (memset of 2x L2), outside the step's events",
+                   "step_hbm_gbs": ab["step"] / (total_ms / K / 1e3) / 1e9,
+                   "step_bytes": ab["step"]},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic_per_launch(),
+                     "kernel": "attention_kernel<128,false>",
+                     "kernel_ms": statistics.mean(main_ms),
+                     "bytes_per_launch": ab["kernel"],
+                     "peak_kind": f"{peak_kind} hbm_gbs"},
+        "e2e": {"value": e2e_value, "unit": UNIT,
+                "h2d_bytes_per_step": int(q.numel() * q.element_size()),
+                "d2h_bytes_per_step": int(out.numel() * out.element_size())},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "outputs_finite": ok,
+    }
+    return res
+
+
+def run_reference(args):
+    import workloads
+    w = workloads.make_workload(WORKLOAD)
+    # size each step so the whole run ends within a few minutes
+    _, _, per_pair_1k = oracle_rate(w, 1e9, n_pairs_max=1, keys=1024)
+    budget = 150.0
+    n = args.steps + args.warmup
+    T = int(w.seq_lens.max())
+    keys = int(max(16, min(T, T * budget / max(1e-9, n * per_pair_1k * T / 1024.0))))
+    keys = (keys // 16) * 16 or 16
+    oracle_rate(w, 1e9, n_pairs_max=args.warmup, keys=keys)
+    rate, done, dt = oracle_rate(w, 1e9, n_pairs_max=args.steps, keys=keys)
+    res = {
+        "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / max(1, done) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": workload_desc(w), "parallelism": "host CPU, 1 thread"},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "kind": "oracle", "cores": 1,
+                         "sample": f"each step: the fp64 oracle on one (agent, kv-head) pair over "
+                                   f"the first {keys} of {T} keys, scaled to full-context "
+                                   f"agent-tokens ({keys}/{T} x 1/{w.H_kv} per step)"},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-child", type=float, default=None)
+    args = ap.parse_args()
+    if args.cpu_baseline_child is not None:
+        cpu_baseline_child(args.cpu_baseline_child)
+        return
+    args.warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        os.environ["OMP_NUM_THREADS"] = os.environ.get("OMP_NUM_THREADS", "1")
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline()          # before the first GPU call, in a fresh process
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+    res = run_gb300(args, rank, world, local_rank)
+    if cpu is not None:
+        res["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -237,6 +237,13 @@ fk_status fk_residual_attention(fk_pool* pool, int layer, const uint16_t* q,
 /* Number of kernel launches the last fk_residual_attention enqueued. */
 int fk_last_launch_count(const fk_pool* pool);
 
+/* Measurement hook: if `event` (a cudaEvent_t, or NULL to clear) is set,
+ * every later fk_residual_attention records it on its stream right after
+ * the main attention kernel and before the split-K combine, so the main
+ * kernel can be timed alone with CUDA events.  The event stays owned by the
+ * caller. */
+fk_status fk_pool_set_profile_event(fk_pool* pool, void* event);
+
 /* Synchronise `stream` and read the pool's device error word: FK_OK, or
  * FK_ERR_DEVICE_CHECK if a kernel's bounds check fired since the last
  * fk_check (the word is then cleared). */

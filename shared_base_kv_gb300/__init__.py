@@ -38,7 +38,7 @@ EXPORTS = (
     "fk_fork", "fk_page_refcount", "fk_agent_register", "fk_agent_release",
     "fk_base_append", "fk_residual_append", "fk_pool_compress",
     "fk_pool_load_compressed", "fk_residual_attention", "fk_last_launch_count",
-    "fk_check", "fk_plan_host",
+    "fk_check", "fk_plan_host", "fk_pool_set_profile_event",
 )
 
 
@@ -103,6 +103,7 @@ def lib() -> ctypes.CDLL:
                                             i32, vp, vp]),
             "fk_last_launch_count": (i32, [vp]),
             "fk_check": (i32, [vp, vp]),
+            "fk_pool_set_profile_event": (i32, [vp, vp]),
             "fk_plan_host": (i32, [i32, i32, i32, i32, i32, P32, i32, P32, P32, i32, i32, i32,
                                    ctypes.POINTER(fk_work_item), i32, P32,
                                    P32, P32, i32, P32, P32, i32, P32, P32, i32, P32]),
@@ -243,6 +244,12 @@ def fk_residual_attention(h, layer: int, q, agents, block_table, seq_lens, causa
 
 def fk_last_launch_count(h) -> int:
     return lib().fk_last_launch_count(h)
+
+
+def fk_pool_set_profile_event(h, event) -> None:
+    """``event``: a torch.cuda.Event (recorded after the main kernel) or None."""
+    ptr = None if event is None else event.cuda_event
+    _check(lib().fk_pool_set_profile_event(h, ptr))
 
 
 def fk_check(h, stream=None) -> None:

@@ -32,6 +32,7 @@ struct HostPlan {
   std::vector<fk_work_item> items;
   std::vector<int32_t> row_agent, row_cg, pages, tile_agents;
   std::vector<int32_t> csr_ptr, csr_slots;
+  std::vector<int32_t> cta_begin;   // items [cta_begin[c], cta_begin[c+1]) run on CTA c
   int n_partials = 0;
 };
 
@@ -69,6 +70,7 @@ struct fk_pool {
   HostPlan plan;
   PlanDev plan_dev{};
   int last_launches = 0;
+  void* profile_event = nullptr;
 };
 
 namespace {
@@ -268,9 +270,16 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
     }
     work.push_back(std::move(sw));
   }
-  int64_t ppi = std::max<int64_t>(1, (total_units + target_items - 1) / std::max(1, target_items));
-  // 4. emit items
+  // 4. emit items.  Segments = (tile, head, page run) in set / tile / head /
+  // run order; their pages, weighted by the per-page work (base + one unit
+  // per agent), are cut into `target_items` contiguous pieces of equal
+  // weight, one per CTA.  A piece that crosses segment boundaries becomes
+  // several items run back to back by the same CTA.
+  (void)total_units;
   HostPlan pl;
+  struct Seg { int tile_row0, tile_ag0, n_rows, n_ag, rank_sum, head, page0, lp0, len; };
+  std::vector<Seg> segs;
+  int64_t total_w = 0;
   for (auto& sw : work) {
     std::vector<int> tile_row0, tile_ag0;
     for (auto& t : sw.tiles) {
@@ -279,33 +288,55 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
       tile_ag0.push_back((int)pl.tile_agents.size());
       for (int32_t a : t.agents) pl.tile_agents.push_back(a);
     }
+    std::vector<int> run_page0;
     for (auto& run : sw.runs) {
-      int64_t len = (int64_t)run.size();
-      int64_t nch = (len + ppi - 1) / ppi;
-      for (int64_t ch = 0; ch < nch; ++ch) {
-        int64_t b = len * ch / nch, e = len * (ch + 1) / nch;
-        int page_begin = (int)pl.pages.size();
-        for (int64_t k = b; k < e; ++k) pl.pages.push_back(run[k].second);
-        for (size_t ti = 0; ti < sw.tiles.size(); ++ti) {
-          for (int h = 0; h < H_kv; ++h) {
-            fk_work_item it{};
-            it.head = h;
-            it.row_begin = tile_row0[ti];
-            it.n_rows = (int)sw.tiles[ti].rows.size();
-            it.page_begin = page_begin;
-            it.n_pages = (int)(e - b);
-            it.lp_begin = run[b].first;
-            it.agent_begin = tile_ag0[ti];
-            it.n_agents = (int)sw.tiles[ti].agents.size();
-            it.partial_begin = pl.n_partials;
-            it.sum_rank = sw.tiles[ti].rank_sum;
-            pl.n_partials += it.n_rows;
-            pl.items.push_back(it);
-          }
+      run_page0.push_back((int)pl.pages.size());
+      for (auto& pr : run) pl.pages.push_back(pr.second);
+    }
+    for (size_t ti = 0; ti < sw.tiles.size(); ++ti)
+      for (int h = 0; h < H_kv; ++h)
+        for (size_t ri = 0; ri < sw.runs.size(); ++ri) {
+          Seg sg{tile_row0[ti], tile_ag0[ti], (int)sw.tiles[ti].rows.size(),
+                 (int)sw.tiles[ti].agents.size(), sw.tiles[ti].rank_sum, h, run_page0[ri],
+                 sw.runs[ri][0].first, (int)sw.runs[ri].size()};
+          segs.push_back(sg);
+          total_w += (int64_t)sg.len * (2 + sg.n_ag);
         }
-      }
+  }
+  int64_t total_pages = 0;
+  for (auto& sg : segs) total_pages += sg.len;
+  const int n_ctas = (int)std::max<int64_t>(1, std::min<int64_t>(target_items, total_pages));
+  pl.cta_begin.assign(n_ctas + 1, 0);
+  size_t si = 0;
+  int off = 0;           // pages of segs[si] already handed out
+  int64_t acc = 0;       // weight handed out so far
+  for (int c = 0; c < n_ctas; ++c) {
+    pl.cta_begin[c] = (int)pl.items.size();
+    const int64_t goal = total_w * (c + 1) / n_ctas;
+    while (si < segs.size() && (acc < goal || c == n_ctas - 1)) {
+      const Seg& sg = segs[si];
+      const int64_t wpp = 2 + sg.n_ag;
+      int64_t want = (c == n_ctas - 1) ? (sg.len - off) : (goal - acc + wpp - 1) / wpp;
+      int take = (int)std::max<int64_t>(1, std::min<int64_t>(want, sg.len - off));
+      fk_work_item it{};
+      it.head = sg.head;
+      it.row_begin = sg.tile_row0;
+      it.n_rows = sg.n_rows;
+      it.page_begin = sg.page0 + off;
+      it.n_pages = take;
+      it.lp_begin = sg.lp0 + off;
+      it.agent_begin = sg.tile_ag0;
+      it.n_agents = sg.n_ag;
+      it.partial_begin = pl.n_partials;
+      it.sum_rank = sg.rank_sum;
+      pl.n_partials += it.n_rows;
+      pl.items.push_back(it);
+      acc += take * wpp;
+      off += take;
+      if (off == sg.len) { ++si; off = 0; }
     }
   }
+  pl.cta_begin[n_ctas] = (int)pl.items.size();
   // 5. combine lists: output row (i, c, hq) -> partial slots
   const int n_out = A * C * H_q;
   std::vector<int32_t> cnt(n_out + 1, 0);
@@ -384,16 +415,19 @@ fk_status fk_pool_create(const fk_pool_config* cfg, void* dev_buf, size_t bytes,
   if (e == cudaSuccess && g.compressed)
     e = cudaMemset(p->g.base + g.off_kq, 0, g.off_kmax + 4LL * g.L - g.off_kq);
   if (e != cudaSuccess) { cudaEventDestroy(p->stage.done); delete p; return cuda_fail(e, "cudaMemset"); }
-  std::vector<float> rope(4 * 64, 0.f);
+  // RoPE table: theta_i as fp32, then theta_i / (2 pi) as a 64-bit binary
+  // fraction so that kernels reduce t * theta_i modulo 2 pi exactly with an
+  // integer multiply.
+  std::vector<uint8_t> rope(64 * 4 + 64 * 8, 0);
   for (int i = 0; i < g.d / 2; ++i) {
-    double th = std::pow((double)g.rope_base, -2.0 * i / g.d);
-    float hi = (float)th;
-    rope[i] = hi;
-    rope[64 + i] = (float)(th - (double)hi);
-    rope[128 + i] = (float)std::cos(kTileTok * th);
-    rope[192 + i] = (float)std::sin(kTileTok * th);
+    long double th = std::pow((long double)g.rope_base, -2.0L * i / g.d);
+    float f = (float)th;
+    std::memcpy(rope.data() + 4 * i, &f, 4);
+    long double frac = th / (2.0L * 3.14159265358979323846264338327950288L);
+    unsigned long long fx = (unsigned long long)std::ldexp(frac, 64);
+    std::memcpy(rope.data() + 256 + 8 * i, &fx, 8);
   }
-  e = cudaMemcpy(p->g.base + g.off_rope, rope.data(), rope.size() * 4, cudaMemcpyHostToDevice);
+  e = cudaMemcpy(p->g.base + g.off_rope, rope.data(), rope.size(), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) { cudaEventDestroy(p->stage.done); delete p; return cuda_fail(e, "cudaMemcpy"); }
   *out = p;
   return FK_OK;
@@ -626,15 +660,15 @@ fk_status fk_pool_compress(fk_pool* p, int layer, void* stream) {
   if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
   if (!p->g.compressed) return fail(FK_ERR_INVALID_ARG, "pool has no compressed copy");
   if (layer < 0 || layer >= p->g.L) return fail(FK_ERR_INVALID_ARG, "layer out of range");
-  std::vector<int32_t> buf;
+  std::vector<int32_t> ids, fills;
   for (int id = 0; id < p->g.num_pages; ++id) {
     int f = p->fill[(size_t)layer * p->g.num_pages + id];
-    if (p->refcount[id] > 0 && f > 0) { buf.push_back(id); }
+    if (p->refcount[id] > 0 && f > 0) { ids.push_back(id); fills.push_back(f); }
   }
-  int n = (int)buf.size();
-  std::vector<int32_t> fills(n);
-  for (int i = 0; i < n; ++i) fills[i] = p->fill[(size_t)layer * p->g.num_pages + buf[i]];
-  buf.insert(buf.end(), fills.begin(), fills.end());
+  const int n = (int)ids.size();
+  std::vector<int32_t> buf(2 * (size_t)n);
+  std::copy(ids.begin(), ids.end(), buf.begin());
+  std::copy(fills.begin(), fills.end(), buf.begin() + n);
   if ((int64_t)buf.size() * 4 > p->g.meta_bytes) return fail(FK_ERR_OOM, "meta region too small");
   cudaStream_t st = (cudaStream_t)stream;
   int32_t* d = (int32_t*)(p->g.base + p->g.off_meta);
@@ -764,6 +798,8 @@ fk_status fk_residual_attention(fk_pool* p, int layer, const uint16_t* q, const 
     pd.off_call_agents = put(ca.data(), ca.size() * sizeof(CallAgent));
     pd.off_csr_ptr = put(pl.csr_ptr.data(), pl.csr_ptr.size() * 4);
     pd.off_csr_slots = put(pl.csr_slots.data(), pl.csr_slots.size() * 4);
+    pd.off_cta = put(pl.cta_begin.data(), pl.cta_begin.size() * 4);
+    pd.n_ctas = (int)pl.cta_begin.size() - 1;
     pd.off_partials = align_up((int64_t)blob.size(), 256);
     int64_t need = pd.off_partials + (int64_t)pd.n_partials * pd.partial_stride * 4;
     if (need > g.ws_bytes) return fail(FK_ERR_OOM, "workspace too small for this call");
@@ -776,13 +812,19 @@ fk_status fk_residual_attention(fk_pool* p, int layer, const uint16_t* q, const 
   }
   int launches = 0;
   int e = launch_attention(g, p->plan_dev, layer, q, out, compressed ? 1 : 0, p->num_sms,
-                           stream, &launches);
+                           stream, &launches, p->profile_event);
   if (e != 0) return cuda_fail((cudaError_t)e, "attention kernels");
   p->last_launches = launches;
   return FK_OK;
 }
 
 int fk_last_launch_count(const fk_pool* p) { return p ? p->last_launches : 0; }
+
+fk_status fk_pool_set_profile_event(fk_pool* p, void* event) {
+  if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
+  p->profile_event = event;
+  return FK_OK;
+}
 
 fk_status fk_check(fk_pool* p, void* stream) {
   if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");

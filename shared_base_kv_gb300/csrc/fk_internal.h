@@ -67,8 +67,9 @@ struct PlanDev {
   int32_t n_out_rows;      // A * C * H_q
   int32_t n_partials;      // partial slots
   int32_t partial_stride;  // floats per partial slot: d + rmax_pad + 4
+  int32_t n_ctas;          // persistent CTAs; CTA c runs items cta[c] .. cta[c+1]-1
   int64_t off_items, off_row_agent, off_row_cg, off_pages, off_tile_agents,
-          off_call_agents, off_csr_ptr, off_csr_slots, off_partials;
+          off_call_agents, off_csr_ptr, off_csr_slots, off_partials, off_cta;
 };
 
 // Host launchers (fk_kernels.cu).  All return a cudaError_t as int.
@@ -88,6 +89,7 @@ int launch_load_compressed(const PoolGeom& g, int layer, const int32_t* d_pages,
                            const float* vnorm, float k_scale, void* stream);
 int launch_attention(const PoolGeom& g, const PlanDev& p, int layer,
                      const uint16_t* q, uint16_t* out, int compressed,
-                     int num_sms, void* stream, int* n_launches);
+                     int num_sms, void* stream, int* n_launches,
+                     void* event_after_main);
 
 }  // namespace fk

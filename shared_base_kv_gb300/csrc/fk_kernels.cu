@@ -276,8 +276,14 @@ namespace attn {
 constexpr int kThreads = 256;
 constexpr int kPRowGroup = 2304;        // P: 16 token-chunks x 144 B
 constexpr int kPChunk = 144;
+constexpr int kA = kMaxAgentsPerTile;
 // TMEM columns
-constexpr uint32_t kTmS = 0, kTmU0 = 64, kTmU1 = 192, kTmOT = 320, kTmOL = 384, kTmL = 448;
+constexpr uint32_t kTmS = 0, kTmU0 = 64, kTmU1 = 192, kTmOT = 320, kTmOL = 384;
+constexpr int kOnesLane = 64;   // lane of OL^T that sums P (row sums)
+// Lv^T stage: per token-chunk 9 r-groups (8 of ranks, 1 of ones).  The M=128
+// MMA reads 16 r-groups; groups 9..15 fall in the next chunk (finite data,
+// lanes 72..127 of OL^T are never used).
+constexpr int kLvChunk = 9 * 128;
 
 template <int D, bool COMP>
 struct Layout {
@@ -286,18 +292,18 @@ struct Layout {
   static constexpr int KB_B = kTilePages * PAGE_B;
   static constexpr int LK_B = kMaxRankSum * kTileTok * 2;
   static constexpr int VB_B = KB_B;
-  static constexpr int LV_B = LK_B;
+  static constexpr int LV_B = 16 * kLvChunk;    // Lv^T of all agents + ones row, per token-chunk
   static constexpr int BK_B = kMaxRankSum * D * 2;
   static constexpr int Q_B = kMaxRows * D * 2;
   static constexpr int QM_B = 4 * 16 * D * 2;
-  static constexpr int ONES_B = 16 * kTileTok * 2;
+  static constexpr int ONES_B = 0;
   static constexpr int KQ_B = COMP ? kTilePages * kPage * D : 0;
   static constexpr int VC_B = COMP ? kTilePages * kPage * (3 * D / 8) : 0;
   static constexpr int VN_B = COMP ? kTilePages * kPage * 4 : 0;
   static constexpr int oP = 0;
   static constexpr int oKB = oP + P_B;              // the OL MMA reads 16 row-groups of P:
   static constexpr int oLK0 = oKB + KB_B;           // the 8 past P_B fall in KB/LK (finite)
-  static constexpr int oLK1 = oLK0 + LK_B;
+  static constexpr int oLK1 = COMP ? oLK0 : oLK0 + LK_B;   // one Lk buffer when compressed
   static constexpr int oVB = oLK1 + LK_B;
   static constexpr int oLV = oVB + VB_B;            // d=64 reads 1 KB past VB: lands in LV
   static constexpr int oBK = oLV + LV_B;
@@ -307,7 +313,9 @@ struct Layout {
   static constexpr int oKQ = oONES + ONES_B;
   static constexpr int oVC = oKQ + KQ_B;
   static constexpr int oVN = oVC + VC_B;
-  static constexpr int oMISC = (oVN + VN_B + 127) / 128 * 128;
+  static constexpr int TAU_B = (D / 2) * 128 * 4;      // per-thread tau rotations, [word][lane]
+  static constexpr int oTAU = (oVN + VN_B + 127) / 128 * 128;
+  static constexpr int oMISC = oTAU + TAU_B;
   static constexpr int MISC_B = 4096;
   static constexpr int TOTAL = oMISC + MISC_B;
 };
@@ -319,6 +327,11 @@ enum {
   B_R_FULL1, B_UFREE0, B_UFREE1, B_S_FULL, B_S_EMPTY, B_P_FULL, B_PV_DONE, B_ACC_EMPTY,
   B_KQ_FULL, B_KQ_EMPTY, B_VC_FULL, B_VC_EMPTY, B_FINAL, B_COUNT
 };
+// barriers a role waits on as "empty" start one phase ahead
+constexpr uint32_t kEmptyMask = (1u << B_KB_EMPTY) | (1u << B_LK_EMPTY0) | (1u << B_LK_EMPTY1) |
+                                (1u << B_VL_EMPTY) | (1u << B_BK_EMPTY) | (1u << B_Q_EMPTY) |
+                                (1u << B_UFREE0) | (1u << B_UFREE1) | (1u << B_S_EMPTY) |
+                                (1u << B_ACC_EMPTY) | (1u << B_KQ_EMPTY) | (1u << B_VC_EMPTY);
 
 struct Misc {
   uint64_t bar[B_COUNT];
@@ -329,17 +342,21 @@ struct Misc {
   float red[4][kMaxRows];
   int32_t row_T[kMaxRows];
   int32_t row_pos[kMaxRows];
-  int32_t row_tagent[kMaxRows];
-  uint32_t rot0[64];       // per tile: f16x2 (cos) pairs then (sin) pairs
+  int32_t row_col[kMaxRows];     // first OL column of the row's agent
+  int32_t row_rp[kMaxRows];      // padded rank of the row's agent
+  uint32_t rot0[64];             // per tile: f16x2 (cos) pairs then (sin) pairs
+  float theta[64];               // RoPE theta_i
+  unsigned long long frac[64];   // theta_i / (2 pi) as a 64-bit binary fraction
 };
 
-// What every role derives from a work item.
+// What every role derives from a work item.  Per-agent arrays are only
+// indexed with compile-time indices (unrolled loops), so they stay in
+// registers.
 struct ItemInfo {
-  int head, n_rows, nrp, n_pages, lp_begin, n_ag, partial_begin, row_begin, n_tiles;
-  int rp[4], ol_col[4], lk_off[4], bk_off[4], qm_off[4], g0[4], ng[4], ra0[4], ra1[4];
-  int call_agent[4], pool_agent[4];
-  float s[4];
-  int64_t rc_off[4];
+  int head, n_rows, nrp, n_pages, lp_begin, n_ag, partial_begin, row_begin, n_tiles, page_begin;
+  int rp[kA], col[kA], g0[kA], ng[kA], ra0[kA], ra1[kA], call_agent[kA], pool_agent[kA], qm[kA];
+  float s[kA];
+  int64_t rc_off[kA];
 };
 
 __device__ __forceinline__ void load_item(const PoolGeom& g, const PlanDev& p, const uint8_t* ws,
@@ -356,10 +373,14 @@ __device__ __forceinline__ void load_item(const PoolGeom& g, const PlanDev& p, c
   I.n_ag = w.n_agents;
   I.partial_begin = w.partial_begin;
   I.row_begin = w.row_begin;
+  I.page_begin = w.page_begin;
   I.n_tiles = (w.n_pages + kTilePages - 1) / kTilePages;
   const int rpa = g.G * p.C;
   int col = 0, qm = 0;
-  for (int a = 0; a < 4; ++a) {
+#pragma unroll
+  for (int a = 0; a < kA; ++a) {
+    I.rp[a] = 0; I.ng[a] = 0; I.g0[a] = 0; I.col[a] = col; I.qm[a] = qm; I.s[a] = 0.f;
+    I.rc_off[a] = 0; I.call_agent[a] = -1; I.pool_agent[a] = 0; I.ra0[a] = 0; I.ra1[a] = 0;
     if (a < I.n_ag) {
       int ci = tile_agents[w.agent_begin + a];
       int pa = ca[ci].pool_agent;
@@ -369,30 +390,13 @@ __device__ __forceinline__ void load_item(const PoolGeom& g, const PlanDev& p, c
       I.rp[a] = dv.rp;
       I.s[a] = dv.s;
       I.rc_off[a] = dv.rc_off;
-      I.ol_col[a] = col;
-      I.lk_off[a] = col * kTileTok * 2;     // Lk/Lv stage blocks: rp x 128 tokens
-      I.bk_off[a] = 0;                      // byte offsets: item_offsets<D>
       col += dv.rp;
       if (I.n_ag == 1) { I.ra0[a] = 0; I.ra1[a] = w.n_rows; }
       else { I.ra0[a] = a * rpa; I.ra1[a] = (a + 1) * rpa; }
       I.g0[a] = I.ra0[a] / 16;
       I.ng[a] = (I.ra1[a] - 1) / 16 - I.g0[a] + 1;
-      I.qm_off[a] = qm;
       qm += I.ng[a];
-    } else {
-      I.rp[a] = 0; I.ng[a] = 0; I.call_agent[a] = 0; I.pool_agent[a] = 0;
     }
-  }
-}
-
-template <int D>
-__device__ __forceinline__ void item_offsets(ItemInfo& I) {
-  int col = 0, qm = 0;
-  for (int a = 0; a < I.n_ag; ++a) {
-    I.bk_off[a] = col * D * 2;
-    I.qm_off[a] = qm * 16 * D * 2;
-    col += I.rp[a];
-    qm += I.ng[a];
   }
 }
 
@@ -407,6 +411,104 @@ __device__ __forceinline__ const uint8_t* rc_lv(const PoolGeom& g, const ItemInf
 
 }  // namespace attn
 
+// Masked online softmax of one tile for NRP (16/32/48/64) padded query
+// rows: scores from TMEM (lane = token), running-max update only when a
+// row's max grows by more than 2^8 (then O, OL and L are rescaled in TMEM),
+// P in bf16 to smem in the K-major layout of the PV / OL / L MMAs.  Rows
+// past n_rows have row_T = 0 and come out as P = 0.
+template <int NRP, int D, bool COMP, typename Wait>
+__device__ __forceinline__ void softmax_tile(uint8_t* smem, attn::Misc& M, uint32_t tmem,
+                                             uint32_t lane_off, int ln, int warp, int lane, int k,
+                                             int t0, int ntok, int n_rows, float scale_log2,
+                                             Wait& wait, uint32_t bar_s_empty) {
+  using namespace attn;
+  using LY = Layout<D, COMP>;
+  enum { B_PV_DONE_ = B_PV_DONE, B_S_FULL_ = B_S_FULL };
+        // ---- masked online softmax over this tile's 128 tokens
+  wait(B_S_FULL_);
+        tc_fence_after();
+        float sv[NRP];
+        {
+          uint32_t raw[NRP];
+#pragma unroll
+          for (int c0 = 0; c0 < NRP; c0 += 16)
+            tmem_ld16(tmem + kTmS + c0 + lane_off, raw + c0);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < NRP; ++e) sv[e] = __uint_as_float(raw[e]);
+        }
+        tc_fence_before();
+        named_bar(1, 128);
+        if (ln == 0) mbar_arrive(bar_s_empty);
+        const int tabs = t0 + ln;
+        bool need = false;
+#pragma unroll
+        for (int j = 0; j < NRP; ++j) {
+          bool ok = ln < ntok && tabs < M.row_T[j] && tabs <= M.row_pos[j];
+          float s = ok ? sv[j] * scale_log2 : -INFINITY;
+          sv[j] = s;
+          need |= s > M.m_used[j] + 8.f;
+        }
+        int any;
+        asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 2, 128, p; selp.u32 %0, 1, 0, q; }"
+                     : "=r"(any) : "r"((int)need));
+        if (k > 0) wait(B_PV_DONE_);
+        if (any) {
+          // column max over the tile, new running max, rescale accumulators
+#pragma unroll
+          for (int j = 0; j < NRP; ++j) {
+            float v = sv[j];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0) M.red[warp - 4][j] = v;
+          }
+          named_bar(1, 128);
+          if (ln < NRP) {
+            float al = 1.f;
+            if (ln < n_rows) {
+              float cm = fmaxf(fmaxf(M.red[0][ln], M.red[1][ln]), fmaxf(M.red[2][ln], M.red[3][ln]));
+              float mo = M.m_used[ln];
+              float mn = fmaxf(mo, cm);
+              if (mn > mo) { al = (mo == -INFINITY) ? 0.f : exp2f(mo - mn); M.m_used[ln] = mn; }
+            }
+            M.alpha[ln] = al;
+          }
+          named_bar(1, 128);
+          if (k > 0) {
+            tc_fence_after();
+            // O^T: lane = d, columns = rows
+            uint32_t raw[16];
+            for (int c0 = 0; c0 < NRP; c0 += 16) {
+              tmem_ld16(tmem + kTmOT + c0 + lane_off, raw);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * M.alpha[c0 + e]);
+              tmem_st16(tmem + kTmOT + c0 + lane_off, raw);
+            }
+            // OL^T: lane = (agent, r) or the ones lane, columns = rows
+            for (int c0 = 0; c0 < NRP; c0 += 16) {
+              tmem_ld16(tmem + kTmOL + c0 + lane_off, raw);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * M.alpha[c0 + e]);
+              tmem_st16(tmem + kTmOL + c0 + lane_off, raw);
+            }
+            tmem_wait_st();
+          }
+        }
+        // ---- P (bf16) -> smem, K-major for the PV / OL / L MMAs
+        {
+          const int tc = ln / 8, tr = ln % 8;
+#pragma unroll
+          for (int j = 0; j < NRP; ++j) {
+            float m = M.m_used[j];
+            float pv = (sv[j] == -INFINITY || m == -INFINITY) ? 0.f : exp2f(sv[j] - m);
+            *(__nv_bfloat16*)(smem + LY::oP + (j / 8) * kPRowGroup + tc * kPChunk + (j % 8) * 16 + tr * 2) =
+                __float2bfloat16_rn(pv);
+          }
+        }
+}
+
 template <int D, bool COMP>
 __global__ void __launch_bounds__(attn::kThreads, 1)
     attention_kernel(PoolGeom g, PlanDev p, int layer, const uint16_t* __restrict__ q) {
@@ -416,16 +518,45 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
   Misc& M = *reinterpret_cast<Misc*>(smem + LY::oMISC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint8_t* ws = g.base + g.off_ws;
+  const int32_t* cta_items = (const int32_t*)(ws + p.off_cta);
   uint32_t* errw = err_word(g);
   volatile int* abort_flag = &M.abort_flag;
   const uint32_t sbase = smem_u32(smem);
   auto bar = [&](int i) { return smem_u32(&M.bar[i]); };
+  // Each role keeps the parity it waits for on barrier i in bit i.
+  uint32_t ph = kEmptyMask;
+  auto wait = [&](int i) {
+    uint32_t par = (ph >> i) & 1u;
+    mbar_wait(bar(i), par, abort_flag, errw);
+    ph ^= 1u << i;
+  };
 
   // ---- set-up: zero smem (junk rows read by padded MMAs stay finite),
-  // ones block, barriers, TMEM.
+  // ones block, RoPE tables, barriers, TMEM.
   for (int i = tid * 16; i < LY::TOTAL; i += kThreads * 16) *(uint4*)(smem + i) = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  for (int i = tid; i < LY::ONES_B / 2; i += kThreads) ((uint16_t*)(smem + LY::oONES))[i] = 0x3F80;
+  // Lv^T stage: r-group 8 (lane 64 of OL^T) row 0 is all ones, so the same
+  // MMA that forms P Lv also forms the row sums of P.
+  for (int i = tid; i < 16 * 8; i += kThreads)
+    ((uint16_t*)(smem + LY::oLV + (i / 8) * kLvChunk + (kOnesLane / 8) * 128))[i % 8] = 0x3F80;
+  if (tid < 64) {
+    M.theta[tid] = ((const float*)(g.base + g.off_rope))[tid];
+    M.frac[tid] = ((const unsigned long long*)(g.base + g.off_rope + 256))[tid];
+  }
+  __syncthreads();
+  if (tid >= 128) {
+    // rotation of each tile offset tau = tid - 128 (f16 pairs), kept in smem
+    // as [word][lane] so that a warp reads 32 consecutive words
+    const int tau = tid - 128;
+    uint32_t* T = (uint32_t*)(smem + LY::oTAU);
+    for (int j = 0; j < D / 4; ++j) {
+      float c0, s0, c1, s1;
+      sincosf((float)tau * M.theta[2 * j], &s0, &c0);
+      sincosf((float)tau * M.theta[2 * j + 1], &s1, &c1);
+      T[j * 128 + tau] = pack_h2(c0, c1);
+      T[(D / 4 + j) * 128 + tau] = pack_h2(s0, s1);
+    }
+  }
   if (tid == 0) {
     for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), (i == B_VL_FULL && COMP) ? 2u : 1u);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -439,66 +570,33 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ================================================== producer ====
-    uint32_t ph_kb_empty = 1, ph_lk_empty[2] = {1, 1}, ph_vl_empty = 1, ph_bk_empty = 1;
-    uint32_t ph_kq_empty = 1, ph_vc_empty = 1;
     int tile_ctr = 0;
-    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+    for (int it = cta_items[blockIdx.x]; it < cta_items[blockIdx.x + 1]; ++it) {
       ItemInfo I;
       load_item(g, p, ws, it, I);
-      item_offsets<D>(I);
-      const int32_t* pages = (const int32_t*)(ws + p.off_pages) + ((const fk_work_item*)(ws + p.off_items))[it].page_begin;
+      const int32_t* pages = (const int32_t*)(ws + p.off_pages) + I.page_begin;
       // B_k^T of the item's agents, for this head
-      mbar_wait(bar(B_BK_EMPTY), ph_bk_empty, abort_flag, errw);
+      wait(B_BK_EMPTY);
       {
         uint32_t bytes = 0;
-        for (int a = 0; a < I.n_ag; ++a) bytes += D * I.rp[a] * 2;
+#pragma unroll
+        for (int a = 0; a < kA; ++a) bytes += D * I.rp[a] * 2;
         mbar_expect_tx(bar(B_BK_FULL), bytes);
-        for (int a = 0; a < I.n_ag; ++a) {
-          const uint8_t* src = g.base + g.off_bk + (int64_t)I.pool_agent[a] * g.bk_agent_bytes +
-                               ((int64_t)layer * g.H_kv + I.head) * (int64_t)D * g.rmax_pad * 2;
-          bulk_g2s(sbase + LY::oBK + I.bk_off[a], src, D * I.rp[a] * 2, bar(B_BK_FULL));
-        }
+#pragma unroll
+        for (int a = 0; a < kA; ++a)
+          if (a < I.n_ag) {
+            const uint8_t* src = g.base + g.off_bk + (int64_t)I.pool_agent[a] * g.bk_agent_bytes +
+                                 ((int64_t)layer * g.H_kv + I.head) * (int64_t)D * g.rmax_pad * 2;
+            bulk_g2s(sbase + LY::oBK + I.col[a] * D * 2, src, D * I.rp[a] * 2, bar(B_BK_FULL));
+          }
       }
-      for (int k = 0; k < I.n_tiles; ++k, ++tile_ctr) {
+      // keys of tile k, then the values of tile k-1 (consumed one tile later)
+      auto load_values = [&](int k) {
         const int p0 = k * kTilePages;
         const int np = min(kTilePages, I.n_pages - p0);
         const int t0 = (I.lp_begin + p0) * kPage;
-        // keys
-        if (!COMP) {
-          mbar_wait(bar(B_KB_EMPTY), ph_kb_empty, abort_flag, errw);
-          mbar_expect_tx(bar(B_KB_FULL), np * LY::PAGE_B);
-          for (int j = 0; j < np; ++j) {
-            int pg = pages[p0 + j];
-            const uint8_t* src = g.base + g.off_kb + (int64_t)layer * g.kb_layer_bytes +
-                                 ((int64_t)pg * g.H_kv + I.head) * LY::PAGE_B;
-            bulk_g2s(sbase + LY::oKB + j * LY::PAGE_B, src, LY::PAGE_B, bar(B_KB_FULL));
-          }
-        } else {
-          mbar_wait(bar(B_KQ_EMPTY), ph_kq_empty, abort_flag, errw);
-          mbar_expect_tx(bar(B_KQ_FULL), np * kPage * D);
-          for (int j = 0; j < np; ++j) {
-            int pg = pages[p0 + j];
-            const uint8_t* src = g.base + g.off_kq +
-                                 ((((int64_t)layer * g.num_pages + pg) * g.H_kv + I.head) * kPage) * D;
-            bulk_g2s(sbase + LY::oKQ + j * kPage * D, src, kPage * D, bar(B_KQ_FULL));
-          }
-        }
-        // residual keys of every agent (128 tokens, clamped to the capacity)
-        {
-          const int b = tile_ctr & 1;
-          mbar_wait(bar(B_LK_EMPTY0 + b), ph_lk_empty[b], abort_flag, errw);
-          const int ntok = min(kTileTok, g.tcap - t0);
-          uint32_t bytes = 0;
-          for (int a = 0; a < I.n_ag; ++a) bytes += ntok * I.rp[a] * 2;
-          mbar_expect_tx(bar(B_LK_FULL0 + b), bytes);
-          for (int a = 0; a < I.n_ag; ++a)
-            bulk_g2s(sbase + (b ? LY::oLK1 : LY::oLK0) + I.lk_off[a],
-                     rc_lk(g, I, a, layer) + (int64_t)t0 * I.rp[a] * 2, ntok * I.rp[a] * 2,
-                     bar(B_LK_FULL0 + b));
-        }
-        // values (consumed at the end of the tile)
         if (COMP) {
-          mbar_wait(bar(B_VC_EMPTY), ph_vc_empty, abort_flag, errw);
+          wait(B_VC_EMPTY);
           mbar_expect_tx(bar(B_VC_FULL), np * kPage * (3 * D / 8 + 4));
           for (int j = 0; j < np; ++j) {
             int pg = pages[p0 + j];
@@ -509,103 +607,147 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
                      bar(B_VC_FULL));
           }
         }
-        mbar_wait(bar(B_VL_EMPTY), ph_vl_empty, abort_flag, errw);
-        {
-          const int ntok = min(kTileTok, g.tcap - t0);
-          uint32_t bytes = COMP ? 0 : np * LY::PAGE_B;
-          for (int a = 0; a < I.n_ag; ++a) bytes += ntok * I.rp[a] * 2;
-          mbar_expect_tx(bar(B_VL_FULL), bytes);
-          if (!COMP)
-            for (int j = 0; j < np; ++j) {
-              int pg = pages[p0 + j];
-              const uint8_t* src = g.base + g.off_vb + (int64_t)layer * g.kb_layer_bytes +
-                                   ((int64_t)pg * g.H_kv + I.head) * LY::PAGE_B;
-              bulk_g2s(sbase + LY::oVB + j * LY::PAGE_B, src, LY::PAGE_B, bar(B_VL_FULL));
-            }
-          for (int a = 0; a < I.n_ag; ++a)
-            bulk_g2s(sbase + LY::oLV + I.lk_off[a], rc_lv(g, I, a, layer) + (int64_t)t0 * I.rp[a] * 2,
-                     ntok * I.rp[a] * 2, bar(B_VL_FULL));
+        wait(B_VL_EMPTY);
+        const int ntok = min(kTileTok, g.tcap - t0);
+        uint32_t bytes = COMP ? 0 : np * LY::PAGE_B;
+#pragma unroll
+        for (int a = 0; a < kA; ++a) bytes += ntok * I.rp[a] * 2;
+        mbar_expect_tx(bar(B_VL_FULL), bytes);
+        if (!COMP)
+          for (int j = 0; j < np; ++j) {
+            int pg = pages[p0 + j];
+            const uint8_t* src = g.base + g.off_vb + (int64_t)layer * g.kb_layer_bytes +
+                                 ((int64_t)pg * g.H_kv + I.head) * LY::PAGE_B;
+            bulk_g2s(sbase + LY::oVB + j * LY::PAGE_B, src, LY::PAGE_B, bar(B_VL_FULL));
+          }
+#pragma unroll
+        for (int a = 0; a < kA; ++a)
+          if (a < I.n_ag) {
+            const uint8_t* src = rc_lv(g, I, a, layer) + (int64_t)t0 * I.rp[a] * 2;
+            const int cb = I.rp[a] * 16;            // one token-chunk of this agent
+            for (int c = 0; c < ntok / 8; ++c)
+              bulk_g2s(sbase + LY::oLV + c * kLvChunk + (I.col[a] / 8) * 128, src + c * cb, cb,
+                       bar(B_VL_FULL));
+          }
+      };
+      for (int k = 0; k < I.n_tiles; ++k, ++tile_ctr) {
+        const int p0 = k * kTilePages;
+        const int np = min(kTilePages, I.n_pages - p0);
+        const int t0 = (I.lp_begin + p0) * kPage;
+        if (!COMP) {
+          wait(B_KB_EMPTY);
+          mbar_expect_tx(bar(B_KB_FULL), np * LY::PAGE_B);
+          for (int j = 0; j < np; ++j) {
+            int pg = pages[p0 + j];
+            const uint8_t* src = g.base + g.off_kb + (int64_t)layer * g.kb_layer_bytes +
+                                 ((int64_t)pg * g.H_kv + I.head) * LY::PAGE_B;
+            bulk_g2s(sbase + LY::oKB + j * LY::PAGE_B, src, LY::PAGE_B, bar(B_KB_FULL));
+          }
+        } else {
+          wait(B_KQ_EMPTY);
+          mbar_expect_tx(bar(B_KQ_FULL), np * kPage * D);
+          for (int j = 0; j < np; ++j) {
+            int pg = pages[p0 + j];
+            const uint8_t* src = g.base + g.off_kq +
+                                 ((((int64_t)layer * g.num_pages + pg) * g.H_kv + I.head) * kPage) * D;
+            bulk_g2s(sbase + LY::oKQ + j * kPage * D, src, kPage * D, bar(B_KQ_FULL));
+          }
         }
+        {
+          const int b = COMP ? 0 : (tile_ctr & 1);
+          wait(B_LK_EMPTY0 + b);
+          const int ntok = min(kTileTok, g.tcap - t0);
+          uint32_t bytes = 0;
+#pragma unroll
+          for (int a = 0; a < kA; ++a) bytes += ntok * I.rp[a] * 2;
+          mbar_expect_tx(bar(B_LK_FULL0 + b), bytes);
+#pragma unroll
+          for (int a = 0; a < kA; ++a)
+            if (a < I.n_ag)
+              bulk_g2s(sbase + (b ? LY::oLK1 : LY::oLK0) + I.col[a] * kTileTok * 2,
+                       rc_lk(g, I, a, layer) + (int64_t)t0 * I.rp[a] * 2, ntok * I.rp[a] * 2,
+                       bar(B_LK_FULL0 + b));
+        }
+        if (k > 0) load_values(k - 1);
       }
+      load_values(I.n_tiles - 1);
     }
   } else if (warp == 1 && lane == 0) {
     // ===================================================== MMA issuer ====
-    uint32_t ph_kb_full = 0, ph_lk_full[2] = {0, 0}, ph_vl_full = 0, ph_bk_full = 0, ph_q_full = 0;
-    uint32_t ph_r_full[2] = {0, 0}, ph_ufree[2] = {1, 1}, ph_s_empty = 1, ph_p_full = 0;
-    uint32_t ph_acc_empty = 1;
     int tile_ctr = 0;
-    const uint32_t t_S = tmem + kTmS, t_OT = tmem + kTmOT, t_OL = tmem + kTmOL, t_L = tmem + kTmL;
-    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+    const uint32_t t_S = tmem + kTmS, t_OT = tmem + kTmOT, t_OL = tmem + kTmOL;
+    for (int it = cta_items[blockIdx.x]; it < cta_items[blockIdx.x + 1]; ++it) {
       ItemInfo I;
       load_item(g, p, ws, it, I);
-      item_offsets<D>(I);
-      mbar_wait(bar(B_BK_FULL), ph_bk_full, abort_flag, errw);
-      mbar_wait(bar(B_Q_FULL), ph_q_full, abort_flag, errw);
+      wait(B_BK_FULL);
+      wait(B_Q_FULL);
       tc_fence_after();
       const uint32_t id_S = idesc_f16(128, I.nrp, 1);
       const uint32_t id_U = idesc_f16(128, D, 1);
       const uint32_t id_PV = idesc_f16(128, I.nrp, 1);
-      const uint32_t id_L = idesc_f16(128, 16, 1);
-      auto residual = [&](int a) {
+      auto residual = [&](int a) {   // a: compile-time after unrolling
         const int b = a & 1;
-        mbar_wait(bar(B_R_FULL0 + b), ph_r_full[b], abort_flag, errw);
+        wait(B_R_FULL0 + b);
         tc_fence_after();
         const uint32_t id_R = idesc_f16(128, 16 * I.ng[a], 0);
         const uint32_t t_R = tmem + (b ? kTmU1 : kTmU0);
+#pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           mma_ts(t_S + 16 * I.g0[a], t_R + 8 * ks,
-                 sdesc(sbase + LY::oQM + I.qm_off[a] + ks * 128, (D / 16) * 128, (D / 8) * 128),
+                 sdesc(sbase + LY::oQM + I.qm[a] * 16 * D * 2 + ks * 128, (D / 16) * 128, (D / 8) * 128),
                  id_R, 1);
         mma_commit(bar(B_UFREE0 + b));
       };
       auto pv = [&](int j) {
-        mbar_wait(bar(B_P_FULL), ph_p_full, abort_flag, errw);
-        mbar_wait(bar(B_VL_FULL), ph_vl_full, abort_flag, errw);
-        if (j == 0) mbar_wait(bar(B_ACC_EMPTY), ph_acc_empty, abort_flag, errw);
+        wait(B_P_FULL);
+        wait(B_VL_FULL);
+        if (j == 0) wait(B_ACC_EMPTY);
         tc_fence_after();
+#pragma unroll 1
         for (int ks = 0; ks < kTileTok / 16; ++ks) {
           const uint32_t acc = (j == 0 && ks == 0) ? 0u : 1u;
           const uint64_t dP = sdesc(sbase + LY::oP + ks * 2 * kPChunk, kPChunk, kPRowGroup);
           mma_ss(t_OT, sdesc(sbase + LY::oVB + ks * LY::PAGE_B, (D / 8) * 128, 128), dP, id_PV, acc);
-          for (int a = 0; a < I.n_ag; ++a) {
-            const int rc = I.rp[a] / 8;
-            mma_ss(t_OL + I.ol_col[a], dP,
-                   sdesc(sbase + LY::oLV + I.lk_off[a] + ks * 2 * rc * 128, rc * 128, 128),
-                   idesc_f16(128, I.rp[a], 1), acc);
-          }
-          mma_ss(t_L, dP, sdesc(sbase + LY::oONES + ks * 256, 128, 2048), id_L, acc);
+          mma_ss(t_OL, sdesc(sbase + LY::oLV + ks * 2 * kLvChunk, kLvChunk, 128), dP, id_PV, acc);
         }
         mma_commit(bar(B_VL_EMPTY));
         mma_commit(bar(B_PV_DONE));
       };
       for (int k = 0; k < I.n_tiles; ++k, ++tile_ctr) {
         // S = Kb Q^T
-        mbar_wait(bar(B_S_EMPTY), ph_s_empty, abort_flag, errw);
-        mbar_wait(bar(B_KB_FULL), ph_kb_full, abort_flag, errw);
+        wait(B_S_EMPTY);
+        wait(B_KB_FULL);
         tc_fence_after();
+#pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           mma_ss(t_S, sdesc(sbase + LY::oKB + ks * 256, 128, (D / 8) * 128),
                  sdesc(sbase + LY::oQ + ks * 256, 128, (D / 8) * 128), id_S, ks > 0 ? 1u : 0u);
         mma_commit(bar(B_KB_EMPTY));
         // per agent: U_a = Lk_a Bk_a^T, then (one agent behind) S += R Qm^T
-        const int lb = tile_ctr & 1;
-        mbar_wait(bar(B_LK_FULL0 + lb), ph_lk_full[lb], abort_flag, errw);
+        const int lb = COMP ? 0 : (tile_ctr & 1);
+        wait(B_LK_FULL0 + lb);
         tc_fence_after();
-        for (int a = 0; a < I.n_ag; ++a) {
-          const int b = a & 1;
-          mbar_wait(bar(B_UFREE0 + b), ph_ufree[b], abort_flag, errw);
-          tc_fence_after();
-          const int rc = I.rp[a] / 8;
-          const uint32_t t_U = tmem + (b ? kTmU1 : kTmU0);
-          for (int ks = 0; ks < I.rp[a] / 16; ++ks)
-            mma_ss(t_U, sdesc(sbase + (lb ? LY::oLK1 : LY::oLK0) + I.lk_off[a] + ks * 256, 128, rc * 128),
-                   sdesc(sbase + LY::oBK + I.bk_off[a] + ks * 256, 128, rc * 128), id_U,
-                   ks > 0 ? 1u : 0u);
-          mma_commit(bar(B_U_FULL0 + b));
-          if (a > 0) residual(a - 1);
+        const uint32_t lk_base = sbase + (lb ? LY::oLK1 : LY::oLK0);
+#pragma unroll
+        for (int a = 0; a < kA; ++a) {
+          if (a < I.n_ag) {
+            const int b = a & 1;
+            wait(B_UFREE0 + b);
+            tc_fence_after();
+            const int rc = I.rp[a] / 8;
+            const uint32_t t_U = tmem + (b ? kTmU1 : kTmU0);
+            for (int ks = 0; ks < I.rp[a] / 16; ++ks)
+              mma_ss(t_U, sdesc(lk_base + I.col[a] * kTileTok * 2 + ks * 256, 128, rc * 128),
+                     sdesc(sbase + LY::oBK + I.col[a] * D * 2 + ks * 256, 128, rc * 128), id_U,
+                     ks > 0 ? 1u : 0u);
+            mma_commit(bar(B_U_FULL0 + b));
+            if (a > 0) residual(a - 1);
+          }
         }
         mma_commit(bar(B_LK_EMPTY0 + lb));
-        residual(I.n_ag - 1);
+#pragma unroll
+        for (int a = 0; a < kA; ++a)
+          if (a == I.n_ag - 1) residual(a);
         mma_commit(bar(B_S_FULL));
         if (k > 0) pv(k - 1);
       }
@@ -614,26 +756,25 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
       mma_commit(bar(B_BK_EMPTY));
     }
     // every MMA this CTA issued has completed before TMEM is released
-    uint32_t ph_final = 0;
     mma_commit(bar(B_FINAL));
-    mbar_wait(bar(B_FINAL), ph_final, abort_flag, errw);
+    wait(B_FINAL);
   } else if (COMP && (warp == 2 || warp == 3)) {
     // ================================== dequantiser (compressed pool) ====
     const int ct = tid - 64;   // 0..63
-    uint32_t ph_kq_full = 0, ph_kb_empty = 1, ph_vc_full = 0, ph_vl_empty = 1;
     const float kscale = ((const float*)(g.base + g.off_ks))[layer];
-    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+    for (int it = cta_items[blockIdx.x]; it < cta_items[blockIdx.x + 1]; ++it) {
       ItemInfo I;
       load_item(g, p, ws, it, I);
       for (int k = 0; k < I.n_tiles; ++k) {
         const int np = min(kTilePages, I.n_pages - k * kTilePages);
         // keys: int8 [page][16][D] -> bf16 (value * scale) in the key layout
-        mbar_wait(bar(B_KQ_FULL), ph_kq_full, abort_flag, errw);
-        mbar_wait(bar(B_KB_EMPTY), ph_kb_empty, abort_flag, errw);
+        wait(B_KQ_FULL);
+        wait(B_KB_EMPTY);
         for (int u = ct; u < np * kPage * (D / 8); u += 64) {
           int ch = u % (D / 8), row = (u / (D / 8)) % kPage, pj = u / (kPage * (D / 8));
           const int8_t* src = (const int8_t*)(smem + LY::oKQ) + (pj * kPage + row) * D + ch * 8;
           uint32_t w[4];
+#pragma unroll
           for (int e = 0; e < 4; ++e)
             w[e] = pack_bf2((float)src[2 * e] * kscale, (float)src[2 * e + 1] * kscale);
           *(uint4*)(smem + LY::oKB + pj * LY::PAGE_B + ((row / 8) * (D / 8) + ch) * 128 + (row % 8) * 16) =
@@ -643,12 +784,13 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
         named_bar(3, 64);
         if (ct == 0) { mbar_arrive(bar(B_KB_FULL)); mbar_arrive(bar(B_KQ_EMPTY)); }
         // values: codes -> level * n / D in the value layout (rotated domain)
-        mbar_wait(bar(B_VC_FULL), ph_vc_full, abort_flag, errw);
-        mbar_wait(bar(B_VL_EMPTY), ph_vl_empty, abort_flag, errw);
+        wait(B_VC_FULL);
+        wait(B_VL_EMPTY);
         for (int u = ct; u < np * 2 * (D / 8); u += 64) {
           int dg = u % (D / 8), tc = (u / (D / 8)) % 2, pj = u / (2 * (D / 8));
           float w8[8];
           uint32_t c8[8];
+#pragma unroll
           for (int tt = 0; tt < 8; ++tt) {
             int row = tc * 8 + tt;
             const uint8_t* cb = smem + LY::oVC + (pj * kPage + row) * (3 * D / 8);
@@ -657,10 +799,13 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
             w8[tt] = ((const float*)(smem + LY::oVN))[pj * kPage + row] * (1.0f / D);
           }
           uint8_t* dst = smem + LY::oVB + pj * LY::PAGE_B + (tc * (D / 8) + dg) * 128;
+#pragma unroll
           for (int e = 0; e < 8; ++e) {   // d = 8 dg + e
             uint32_t w[4];
+#pragma unroll
             for (int h2 = 0; h2 < 4; ++h2) {
               float v2[2];
+#pragma unroll
               for (int z = 0; z < 2; ++z) {
                 uint32_t cc = c8[2 * h2 + z];
                 uint32_t code = ((cc >> e) & 1u) | (((cc >> (8 + e)) & 1u) << 1) | (((cc >> (16 + e)) & 1u) << 2);
@@ -680,45 +825,39 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
     // ================================================= compute WG ====
     const int ln = tid - 128;                          // TMEM lane = token / d / row
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-    uint32_t ph_u_full[2] = {0, 0}, ph_s_full = 0, ph_pv_done = 0, ph_q_empty = 1;
-    const float* rope_tab = (const float*)(g.base + g.off_rope);
-    // per-thread rotation by its offset tau = ln inside a tile (f16 pairs)
-    uint32_t ctau[D / 4], stau[D / 4];
-    for (int j = 0; j < D / 4; ++j) {
-      float c0, s0, c1, s1;
-      sincosf((float)ln * rope_tab[2 * j], &s0, &c0);
-      sincosf((float)ln * rope_tab[2 * j + 1], &s1, &c1);
-      ctau[j] = pack_h2(c0, c1);
-      stau[j] = pack_h2(s0, s1);
-    }
+    const uint32_t* TAU = (const uint32_t*)(smem + LY::oTAU);
     const float scale_log2 = 1.4426950408889634f * rsqrtf((float)D);
-    int tile_ctr = 0;
-    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x) {
+    for (int it = cta_items[blockIdx.x]; it < cta_items[blockIdx.x + 1]; ++it) {
       ItemInfo I;
       load_item(g, p, ws, it, I);
-      item_offsets<D>(I);
+      const int n_rows = I.n_rows, nrp = I.nrp, n_ag = I.n_ag;
       const int32_t* row_agent = (const int32_t*)(ws + p.off_row_agent) + I.row_begin;
       const int32_t* row_cg = (const int32_t*)(ws + p.off_row_cg) + I.row_begin;
       const CallAgent* ca = (const CallAgent*)(ws + p.off_call_agents);
       // ---- stage Q (bf16) and per-agent s_a * Q (f16, other agents' rows 0)
-      mbar_wait(bar(B_Q_EMPTY), ph_q_empty, abort_flag, errw);
+      wait(B_Q_EMPTY);
       if (ln < kMaxRows) {
         M.m_used[ln] = -INFINITY;
-        if (ln < I.n_rows) {
+        M.row_T[ln] = 0;
+        M.row_pos[ln] = -1;
+        if (ln < n_rows) {
           int ci = row_agent[ln];
           int T = ca[ci].seq_len;
           int c = row_cg[ln] / g.G;
           M.row_T[ln] = T;
           M.row_pos[ln] = p.causal ? (T - p.C + c) : 0x7fffffff;
-          int ta = 0;
-          for (int a = 0; a < I.n_ag; ++a) if (I.call_agent[a] == ci) ta = a;
-          M.row_tagent[ln] = ta;
+          int col = 0, rp = 0;
+#pragma unroll
+          for (int a = 0; a < kA; ++a)
+            if (I.call_agent[a] == ci) { col = I.col[a]; rp = I.rp[a]; }
+          M.row_col[ln] = col;
+          M.row_rp[ln] = rp;
         }
       }
-      for (int u = ln; u < I.nrp * (D / 8); u += 128) {
+      for (int u = ln; u < nrp * (D / 8); u += 128) {
         int row = u / (D / 8), ch = u % (D / 8);
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < I.n_rows) {
+        if (row < n_rows) {
           int ci = row_agent[row], cg = row_cg[row];
           int c = cg / g.G, gg = cg % g.G;
           int64_t qrow = ((int64_t)ci * p.C + c) * g.H_q + I.head * g.G + gg;
@@ -726,167 +865,98 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
         }
         *(uint4*)(smem + LY::oQ + ((row / 8) * (D / 8) + ch) * 128 + (row % 8) * 16) = v;
       }
-      for (int a = 0; a < I.n_ag; ++a) {
-        for (int u = ln; u < I.ng[a] * 16 * (D / 8); u += 128) {
-          int lr = u / (D / 8), ch = u % (D / 8);
-          int row = I.g0[a] * 16 + lr;
-          uint32_t w[4] = {0, 0, 0, 0};
-          if (row >= I.ra0[a] && row < I.ra1[a] && row < I.n_rows) {
-            int ci = row_agent[row], cg = row_cg[row];
-            int c = cg / g.G, gg = cg % g.G;
-            int64_t qrow = ((int64_t)ci * p.C + c) * g.H_q + I.head * g.G + gg;
-            const __nv_bfloat16* src = (const __nv_bfloat16*)(q + qrow * D + ch * 8);
-            for (int e = 0; e < 4; ++e)
-              w[e] = pack_h2(__bfloat162float(src[2 * e]) * I.s[a], __bfloat162float(src[2 * e + 1]) * I.s[a]);
+#pragma unroll
+      for (int a = 0; a < kA; ++a) {
+        if (a < n_ag) {
+          for (int u = ln; u < I.ng[a] * 16 * (D / 8); u += 128) {
+            int lr = u / (D / 8), ch = u % (D / 8);
+            int row = I.g0[a] * 16 + lr;
+            uint32_t w[4] = {0, 0, 0, 0};
+            if (row >= I.ra0[a] && row < I.ra1[a] && row < n_rows) {
+              int ci = row_agent[row], cg = row_cg[row];
+              int c = cg / g.G, gg = cg % g.G;
+              int64_t qrow = ((int64_t)ci * p.C + c) * g.H_q + I.head * g.G + gg;
+              const __nv_bfloat16* src = (const __nv_bfloat16*)(q + qrow * D + ch * 8);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = pack_h2(__bfloat162float(src[2 * e]) * I.s[a], __bfloat162float(src[2 * e + 1]) * I.s[a]);
+            }
+            *(uint4*)(smem + LY::oQM + I.qm[a] * 16 * D * 2 + ((lr / 8) * (D / 8) + ch) * 128 + (lr % 8) * 16) =
+                make_uint4(w[0], w[1], w[2], w[3]);
           }
-          *(uint4*)(smem + LY::oQM + I.qm_off[a] + ((lr / 8) * (D / 8) + ch) * 128 + (lr % 8) * 16) =
-              make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       fence_proxy_async();
       named_bar(1, 128);
       if (ln == 0) mbar_arrive(bar(B_Q_FULL));
 
-      for (int k = 0; k < I.n_tiles; ++k, ++tile_ctr) {
+      for (int k = 0; k < I.n_tiles; ++k) {
         const int t0 = (I.lp_begin + k * kTilePages) * kPage;
         const int ntok = min(kTileTok, (I.n_pages - k * kTilePages) * kPage);
-        // ---- rotation of the tile start, exact (fp64 angle, reduced)
+        // ---- rotation of the tile start: t0 * theta_i / (2 pi) reduced
+        // exactly as a 64-bit binary fraction, then an accurate sincos
         if (ln < D / 4) {
           float cc[2], ssn[2];
+#pragma unroll
           for (int z = 0; z < 2; ++z) {
-            int i = 2 * ln + z;
-            double th = (double)rope_tab[i] + (double)rope_tab[64 + i];
-            double ang = (double)t0 * th;
-            double red = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
-            sincosf((float)red, &ssn[z], &cc[z]);
+            unsigned long long fr = (unsigned long long)t0 * M.frac[2 * ln + z];
+            float ang = (float)(unsigned int)(fr >> 32) * 1.4629180792671596e-09f;  // 2 pi / 2^32
+            if (ang > 3.14159265f) ang -= 6.28318531f;
+            sincosf(ang, &ssn[z], &cc[z]);
           }
           M.rot0[ln] = pack_h2(cc[0], cc[1]);
           M.rot0[32 + ln] = pack_h2(ssn[0], ssn[1]);
         }
         named_bar(1, 128);
         uint32_t Cp[D / 4], Sp[D / 4];
+#pragma unroll
         for (int j = 0; j < D / 4; ++j) {
           __half2 c0 = as_h2(M.rot0[j]), s0 = as_h2(M.rot0[32 + j]);
-          __half2 ct = as_h2(ctau[j]), st = as_h2(stau[j]);
+          __half2 ct = as_h2(TAU[j * 128 + ln]), st = as_h2(TAU[(D / 4 + j) * 128 + ln]);
           Cp[j] = as_u32(__hfma2(c0, ct, __hneg2(__hmul2(s0, st))));
           Sp[j] = as_u32(__hfma2(s0, ct, __hmul2(c0, st)));
         }
         // ---- RoPE of each agent's residual keys, written back as f16 pairs
-        for (int a = 0; a < I.n_ag; ++a) {
+        for (int a = 0; a < n_ag; ++a) {
           const int b = a & 1;
           const uint32_t t_U = tmem + (b ? kTmU1 : kTmU0) + lane_off;
-          mbar_wait(bar(B_U_FULL0 + b), ph_u_full[b], abort_flag, errw);
+          wait(B_U_FULL0 + b);
           tc_fence_after();
 #pragma unroll
-          for (int ci = 0; ci < D / 16; ++ci) {
-            uint32_t lo[8], hi[8], r8[8];
-            tmem_ld8(t_U + 8 * ci, lo);
-            tmem_ld8(t_U + D / 2 + 8 * ci, hi);
+          for (int cb = 0; cb < D / 16; cb += 4) {
+            uint32_t lo[4][8], hi[4][8];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              tmem_ld8(t_U + 8 * (cb + c), lo[c]);
+              tmem_ld8(t_U + D / 2 + 8 * (cb + c), hi[c]);
+            }
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              __half2 xl = __floats2half2_rn(__uint_as_float(lo[2 * j]), __uint_as_float(lo[2 * j + 1]));
-              __half2 xh = __floats2half2_rn(__uint_as_float(hi[2 * j]), __uint_as_float(hi[2 * j + 1]));
-              __half2 C = as_h2(Cp[4 * ci + j]), S = as_h2(Sp[4 * ci + j]);
-              r8[j] = as_u32(__hfma2(xl, C, __hneg2(__hmul2(xh, S))));
-              r8[4 + j] = as_u32(__hfma2(xh, C, __hmul2(xl, S)));
+            for (int c = 0; c < 4; ++c) {
+              const int ci = cb + c;
+              uint32_t r8[8];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                __half2 xl = __floats2half2_rn(__uint_as_float(lo[c][2 * j]), __uint_as_float(lo[c][2 * j + 1]));
+                __half2 xh = __floats2half2_rn(__uint_as_float(hi[c][2 * j]), __uint_as_float(hi[c][2 * j + 1]));
+                __half2 C = as_h2(Cp[4 * ci + j]), S = as_h2(Sp[4 * ci + j]);
+                r8[j] = as_u32(__hfma2(xl, C, __hneg2(__hmul2(xh, S))));
+                r8[4 + j] = as_u32(__hfma2(xh, C, __hmul2(xl, S)));
+              }
+              tmem_st8(t_U + 8 * ci, r8);
             }
-            tmem_st8(t_U + 8 * ci, r8);
           }
           tmem_wait_st();
           tc_fence_before();
           named_bar(1, 128);
           if (ln == 0) mbar_arrive(bar(B_R_FULL0 + b));
         }
-        // ---- masked online softmax over this tile's 128 tokens
-        mbar_wait(bar(B_S_FULL), ph_s_full, abort_flag, errw);
-        tc_fence_after();
-        float sv[kMaxRows];
-        {
-          uint32_t raw[16];
-#pragma unroll
-          for (int c0 = 0; c0 < kMaxRows; c0 += 16) {
-            if (c0 < I.nrp) {
-              tmem_ld16(tmem + kTmS + c0 + lane_off, raw);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 16; ++e) sv[c0 + e] = __uint_as_float(raw[e]);
-            }
-          }
-        }
-        tc_fence_before();
-        named_bar(1, 128);
-        if (ln == 0) mbar_arrive(bar(B_S_EMPTY));
-        const int tabs = t0 + ln;
-        bool need = false;
-#pragma unroll
-        for (int j = 0; j < kMaxRows; ++j) {
-          if (j < I.n_rows) {
-            bool ok = ln < ntok && tabs < M.row_T[j] && tabs <= M.row_pos[j];
-            float s = ok ? sv[j] * scale_log2 : -INFINITY;
-            sv[j] = s;
-            need |= s > M.m_used[j] + 8.f;
-          }
-        }
-        int any;
-        asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 2, 128, p; selp.u32 %0, 1, 0, q; }"
-                     : "=r"(any) : "r"((int)need));
-        if (k > 0) mbar_wait(bar(B_PV_DONE), ph_pv_done, abort_flag, errw);
-        if (any) {
-          // column max over the tile, new running max, rescale accumulators
-#pragma unroll
-          for (int j = 0; j < kMaxRows; ++j) {
-            if (j < I.n_rows) {
-              float v = sv[j];
-              for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-              if (lane == 0) M.red[warp - 4][j] = v;
-            }
-          }
-          named_bar(1, 128);
-          if (ln < kMaxRows) {
-            float al = 1.f;
-            if (ln < I.n_rows) {
-              float cm = fmaxf(fmaxf(M.red[0][ln], M.red[1][ln]), fmaxf(M.red[2][ln], M.red[3][ln]));
-              float mo = M.m_used[ln];
-              float mn = fmaxf(mo, cm);
-              if (mn > mo) { al = (mo == -INFINITY) ? 0.f : exp2f(mo - mn); M.m_used[ln] = mn; }
-            }
-            M.alpha[ln] = al;
-          }
-          named_bar(1, 128);
-          if (k > 0) {
-            tc_fence_after();
-            // O^T: lane = d, columns = rows
-            uint32_t raw[16];
-            for (int c0 = 0; c0 < I.nrp; c0 += 16) {
-              tmem_ld16(tmem + kTmOT + c0 + lane_off, raw);
-              tmem_wait_ld();
-              for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * M.alpha[c0 + e]);
-              tmem_st16(tmem + kTmOT + c0 + lane_off, raw);
-            }
-            // OL and L: lane = row
-            const float al = ln < kMaxRows ? M.alpha[ln] : 1.f;
-            for (int c0 = 0; c0 < 80; c0 += 16) {
-              tmem_ld16(tmem + kTmOL + c0 + lane_off, raw);
-              tmem_wait_ld();
-              for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * al);
-              tmem_st16(tmem + kTmOL + c0 + lane_off, raw);
-            }
-            tmem_wait_st();
-          }
-        }
-        // ---- P (bf16) -> smem, K-major for the PV / OL / L MMAs
-        {
-          const int tc = ln / 8, tr = ln % 8;
-#pragma unroll
-          for (int j = 0; j < kMaxRows; ++j) {
-            if (j < I.n_rows) {
-              float m = M.m_used[j];
-              float pv = (sv[j] == -INFINITY || m == -INFINITY) ? 0.f : exp2f(sv[j] - m);
-              *(__nv_bfloat16*)(smem + LY::oP + (j / 8) * kPRowGroup + tc * kPChunk + (j % 8) * 16 + tr * 2) =
-                  __float2bfloat16_rn(pv);
-            }
-          }
+        // ---- masked online softmax over this tile's 128 tokens, P -> smem
+        switch (nrp) {
+          case 16: softmax_tile<16, D, COMP>(smem, M, tmem, lane_off, ln, warp, lane, k, t0, ntok, n_rows, scale_log2, wait, bar(B_S_EMPTY)); break;
+          case 32: softmax_tile<32, D, COMP>(smem, M, tmem, lane_off, ln, warp, lane, k, t0, ntok, n_rows, scale_log2, wait, bar(B_S_EMPTY)); break;
+          case 48: softmax_tile<48, D, COMP>(smem, M, tmem, lane_off, ln, warp, lane, k, t0, ntok, n_rows, scale_log2, wait, bar(B_S_EMPTY)); break;
+          default: softmax_tile<64, D, COMP>(smem, M, tmem, lane_off, ln, warp, lane, k, t0, ntok, n_rows, scale_log2, wait, bar(B_S_EMPTY)); break;
         }
         fence_proxy_async();
         tc_fence_before();
@@ -894,35 +964,45 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
         if (ln == 0) mbar_arrive(bar(B_P_FULL));
       }
       // ---- epilogue: write this item's split partials
-      mbar_wait(bar(B_PV_DONE), ph_pv_done, abort_flag, errw);
+      wait(B_PV_DONE);
       tc_fence_after();
       float* part = (float*)(ws + p.off_partials);
       const int PS = p.partial_stride;
       {
         uint32_t raw[16];
-        for (int c0 = 0; c0 < I.nrp; c0 += 16) {
+        for (int c0 = 0; c0 < nrp; c0 += 16) {
           tmem_ld16(tmem + kTmOT + c0 + lane_off, raw);
           tmem_wait_ld();
-          if (ln < D)
+          if (ln < D) {
+#pragma unroll
             for (int e = 0; e < 16; ++e)
-              if (c0 + e < I.n_rows) part[(int64_t)(I.partial_begin + c0 + e) * PS + 4 + ln] = __uint_as_float(raw[e]);
+              if (c0 + e < n_rows) part[(int64_t)(I.partial_begin + c0 + e) * PS + 4 + ln] = __uint_as_float(raw[e]);
+          }
         }
-        uint32_t ol[80];
-        for (int c0 = 0; c0 < 80; c0 += 16) {
+        // OL^T lane ln: residual column r = ln - col of the agent whose
+        // columns hold ln (rows of that agent take it), or the row sums.
+        int oa = -1, orr = 0;
+#pragma unroll
+        for (int a = 0; a < kA; ++a)
+          if (a < n_ag && ln >= I.col[a] && ln < I.col[a] + I.rp[a]) { oa = a; orr = ln - I.col[a]; }
+        int ra0 = 0, ra1 = 0;
+#pragma unroll
+        for (int a = 0; a < kA; ++a)
+          if (a == oa) { ra0 = I.ra0[a]; ra1 = I.ra1[a]; }
+        for (int c0 = 0; c0 < nrp; c0 += 16) {
           tmem_ld16(tmem + kTmOL + c0 + lane_off, raw);
           tmem_wait_ld();
-          for (int e = 0; e < 16; ++e) ol[c0 + e] = raw[e];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int j = c0 + e;
+            if (j < n_rows) {
+              float* dst = part + (int64_t)(I.partial_begin + j) * PS;
+              if (ln == kOnesLane) dst[1] = __uint_as_float(raw[e]);
+              if (oa >= 0 && j >= ra0 && j < ra1) dst[4 + D + orr] = __uint_as_float(raw[e]);
+            }
+          }
         }
-        if (ln < I.n_rows) {
-          float* dst = part + (int64_t)(I.partial_begin + ln) * PS;
-          const int ta = M.row_tagent[ln];
-          dst[0] = M.m_used[ln];
-          dst[1] = __uint_as_float(ol[kTmL - kTmOL]);
-          int col0 = 0;
-          for (int a = 0; a < I.n_ag; ++a) if (a < ta) col0 += I.rp[a];
-          for (int kk = 0; kk < 64; ++kk)
-            if (kk < I.rp[ta]) dst[4 + D + kk] = __uint_as_float(ol[col0 + kk]);
-        }
+        if (ln < n_rows) part[(int64_t)(I.partial_begin + ln) * PS] = M.m_used[ln];
       }
       tc_fence_before();
       named_bar(1, 128);
@@ -1071,7 +1151,7 @@ int launch_load_compressed(const PoolGeom& g, int layer, const int32_t* d_pages,
 
 template <int D, bool COMP>
 static int launch_attn_t(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q,
-                         uint16_t* out, int num_sms, cudaStream_t st) {
+                         uint16_t* out, int num_sms, cudaStream_t st, cudaEvent_t ev) {
   using LY = attn::Layout<D, COMP>;
   static bool attr_done = false;
   if (!attr_done) {
@@ -1080,24 +1160,29 @@ static int launch_attn_t(const PoolGeom& g, const PlanDev& p, int layer, const u
     if (e != cudaSuccess) return (int)e;
     attr_done = true;
   }
-  int grid = p.n_items < num_sms ? p.n_items : num_sms;
-  attention_kernel<D, COMP><<<grid, attn::kThreads, LY::TOTAL, st>>>(g, p, layer, q);
+  attention_kernel<D, COMP><<<p.n_ctas, attn::kThreads, LY::TOTAL, st>>>(g, p, layer, q);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
+  if (ev) {
+    e = cudaEventRecord(ev, st);
+    if (e != cudaSuccess) return (int)e;
+  }
   combine_kernel<D, COMP><<<(p.n_out_rows + 3) / 4, 128, 0, st>>>(g, p, layer, out);
   return (int)cudaGetLastError();
 }
 
 int launch_attention(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q,
-                     uint16_t* out, int compressed, int num_sms, void* stream, int* n_launches) {
+                     uint16_t* out, int compressed, int num_sms, void* stream, int* n_launches,
+                     void* event_after_main) {
   cudaStream_t st = (cudaStream_t)stream;
+  cudaEvent_t ev = (cudaEvent_t)event_after_main;
   *n_launches = 2;
   if (g.d == 128) {
-    return compressed ? launch_attn_t<128, true>(g, p, layer, q, out, num_sms, st)
-                      : launch_attn_t<128, false>(g, p, layer, q, out, num_sms, st);
+    return compressed ? launch_attn_t<128, true>(g, p, layer, q, out, num_sms, st, ev)
+                      : launch_attn_t<128, false>(g, p, layer, q, out, num_sms, st, ev);
   }
-  return compressed ? launch_attn_t<64, true>(g, p, layer, q, out, num_sms, st)
-                    : launch_attn_t<64, false>(g, p, layer, q, out, num_sms, st);
+  return compressed ? launch_attn_t<64, true>(g, p, layer, q, out, num_sms, st, ev)
+                    : launch_attn_t<64, false>(g, p, layer, q, out, num_sms, st, ev);
 }
 
 }  // namespace fk
