@@ -200,6 +200,20 @@ def run_cpu_baseline(budget_s: float = 15.0) -> dict:
 
 # -------------------------------------------------------------- GPU arm --
 
+def reduce_over_ranks(total_ms: float, e2e_ms: float, units: int, e2e_units: int, world: int,
+                      device) -> tuple:
+    """Whole-job throughput of N independent replicas: the units every rank
+    processed divided by the slowest rank's time (max over ranks)."""
+    import torch
+    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = float(t[0]), float(t[1])
+    return (units * world / (total_ms / 1e3), total_ms,
+            e2e_units * world / (e2e_ms / 1e3), e2e_ms)
+
+
 def run_gb300(args, rank: int, world: int, local_rank: int):
     import numpy as np
     import torch
@@ -276,13 +290,8 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
     e2e_ms = sum(e_s[k].elapsed_time(e_e[k]) for k in range(KE))
     ok = bool(torch.isfinite(out.float()).all().item())
     dw.check()
-    tot = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = float(tot[0]), float(tot[1])
-    units = w.A * K * world
-    value = units / (total_ms / 1e3)
-    e2e_value = (w.A * KE * world) / (e2e_ms / 1e3)
+    value, total_ms, e2e_value, e2e_ms = reduce_over_ranks(
+        total_ms, e2e_ms, w.A * K, w.A * KE, world, dev)
     ab = algorithmic_bytes(w)
     main_avg_s = statistics.mean(main_ms) / 1e3
     peak, peak_kind = measured_peak_hbm()

@@ -160,6 +160,13 @@ fk_status fk_agent_register(fk_pool* pool, int agent, int rank, float s,
                             void* stream);
 fk_status fk_agent_release(fk_pool* pool, int agent);
 
+/* Where agent `agent`'s residual cache lives: byte offset (from the pool
+ * carve-out) of its layer-0 Lk block, the bytes one layer of Lk+Lv takes
+ * (Lv follows Lk after half of them), and its padded rank (rank rounded up
+ * to 16).  For reading the pool back in tests and tools. */
+fk_status fk_agent_rcache(const fk_pool* pool, int agent, size_t* lk_offset,
+                          size_t* layer_bytes, int* padded_rank);
+
 /* ---- appends ---- */
 
 /* Write base keys/values of tokens pos..pos+n-1 of one sequence into layer

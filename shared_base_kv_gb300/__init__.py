@@ -38,7 +38,7 @@ EXPORTS = (
     "fk_fork", "fk_page_refcount", "fk_agent_register", "fk_agent_release",
     "fk_base_append", "fk_residual_append", "fk_pool_compress",
     "fk_pool_load_compressed", "fk_residual_attention", "fk_last_launch_count",
-    "fk_check", "fk_plan_host", "fk_pool_set_profile_event",
+    "fk_check", "fk_plan_host", "fk_pool_set_profile_event", "fk_agent_rcache",
 )
 
 
@@ -104,6 +104,8 @@ def lib() -> ctypes.CDLL:
             "fk_last_launch_count": (i32, [vp]),
             "fk_check": (i32, [vp, vp]),
             "fk_pool_set_profile_event": (i32, [vp, vp]),
+            "fk_agent_rcache": (i32, [vp, i32, ctypes.POINTER(ctypes.c_size_t),
+                                      ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(i32)]),
             "fk_plan_host": (i32, [i32, i32, i32, i32, i32, P32, i32, P32, P32, i32, i32, i32,
                                    ctypes.POINTER(fk_work_item), i32, P32,
                                    P32, P32, i32, P32, P32, i32, P32, P32, i32, P32]),
@@ -201,6 +203,13 @@ def fk_agent_register(h, agent: int, rank: int, s: float, Bk, Bv, stream=None) -
 
 def fk_agent_release(h, agent: int) -> None:
     _check(lib().fk_agent_release(h, agent))
+
+
+def fk_agent_rcache(h, agent: int):
+    """(byte offset of layer-0 Lk, bytes per layer of Lk+Lv, padded rank)."""
+    off, lb, rp = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_int()
+    _check(lib().fk_agent_rcache(h, agent, ctypes.byref(off), ctypes.byref(lb), ctypes.byref(rp)))
+    return off.value, lb.value, rp.value
 
 
 def fk_base_append(h, layer: int, block_table_row: np.ndarray, pos: int, Kb, Vb,

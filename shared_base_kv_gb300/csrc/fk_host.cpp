@@ -569,6 +569,18 @@ fk_status fk_agent_release(fk_pool* p, int agent) {
   return upload_agent(p, agent, nullptr);
 }
 
+fk_status fk_agent_rcache(const fk_pool* p, int agent, size_t* lk_offset, size_t* layer_bytes,
+                          int* padded_rank) {
+  if (!p || !lk_offset || !layer_bytes || !padded_rank) return fail(FK_ERR_INVALID_ARG, "NULL argument");
+  if (agent < 0 || agent >= p->g.max_agents || !p->agents[agent].live)
+    return fail(FK_ERR_INVALID_ARG, "agent not registered");
+  const auto& A = p->agents[agent];
+  *lk_offset = (size_t)A.rc_off;
+  *layer_bytes = (size_t)rc_layer_bytes(p->g, A.rp);
+  *padded_rank = A.rp;
+  return FK_OK;
+}
+
 fk_status fk_base_append(fk_pool* p, int layer, int32_t* row, int max_pages, int pos,
                          int n, const uint16_t* Kb, const uint16_t* Vb, void* stream) {
   if (!p || !row) return fail(FK_ERR_INVALID_ARG, "NULL argument");

@@ -24,7 +24,8 @@ from . import (Pool, fk_agent_register, fk_base_append, fk_check, fk_fork, fk_la
 class DeviceWorkload:
     def __init__(self, w, *, layers: Optional[list] = None, device: str = "cuda",
                  compressed: Optional[str] = None, codes: Optional[dict] = None,
-                 spare_pages: int = 0, workspace_bytes: int = 0):
+                 spare_pages: int = 0, workspace_bytes: int = 0,
+                 page_shuffle_seed: Optional[int] = None):
         """``compressed``: None, ``"gpu"`` (encode with fk_pool_compress) or
         ``"codes"`` (load the per-layer codes in ``codes[layer] = (kq,
         k_scale, vcodes_packed, vnorm)``, slot-ordered host arrays)."""
@@ -39,7 +40,15 @@ class DeviceWorkload:
                          compressed=compressed is not None, device=self.dev,
                          workspace_bytes=workspace_bytes)
         h = self.pool.h
-        self.slot_page = fk_pages_alloc(h, w.n_slots)            # slot -> pool page id
+        if page_shuffle_seed is None:
+            self.slot_page = fk_pages_alloc(h, w.n_slots)        # slot -> pool page id
+        else:
+            # take every page, place the slots on a seeded random subset
+            ids = fk_pages_alloc(h, w.n_slots + spare_pages)
+            order = np.random.default_rng(page_shuffle_seed).permutation(ids.size)
+            self.slot_page = ids[order[:w.n_slots]].astype(np.int32)
+            if spare_pages:
+                fk_pages_release(h, ids[order[w.n_slots:]])
         bt = w.block_table
         self.block_table = np.where(bt >= 0, self.slot_page[np.maximum(bt, 0)], -1).astype(np.int32)
         # Agents: register with all layers' up-projections.

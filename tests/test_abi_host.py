@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+symbol the header declares, rejects bad configurations, and its work-list
+planner covers exactly the sharing classes the oracle derives."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import shared_base_kv_gb300 as fk
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "forkkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fk_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_symbols()
+    assert len(names) >= 20
+    L = fk.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(fk.EXPORTS)
+
+
+def test_version_and_error_string():
+    assert "sm_103a" in fk.fk_version()
+    cfg = fk.fk_pool_config(1, 32, 8, 96, 16, 10, 4, 16, 100, 0, 0, 10000.0, 0)
+    with pytest.raises(fk.FKError) as e:
+        fk.fk_pool_bytes(cfg)
+    assert "head_dim" in str(e.value)
+
+
+@pytest.mark.parametrize("field,value,msg", [
+    ("page_size", 32, "page_size"), ("max_rank", 12, "max_rank"),
+    ("n_q_heads", 30, "multiple"), ("num_pages", 0, "num_pages"),
+    ("rope_base", 0.5, "rope_base")])
+def test_bad_configs_are_rejected(field, value, msg):
+    cfg = fk.fk_pool_config(1, 32, 8, 128, 16, 10, 4, 16, 100, 0, 0, 10000.0, 0)
+    setattr(cfg, field, value)
+    with pytest.raises(fk.FKError) as e:
+        fk.fk_pool_bytes(cfg)
+    assert msg in str(e.value)
+
+
+def test_pool_bytes_accounts_for_every_region():
+    cfg = fk.fk_pool_config(2, 32, 8, 128, 16, 100, 4, 16, 1000, 0, 1 << 20, 10000.0, 1)
+    n = fk.fk_pool_bytes(cfg)
+    page_bytes = 2 * 2 * 100 * 8 * 16 * 128 * 2               # K and V pages, 2 layers
+    rc = 4 * 16 * 2 * 1024 * 2 * 2                             # 4 agents, rank 16, 2 layers
+    comp = 2 * 100 * 8 * 16 * (128 + 48 + 4)
+    assert n >= page_bytes + rc + comp + (1 << 20)
+    assert n < (page_bytes + rc + comp + (1 << 20)) * 1.5
+
+
+def _plan(w, target=152):
+    return fk.fk_plan_host(w.A, w.C, w.H_q, w.H_kv, w.block_table, w.seq_lens, w.ranks, target)
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("llama8b_32k", dict(prefix=1000, A=8)),
+    ("agents32_layers32", dict(prefix=200, suffix=(0, 40), A=9, n_layers=1)),
+    ("qwen72b_chunk", dict(prefix=100, A=3)),
+    ("compressed", dict(prefix=333, A=15)),
+    ("tiny", {}),
+])
+def test_plan_covers_sharing_classes_exactly_once(name, kw):
+    w = workloads.make_workload(name, **kw)
+    items, row_agent, row_cg, pages, tile_agents = _plan(w)
+    cov = oracle.coverage(w.block_table, w.seq_lens, w.P)
+    classes = {(lp, ph): set(ag) for lp, ph, ag in oracle.page_classes(w.block_table, w.seq_lens, w.P)}
+    G = w.H_q // w.H_kv
+    for h in range(w.H_kv):
+        seen = {}
+        for it in items:
+            if it["head"] != h:
+                continue
+            ags = tile_agents[it["agent_begin"]: it["agent_begin"] + it["n_agents"]]
+            rows = list(zip(row_agent[it["row_begin"]: it["row_begin"] + it["n_rows"]],
+                            row_cg[it["row_begin"]: it["row_begin"] + it["n_rows"]]))
+            assert set(a for a, _ in rows) == set(int(a) for a in ags)
+            assert it["n_rows"] <= 64 and it["n_agents"] <= 4
+            assert sum(((int(w.ranks[a]) + 15) // 16) * 16 for a in ags) <= 64
+            for k in range(it["n_pages"]):
+                lp = it["lp_begin"] + k
+                ph = int(pages[it["page_begin"] + k])
+                assert set(int(a) for a in ags) <= classes[(lp, ph)]
+                for a, cg in rows:
+                    key = (int(a), lp, ph, int(cg))
+                    seen[key] = seen.get(key, 0) + 1
+        expect = {(a, lp, ph, cg) for a, lp, ph in cov for cg in range(G * w.C)}
+        assert set(seen) == expect
+        assert all(v == 1 for v in seen.values())
+
+
+def test_plan_balances_pieces():
+    w = workloads.make_workload("llama8b_32k")
+    items, *_ = _plan(w, 152)
+    pages_per_head = {}
+    for it in items:
+        pages_per_head[it["head"]] = pages_per_head.get(it["head"], 0) + it["n_pages"]
+    # every head covers all 2048 pages twice (two 4-agent row tiles)
+    assert set(pages_per_head.values()) == {2 * 2048}
+    assert len(items) <= 152 + 16
+
+
+def test_plan_rejects_bad_tables():
+    w = workloads.make_workload("tiny")
+    bt = w.block_table.copy()
+    bt[1, 3] = -1
+    with pytest.raises(fk.FKError):
+        fk.fk_plan_host(w.A, w.C, w.H_q, w.H_kv, bt, w.seq_lens, w.ranks, 16)
+    seq = w.seq_lens.copy()
+    seq[0] = 0
+    with pytest.raises(fk.FKError):
+        fk.fk_plan_host(w.A, w.C, w.H_q, w.H_kv, w.block_table, seq, w.ranks, 16)
