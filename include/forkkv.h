@@ -241,6 +241,36 @@ fk_status fk_residual_attention(fk_pool* pool, int layer, const uint16_t* q,
                                 int causal, int compressed, uint16_t* out,
                                 void* stream);
 
+/* Same computation and arguments as fk_residual_attention, for callers
+ * that must not allocate device memory per call or share the pool's
+ * workspace: for example a plug-in living inside a host program that owns
+ * all of the GPU's memory through its own allocator (and has handed nearly
+ * all of it to KV pages), so that any cudaMalloc from this library would
+ * fail or would break that program's memory accounting.  No page of the
+ * paper describes this call; it is a deployment aid.
+ *
+ * The per-call scratch (the work list and the split-K partials) lives in a
+ * file-scope device array of FK_NOALLOC_SCRATCH_BYTES bytes inside the
+ * library instead of the pool's workspace; every GPU that loads the library
+ * keeps that array until the process exits.  The call allocates nothing: no
+ * cudaMalloc, cudaFree, pinned-host or other allocating routine.  Calls
+ * whose work list and partials need more than FK_NOALLOC_SCRATCH_BYTES
+ * fail with FK_ERR_OOM and a message giving the size needed.  The first
+ * call on a device looks up the array's device address (set-up done once
+ * per device), so make that first call before any stream capture.  All
+ * calls share the one array, which keeps the last call's contents; calls
+ * whose kernels overlap on the GPU (other streams, other pools) race on it
+ * and must be ordered by the caller. */
+#define FK_NOALLOC_SCRATCH_BYTES (16u << 20)
+fk_status fk_residual_attention_noalloc(fk_pool* pool, int layer,
+                                        const uint16_t* q,
+                                        const int32_t* agents,
+                                        const int32_t* block_table,
+                                        int max_pages,
+                                        const int32_t* seq_lens, int A, int C,
+                                        int causal, int compressed,
+                                        uint16_t* out, void* stream);
+
 /* Number of kernel launches the last fk_residual_attention enqueued. */
 int fk_last_launch_count(const fk_pool* pool);
 

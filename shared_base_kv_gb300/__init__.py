@@ -39,6 +39,7 @@ EXPORTS = (
     "fk_base_append", "fk_residual_append", "fk_pool_compress",
     "fk_pool_load_compressed", "fk_residual_attention", "fk_last_launch_count",
     "fk_check", "fk_plan_host", "fk_pool_set_profile_event", "fk_agent_rcache",
+    "fk_residual_attention_noalloc",
 )
 
 
@@ -101,6 +102,8 @@ def lib() -> ctypes.CDLL:
             "fk_pool_load_compressed": (i32, [vp, i32, P32, i32, vp, vp, vp, ctypes.c_float, vp]),
             "fk_residual_attention": (i32, [vp, i32, vp, P32, P32, i32, P32, i32, i32, i32,
                                             i32, vp, vp]),
+            "fk_residual_attention_noalloc": (i32, [vp, i32, vp, P32, P32, i32, P32, i32, i32,
+                                                    i32, i32, vp, vp]),
             "fk_last_launch_count": (i32, [vp]),
             "fk_check": (i32, [vp, vp]),
             "fk_pool_set_profile_event": (i32, [vp, vp]),
@@ -249,6 +252,24 @@ def fk_residual_attention(h, layer: int, q, agents, block_table, seq_lens, causa
     _check(lib().fk_residual_attention(h, layer, _dev(q), _p32(ag), _p32(bt), bt.shape[1],
                                        _p32(sl), A, C, int(bool(causal)), int(bool(compressed)),
                                        _dev(out), _stream(stream)))
+
+
+FK_NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def fk_residual_attention_noalloc(h, layer: int, q, agents, block_table, seq_lens, causal: bool,
+                                  compressed: bool, out, stream=None) -> None:
+    """fk_residual_attention for callers that must not allocate device
+    memory: its scratch is a fixed 16 MiB array inside the library (see the
+    header); the first call on a device sets it up, so make it before any
+    stream capture, and do not overlap two such calls on the GPU."""
+    ag, bt, sl = _i32(agents), _i32(block_table), _i32(seq_lens)
+    A, C = int(q.shape[0]), int(q.shape[1])
+    if bt.ndim != 2 or bt.shape[0] != A:
+        raise ValueError("block_table must be [A, max_pages]")
+    _check(lib().fk_residual_attention_noalloc(h, layer, _dev(q), _p32(ag), _p32(bt), bt.shape[1],
+                                               _p32(sl), A, C, int(bool(causal)),
+                                               int(bool(compressed)), _dev(out), _stream(stream)))
 
 
 def fk_last_launch_count(h) -> int:

@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -825,6 +826,119 @@ fk_status fk_residual_attention(fk_pool* p, int layer, const uint16_t* q, const 
   int launches = 0;
   int e = launch_attention(g, p->plan_dev, layer, q, out, compressed ? 1 : 0, p->num_sms,
                            stream, &launches, p->profile_event);
+  if (e != 0) return cuda_fail((cudaError_t)e, "attention kernels");
+  p->last_launches = launches;
+  return FK_OK;
+}
+
+// Work list of fk_residual_attention_noalloc, kept apart from the pool's own
+// cache: the static scratch is shared by every pool of the process.
+namespace {
+struct NoallocCache {
+  const fk_pool* pool = nullptr;
+  int device = -1;
+  std::vector<int32_t> key;
+  PlanDev pd{};
+};
+NoallocCache g_noalloc[64];
+std::mutex g_noalloc_mu;
+}  // namespace
+
+fk_status fk_residual_attention_noalloc(fk_pool* p, int layer, const uint16_t* q,
+                                        const int32_t* agents, const int32_t* bt, int max_pages,
+                                        const int32_t* seq, int A, int C, int causal,
+                                        int compressed, uint16_t* out, void* stream) {
+  if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
+  const PoolGeom& g = p->g;
+  if (layer < 0 || layer >= g.L) return fail(FK_ERR_INVALID_ARG, "layer out of range");
+  if (!q || !out || !agents || !bt || !seq) return fail(FK_ERR_INVALID_ARG, "NULL argument");
+  if (A < 1 || C < 1 || max_pages < 1) return fail(FK_ERR_INVALID_ARG, "A, C, max_pages must be >= 1");
+  if (compressed && !g.compressed) return fail(FK_ERR_INVALID_ARG, "pool has no compressed copy");
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
+  int ce = noalloc_scratch(&scratch, &scratch_bytes);
+  if (ce != 0) return cuda_fail((cudaError_t)ce, "static scratch lookup");
+  cudaStream_t st = (cudaStream_t)stream;
+  std::vector<int32_t> key;
+  key.reserve(8 + 2 * A + (size_t)A * max_pages);
+  key.insert(key.end(), {A, C, causal ? 1 : 0, max_pages});
+  key.insert(key.end(), agents, agents + A);
+  key.insert(key.end(), seq, seq + A);
+  key.insert(key.end(), bt, bt + (int64_t)A * max_pages);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoallocCache& cache = g_noalloc[p->device & 63];
+  if (cache.pool != p || cache.device != p->device || cache.key != key) {
+    cache.pool = nullptr;
+    std::vector<int32_t> rp(A), seen(g.max_agents, 0);
+    for (int i = 0; i < A; ++i) {
+      int a = agents[i];
+      if (a < 0 || a >= g.max_agents || !p->agents[a].live)
+        return fail(FK_ERR_INVALID_ARG, "agents[] names an unregistered agent");
+      if (seen[a]++) return fail(FK_ERR_INVALID_ARG, "agents[] repeats an agent");
+      if (seq[i] > p->cfg.max_tokens) return fail(FK_ERR_INVALID_ARG, "seq_len beyond rCache capacity");
+      rp[i] = p->agents[a].rp;
+      int np = (seq[i] + kPage - 1) / kPage;
+      for (int lp = 0; lp < std::min(np, max_pages); ++lp) {
+        int32_t id = bt[(int64_t)i * max_pages + lp];
+        if (id >= g.num_pages || (id >= 0 && p->refcount[id] <= 0))
+          return fail(FK_ERR_INVALID_ARG, "block table names a free or invalid page");
+      }
+    }
+    HostPlan pl;
+    fk_status s = plan_build(A, C, g.H_q, g.H_kv, kPage, bt, max_pages, seq, rp.data(),
+                             kMaxRows, kMaxRankSum, p->num_sms, pl);
+    if (s != FK_OK) return s;
+    PlanDev pd{};
+    pd.n_items = (int)pl.items.size();
+    pd.n_rows = (int)pl.row_agent.size();
+    pd.n_pages = (int)pl.pages.size();
+    pd.n_tile_agents = (int)pl.tile_agents.size();
+    pd.A = A; pd.C = C; pd.causal = causal ? 1 : 0;
+    pd.n_out_rows = A * C * g.H_q;
+    pd.n_partials = pl.n_partials;
+    pd.partial_stride = g.d + g.rmax_pad + 4;
+    std::vector<uint8_t> blob;
+    auto put = [&](const void* src, size_t bytes) {
+      int64_t o = align_up((int64_t)blob.size(), 256);
+      blob.resize(o + bytes);
+      if (bytes) std::memcpy(blob.data() + o, src, bytes);
+      return o;
+    };
+    std::vector<CallAgent> ca(A);
+    for (int i = 0; i < A; ++i) ca[i] = CallAgent{agents[i], seq[i]};
+    pd.off_items = put(pl.items.data(), pl.items.size() * sizeof(fk_work_item));
+    pd.off_row_agent = put(pl.row_agent.data(), pl.row_agent.size() * 4);
+    pd.off_row_cg = put(pl.row_cg.data(), pl.row_cg.size() * 4);
+    pd.off_pages = put(pl.pages.data(), pl.pages.size() * 4);
+    pd.off_tile_agents = put(pl.tile_agents.data(), pl.tile_agents.size() * 4);
+    pd.off_call_agents = put(ca.data(), ca.size() * sizeof(CallAgent));
+    pd.off_csr_ptr = put(pl.csr_ptr.data(), pl.csr_ptr.size() * 4);
+    pd.off_csr_slots = put(pl.csr_slots.data(), pl.csr_slots.size() * 4);
+    pd.off_cta = put(pl.cta_begin.data(), pl.cta_begin.size() * 4);
+    pd.n_ctas = (int)pl.cta_begin.size() - 1;
+    pd.off_partials = align_up((int64_t)blob.size(), 256);
+    int64_t need = pd.off_partials + (int64_t)pd.n_partials * pd.partial_stride * 4;
+    if (need > (int64_t)scratch_bytes) {
+      char msg[160];
+      std::snprintf(msg, sizeof msg,
+                    "call needs %lld bytes of scratch; the static array holds %zu",
+                    (long long)need, scratch_bytes);
+      return fail(FK_ERR_OOM, msg);
+    }
+    // pageable source: the copy is staged before the call returns
+    cudaError_t e = cudaMemcpyAsync(scratch, blob.data(), blob.size(), cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "work list upload");
+    cache.pool = p;
+    cache.device = p->device;
+    cache.key = std::move(key);
+    cache.pd = pd;
+  }
+  PoolGeom g2 = g;
+  g2.off_ws = (int64_t)((uint8_t*)scratch - g.base);
+  g2.ws_bytes = (int64_t)scratch_bytes;
+  int launches = 0;
+  int e = launch_attention(g2, cache.pd, layer, q, out, compressed ? 1 : 0, p->num_sms, stream,
+                           &launches, nullptr);
   if (e != 0) return cuda_fail((cudaError_t)e, "attention kernels");
   p->last_launches = launches;
   return FK_OK;

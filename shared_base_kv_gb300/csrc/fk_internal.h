@@ -92,4 +92,8 @@ int launch_attention(const PoolGeom& g, const PlanDev& p, int layer,
                      int num_sms, void* stream, int* n_launches,
                      void* event_after_main);
 
+// Device address and size of the static scratch array that
+// fk_residual_attention_noalloc uses (looked up once per device).
+int noalloc_scratch(void** ptr, size_t* bytes);
+
 }  // namespace fk

@@ -8,11 +8,14 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "fk_device.cuh"
 #include "fk_internal.h"
 
 namespace fk {
+
+constexpr int kMaxDevices = 64;
 
 __device__ __forceinline__ uint32_t* err_word(const PoolGeom& g) {
   return (uint32_t*)(g.base + g.off_err);
@@ -1169,6 +1172,31 @@ static int launch_attn_t(const PoolGeom& g, const PlanDev& p, int layer, const u
   }
   combine_kernel<D, COMP><<<(p.n_out_rows + 3) / 4, 128, 0, st>>>(g, p, layer, out);
   return (int)cudaGetLastError();
+}
+
+// Scratch of fk_residual_attention_noalloc (work list and split partials of
+// one call), so that the call needs no allocation.  Host code must not pass
+// this symbol to a kernel: its host-side name is only a stand-in; the device
+// address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[FK_NOALLOC_SCRATCH_BYTES];
+
+int noalloc_scratch(void** ptr, size_t* bytes) {
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return (int)e;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  *bytes = FK_NOALLOC_SCRATCH_BYTES;
+  return 0;
 }
 
 int launch_attention(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q,

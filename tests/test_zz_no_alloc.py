@@ -1,0 +1,57 @@
+"""fk_residual_attention_noalloc: the same attention for callers that may not
+allocate device memory (its scratch is a fixed array inside the library).
+Checked through the C ABI against fk_residual_attention on two calls in a
+row; collected last so that a stop at the first failure has already run
+everything else, and written to pass in a fresh process as well."""
+import numpy as np
+import pytest
+import torch
+
+import shared_base_kv_gb300 as fk
+import workloads
+from shared_base_kv_gb300 import harness
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _call(fn, dw, q):
+    w = dw.w
+    out = torch.full_like(q, float("nan"))
+    fn(dw.pool.h, 0, q, np.arange(w.A, dtype=np.int32), dw.block_table, w.seq_lens, w.causal,
+       dw.compressed is not None, out)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("llama8b_32k", dict(prefix=1000, A=8)),
+    ("agents32_layers32", dict(prefix=200, suffix=(0, 40), A=9, n_layers=1)),
+])
+def test_noalloc_matches_pool_workspace_call(name, kw):
+    w = workloads.make_workload(name, "strong", **kw)
+    dw = harness.DeviceWorkload(w)
+    q = dw.queries(0)
+    ref = _call(fk.fk_residual_attention, dw, q).float()
+    for _ in range(2):                      # two calls in a row share the array
+        got = _call(fk.fk_residual_attention_noalloc, dw, q).float()
+        assert torch.isfinite(got).all()
+        err = (got - ref).abs()
+        assert err.max().item() <= 2e-2 and err.mean().item() <= 2e-3
+        assert torch.equal(got, ref)        # same kernels, same work list
+    dw.check()
+
+
+def test_noalloc_rejects_calls_beyond_the_array():
+    w = workloads.make_workload("qwen72b_chunk", prefix=4096, A=16)
+    dw = harness.DeviceWorkload(w)
+    q = dw.queries(0)
+    with pytest.raises(fk.FKError) as e:
+        _call(fk.fk_residual_attention_noalloc, dw, q)
+    assert e.value.code == fk.FK_ERR_OOM
+    assert "static array" in str(e.value)
