@@ -276,7 +276,7 @@ __global__ void load_compressed_kernel(PoolGeom g, int layer, const int32_t* __r
 
 namespace attn {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kPRowGroup = 2304;        // P: 16 token-chunks x 144 B
 constexpr int kPChunk = 144;
 constexpr int kA = kMaxAgentsPerTile;
@@ -328,13 +328,24 @@ enum {
   B_KB_FULL, B_KB_EMPTY, B_LK_FULL0, B_LK_FULL1, B_LK_EMPTY0, B_LK_EMPTY1, B_VL_FULL,
   B_VL_EMPTY, B_BK_FULL, B_BK_EMPTY, B_Q_FULL, B_Q_EMPTY, B_U_FULL0, B_U_FULL1, B_R_FULL0,
   B_R_FULL1, B_UFREE0, B_UFREE1, B_S_FULL, B_S_EMPTY, B_P_FULL, B_PV_DONE, B_ACC_EMPTY,
-  B_KQ_FULL, B_KQ_EMPTY, B_VC_FULL, B_VC_EMPTY, B_FINAL, B_COUNT
+  B_KQ_FULL, B_KQ_EMPTY, B_VC_FULL, B_VC_EMPTY, B_FINAL, B_ROT_FULL0, B_ROT_FULL1,
+  B_ROT_EMPTY0, B_ROT_EMPTY1, B_COUNT
 };
+// Arrival counts: 1 = one thread or an MMA commit, 4 = one lane per warp of
+// a warpgroup, 2 = the value stage of the compressed pool (the producer's
+// transaction count plus the dequantiser).
+__host__ __device__ constexpr uint32_t bar_count(int i, bool comp) {
+  return (i == B_Q_FULL || i == B_R_FULL0 || i == B_R_FULL1 || i == B_S_EMPTY || i == B_P_FULL ||
+          i == B_ACC_EMPTY || i == B_ROT_EMPTY0 || i == B_ROT_EMPTY1)
+             ? 4u
+             : (i == B_VL_FULL && comp) ? 2u : 1u;
+}
 // barriers a role waits on as "empty" start one phase ahead
 constexpr uint32_t kEmptyMask = (1u << B_KB_EMPTY) | (1u << B_LK_EMPTY0) | (1u << B_LK_EMPTY1) |
                                 (1u << B_VL_EMPTY) | (1u << B_BK_EMPTY) | (1u << B_Q_EMPTY) |
                                 (1u << B_UFREE0) | (1u << B_UFREE1) | (1u << B_S_EMPTY) |
-                                (1u << B_ACC_EMPTY) | (1u << B_KQ_EMPTY) | (1u << B_VC_EMPTY);
+                                (1u << B_ACC_EMPTY) | (1u << B_KQ_EMPTY) | (1u << B_VC_EMPTY) |
+                                (1u << B_ROT_EMPTY0) | (1u << B_ROT_EMPTY1);
 
 struct Misc {
   uint64_t bar[B_COUNT];
@@ -345,12 +356,12 @@ struct Misc {
   float red[4][kMaxRows];
   int32_t row_T[kMaxRows];
   int32_t row_pos[kMaxRows];
-  int32_t row_col[kMaxRows];     // first OL column of the row's agent
-  int32_t row_rp[kMaxRows];      // padded rank of the row's agent
-  uint32_t rot0[64];             // per tile: f16x2 (cos) pairs then (sin) pairs
+  uint32_t rot[2][64];           // tile-start rotations, a 2-tile ring: f16x2 cos pairs, sin pairs
   float theta[64];               // RoPE theta_i
   unsigned long long frac[64];   // theta_i / (2 pi) as a 64-bit binary fraction
 };
+
+static_assert(sizeof(Misc) <= 4096, "Misc must fit its smem slot (Layout::MISC_B)");
 
 // What every role derives from a work item.  Per-agent arrays are only
 // indexed with compile-time indices (unrolled loops), so they stay in
@@ -415,101 +426,88 @@ __device__ __forceinline__ const uint8_t* rc_lv(const PoolGeom& g, const ItemInf
 }  // namespace attn
 
 // Masked online softmax of one tile for NRP (16/32/48/64) padded query
-// rows: scores from TMEM (lane = token), running-max update only when a
-// row's max grows by more than 2^8 (then O, OL and L are rescaled in TMEM),
-// P in bf16 to smem in the K-major layout of the PV / OL / L MMAs.  Rows
-// past n_rows have row_T = 0 and come out as P = 0.
+// rows, run by the softmax warpgroup (lane = token): scores from TMEM, the
+// running max of a row moves only when the row's tile max exceeds it by more
+// than 2^8 (then O^T and OL^T are rescaled in TMEM), P in bf16 to smem in the
+// K-major layout of the PV MMAs.  Rows past n_rows have row_T = 0 and come
+// out as P = 0.
 template <int NRP, int D, bool COMP, typename Wait>
 __device__ __forceinline__ void softmax_tile(uint8_t* smem, attn::Misc& M, uint32_t tmem,
-                                             uint32_t lane_off, int ln, int warp, int lane, int k,
+                                             uint32_t lane_off, int ln, int sw, int lane, int k,
                                              int t0, int ntok, int n_rows, float scale_log2,
                                              Wait& wait, uint32_t bar_s_empty) {
   using namespace attn;
   using LY = Layout<D, COMP>;
-  enum { B_PV_DONE_ = B_PV_DONE, B_S_FULL_ = B_S_FULL };
-        // ---- masked online softmax over this tile's 128 tokens
-  wait(B_S_FULL_);
-        tc_fence_after();
-        float sv[NRP];
-        {
-          uint32_t raw[NRP];
+  wait(B_S_FULL);
+  tc_fence_after();
+  uint32_t sv[NRP];                 // scores, then log2-domain scores (float bits)
 #pragma unroll
-          for (int c0 = 0; c0 < NRP; c0 += 16)
-            tmem_ld16(tmem + kTmS + c0 + lane_off, raw + c0);
-          tmem_wait_ld();
+  for (int c0 = 0; c0 < NRP; c0 += 16) tmem_ld16(tmem + kTmS + c0 + lane_off, sv + c0);
+  tmem_wait_ld();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar_s_empty);
+  const int tabs = t0 + ln;
+  bool need = false;
 #pragma unroll
-          for (int e = 0; e < NRP; ++e) sv[e] = __uint_as_float(raw[e]);
-        }
-        tc_fence_before();
-        named_bar(1, 128);
-        if (ln == 0) mbar_arrive(bar_s_empty);
-        const int tabs = t0 + ln;
-        bool need = false;
+  for (int j = 0; j < NRP; ++j) {
+    bool ok = ln < ntok && tabs < M.row_T[j] && tabs <= M.row_pos[j];
+    float s = ok ? __uint_as_float(sv[j]) * scale_log2 : -INFINITY;
+    sv[j] = __float_as_uint(s);
+    need |= s > M.m_used[j] + 8.f;
+  }
+  int any;
+  asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 3, 128, p; selp.u32 %0, 1, 0, q; }"
+               : "=r"(any) : "r"((int)need));
+  if (k > 0) wait(B_PV_DONE);
+  if (any) {
 #pragma unroll
-        for (int j = 0; j < NRP; ++j) {
-          bool ok = ln < ntok && tabs < M.row_T[j] && tabs <= M.row_pos[j];
-          float s = ok ? sv[j] * scale_log2 : -INFINITY;
-          sv[j] = s;
-          need |= s > M.m_used[j] + 8.f;
-        }
-        int any;
-        asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 2, 128, p; selp.u32 %0, 1, 0, q; }"
-                     : "=r"(any) : "r"((int)need));
-        if (k > 0) wait(B_PV_DONE_);
-        if (any) {
-          // column max over the tile, new running max, rescale accumulators
+    for (int j = 0; j < NRP; ++j) {
+      float v = __uint_as_float(sv[j]);
 #pragma unroll
-          for (int j = 0; j < NRP; ++j) {
-            float v = sv[j];
+      for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+      if (lane == 0) M.red[sw][j] = v;
+    }
+    named_bar(2, 128);
+    if (ln < NRP) {
+      float al = 1.f;
+      if (ln < n_rows) {
+        float cm = fmaxf(fmaxf(M.red[0][ln], M.red[1][ln]), fmaxf(M.red[2][ln], M.red[3][ln]));
+        float mo = M.m_used[ln];
+        float mn = fmaxf(mo, cm);
+        if (mn > mo) { al = (mo == -INFINITY) ? 0.f : exp2f(mo - mn); M.m_used[ln] = mn; }
+      }
+      M.alpha[ln] = al;
+    }
+    named_bar(2, 128);
+    if (k > 0) {
+      tc_fence_after();
+      uint32_t raw[16];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (lane == 0) M.red[warp - 4][j] = v;
-          }
-          named_bar(1, 128);
-          if (ln < NRP) {
-            float al = 1.f;
-            if (ln < n_rows) {
-              float cm = fmaxf(fmaxf(M.red[0][ln], M.red[1][ln]), fmaxf(M.red[2][ln], M.red[3][ln]));
-              float mo = M.m_used[ln];
-              float mn = fmaxf(mo, cm);
-              if (mn > mo) { al = (mo == -INFINITY) ? 0.f : exp2f(mo - mn); M.m_used[ln] = mn; }
-            }
-            M.alpha[ln] = al;
-          }
-          named_bar(1, 128);
-          if (k > 0) {
-            tc_fence_after();
-            // O^T: lane = d, columns = rows
-            uint32_t raw[16];
-            for (int c0 = 0; c0 < NRP; c0 += 16) {
-              tmem_ld16(tmem + kTmOT + c0 + lane_off, raw);
-              tmem_wait_ld();
+      for (int c0 = 0; c0 < NRP; c0 += 16) {
+        tmem_ld16(tmem + kTmOT + c0 + lane_off, raw);
+        tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * M.alpha[c0 + e]);
-              tmem_st16(tmem + kTmOT + c0 + lane_off, raw);
-            }
-            // OL^T: lane = (agent, r) or the ones lane, columns = rows
-            for (int c0 = 0; c0 < NRP; c0 += 16) {
-              tmem_ld16(tmem + kTmOL + c0 + lane_off, raw);
-              tmem_wait_ld();
+        for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * M.alpha[c0 + e]);
+        tmem_st16(tmem + kTmOT + c0 + lane_off, raw);
+        tmem_ld16(tmem + kTmOL + c0 + lane_off, raw);
+        tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * M.alpha[c0 + e]);
-              tmem_st16(tmem + kTmOL + c0 + lane_off, raw);
-            }
-            tmem_wait_st();
-          }
-        }
-        // ---- P (bf16) -> smem, K-major for the PV / OL / L MMAs
-        {
-          const int tc = ln / 8, tr = ln % 8;
+        for (int e = 0; e < 16; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * M.alpha[c0 + e]);
+        tmem_st16(tmem + kTmOL + c0 + lane_off, raw);
+      }
+      tmem_wait_st();
+    }
+  }
+  const int tc = ln / 8, tr = ln % 8;
 #pragma unroll
-          for (int j = 0; j < NRP; ++j) {
-            float m = M.m_used[j];
-            float pv = (sv[j] == -INFINITY || m == -INFINITY) ? 0.f : exp2f(sv[j] - m);
-            *(__nv_bfloat16*)(smem + LY::oP + (j / 8) * kPRowGroup + tc * kPChunk + (j % 8) * 16 + tr * 2) =
-                __float2bfloat16_rn(pv);
-          }
-        }
+  for (int j = 0; j < NRP; ++j) {
+    float m = M.m_used[j];
+    float s = __uint_as_float(sv[j]);
+    float pv = (s == -INFINITY || m == -INFINITY) ? 0.f : exp2f(s - m);
+    *(__nv_bfloat16*)(smem + LY::oP + (j / 8) * kPRowGroup + tc * kPChunk + (j % 8) * 16 + tr * 2) =
+        __float2bfloat16_rn(pv);
+  }
 }
 
 template <int D, bool COMP>
@@ -533,13 +531,14 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
     mbar_wait(bar(i), par, abort_flag, errw);
     ph ^= 1u << i;
   };
+  // the dependent combine grid may be scheduled now; it waits for this
+  // grid's completion before reading the partials
+  asm volatile("griddepcontrol.launch_dependents;");
 
   // ---- set-up: zero smem (junk rows read by padded MMAs stay finite),
-  // ones block, RoPE tables, barriers, TMEM.
+  // ones row of the Lv^T stage, RoPE tables, barriers, TMEM.
   for (int i = tid * 16; i < LY::TOTAL; i += kThreads * 16) *(uint4*)(smem + i) = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  // Lv^T stage: r-group 8 (lane 64 of OL^T) row 0 is all ones, so the same
-  // MMA that forms P Lv also forms the row sums of P.
   for (int i = tid; i < 16 * 8; i += kThreads)
     ((uint16_t*)(smem + LY::oLV + (i / 8) * kLvChunk + (kOnesLane / 8) * 128))[i % 8] = 0x3F80;
   if (tid < 64) {
@@ -547,8 +546,8 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
     M.frac[tid] = ((const unsigned long long*)(g.base + g.off_rope + 256))[tid];
   }
   __syncthreads();
-  if (tid >= 128) {
-    // rotation of each tile offset tau = tid - 128 (f16 pairs), kept in smem
+  if (tid >= 128 && tid < 256) {
+    // rotation by each tile offset tau = tid - 128 (f16 pairs), kept in smem
     // as [word][lane] so that a warp reads 32 consecutive words
     const int tau = tid - 128;
     uint32_t* T = (uint32_t*)(smem + LY::oTAU);
@@ -561,7 +560,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
     }
   }
   if (tid == 0) {
-    for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), (i == B_VL_FULL && COMP) ? 2u : 1u);
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), bar_count(i, COMP));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) tmem_alloc(smem_u32(&M.tmem_base), 512);
@@ -578,7 +577,6 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
       ItemInfo I;
       load_item(g, p, ws, it, I);
       const int32_t* pages = (const int32_t*)(ws + p.off_pages) + I.page_begin;
-      // B_k^T of the item's agents, for this head
       wait(B_BK_EMPTY);
       {
         uint32_t bytes = 0;
@@ -717,7 +715,6 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
         mma_commit(bar(B_PV_DONE));
       };
       for (int k = 0; k < I.n_tiles; ++k, ++tile_ctr) {
-        // S = Kb Q^T
         wait(B_S_EMPTY);
         wait(B_KB_FULL);
         tc_fence_after();
@@ -726,7 +723,6 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
           mma_ss(t_S, sdesc(sbase + LY::oKB + ks * 256, 128, (D / 8) * 128),
                  sdesc(sbase + LY::oQ + ks * 256, 128, (D / 8) * 128), id_S, ks > 0 ? 1u : 0u);
         mma_commit(bar(B_KB_EMPTY));
-        // per agent: U_a = Lk_a Bk_a^T, then (one agent behind) S += R Qm^T
         const int lb = COMP ? 0 : (tile_ctr & 1);
         wait(B_LK_FULL0 + lb);
         tc_fence_after();
@@ -758,12 +754,38 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
       mma_commit(bar(B_Q_EMPTY));
       mma_commit(bar(B_BK_EMPTY));
     }
-    // every MMA this CTA issued has completed before TMEM is released
     mma_commit(bar(B_FINAL));
     wait(B_FINAL);
-  } else if (COMP && (warp == 2 || warp == 3)) {
-    // ================================== dequantiser (compressed pool) ====
-    const int ct = tid - 64;   // 0..63
+  } else if (warp == 2) {
+    // =========================== tile-start rotations, one tile ahead ====
+    // Exact t0 * theta_i reduced modulo 2 pi with a 64-bit binary fraction,
+    // then an accurate sincos; lane j writes the f16 pairs of freqs 2j, 2j+1.
+    int tile_ctr = 0;
+    for (int it = cta_items[blockIdx.x]; it < cta_items[blockIdx.x + 1]; ++it) {
+      ItemInfo I;
+      load_item(g, p, ws, it, I);
+      for (int k = 0; k < I.n_tiles; ++k, ++tile_ctr) {
+        const int b = tile_ctr & 1;
+        wait(B_ROT_EMPTY0 + b);
+        const int t0 = (I.lp_begin + k * kTilePages) * kPage;
+        if (lane < D / 4) {
+          float cc[2], ssn[2];
+#pragma unroll
+          for (int z = 0; z < 2; ++z) {
+            unsigned long long fr = (unsigned long long)t0 * M.frac[2 * lane + z];
+            float ang = (float)(unsigned int)(fr >> 32) * 1.4629180792671596e-09f;  // 2 pi / 2^32
+            if (ang > 3.14159265f) ang -= 6.28318531f;
+            sincosf(ang, &ssn[z], &cc[z]);
+          }
+          M.rot[b][lane] = pack_h2(cc[0], cc[1]);
+          M.rot[b][32 + lane] = pack_h2(ssn[0], ssn[1]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_ROT_FULL0 + b));
+      }
+    }
+  } else if (COMP && warp == 3) {
+    // ====================================== dequantiser (compressed pool) ====
     const float kscale = ((const float*)(g.base + g.off_ks))[layer];
     for (int it = cta_items[blockIdx.x]; it < cta_items[blockIdx.x + 1]; ++it) {
       ItemInfo I;
@@ -773,7 +795,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
         // keys: int8 [page][16][D] -> bf16 (value * scale) in the key layout
         wait(B_KQ_FULL);
         wait(B_KB_EMPTY);
-        for (int u = ct; u < np * kPage * (D / 8); u += 64) {
+        for (int u = lane; u < np * kPage * (D / 8); u += 32) {
           int ch = u % (D / 8), row = (u / (D / 8)) % kPage, pj = u / (kPage * (D / 8));
           const int8_t* src = (const int8_t*)(smem + LY::oKQ) + (pj * kPage + row) * D + ch * 8;
           uint32_t w[4];
@@ -784,12 +806,12 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
               make_uint4(w[0], w[1], w[2], w[3]);
         }
         fence_proxy_async();
-        named_bar(3, 64);
-        if (ct == 0) { mbar_arrive(bar(B_KB_FULL)); mbar_arrive(bar(B_KQ_EMPTY)); }
+        __syncwarp();
+        if (lane == 0) { mbar_arrive(bar(B_KB_FULL)); mbar_arrive(bar(B_KQ_EMPTY)); }
         // values: codes -> level * n / D in the value layout (rotated domain)
         wait(B_VC_FULL);
         wait(B_VL_EMPTY);
-        for (int u = ct; u < np * 2 * (D / 8); u += 64) {
+        for (int u = lane; u < np * 2 * (D / 8); u += 32) {
           int dg = u % (D / 8), tc = (u / (D / 8)) % 2, pj = u / (2 * (D / 8));
           float w8[8];
           uint32_t c8[8];
@@ -820,15 +842,77 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
           }
         }
         fence_proxy_async();
-        named_bar(3, 64);
-        if (ct == 0) { mbar_arrive(bar(B_VL_FULL)); mbar_arrive(bar(B_VC_EMPTY)); }
+        __syncwarp();
+        if (lane == 0) { mbar_arrive(bar(B_VL_FULL)); mbar_arrive(bar(B_VC_EMPTY)); }
       }
     }
-  } else if (warp >= 4) {
-    // ================================================= compute WG ====
-    const int ln = tid - 128;                          // TMEM lane = token / d / row
+  } else if (warp >= 4 && warp < 8) {
+    // ================================================ RoPE warpgroup ====
+    const int ln = tid - 128;                          // TMEM lane = token
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t* TAU = (const uint32_t*)(smem + LY::oTAU);
+    int tile_ctr = 0;
+    for (int it = cta_items[blockIdx.x]; it < cta_items[blockIdx.x + 1]; ++it) {
+      ItemInfo I;
+      load_item(g, p, ws, it, I);
+      const int n_ag = I.n_ag;
+      for (int k = 0; k < I.n_tiles; ++k, ++tile_ctr) {
+        // rotation of this thread's token: tile start (ring) composed with
+        // its offset in the tile
+        const int rb = tile_ctr & 1;
+        wait(B_ROT_FULL0 + rb);
+        uint32_t Cp[D / 4], Sp[D / 4];
+#pragma unroll
+        for (int j = 0; j < D / 4; ++j) {
+          __half2 c0 = as_h2(M.rot[rb][j]), s0 = as_h2(M.rot[rb][32 + j]);
+          __half2 ct = as_h2(TAU[j * 128 + ln]), st = as_h2(TAU[(D / 4 + j) * 128 + ln]);
+          Cp[j] = as_u32(__hfma2(c0, ct, __hneg2(__hmul2(s0, st))));
+          Sp[j] = as_u32(__hfma2(s0, ct, __hmul2(c0, st)));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_ROT_EMPTY0 + rb));
+        // RoPE of each agent's residual keys, written back as f16 pairs
+        for (int a = 0; a < n_ag; ++a) {
+          const int b = a & 1;
+          const uint32_t t_U = tmem + (b ? kTmU1 : kTmU0) + lane_off;
+          wait(B_U_FULL0 + b);
+          tc_fence_after();
+#pragma unroll
+          for (int cb = 0; cb < D / 16; cb += 4) {
+            uint32_t lo[4][8], hi[4][8];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              tmem_ld8(t_U + 8 * (cb + c), lo[c]);
+              tmem_ld8(t_U + D / 2 + 8 * (cb + c), hi[c]);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int ci = cb + c;
+              uint32_t r8[8];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                __half2 xl = __floats2half2_rn(__uint_as_float(lo[c][2 * j]), __uint_as_float(lo[c][2 * j + 1]));
+                __half2 xh = __floats2half2_rn(__uint_as_float(hi[c][2 * j]), __uint_as_float(hi[c][2 * j + 1]));
+                __half2 C = as_h2(Cp[4 * ci + j]), S = as_h2(Sp[4 * ci + j]);
+                r8[j] = as_u32(__hfma2(xl, C, __hneg2(__hmul2(xh, S))));
+                r8[4 + j] = as_u32(__hfma2(xh, C, __hmul2(xl, S)));
+              }
+              tmem_st8(t_U + 8 * ci, r8);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_R_FULL0 + b));
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ============================================= softmax warpgroup ====
+    const int ln = tid - 256;                          // TMEM lane = token / d / row
+    const int sw = warp - 8;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float scale_log2 = 1.4426950408889634f * rsqrtf((float)D);
     for (int it = cta_items[blockIdx.x]; it < cta_items[blockIdx.x + 1]; ++it) {
       ItemInfo I;
@@ -849,12 +933,6 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
           int c = row_cg[ln] / g.G;
           M.row_T[ln] = T;
           M.row_pos[ln] = p.causal ? (T - p.C + c) : 0x7fffffff;
-          int col = 0, rp = 0;
-#pragma unroll
-          for (int a = 0; a < kA; ++a)
-            if (I.call_agent[a] == ci) { col = I.col[a]; rp = I.rp[a]; }
-          M.row_col[ln] = col;
-          M.row_rp[ln] = rp;
         }
       }
       for (int u = ln; u < nrp * (D / 8); u += 128) {
@@ -890,81 +968,22 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
         }
       }
       fence_proxy_async();
-      named_bar(1, 128);
-      if (ln == 0) mbar_arrive(bar(B_Q_FULL));
+      named_bar(2, 128);                 // row tables visible to every softmax warp
+      if (lane == 0) mbar_arrive(bar(B_Q_FULL));
 
       for (int k = 0; k < I.n_tiles; ++k) {
         const int t0 = (I.lp_begin + k * kTilePages) * kPage;
         const int ntok = min(kTileTok, (I.n_pages - k * kTilePages) * kPage);
-        // ---- rotation of the tile start: t0 * theta_i / (2 pi) reduced
-        // exactly as a 64-bit binary fraction, then an accurate sincos
-        if (ln < D / 4) {
-          float cc[2], ssn[2];
-#pragma unroll
-          for (int z = 0; z < 2; ++z) {
-            unsigned long long fr = (unsigned long long)t0 * M.frac[2 * ln + z];
-            float ang = (float)(unsigned int)(fr >> 32) * 1.4629180792671596e-09f;  // 2 pi / 2^32
-            if (ang > 3.14159265f) ang -= 6.28318531f;
-            sincosf(ang, &ssn[z], &cc[z]);
-          }
-          M.rot0[ln] = pack_h2(cc[0], cc[1]);
-          M.rot0[32 + ln] = pack_h2(ssn[0], ssn[1]);
-        }
-        named_bar(1, 128);
-        uint32_t Cp[D / 4], Sp[D / 4];
-#pragma unroll
-        for (int j = 0; j < D / 4; ++j) {
-          __half2 c0 = as_h2(M.rot0[j]), s0 = as_h2(M.rot0[32 + j]);
-          __half2 ct = as_h2(TAU[j * 128 + ln]), st = as_h2(TAU[(D / 4 + j) * 128 + ln]);
-          Cp[j] = as_u32(__hfma2(c0, ct, __hneg2(__hmul2(s0, st))));
-          Sp[j] = as_u32(__hfma2(s0, ct, __hmul2(c0, st)));
-        }
-        // ---- RoPE of each agent's residual keys, written back as f16 pairs
-        for (int a = 0; a < n_ag; ++a) {
-          const int b = a & 1;
-          const uint32_t t_U = tmem + (b ? kTmU1 : kTmU0) + lane_off;
-          wait(B_U_FULL0 + b);
-          tc_fence_after();
-#pragma unroll
-          for (int cb = 0; cb < D / 16; cb += 4) {
-            uint32_t lo[4][8], hi[4][8];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              tmem_ld8(t_U + 8 * (cb + c), lo[c]);
-              tmem_ld8(t_U + D / 2 + 8 * (cb + c), hi[c]);
-            }
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int ci = cb + c;
-              uint32_t r8[8];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                __half2 xl = __floats2half2_rn(__uint_as_float(lo[c][2 * j]), __uint_as_float(lo[c][2 * j + 1]));
-                __half2 xh = __floats2half2_rn(__uint_as_float(hi[c][2 * j]), __uint_as_float(hi[c][2 * j + 1]));
-                __half2 C = as_h2(Cp[4 * ci + j]), S = as_h2(Sp[4 * ci + j]);
-                r8[j] = as_u32(__hfma2(xl, C, __hneg2(__hmul2(xh, S))));
-                r8[4 + j] = as_u32(__hfma2(xh, C, __hmul2(xl, S)));
-              }
-              tmem_st8(t_U + 8 * ci, r8);
-            }
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          named_bar(1, 128);
-          if (ln == 0) mbar_arrive(bar(B_R_FULL0 + b));
-        }
-        // ---- masked online softmax over this tile's 128 tokens, P -> smem
         switch (nrp) {
-          case 16: softmax_tile<16, D, COMP>(smem, M, tmem, lane_off, ln, warp, lane, k, t0, ntok, n_rows, scale_log2, wait, bar(B_S_EMPTY)); break;
-          case 32: softmax_tile<32, D, COMP>(smem, M, tmem, lane_off, ln, warp, lane, k, t0, ntok, n_rows, scale_log2, wait, bar(B_S_EMPTY)); break;
-          case 48: softmax_tile<48, D, COMP>(smem, M, tmem, lane_off, ln, warp, lane, k, t0, ntok, n_rows, scale_log2, wait, bar(B_S_EMPTY)); break;
-          default: softmax_tile<64, D, COMP>(smem, M, tmem, lane_off, ln, warp, lane, k, t0, ntok, n_rows, scale_log2, wait, bar(B_S_EMPTY)); break;
+          case 16: softmax_tile<16, D, COMP>(smem, M, tmem, lane_off, ln, sw, lane, k, t0, ntok, n_rows, scale_log2, wait, bar(B_S_EMPTY)); break;
+          case 32: softmax_tile<32, D, COMP>(smem, M, tmem, lane_off, ln, sw, lane, k, t0, ntok, n_rows, scale_log2, wait, bar(B_S_EMPTY)); break;
+          case 48: softmax_tile<48, D, COMP>(smem, M, tmem, lane_off, ln, sw, lane, k, t0, ntok, n_rows, scale_log2, wait, bar(B_S_EMPTY)); break;
+          default: softmax_tile<64, D, COMP>(smem, M, tmem, lane_off, ln, sw, lane, k, t0, ntok, n_rows, scale_log2, wait, bar(B_S_EMPTY)); break;
         }
         fence_proxy_async();
         tc_fence_before();
-        named_bar(1, 128);
-        if (ln == 0) mbar_arrive(bar(B_P_FULL));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_P_FULL));
       }
       // ---- epilogue: write this item's split partials
       wait(B_PV_DONE);
@@ -1008,8 +1027,8 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
         if (ln < n_rows) part[(int64_t)(I.partial_begin + ln) * PS] = M.m_used[ln];
       }
       tc_fence_before();
-      named_bar(1, 128);
-      if (ln == 0) mbar_arrive(bar(B_ACC_EMPTY));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_ACC_EMPTY));
     }
   }
   // ---- tear-down.  After a timed-out wait, give bulk copies still in
@@ -1025,14 +1044,18 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
 }
 
 // ============================================================ combine ====
-// One warp per output row: merge the row's split partials (log-sum-exp in
-// base 2), apply Bv once to the merged P Lv (LRAgent summary, section 3),
-// rotate back the value sum of a compressed pool (inverse FWHT), normalise.
+// One CTA of D threads per output row: merge the row's split partials
+// (log-sum-exp in base 2), apply Bv once to the merged P Lv (LRAgent
+// summary, section 3), rotate the value sum of a compressed pool back
+// (inverse FWHT), normalise, round to bf16.
 template <int D, bool COMP>
-__global__ void combine_kernel(PoolGeom g, PlanDev p, int layer, uint16_t* __restrict__ out) {
-  const int lane = threadIdx.x & 31;
-  const int row = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
-  if (row >= p.n_out_rows) return;
+__global__ void __launch_bounds__(D) combine_kernel(PoolGeom g, PlanDev p, int layer,
+                                                    uint16_t* __restrict__ out) {
+  // partials are written by the preceding attention grid
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ float sol[kMaxRankPad];
+  __shared__ float sx[D];
+  const int row = blockIdx.x, d = threadIdx.x;
   const uint8_t* ws = g.base + g.off_ws;
   const int32_t* ptr = (const int32_t*)(ws + p.off_csr_ptr);
   const int32_t* slots = (const int32_t*)(ws + p.off_csr_slots);
@@ -1045,50 +1068,42 @@ __global__ void combine_kernel(PoolGeom g, PlanDev p, int layer, uint16_t* __res
   const int h = hq / g.G;
   const int pa = ca[i].pool_agent;
   const AgentDev dv = ag[pa];
-  constexpr int PER = D / 32;
   const int b = ptr[row], e = ptr[row + 1];
   float Mx = -INFINITY;
   for (int k = b; k < e; ++k) Mx = fmaxf(Mx, part[(int64_t)slots[k] * PS]);
-  float L = 0.f, o[PER], ol[2] = {0.f, 0.f};
-  for (int x = 0; x < PER; ++x) o[x] = 0.f;
+  float L = 0.f, o = 0.f, ol = 0.f;
   for (int k = b; k < e; ++k) {
     const float* s = part + (int64_t)slots[k] * PS;
-    float m = s[0];
-    float w = (m == -INFINITY) ? 0.f : exp2f(m - Mx);
+    const float m = s[0];
+    const float w = (m == -INFINITY) ? 0.f : exp2f(m - Mx);
     L += w * s[1];
-    for (int x = 0; x < PER; ++x) o[x] += w * s[4 + lane * PER + x];
-    for (int x = 0; x < 2; ++x)
-      if (2 * lane + x < dv.rp) ol[x] += w * s[4 + D + 2 * lane + x];
+    o += w * s[4 + d];
+    if (d < dv.rp) ol += w * s[4 + D + d];
   }
+  if (d < kMaxRankPad) sol[d] = d < dv.rp ? ol : 0.f;
   if (COMP) {
-    for (int hh = 1; hh < PER; hh <<= 1)
-      for (int x = 0; x < PER; ++x)
-        if (!(x & hh)) { float a0 = o[x], a1 = o[x + hh]; o[x] = a0 + a1; o[x + hh] = a0 - a1; }
-    for (int hl = 1; hl < 32; hl <<= 1)
-      for (int x = 0; x < PER; ++x) {
-        float ot = __shfl_xor_sync(0xffffffffu, o[x], hl);
-        o[x] = (lane & hl) ? (ot - o[x]) : (o[x] + ot);
-      }
+    sx[d] = o;
+    __syncthreads();
+    for (int hh = 1; hh < D; hh <<= 1) {      // unnormalised FWHT, natural order
+      const float a0 = sx[d & ~hh], a1 = sx[d | hh];
+      __syncthreads();
+      sx[d] = (d & hh) ? (a0 - a1) : (a0 + a1);
+      __syncthreads();
+    }
+    o = sx[d];
+  } else {
+    __syncthreads();
   }
   // up-projection of the merged low-rank value sum: (sum_t p_t Lv_t) Bv
   const uint16_t* bv = (const uint16_t*)(g.base + g.off_bv + (int64_t)pa * g.bv_agent_bytes) +
-                       (int64_t)layer * g.rmax_pad * g.H_kv * D + h * D;
-  float up[PER];
-  for (int x = 0; x < PER; ++x) up[x] = 0.f;
+                       (int64_t)layer * g.rmax_pad * g.H_kv * D + h * D + d;
+  float up = 0.f;
   for (int kk = 0; kk < dv.rp; ++kk) {
-    float olk = __shfl_sync(0xffffffffu, ol[kk & 1], kk >> 1);
-    const uint16_t* br = bv + (int64_t)kk * g.H_kv * D + lane * PER;
-    for (int x = 0; x < PER; ++x) {
-      uint16_t u = br[x];
-      up[x] = fmaf(olk, __bfloat162float(*(const __nv_bfloat16*)&u), up[x]);
-    }
+    uint16_t u = bv[(int64_t)kk * g.H_kv * D];
+    up = fmaf(sol[kk], __bfloat162float(*(const __nv_bfloat16*)&u), up);
   }
-  const float inv = 1.f / L;
-  uint16_t* dst = out + (int64_t)row * D + lane * PER;
-  for (int x = 0; x < PER; ++x) {
-    __nv_bfloat16 r = __float2bfloat16_rn((o[x] + dv.s * up[x]) * inv);
-    dst[x] = *(uint16_t*)&r;
-  }
+  __nv_bfloat16 r = __float2bfloat16_rn((o + dv.s * up) / L);
+  out[(int64_t)row * D + d] = *(uint16_t*)&r;
 }
 
 // ============================================================ launchers ==
@@ -1170,8 +1185,34 @@ static int launch_attn_t(const PoolGeom& g, const PlanDev& p, int layer, const u
     e = cudaEventRecord(ev, st);
     if (e != cudaSuccess) return (int)e;
   }
-  combine_kernel<D, COMP><<<(p.n_out_rows + 3) / 4, 128, 0, st>>>(g, p, layer, out);
-  return (int)cudaGetLastError();
+  // the combine may be launched while the attention grid drains; it waits
+  // for that grid inside (programmatic dependent launch)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.n_out_rows);
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, combine_kernel<D, COMP>, g, p, layer, out);
+  return (int)e;
+}
+
+int launch_attention(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q,
+                     uint16_t* out, int compressed, int num_sms, void* stream, int* n_launches,
+                     void* event_after_main) {
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaEvent_t ev = (cudaEvent_t)event_after_main;
+  *n_launches = 2;
+  if (g.d == 128) {
+    return compressed ? launch_attn_t<128, true>(g, p, layer, q, out, num_sms, st, ev)
+                      : launch_attn_t<128, false>(g, p, layer, q, out, num_sms, st, ev);
+  }
+  return compressed ? launch_attn_t<64, true>(g, p, layer, q, out, num_sms, st, ev)
+                    : launch_attn_t<64, false>(g, p, layer, q, out, num_sms, st, ev);
 }
 
 // Scratch of fk_residual_attention_noalloc (work list and split partials of
@@ -1199,18 +1240,5 @@ int noalloc_scratch(void** ptr, size_t* bytes) {
   return 0;
 }
 
-int launch_attention(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q,
-                     uint16_t* out, int compressed, int num_sms, void* stream, int* n_launches,
-                     void* event_after_main) {
-  cudaStream_t st = (cudaStream_t)stream;
-  cudaEvent_t ev = (cudaEvent_t)event_after_main;
-  *n_launches = 2;
-  if (g.d == 128) {
-    return compressed ? launch_attn_t<128, true>(g, p, layer, q, out, num_sms, st, ev)
-                      : launch_attn_t<128, false>(g, p, layer, q, out, num_sms, st, ev);
-  }
-  return compressed ? launch_attn_t<64, true>(g, p, layer, q, out, num_sms, st, ev)
-                    : launch_attn_t<64, false>(g, p, layer, q, out, num_sms, st, ev);
-}
 
 }  // namespace fk
