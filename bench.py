@@ -307,7 +307,7 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
                    "step_bytes": ab["step"]},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic_per_launch(),
-                     "kernel": "attention_kernel<128,false>",
+                     "kernel": "mbuild_kernel<128> + decode_kernel<128,false>",
                      "kernel_ms": statistics.mean(main_ms),
                      "bytes_per_launch": ab["kernel"],
                      "peak_kind": f"{peak_kind} hbm_gbs"},

@@ -1,6 +1,6 @@
 """Build libforkkv.so in-tree with nvcc for sm_103a (no cmake, no torch).
 
-The two translation units compile in parallel; the result lands next to
+The translation units compile in parallel; the result lands next to
 this file, where ``shared_base_kv_gb300`` loads it.
 """
 from __future__ import annotations
@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libforkkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["fk_host.cpp", "fk_kernels.cu"]
+SOURCES = ["fk_host.cpp", "fk_kernels.cu", "fk_decode.cu"]
 
 
 def _nvcc() -> str:

@@ -1,0 +1,965 @@
+// Residual attention for decode-shaped work tiles (four query rows per
+// agent, e.g. one decode query of a GQA group of four heads).
+//
+// The scores of agent a at key position t are (ForkKV guide,
+// "Mathematical Formulation of ResidualAttention")
+//     q . (Kb[t] + s RoPE_t(Lk[t] Bk)) / sqrt(d).
+// RoPE is linear and acts per frequency pair (i, i + d/2), so the residual
+// term regroups as
+//     q . RoPE_t(Lk[t] Bk) = sum_k Lk[t,k] Z[t,(k,g)],
+//     Z[t,(k,g)] = sum_i cos(t th_i) Mc[i,(k,g)] + sin(t th_i) Ms[i,(k,g)],
+//     Mc = q_i Bk[k,i] + q_{i+d/2} Bk[k,i+d/2],
+//     Ms = q_{i+d/2} Bk[k,i] - q_i Bk[k,i+d/2].
+// Z is one dense contraction per 128-key tile, Trig(t) [128 x d] times
+// M [d x 4 r] (M built once per work item from Bk and the queries), run on
+// the tensor cores with N = 4 r; the length-r sum against Lk[t] runs on the
+// CUDA cores next to the softmax.  Compared with rebuilding
+// RoPE(Lk Bk) for every key and agent and contracting it with four query
+// rows, this issues a quarter of the MMA instructions (each N = 16 MMA
+// costs as much tensor-pipe time as an N = 96 one on GB300) and replaces
+// the d-wide RoPE pass by an r-wide dot product.
+//
+// The value residual keeps its factored form (LRAgent summary, section 3):
+// O^T = Vb^T P and OL^T = [Lv | 1]^T P on the tensor cores, Bv applied once
+// per row in the combine.  Partials and the combine are shared with the
+// general kernel.
+//
+// M is built per (agent tile, kv head) by a small preceding grid straight
+// into the workspace in the kernel's shared-memory image (the kernel starts
+// under programmatic dependent launch and waits for that grid only before
+// its first copy of M).
+//
+// Warp roles (352 threads): warp 0 bulk copies, warp 1 MMA issue (converged
+// warp, elect.sync), warp 2 dequantiser of the compressed pool, warps 3-6
+// and 7-10 two compute warpgroups.  Warpgroup w owns query rows 8w .. 8w+7
+// (agents 2w, 2w+1): their Z reduction, online softmax, P and epilogue; it
+// also writes its half of the RoPE frequencies of each Trig tile.  Two warps of identical code per SM
+// sub-partition hide each other's latencies.  A warp reaches TMEM lanes
+// 32 (warp % 4) .. +31, so a thread of TMEM lane 32 (warp % 4) + lane
+// handles the key (or d, or rank) of that lane.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fk_device.cuh"
+#include "fk_internal.h"
+
+namespace fk {
+namespace dec {
+
+constexpr int kThreads = 352;       // 11 warps
+constexpr int kRPA = 4;               // query rows per agent
+constexpr int kRows = 16;             // padded query rows of a tile (<= 4 agents)
+constexpr int kA = kMaxAgentsPerTile;
+constexpr int kMaxZ = kRPA * kMaxRankSum;   // Z columns of a tile: (rank, row) pairs
+constexpr int kZBuf = 128;            // Z columns per TMEM buffer
+constexpr int kPChunk = 144;          // P: 8 keys x 8 rows core matrix, padded
+constexpr int kPRowGroup = 16 * kPChunk;
+constexpr int kLvChunk = 9 * 128;     // Lv^T: 8 rank groups + the ones group
+constexpr int kOnesLane = 64;
+// TMEM columns: base scores, O^T, OL^T (16 rows each), the generator's
+// per-lane rotation table, two Trig stages, two Z buffers
+constexpr uint32_t kTmS = 0, kTmOT = 16, kTmOL = 32, kTmTau = 64, kTmTrig = 128, kTmZ = 256;
+
+template <int D, bool COMP>
+struct Layout {
+  static constexpr int PAGE_B = kPage * D * 2;
+  static constexpr int TILE_B = kTilePages * PAGE_B;
+  static constexpr int NKB = 2;
+  static constexpr int NVB = COMP ? 1 : 2;
+  static constexpr int M_B = (kMaxZ / 8) * (D / 8) * 128;
+  static constexpr int LV_B = 16 * kLvChunk;
+  static constexpr int Q_B = kRows * D * 2;
+  static constexpr int P_B = 2 * kPRowGroup;
+  static constexpr int KQ_B = COMP ? kTilePages * kPage * D : 0;
+  static constexpr int VC_B = COMP ? kTilePages * kPage * (3 * D / 8) : 0;
+  static constexpr int VN_B = COMP ? kTilePages * kPage * 4 : 0;
+  static constexpr int oM = 0;
+  static constexpr int oKB = oM + M_B;
+  static constexpr int oVB = oKB + NKB * TILE_B;   // d = 64: the Vb^T MMA reads 1 KB past a
+  static constexpr int oLV = oVB + NVB * TILE_B;   // stage; the Lv^T MMA reads 896 B past LV
+  static constexpr int oQ = oLV + LV_B;            // (both land in finite data)
+  static constexpr int oP = oQ + Q_B;
+  static constexpr int oKQ = oP + 2 * P_B;
+  static constexpr int oVC = oKQ + KQ_B;
+  static constexpr int oVN = oVC + VC_B;
+  static constexpr int oMISC = (oVN + VN_B + 127) / 128 * 128;
+  static constexpr int MISC_B = 3072;
+  static constexpr int TOTAL = oMISC + MISC_B;
+  static_assert(Q_B >= 1024, "the Lv^T over-read must land in Q");
+};
+
+enum {
+  B_KB_FULL0, B_KB_FULL1, B_KB_EMPTY0, B_KB_EMPTY1, B_VB_FULL0, B_VB_FULL1, B_VB_EMPTY0,
+  B_VB_EMPTY1, B_LV_FULL, B_LV_EMPTY, B_M_FULL, B_M_EMPTY, B_ITEM_FULL, B_TRIG_FULL0, B_TRIG_FULL1, B_S_FULL,
+  B_S_EMPTY, B_Z_FULL0, B_Z_FULL1, B_Z_FREE0, B_Z_FREE1, B_P_FULL0, B_P_FULL1, B_PV_DONE0,
+  B_PV_DONE1, B_ACC_EMPTY, B_KQ_FULL, B_KQ_EMPTY, B_VC_FULL, B_VC_EMPTY, B_FINAL, B_COUNT
+};
+// Arrival counts: 8 = lane 0 of each warp of both compute warpgroups; 1 =
+// one thread, a bulk-copy transaction count or an MMA commit.
+__host__ __device__ constexpr uint32_t bar_count(int i) {
+  return (i == B_ITEM_FULL || i == B_TRIG_FULL0 || i == B_TRIG_FULL1 || i == B_S_EMPTY ||
+          i == B_Z_FREE0 || i == B_Z_FREE1 || i == B_P_FULL0 || i == B_P_FULL1 ||
+          i == B_ACC_EMPTY)
+             ? 8u
+             : 1u;
+}
+constexpr uint64_t kEmptyMask =
+    (1ull << B_KB_EMPTY0) | (1ull << B_KB_EMPTY1) | (1ull << B_VB_EMPTY0) | (1ull << B_VB_EMPTY1) |
+    (1ull << B_LV_EMPTY) | (1ull << B_M_EMPTY) | (1ull << B_S_EMPTY) | (1ull << B_Z_FREE0) | (1ull << B_Z_FREE1) |
+    (1ull << B_ACC_EMPTY) | (1ull << B_KQ_EMPTY) | (1ull << B_VC_EMPTY);
+static_assert(B_COUNT <= 64, "one parity bit per barrier");
+
+struct Misc {
+  uint64_t bar[B_COUNT];
+  uint32_t tmem_base;
+  int abort_flag;
+  float m_used[kRows];
+  float alpha[kRows];
+  float red[4][kRows];
+  int32_t row_lim[kRows];          // key t is visible to row j iff t < row_lim[j]
+  int32_t lim_min[2];              // smallest row_lim of each warpgroup's rows (0: padded rows)
+  float2 rot[2][64];               // cos, sin of t0 * theta_i of a tile (2-tile ring)
+  unsigned long long frac[64];     // theta_i / (2 pi) as a 64-bit binary fraction
+  // per compute warpgroup and 8-rank group j: owning agent (0 or 1 within the
+  // warpgroup) and the address of key t's 8 ranks,
+  // gbase + (t / 8) * gstride + (t % 8) * 16
+  const uint8_t* gbase[2][8];
+  int32_t gstride[2][8];
+  int32_t gagent[2][8];
+};
+static_assert(sizeof(Misc) <= 3072, "Misc must fit its smem slot");
+
+struct Item {
+  int head, n_rows, n_pages, lp_begin, n_ag, partial_begin, row_begin, n_tiles, page_begin,
+      sum_rp;
+  int rp[kA], col[kA], pool_agent[kA];
+  float s[kA];
+  int64_t rc_off[kA];
+};
+
+__device__ __forceinline__ void load_item(const PoolGeom& g, const PlanDev& p, const uint8_t* ws,
+                                          int it, Item& I) {
+  const fk_work_item& w = ((const fk_work_item*)(ws + p.off_items))[it];
+  const int32_t* tile_agents = (const int32_t*)(ws + p.off_tile_agents);
+  const CallAgent* ca = (const CallAgent*)(ws + p.off_call_agents);
+  const AgentDev* ag = (const AgentDev*)(g.base + g.off_agents);
+  I.head = w.head;
+  I.n_rows = w.n_rows;
+  I.n_pages = w.n_pages;
+  I.lp_begin = w.lp_begin;
+  I.n_ag = w.n_agents;
+  I.partial_begin = w.partial_begin;
+  I.row_begin = w.row_begin;
+  I.page_begin = w.page_begin;
+  I.n_tiles = (w.n_pages + kTilePages - 1) / kTilePages;
+  int col = 0;
+#pragma unroll
+  for (int a = 0; a < kA; ++a) {
+    I.rp[a] = 0; I.col[a] = col; I.pool_agent[a] = 0; I.s[a] = 0.f; I.rc_off[a] = 0;
+    if (a < I.n_ag) {
+      const int pa = ca[tile_agents[w.agent_begin + a]].pool_agent;
+      const AgentDev dv = ag[pa];
+      I.pool_agent[a] = pa;
+      I.rp[a] = dv.rp;
+      I.s[a] = dv.s;
+      I.rc_off[a] = dv.rc_off;
+      col += dv.rp;
+    }
+  }
+  I.sum_rp = col;
+}
+
+__device__ __forceinline__ const uint8_t* rc_lk(const PoolGeom& g, const Item& I, int a, int layer) {
+  return g.base + I.rc_off[a] + (int64_t)layer * rc_layer_bytes(g, I.rp[a]);
+}
+
+__device__ __forceinline__ uint32_t* err_word(const PoolGeom& g) {
+  return (uint32_t*)(g.base + g.off_err);
+}
+
+// cos, sin of t * theta_i from the exact product of t with theta_i / 2 pi
+// as a 64-bit fraction (the wrap modulo 2 pi is the integer overflow), so
+// the hardware sine and cosine only ever see arguments in [-pi, pi].
+__device__ __forceinline__ float2 rot_at(unsigned long long frac, int t) {
+  const unsigned long long fr = (unsigned long long)(unsigned)t * frac;
+  float ang = (float)(unsigned int)(fr >> 32) * 1.4629180792671596e-09f;   // 2 pi / 2^32
+  if (ang > 3.14159265f) ang -= 6.28318531f;
+  float sn, cs;
+  __sincosf(ang, &sn, &cs);          // |ang| <= pi: absolute error ~4e-7, far below f16
+  return make_float2(cs, sn);
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+}  // namespace dec
+
+// Online-softmax max update of one compute warpgroup's 8 rows (rare: only
+// when some row's tile max exceeds its running max by more than 2^8): new
+// running maxima, rescale factors, and O^T, OL^T rescaled in TMEM.  Kept out
+// of line so the tile loop stays small.
+static __device__ __noinline__ void raise_max(dec::Misc& M, uint32_t s0, uint32_t s1, uint32_t s2,
+                                              uint32_t s3, uint32_t s4, uint32_t s5, uint32_t s6,
+                                              uint32_t s7, int r0, int sw, int lane, int ln,
+                                              int bar_sync, bool rescale, uint32_t t_ot,
+                                              uint32_t t_ol) {
+  const uint32_t sv[8] = {s0, s1, s2, s3, s4, s5, s6, s7};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float v = __uint_as_float(sv[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (lane == 0) M.red[sw][r0 + j] = v;
+  }
+  named_bar(bar_sync, 128);
+  if (ln < 8) {             // padded rows see only -inf: alpha stays 1
+    const int j = r0 + ln;
+    float al = 1.f;
+    const float cm = fmaxf(fmaxf(M.red[0][j], M.red[1][j]), fmaxf(M.red[2][j], M.red[3][j]));
+    const float mo = M.m_used[j];
+    const float mn = fmaxf(mo, cm);
+    if (mn > mo) { al = (mo == -INFINITY) ? 0.f : exp2f(mo - mn); M.m_used[j] = mn; }
+    M.alpha[j] = al;
+  }
+  named_bar(bar_sync, 128);
+  if (rescale) {
+    tc_fence_after();
+    uint32_t raw[8];
+    tmem_ld8_wait(t_ot, raw);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * M.alpha[r0 + e]);
+    tmem_st8(t_ot, raw);
+    tmem_ld8_wait(t_ol, raw);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * M.alpha[r0 + e]);
+    tmem_st8(t_ol, raw);
+    tmem_wait_st();
+  }
+}
+
+template <int D, bool COMP>
+__global__ void __launch_bounds__(dec::kThreads, 1)
+    decode_kernel(PoolGeom g, PlanDev p, int layer, const uint16_t* __restrict__ q) {
+  using namespace dec;
+  using LY = Layout<D, COMP>;
+  constexpr int NF = D / 2;                  // RoPE frequencies
+  constexpr int SBO_M = (D / 8) * 128;       // M: K-major core matrices, features along K
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Misc& M = *reinterpret_cast<Misc*>(smem + LY::oMISC);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint8_t* ws = g.base + g.off_ws;
+  const int32_t* cta_items = (const int32_t*)(ws + p.off_cta);
+  uint32_t* errw = err_word(g);
+  volatile int* abort_flag = &M.abort_flag;
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) { return smem_u32(&M.bar[i]); };
+  uint64_t ph = kEmptyMask;          // parity each role waits for, bit i for barrier i
+  auto wait = [&](int i) {
+    uint32_t par = (uint32_t)(ph >> i) & 1u;
+    mbar_wait(bar(i), par, abort_flag, errw);
+    ph ^= 1ull << i;
+  };
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  // ---- set-up: zero smem (rows the padded MMAs read stay finite), the
+  // ones row of the Lv^T stage, RoPE fractions, barriers, TMEM.
+  for (int i = tid * 16; i < LY::TOTAL; i += kThreads * 16) *(uint4*)(smem + i) = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  for (int i = tid; i < 16 * 8; i += kThreads)
+    ((uint16_t*)(smem + LY::oLV + (i / 8) * kLvChunk + (kOnesLane / 8) * 128))[i % 8] = 0x3F80;
+  if (tid < 64) M.frac[tid] = ((const unsigned long long*)(g.base + g.off_rope + 256))[tid];
+  if (tid == 0) {
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), bar_count(i));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&M.tmem_base), 512);
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = M.tmem_base;
+  const int it_begin = cta_items[blockIdx.x], it_end = cta_items[blockIdx.x + 1];
+
+  if (warp == 0) {
+    // ============================================ producer (whole warp) ====
+    // every lane waits; lane 0 posts the transaction count; the lanes then
+    // split the tile's bulk copies (one page or one 8-key Lv chunk each)
+    int tc = 0;
+    for (int it = it_begin; it < it_end; ++it) {
+      Item I;
+      load_item(g, p, ws, it, I);
+      const int32_t* pages = (const int32_t*)(ws + p.off_pages) + I.page_begin;
+      // the item's M (built by the preceding grid) once the previous item's
+      // Z MMAs are done with the buffer
+      {
+        const MPair mpr = ((const MPair*)(ws + p.off_mpairs))[((const int32_t*)(ws + p.off_item_mpair))[it]];
+        const uint32_t mbytes = (uint32_t)mpr.zcols * D * 2;
+        wait(B_M_EMPTY);
+        if (it == it_begin) asm volatile("griddepcontrol.wait;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_expect_tx(bar(B_M_FULL), mbytes);
+        __syncwarp();
+        for (uint32_t o = lane * 4096u; o < mbytes; o += 32u * 4096u)
+          bulk_g2s(sbase + LY::oM + o, ws + mpr.mofs + o, min(4096u, mbytes - o), bar(B_M_FULL));
+      }
+      // values of tile k (stage vt % NVB) and the Lv^T stage
+      auto load_values = [&](int k, int vt) {
+        const int p0 = k * kTilePages;
+        const int np = min(kTilePages, I.n_pages - p0);
+        const int t0 = (I.lp_begin + p0) * kPage;
+        if (COMP) {
+          wait(B_VC_EMPTY);
+          __syncwarp();
+          if (lane == 0) mbar_expect_tx(bar(B_VC_FULL), np * kPage * (3 * D / 8 + 4));
+          __syncwarp();
+          if (lane < np) {
+            const int64_t tok = (((int64_t)layer * g.num_pages + pages[p0 + lane]) * g.H_kv + I.head) * kPage;
+            bulk_g2s(sbase + LY::oVC + lane * kPage * (3 * D / 8), g.base + g.off_vc + tok * (3 * D / 8),
+                     kPage * (3 * D / 8), bar(B_VC_FULL));
+            bulk_g2s(sbase + LY::oVN + lane * kPage * 4, g.base + g.off_vn + tok * 4, kPage * 4,
+                     bar(B_VC_FULL));
+          }
+        } else {
+          const int st = vt % LY::NVB;
+          wait(B_VB_EMPTY0 + st);
+          __syncwarp();
+          if (lane == 0) mbar_expect_tx(bar(B_VB_FULL0 + st), np * LY::PAGE_B);
+          __syncwarp();
+          if (lane < np) {
+            const uint8_t* src = g.base + g.off_vb + (int64_t)layer * g.kb_layer_bytes +
+                                 ((int64_t)pages[p0 + lane] * g.H_kv + I.head) * LY::PAGE_B;
+            bulk_g2s(sbase + LY::oVB + st * LY::TILE_B + lane * LY::PAGE_B, src, LY::PAGE_B,
+                     bar(B_VB_FULL0 + st));
+          }
+        }
+        wait(B_LV_EMPTY);
+        const int ntok = min(kTileTok, g.tcap - t0);
+        const int nch = ntok / 8;                 // 8-key chunks
+        __syncwarp();
+        if (lane == 0) {
+          uint32_t bytes = 0;
+#pragma unroll
+          for (int a = 0; a < kA; ++a) bytes += ntok * I.rp[a] * 2;
+          mbar_expect_tx(bar(B_LV_FULL), bytes);
+        }
+        __syncwarp();
+        for (int x = lane; x < I.n_ag * nch; x += 32) {
+          const int ax = x / nch, c = x % nch;
+          const uint8_t* src = nullptr;
+          int cb = 0, cl = 0;
+#pragma unroll
+          for (int a = 0; a < kA; ++a)
+            if (a == ax) {
+              cb = I.rp[a] * 16;                 // one 8-key chunk of this agent's Lv
+              cl = I.col[a];
+              src = rc_lk(g, I, a, layer) + (int64_t)g.tcap * I.rp[a] * 2 + (int64_t)t0 * I.rp[a] * 2;
+            }
+          bulk_g2s(sbase + LY::oLV + c * kLvChunk + (cl / 8) * 128, src + c * cb, cb, bar(B_LV_FULL));
+        }
+      };
+      // keys of tile k, then the values of tile k - 1 (consumed one tile later);
+      // one call site each keeps the warp's loop small
+      const int tc0 = tc;
+      for (int k = 0; k <= I.n_tiles; ++k) {
+        const int p0 = k * kTilePages;
+        const int np = min(kTilePages, I.n_pages - p0);
+        tc = tc0 + k;
+        if (k == I.n_tiles) {
+        } else if (!COMP) {
+          const int st = tc & 1;
+          wait(B_KB_EMPTY0 + st);
+          __syncwarp();
+          if (lane == 0) mbar_expect_tx(bar(B_KB_FULL0 + st), np * LY::PAGE_B);
+          __syncwarp();
+          if (lane < np) {
+            const uint8_t* src = g.base + g.off_kb + (int64_t)layer * g.kb_layer_bytes +
+                                 ((int64_t)pages[p0 + lane] * g.H_kv + I.head) * LY::PAGE_B;
+            bulk_g2s(sbase + LY::oKB + st * LY::TILE_B + lane * LY::PAGE_B, src, LY::PAGE_B,
+                     bar(B_KB_FULL0 + st));
+          }
+        } else {
+          wait(B_KQ_EMPTY);
+          __syncwarp();
+          if (lane == 0) mbar_expect_tx(bar(B_KQ_FULL), np * kPage * D);
+          __syncwarp();
+          if (lane < np) {
+            const uint8_t* src = g.base + g.off_kq +
+                                 ((((int64_t)layer * g.num_pages + pages[p0 + lane]) * g.H_kv + I.head) * kPage) * D;
+            bulk_g2s(sbase + LY::oKQ + lane * kPage * D, src, kPage * D, bar(B_KQ_FULL));
+          }
+        }
+        if (k > 0) load_values(k - 1, tc0 + k - 1);
+      }
+      tc = tc0 + I.n_tiles;
+    }
+  } else if (warp == 1) {
+    // ======================================= MMA issue (converged warp) ====
+    int tc = 0, zq = 0;
+    const uint32_t idS = idesc_f16(128, kRows, 1);
+    for (int it = it_begin; it < it_end; ++it) {
+      Item I;
+      load_item(g, p, ws, it, I);
+      const int zcols = kRPA * I.sum_rp;
+      const int n_zc = (zcols + kZBuf - 1) / kZBuf;
+      wait(B_M_FULL);                    // the item's M
+      wait(B_ITEM_FULL);                 // its Q, row tables
+      tc_fence_after();
+      auto pv = [&](int j, int pt) {
+        const int pb = pt & 1, vs = pt % LY::NVB;
+        wait(B_P_FULL0 + pb);
+        wait(B_VB_FULL0 + vs);
+        wait(B_LV_FULL);
+        if (j == 0) wait(B_ACC_EMPTY);
+        tc_fence_after();
+        __syncwarp();
+        if (elect_one()) {
+          const uint64_t dP = sdesc(sbase + LY::oP + pb * LY::P_B, kPChunk, kPRowGroup);
+          const uint64_t dV = sdesc(sbase + LY::oVB + vs * LY::TILE_B, (D / 8) * 128, 128);
+          const uint64_t dL = sdesc(sbase + LY::oLV, kLvChunk, 128);
+#pragma unroll
+          for (int ks = 0; ks < kTileTok / 16; ++ks) {
+            const uint32_t acc = (j == 0 && ks == 0) ? 0u : 1u;
+            const uint64_t bP = dP + (uint64_t)((ks * 2 * kPChunk) >> 4);
+            mma_ss(tmem + kTmOT, dV + (uint64_t)((ks * LY::PAGE_B) >> 4), bP, idS, acc);
+            mma_ss(tmem + kTmOL, dL + (uint64_t)((ks * 2 * kLvChunk) >> 4), bP, idS, acc);
+          }
+          mma_commit(bar(B_VB_EMPTY0 + vs));
+          mma_commit(bar(B_LV_EMPTY));
+          mma_commit(bar(B_PV_DONE0 + pb));
+        }
+        __syncwarp();
+      };
+      const int tc0 = tc;
+      for (int k = 0; k <= I.n_tiles; ++k) {
+        if (k == I.n_tiles) {
+          if (elect_one()) mma_commit(bar(B_M_EMPTY));   // every Z MMA of the item is issued
+          __syncwarp();
+          pv(k - 1, tc0 + k - 1);
+          break;
+        }
+        tc = tc0 + k;
+        const int kb = tc & 1;
+        wait(B_S_EMPTY);
+        wait(B_KB_FULL0 + kb);
+        tc_fence_after();
+        __syncwarp();
+        if (elect_one()) {
+          const uint64_t dK = sdesc(sbase + LY::oKB + kb * LY::TILE_B, 128, (D / 8) * 128);
+          const uint64_t dQ = sdesc(sbase + LY::oQ, 128, (D / 8) * 128);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_ss(tmem + kTmS, dK + (uint64_t)(ks * 16), dQ + (uint64_t)(ks * 16), idS,
+                   ks > 0 ? 1u : 0u);
+          mma_commit(bar(B_KB_EMPTY0 + kb));
+          mma_commit(bar(B_S_FULL));
+        }
+        __syncwarp();
+        wait(B_TRIG_FULL0 + kb);
+        for (int c = 0; c < n_zc; ++c, ++zq) {
+          const int zb = zq & 1;
+          const int ncol = min(kZBuf, zcols - c * kZBuf);
+          wait(B_Z_FREE0 + zb);
+          tc_fence_after();
+          __syncwarp();
+          if (elect_one()) {
+            const uint32_t idZ = idesc_f16(128, ncol, 0);
+            const uint64_t dM = sdesc(sbase + LY::oM + c * (kZBuf / 8) * SBO_M, 128, SBO_M);
+            const uint32_t tA = tmem + kTmTrig + kb * NF;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+              mma_ts(tmem + kTmZ + zb * kZBuf, tA + 8 * ks, dM + (uint64_t)(ks * 16), idZ,
+                     ks > 0 ? 1u : 0u);
+            mma_commit(bar(B_Z_FULL0 + zb));
+          }
+          __syncwarp();
+        }
+        if (k > 0) pv(k - 1, tc0 + k - 1);
+      }
+      tc = tc0 + I.n_tiles;
+    }
+    if (elect_one()) mma_commit(bar(B_FINAL));
+    __syncwarp();
+    wait(B_FINAL);
+  } else if (COMP && warp == 2) {
+    // ====================================== dequantiser (compressed pool) ====
+    const float kscale = ((const float*)(g.base + g.off_ks))[layer];
+    int tc = 0;
+    for (int it = it_begin; it < it_end; ++it) {
+      Item I;
+      load_item(g, p, ws, it, I);
+      for (int k = 0; k < I.n_tiles; ++k, ++tc) {
+        const int np = min(kTilePages, I.n_pages - k * kTilePages);
+        const int kb = tc & 1, vs = tc % LY::NVB;
+        // keys: int8 [page][16][D] -> bf16 (value * scale) in the key layout
+        wait(B_KQ_FULL);
+        wait(B_KB_EMPTY0 + kb);
+        uint8_t* kdst = smem + LY::oKB + kb * LY::TILE_B;
+        for (int u = lane; u < np * kPage * (D / 8); u += 32) {
+          const int ch = u % (D / 8), row = (u / (D / 8)) % kPage, pj = u / (kPage * (D / 8));
+          const int8_t* src = (const int8_t*)(smem + LY::oKQ) + (pj * kPage + row) * D + ch * 8;
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf2((float)src[2 * e] * kscale, (float)src[2 * e + 1] * kscale);
+          *(uint4*)(kdst + pj * LY::PAGE_B + ((row / 8) * (D / 8) + ch) * 128 + (row % 8) * 16) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) { mbar_arrive(bar(B_KB_FULL0 + kb)); mbar_arrive(bar(B_KQ_EMPTY)); }
+        // values: codes -> level * norm / D in the value layout (rotated domain)
+        wait(B_VC_FULL);
+        wait(B_VB_EMPTY0 + vs);
+        uint8_t* vdst = smem + LY::oVB + vs * LY::TILE_B;
+        for (int u = lane; u < np * 2 * (D / 8); u += 32) {
+          const int dg = u % (D / 8), tcn = (u / (D / 8)) % 2, pj = u / (2 * (D / 8));
+          float w8[8];
+          uint32_t c8[8];
+#pragma unroll
+          for (int tt = 0; tt < 8; ++tt) {
+            const int row = tcn * 8 + tt;
+            const uint8_t* cb = smem + LY::oVC + (pj * kPage + row) * (3 * D / 8);
+            const uint32_t b0 = cb[dg], b1 = cb[D / 8 + dg], b2 = cb[2 * (D / 8) + dg];
+            c8[tt] = b0 | (b1 << 8) | (b2 << 16);
+            w8[tt] = ((const float*)(smem + LY::oVN))[pj * kPage + row] * (1.0f / D);
+          }
+          uint8_t* dst = vdst + pj * LY::PAGE_B + (tcn * (D / 8) + dg) * 128;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {   // d = 8 dg + e
+            uint32_t w[4];
+#pragma unroll
+            for (int h2 = 0; h2 < 4; ++h2) {
+              float v2[2];
+#pragma unroll
+              for (int z = 0; z < 2; ++z) {
+                const uint32_t cc = c8[2 * h2 + z];
+                const uint32_t code = ((cc >> e) & 1u) | (((cc >> (8 + e)) & 1u) << 1) |
+                                      (((cc >> (16 + e)) & 1u) << 2);
+                v2[z] = c_lloyd[code] * w8[2 * h2 + z];
+              }
+              w[h2] = pack_bf2(v2[0], v2[1]);
+            }
+            *(uint4*)(dst + e * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) { mbar_arrive(bar(B_VB_FULL0 + vs)); mbar_arrive(bar(B_VC_EMPTY)); }
+      }
+    }
+  } else if (warp >= 3) {
+    // ============================================ compute warpgroups ====
+    constexpr int NFH = NF / 2;                      // RoPE frequencies per warpgroup
+    const int cw = (warp - 3) >> 2;                  // warpgroup 0 or 1
+    const int ln = 32 * (warp & 3) + lane;           // TMEM lane = key / d / rank
+    const int sw = warp & 3;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const int bar_sync = 1 + 2 * cw, bar_or = 2 + 2 * cw;   // this warpgroup's named barriers
+    const int r0 = 8 * cw;                           // first query row of this warpgroup
+    const int f0 = NFH * cw;                         // first frequency of this warpgroup
+    const float scale_log2 = 1.4426950408889634f * rsqrtf((float)D);
+    const int32_t* row_agent_all = (const int32_t*)(ws + p.off_row_agent);
+    const int32_t* row_cg_all = (const int32_t*)(ws + p.off_row_cg);
+    const CallAgent* ca = (const CallAgent*)(ws + p.off_call_agents);
+    // rotation of this lane's key offset tau = ln within a tile, for this
+    // warpgroup's frequencies: f16 pairs kept in TMEM
+#pragma unroll 1
+    for (int c0 = 0; c0 < NFH; c0 += 16) {
+      uint32_t w[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float2 r = rot_at(M.frac[f0 + c0 + e], ln);
+        w[e] = pack_h2(r.x, r.y);
+      }
+      tmem_st16(tmem + kTmTau + f0 + c0 + lane_off, w);
+    }
+    tmem_wait_st();
+    // Trig of the tile at keys t0 .. t0 + 127 into stage b: column i holds
+    // [cos, sin]((t0 + lane) theta_i) as an f16 pair
+    auto make_trig = [&](int t0, int b) {
+      if (ln < NFH) M.rot[b][f0 + ln] = rot_at(M.frac[f0 + ln], t0);
+      named_bar(bar_sync, 128);
+#pragma unroll 1
+      for (int c0 = 0; c0 < NFH; c0 += 16) {
+        uint32_t w[16];
+        tmem_ld16_wait(tmem + kTmTau + f0 + c0 + lane_off, w);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float2 rb = M.rot[b][f0 + c0 + e];
+          const float2 rt = __half22float2(as_h2(w[e]));
+          w[e] = pack_h2(rb.x * rt.x - rb.y * rt.y, rb.y * rt.x + rb.x * rt.y);
+        }
+        tmem_st16(tmem + kTmTrig + b * NF + f0 + c0 + lane_off, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_TRIG_FULL0 + b));
+    };
+    int tc = 0, zq = 0, pv_seen = 0;
+    // The value MMAs of tile j signal PV_DONE[j & 1].  They are awaited
+    // lazily (P of tile j reuses the buffer of tile j - 2), so with a single
+    // barrier its phase could run two ahead of the waiter, which parity
+    // waits cannot tell from zero; alternating barriers stay within one.
+    auto pv_until = [&](int n) {
+      while (pv_seen < n) { wait(B_PV_DONE0 + (pv_seen & 1)); ++pv_seen; }
+    };
+    for (int it = it_begin; it < it_end; ++it) {
+      int n_tiles, lp_begin, n_pages, n_zc, g_lo, g_hi;
+      // ---- item set-up.  Every MMA that read the previous item's Q and
+      // Trig stages has completed (this warpgroup waited for all of them),
+      // so those buffers are free without a barrier of their own.
+      named_bar(bar_sync, 128);                 // this warpgroup is done with the tables
+      {
+        Item I;
+        load_item(g, p, ws, it, I);
+        const int n_rows = I.n_rows, n_ag = I.n_ag;
+        n_tiles = I.n_tiles;
+        lp_begin = I.lp_begin;
+        n_pages = I.n_pages;
+        n_zc = (kRPA * I.sum_rp + kZBuf - 1) / kZBuf;
+        // (an unrolled select: indexing the record by the runtime warpgroup
+        // number would move it to local memory)
+        const int c_lo = cw ? I.col[2] : I.col[0], c_hi = cw ? I.sum_rp : I.col[2];
+        g_lo = c_lo / 8;
+        g_hi = c_hi / 8;
+        const int32_t* row_agent = row_agent_all + I.row_begin;
+        const int32_t* row_cg = row_cg_all + I.row_begin;
+        // rows: limits and running maxima
+        if (ln < 8) {
+          const int j = r0 + ln;
+          M.m_used[j] = -INFINITY;
+          int lim = 0;
+          if (j < n_rows) {
+            const int T = ca[row_agent[j]].seq_len;
+            lim = p.causal ? min(T, T - p.C + row_cg[j] / g.G + 1) : T;
+          }
+          M.row_lim[j] = lim;
+        }
+        if (ln == 0) {
+          int mn = 0x7fffffff;
+          for (int j = r0; j < r0 + 8; ++j) {
+            if (j >= n_rows) { mn = 0; break; }     // padded rows must stay masked
+            const int T = ca[row_agent[j]].seq_len;
+            mn = min(mn, p.causal ? min(T, T - p.C + row_cg[j] / g.G + 1) : T);
+          }
+          M.lim_min[cw] = mn;
+        }
+        // Lk group tables of this warpgroup's agents
+        if (ln < 8) {
+          const int j = ln;
+          int aj = 0;
+#pragma unroll
+          for (int a = 1; a < kA; ++a)
+            if (a < n_ag && 8 * j >= I.col[a]) aj = a;
+          M.gagent[cw][j] = aj - 2 * cw;
+          M.gbase[cw][j] = nullptr;
+          M.gstride[cw][j] = 0;
+#pragma unroll
+          for (int a = 0; a < kA; ++a)
+            if (a == aj && j >= g_lo && j < g_hi) {
+              M.gbase[cw][j] = rc_lk(g, I, a, layer) + (int64_t)((8 * j - I.col[a]) / 8) * 128;
+              M.gstride[cw][j] = I.rp[a] * 16;
+            }
+        }
+        // Q rows r0 .. r0 + 7 (bf16, B operand of the base scores)
+        for (int u = ln; u < 8 * (D / 8); u += 128) {
+          const int row = r0 + u / (D / 8), ch = u % (D / 8);
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (row < n_rows) {
+            const int ci = row_agent[row], cg = row_cg[row];
+            const int64_t qrow = ((int64_t)ci * p.C + cg / g.G) * g.H_q + I.head * g.G + cg % g.G;
+            v = *(const uint4*)(q + qrow * D + ch * 8);
+          }
+          *(uint4*)(smem + LY::oQ + ((row / 8) * (D / 8) + ch) * 128 + (row % 8) * 16) = v;
+        }
+        fence_proxy_async();
+        named_bar(bar_sync, 128);               // tables visible to the whole warpgroup
+        if (lane == 0) mbar_arrive(bar(B_ITEM_FULL));
+      }
+      // Lk of this thread's key: prefetched into L1 a tile ahead and loaded
+      // once the tile's base scores are read
+      uint4 lkA[4], lkB[4];            // rank groups 0-3 and 4-7 (two arrays: the chunk
+                                       // select below stays a register select)
+      auto lk_ok = [&](int k) { return (lp_begin + k * kTilePages) * kPage + ln < g.tcap; };
+      auto lk_addr = [&](int k, int j) {
+        const int t = (lp_begin + k * kTilePages) * kPage + ln;
+        return (const uint4*)(M.gbase[cw][j] + (int64_t)(t / 8) * M.gstride[cw][j] + (t % 8) * 16);
+      };
+      auto prefetch_lk = [&](int k) {
+        if (lk_ok(k)) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (j >= g_lo && j < g_hi) asm volatile("prefetch.global.L1 [%0];" ::"l"(lk_addr(k, j)));
+        }
+      };
+      prefetch_lk(0);
+
+      for (int k = 0; k < n_tiles; ++k, ++tc) {
+        const int t0 = (lp_begin + k * kTilePages) * kPage;
+        const int ntok = min(kTileTok, (n_pages - k * kTilePages) * kPage);
+        // base scores of rows r0 .. r0 + 7
+        uint32_t sv[8];
+        wait(B_S_FULL);
+        tc_fence_after();
+        tmem_ld8_wait(tmem + kTmS + r0 + lane_off, sv);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_S_EMPTY));
+        // Trig of the next tile (and of this one at the item's first tile),
+        // into the stage whose previous reader, Z(k - 1), this warpgroup has
+        // already waited for.  The MMA warp needs Trig(k + 1) only after its
+        // value MMAs of tile k, which wait for this tile's P anyway.
+#pragma unroll 1
+        for (int kt = (k == 0 ? 0 : k + 1); kt <= k + 1 && kt < n_tiles; ++kt)
+          make_trig((lp_begin + kt * kTilePages) * kPage, (tc + kt - k) & 1);
+        {
+          const bool ok = lk_ok(k);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            lkA[j] = lkB[j] = make_uint4(0, 0, 0, 0);
+            if (j >= g_lo && j < g_hi && ok) lkA[j] = __ldg(lk_addr(k, j));
+            if (j + 4 >= g_lo && j + 4 < g_hi && ok) lkB[j] = __ldg(lk_addr(k, j + 4));
+          }
+        }
+        // residual scores: acc[4 la + g] = sum_k Lk[t,k] Z[t,(col + k) * 4 + g]
+        // for local agent la of this warpgroup
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < n_zc; ++c, ++zq) {
+          const int zb = zq & 1;
+          wait(B_Z_FULL0 + zb);
+          tc_fence_after();
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = 4 * c + u;      // 8-rank group of these 32 columns
+            if (j >= g_lo && j < g_hi) {
+              const uint4 L = c ? lkB[u] : lkA[u];
+              const uint32_t lw[4] = {L.x, L.y, L.z, L.w};
+              float t4[kRPA] = {0.f, 0.f, 0.f, 0.f};
+              uint32_t v[32];
+              tmem_ld32_wait(tmem + kTmZ + zb * kZBuf + 32 * u + lane_off, v);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float l = (e & 1) ? bf_hi(lw[e / 2]) : bf_lo(lw[e / 2]);
+                ffma2(t4[0], t4[1], l, l, __uint_as_float(v[e * kRPA]), __uint_as_float(v[e * kRPA + 1]));
+                ffma2(t4[2], t4[3], l, l, __uint_as_float(v[e * kRPA + 2]), __uint_as_float(v[e * kRPA + 3]));
+              }
+              if (M.gagent[cw][j] == 0) {
+#pragma unroll
+                for (int gq = 0; gq < kRPA; ++gq) acc[gq] += t4[gq];
+              } else {
+#pragma unroll
+                for (int gq = 0; gq < kRPA; ++gq) acc[kRPA + gq] += t4[gq];
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_Z_FREE0 + zb));
+        }
+        if (k + 1 < n_tiles) prefetch_lk(k + 1);
+        // ---- online softmax (base 2); the running max of a row moves only
+        // when the tile max exceeds it by more than 2^8 (then O^T, OL^T are
+        // rescaled in TMEM)
+        bool need = false;
+        if (ntok == kTileTok && t0 + kTileTok <= M.lim_min[cw]) {
+          // every key of the tile is visible to every row of this warpgroup
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float s = (__uint_as_float(sv[j]) + acc[j]) * scale_log2;
+            sv[j] = __float_as_uint(s);
+            need |= s > M.m_used[r0 + j] + 8.f;
+          }
+        } else {
+          const int tabs = t0 + ln;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const bool ok = ln < ntok && tabs < M.row_lim[r0 + j];
+            const float s = ok ? (__uint_as_float(sv[j]) + acc[j]) * scale_log2 : -INFINITY;
+            sv[j] = __float_as_uint(s);
+            need |= s > M.m_used[r0 + j] + 8.f;
+          }
+        }
+        int any;
+        asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, %2, 128, p; selp.u32 %0, 1, 0, q; }"
+                     : "=r"(any) : "r"((int)need), "r"(bar_or));
+        if (any) {
+          if (k > 0) pv_until(tc);           // O^T, OL^T hold every earlier tile
+          raise_max(M, sv[0], sv[1], sv[2], sv[3], sv[4], sv[5], sv[6], sv[7], r0, sw, lane, ln,
+                    bar_sync, k > 0, tmem + kTmOT + r0 + lane_off, tmem + kTmOL + r0 + lane_off);
+        }
+        // P of this tile into buffer tc & 1 (its previous reader is PV(tc - 2))
+        pv_until(tc - 1);
+        uint8_t* prow = smem + LY::oP + (tc & 1) * LY::P_B + cw * kPRowGroup + (ln / 8) * kPChunk + (ln % 8) * 2;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float m = M.m_used[r0 + j];
+          const float pv = exp2f(__uint_as_float(sv[j]) - (m == -INFINITY ? 0.f : m));
+          *(__nv_bfloat16*)(prow + j * 16) = __float2bfloat16_rn(pv);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_P_FULL0 + (tc & 1)));
+      }
+      // ---- epilogue: this warpgroup's rows of the item's split partials
+      pv_until(tc);
+      tc_fence_after();
+      {
+        Item I;
+        load_item(g, p, ws, it, I);
+        const int n_rows = I.n_rows, n_ag = I.n_ag;
+        float* part = (float*)(ws + p.off_partials);
+        const int PS = p.partial_stride;
+        uint32_t raw[8];
+        tmem_ld8_wait(tmem + kTmOT + r0 + lane_off, raw);
+        if (ln < D) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (r0 + e < n_rows) part[(int64_t)(I.partial_begin + r0 + e) * PS + 4 + ln] = __uint_as_float(raw[e]);
+        }
+        // OL^T lane ln: rank ln - col of the agent whose columns hold ln
+        // (that agent's rows take it), or the row sums on the ones lane
+        int oa = -1, orr = 0;
+#pragma unroll
+        for (int a = 0; a < kA; ++a)
+          if (a < n_ag && ln >= I.col[a] && ln < I.col[a] + I.rp[a]) { oa = a; orr = ln - I.col[a]; }
+        tmem_ld8_wait(tmem + kTmOL + r0 + lane_off, raw);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int row = r0 + e;
+          if (row < n_rows) {
+            float* dst = part + (int64_t)(I.partial_begin + row) * PS;
+            if (ln == kOnesLane) dst[1] = __uint_as_float(raw[e]);
+            if (oa >= 0 && row / kRPA == oa) dst[4 + D + orr] = __uint_as_float(raw[e]);
+          }
+        }
+        if (ln < 8 && r0 + ln < n_rows) part[(int64_t)(I.partial_begin + r0 + ln) * PS] = M.m_used[r0 + ln];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_ACC_EMPTY));
+    }
+  }
+  // ---- tear-down.  After a timed-out wait, give bulk copies still in
+  // flight a bounded grace period before the CTA's smem is released.
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (*abort_flag) {
+    long long t0 = clock64();
+    while (clock64() - t0 < 20000000LL) { }
+  }
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ============================================================= M build ==
+// M of one (agent tile, kv head) pair, in the decode kernel's shared-memory
+// image: column n = (col[a] + k) * 4 + row-in-agent, K-major core matrices
+// of 8 columns x 8 features, feature 2i the cos part, 2i + 1 the sin part,
+// times s_a.  One thread per unit = (8-rank group j, row gq of the agent,
+// frequency i): two 16-byte loads of Bk (ranks 8j.. of features i and
+// i + d/2), two query elements, eight f16 pairs out.
+template <int D>
+__global__ void __launch_bounds__(256) mbuild_kernel(PoolGeom g, PlanDev p, int layer,
+                                                     const uint16_t* __restrict__ q) {
+  using namespace dec;
+  constexpr int NF = D / 2;
+  // the decode grid may be scheduled now; it waits for this grid's
+  // completion before reading M
+  asm volatile("griddepcontrol.launch_dependents;");
+  const uint8_t* ws = g.base + g.off_ws;
+  const MPair mp = ((const MPair*)(ws + p.off_mpairs))[blockIdx.y];
+  const int32_t* tile_agents = (const int32_t*)(ws + p.off_tile_agents);
+  const CallAgent* ca = (const CallAgent*)(ws + p.off_call_agents);
+  const AgentDev* ag = (const AgentDev*)(g.base + g.off_agents);
+  const int32_t* row_agent = (const int32_t*)(ws + p.off_row_agent) + mp.row_begin;
+  const int32_t* row_cg = (const int32_t*)(ws + p.off_row_cg) + mp.row_begin;
+  const int u = blockIdx.x * blockDim.x + threadIdx.x;
+  const int n_units = (mp.zcols / kRPA / 8) * kRPA * NF;
+  if (u >= n_units) return;
+  const int i = u % NF, gq = (u / NF) % kRPA, j = u / (NF * kRPA);
+  // owning agent of rank group j
+  int col = 0, ai = 0, rp = 0, pa = 0;
+  float sa = 0.f;
+  for (int a = 0; a < mp.n_agents; ++a) {
+    const int pa_a = ca[tile_agents[mp.agent_begin + a]].pool_agent;
+    const AgentDev dv = ag[pa_a];
+    if (8 * j >= col && 8 * j < col + dv.rp) { ai = a; rp = dv.rp; pa = pa_a; sa = dv.s; break; }
+    col += dv.rp;
+  }
+  const int row = ai * kRPA + gq;
+  const int ci = row_agent[row], cg = row_cg[row];
+  const int64_t qrow = ((int64_t)ci * p.C + cg / g.G) * g.H_q + mp.head * g.G + cg % g.G;
+  const __nv_bfloat16* qp = (const __nv_bfloat16*)(q + qrow * D);
+  const __nv_bfloat16* bk = (const __nv_bfloat16*)(g.base + g.off_bk + (int64_t)pa * g.bk_agent_bytes) +
+                            ((int64_t)layer * g.H_kv + mp.head) * (int64_t)D * g.rmax_pad;
+  const int RC = rp / 8, kc = (8 * j - col) / 8, i1 = i + NF;
+  const float x0 = sa * __bfloat162float(qp[i]), x1 = sa * __bfloat162float(qp[i1]);
+  const uint4 b0 = *(const uint4*)(bk + ((i / 8) * RC + kc) * 64 + (i % 8) * 8);
+  const uint4 b1 = *(const uint4*)(bk + ((i1 / 8) * RC + kc) * 64 + (i1 % 8) * 8);
+  const uint32_t w0[4] = {b0.x, b0.y, b0.z, b0.w}, w1[4] = {b1.x, b1.y, b1.z, b1.w};
+  uint8_t* M = (uint8_t*)ws + mp.mofs;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    // column n = (8 j + e) * 4 + gq: group n / 8 = 4 j + e / 2, row n % 8 =
+    // 4 (e % 2) + gq; features 2i, 2i + 1
+    const float bi = (e & 1) ? bf_hi(w0[e / 2]) : bf_lo(w0[e / 2]);
+    const float bh = (e & 1) ? bf_hi(w1[e / 2]) : bf_lo(w1[e / 2]);
+    *(uint32_t*)(M + ((4 * j + e / 2) * (D / 8) + i / 4) * 128 + (4 * (e & 1) + gq) * 16 + (i % 4) * 4) =
+        pack_h2(x0 * bi + x1 * bh, x1 * bi - x0 * bh);
+  }
+}
+
+// ============================================================ launcher ==
+
+template <int D, bool COMP>
+static int launch_decode_t(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q,
+                           cudaStream_t st) {
+  using LY = dec::Layout<D, COMP>;
+  static_assert(LY::TOTAL <= 232448, "shared memory over the 227 KB a CTA may use");
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, COMP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL);
+    if (e != cudaSuccess) return (int)e;
+    attr_done = true;
+  }
+  constexpr int units = 8 * dec::kRPA * (D / 2);      // most units of a pair (sum of ranks 64)
+  mbuild_kernel<D><<<dim3((units + 255) / 256, p.n_mpairs), 256, 0, st>>>(g, p, layer, q);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return (int)e;
+  // programmatic dependent launch: the decode grid's set-up overlaps the M
+  // build; it waits for that grid before its first copy of M
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.n_ctas);
+  cfg.blockDim = dim3(dec::kThreads);
+  cfg.dynamicSmemBytes = LY::TOTAL;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, decode_kernel<D, COMP>, g, p, layer, q);
+}
+
+bool decode_applies(const PoolGeom& g, const PlanDev& p) {
+  return g.G * p.C == dec::kRPA && (g.d == 64 || g.d == 128);
+}
+
+int launch_decode(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q,
+                  int compressed, void* stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  if (g.d == 128)
+    return compressed ? launch_decode_t<128, true>(g, p, layer, q, st)
+                      : launch_decode_t<128, false>(g, p, layer, q, st);
+  return compressed ? launch_decode_t<64, true>(g, p, layer, q, st)
+                    : launch_decode_t<64, false>(g, p, layer, q, st);
+}
+
+}  // namespace fk

@@ -11,6 +11,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// Lloyd-Max centroids of N(0,1) at 3 bits (8 levels, ascending), the value
+// codebook of the compressed pool (PolyKV summary, section 2B).  One copy
+// per translation unit.
+static __constant__ float c_lloyd[8] = {-2.1520f, -1.3439f, -0.7560f, -0.2451f,
+                                        0.2451f,  0.7560f,  1.3439f,  2.1520f};
+
 // ---------------------------------------------------------- mbarriers --
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
@@ -38,24 +44,34 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait: gives up after ~2 s of clock (or at once if the CTA has
-// already given up), records the failure in the pool's error word and in
-// the CTA's abort flag, and returns false.  Callers carry on without
-// touching the data, so every role reaches the end of the kernel.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t& parity,
-                                          volatile int* abort_flag,
-                                          uint32_t* err_word) {
-  if (mbar_try(bar, parity)) { parity ^= 1u; return true; }
+// already given up), records the failure in the pool's error words (count
+// in word 1; the first give-up's warp and barrier smem address in word 2)
+// and in the CTA's abort flag, and returns false.  Callers carry on
+// without touching the data, so every role reaches the end of the kernel.
+// Only the first test is inlined at each call site; the polling loop is out
+// of line, which keeps the warp-specialised kernels' hot loops small enough
+// for the instruction cache.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                   volatile int* abort_flag, uint32_t* err_word) {
   long long t0 = clock64();
   while (true) {
-    if (*abort_flag) { parity ^= 1u; return false; }
-    if (mbar_try(bar, parity)) { parity ^= 1u; return true; }
+    if (*abort_flag) return false;
+    if (mbar_try(bar, parity)) return true;
     if (clock64() - t0 > 4000000000LL) {
       *abort_flag = 1;
       atomicAdd(err_word + 1, 1u);
-      parity ^= 1u;
+      atomicCAS(err_word + 2, 0u, 0x80000000u | ((threadIdx.x >> 5) << 20) | (bar & 0xFFFFFu));
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t& parity,
+                                          volatile int* abort_flag,
+                                          uint32_t* err_word) {
+  const uint32_t par = parity;
+  parity ^= 1u;
+  if (mbar_try(bar, par)) return true;
+  return mbar_wait_slow(bar, par, abort_flag, err_word);
 }
 
 // ------------------------------------------------------- bulk copies --
@@ -155,11 +171,91 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
       "r"(v[15]));
 }
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31]));
+}
+// Load and wait in one statement, so no use of the registers can be
+// scheduled between the load and its completion.
+__device__ __forceinline__ void tmem_ld8_wait(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+// Packed fp32 FMA on two lanes of a 64-bit pair: d = a * b + c elementwise.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0,
+                                      float b1) {
+  uint64_t d = ((uint64_t)__float_as_uint(d1) << 32) | __float_as_uint(d0);
+  const uint64_t a = ((uint64_t)__float_as_uint(a1) << 32) | __float_as_uint(a0);
+  const uint64_t b = ((uint64_t)__float_as_uint(b1) << 32) | __float_as_uint(b0);
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+  d0 = __uint_as_float((uint32_t)d);
+  d1 = __uint_as_float((uint32_t)(d >> 32));
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// One lane of a converged warp (the lowest active one) gets true.  MMA
+// issue from a converged warp through elect.sync keeps the operands
+// warp-uniform and measured ~40% cheaper per small MMA on GB300 than issue
+// from a thread that branched away from its warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p = 0;
+  asm volatile("{ .reg .b32 r; .reg .pred q; elect.sync r|q, 0xffffffff; selp.u32 %0, 1, 0, q; }"
+               : "=r"(p));
+  return p != 0;
 }
 
 // Named barrier over `n` threads (ids 1..15; 0 is __syncthreads).

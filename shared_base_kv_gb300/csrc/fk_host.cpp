@@ -35,6 +35,8 @@ struct HostPlan {
   std::vector<int32_t> csr_ptr, csr_slots;
   std::vector<int32_t> cta_begin;   // items [cta_begin[c], cta_begin[c+1]) run on CTA c
   int n_partials = 0;
+  std::vector<MPair> mpairs;        // decode-shaped calls only (4 query rows per agent)
+  std::vector<int32_t> item_mpair;
 };
 
 // Pinned host staging buffer for small host->device uploads.  A new upload
@@ -338,6 +340,26 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
     }
   }
   pl.cta_begin[n_ctas] = (int)pl.items.size();
+  // 4b. decode-shaped calls: one query-side RoPE matrix per (agent tile,
+  // kv head), shared by the items that split that tile's pages
+  if (rpa == 4) {
+    std::map<std::pair<int32_t, int32_t>, int32_t> idx;
+    for (auto& it : pl.items) {
+      auto key = std::make_pair(it.agent_begin, it.head);
+      auto f = idx.find(key);
+      if (f == idx.end()) {
+        MPair m{};
+        m.head = it.head;
+        m.agent_begin = it.agent_begin;
+        m.n_agents = it.n_agents;
+        m.row_begin = it.row_begin;
+        m.zcols = rpa * it.sum_rank;
+        f = idx.emplace(key, (int32_t)pl.mpairs.size()).first;
+        pl.mpairs.push_back(m);
+      }
+      pl.item_mpair.push_back(f->second);
+    }
+  }
   // 5. combine lists: output row (i, c, hq) -> partial slots
   const int n_out = A * C * H_q;
   std::vector<int32_t> cnt(n_out + 1, 0);
@@ -359,6 +381,57 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
     for (int j = 0; j < it.n_rows; ++j) pl.csr_slots[pos[out_row(it, j)]++] = it.partial_begin + j;
   out = std::move(pl);
   return FK_OK;
+}
+
+// Pack a work list into the workspace image: the plan arrays, then the
+// split partials, then the decode kernel's M matrices.  Returns the bytes of
+// workspace the call needs (blob covers the plan arrays only).
+int64_t pack_plan(const HostPlan& pl, int A, int C, int causal, const int32_t* agents,
+                  const int32_t* seq, const PoolGeom& g, std::vector<uint8_t>& blob,
+                  PlanDev& pd) {
+  pd = PlanDev{};
+  pd.n_items = (int)pl.items.size();
+  pd.n_rows = (int)pl.row_agent.size();
+  pd.n_pages = (int)pl.pages.size();
+  pd.n_tile_agents = (int)pl.tile_agents.size();
+  pd.A = A; pd.C = C; pd.causal = causal ? 1 : 0;
+  pd.n_out_rows = A * C * g.H_q;
+  pd.n_partials = pl.n_partials;
+  pd.partial_stride = g.d + g.rmax_pad + 4;
+  blob.clear();
+  auto put = [&](const void* src, size_t bytes) {
+    int64_t o = align_up((int64_t)blob.size(), 256);
+    blob.resize(o + bytes);
+    if (bytes) std::memcpy(blob.data() + o, src, bytes);
+    return o;
+  };
+  std::vector<CallAgent> ca(A);
+  for (int i = 0; i < A; ++i) ca[i] = CallAgent{agents[i], seq[i]};
+  pd.off_items = put(pl.items.data(), pl.items.size() * sizeof(fk_work_item));
+  pd.off_row_agent = put(pl.row_agent.data(), pl.row_agent.size() * 4);
+  pd.off_row_cg = put(pl.row_cg.data(), pl.row_cg.size() * 4);
+  pd.off_pages = put(pl.pages.data(), pl.pages.size() * 4);
+  pd.off_tile_agents = put(pl.tile_agents.data(), pl.tile_agents.size() * 4);
+  pd.off_call_agents = put(ca.data(), ca.size() * sizeof(CallAgent));
+  pd.off_csr_ptr = put(pl.csr_ptr.data(), pl.csr_ptr.size() * 4);
+  pd.off_csr_slots = put(pl.csr_slots.data(), pl.csr_slots.size() * 4);
+  pd.off_cta = put(pl.cta_begin.data(), pl.cta_begin.size() * 4);
+  pd.n_ctas = (int)pl.cta_begin.size() - 1;
+  // M offsets are known only once the partials are placed: reserve the
+  // pair table, fill it below
+  std::vector<MPair> mp = pl.mpairs;
+  pd.n_mpairs = (int)mp.size();
+  pd.off_mpairs = put(mp.data(), mp.size() * sizeof(MPair));
+  pd.off_item_mpair = put(pl.item_mpair.data(), pl.item_mpair.size() * 4);
+  pd.off_partials = align_up((int64_t)blob.size(), 256);
+  int64_t need = pd.off_partials + (int64_t)pd.n_partials * pd.partial_stride * 4;
+  need = align_up(need, 1024);
+  for (auto& m : mp) {
+    m.mofs = need;
+    need += align_up((int64_t)m.zcols * g.d * 2, 1024);
+  }
+  if (!mp.empty()) std::memcpy(blob.data() + pd.off_mpairs, mp.data(), mp.size() * sizeof(MPair));
+  return need;
 }
 
 }  // namespace
@@ -786,35 +859,8 @@ fk_status fk_residual_attention(fk_pool* p, int layer, const uint16_t* q, const 
     if (s != FK_OK) return s;
     // pack into the workspace
     PlanDev pd{};
-    pd.n_items = (int)pl.items.size();
-    pd.n_rows = (int)pl.row_agent.size();
-    pd.n_pages = (int)pl.pages.size();
-    pd.n_tile_agents = (int)pl.tile_agents.size();
-    pd.A = A; pd.C = C; pd.causal = causal ? 1 : 0;
-    pd.n_out_rows = A * C * g.H_q;
-    pd.n_partials = pl.n_partials;
-    pd.partial_stride = g.d + g.rmax_pad + 4;
     std::vector<uint8_t> blob;
-    auto put = [&](const void* src, size_t bytes) {
-      int64_t o = align_up((int64_t)blob.size(), 256);
-      blob.resize(o + bytes);
-      if (bytes) std::memcpy(blob.data() + o, src, bytes);
-      return o;
-    };
-    std::vector<CallAgent> ca(A);
-    for (int i = 0; i < A; ++i) ca[i] = CallAgent{agents[i], seq[i]};
-    pd.off_items = put(pl.items.data(), pl.items.size() * sizeof(fk_work_item));
-    pd.off_row_agent = put(pl.row_agent.data(), pl.row_agent.size() * 4);
-    pd.off_row_cg = put(pl.row_cg.data(), pl.row_cg.size() * 4);
-    pd.off_pages = put(pl.pages.data(), pl.pages.size() * 4);
-    pd.off_tile_agents = put(pl.tile_agents.data(), pl.tile_agents.size() * 4);
-    pd.off_call_agents = put(ca.data(), ca.size() * sizeof(CallAgent));
-    pd.off_csr_ptr = put(pl.csr_ptr.data(), pl.csr_ptr.size() * 4);
-    pd.off_csr_slots = put(pl.csr_slots.data(), pl.csr_slots.size() * 4);
-    pd.off_cta = put(pl.cta_begin.data(), pl.cta_begin.size() * 4);
-    pd.n_ctas = (int)pl.cta_begin.size() - 1;
-    pd.off_partials = align_up((int64_t)blob.size(), 256);
-    int64_t need = pd.off_partials + (int64_t)pd.n_partials * pd.partial_stride * 4;
+    int64_t need = pack_plan(pl, A, C, causal, agents, seq, g, blob, pd);
     if (need > g.ws_bytes) return fail(FK_ERR_OOM, "workspace too small for this call");
     fk_status s2 = stage_upload(p, blob.data(), blob.size(), g.base + g.off_ws, st);
     if (s2 != FK_OK) return s2;
@@ -889,35 +935,8 @@ fk_status fk_residual_attention_noalloc(fk_pool* p, int layer, const uint16_t* q
                              kMaxRows, kMaxRankSum, p->num_sms, pl);
     if (s != FK_OK) return s;
     PlanDev pd{};
-    pd.n_items = (int)pl.items.size();
-    pd.n_rows = (int)pl.row_agent.size();
-    pd.n_pages = (int)pl.pages.size();
-    pd.n_tile_agents = (int)pl.tile_agents.size();
-    pd.A = A; pd.C = C; pd.causal = causal ? 1 : 0;
-    pd.n_out_rows = A * C * g.H_q;
-    pd.n_partials = pl.n_partials;
-    pd.partial_stride = g.d + g.rmax_pad + 4;
     std::vector<uint8_t> blob;
-    auto put = [&](const void* src, size_t bytes) {
-      int64_t o = align_up((int64_t)blob.size(), 256);
-      blob.resize(o + bytes);
-      if (bytes) std::memcpy(blob.data() + o, src, bytes);
-      return o;
-    };
-    std::vector<CallAgent> ca(A);
-    for (int i = 0; i < A; ++i) ca[i] = CallAgent{agents[i], seq[i]};
-    pd.off_items = put(pl.items.data(), pl.items.size() * sizeof(fk_work_item));
-    pd.off_row_agent = put(pl.row_agent.data(), pl.row_agent.size() * 4);
-    pd.off_row_cg = put(pl.row_cg.data(), pl.row_cg.size() * 4);
-    pd.off_pages = put(pl.pages.data(), pl.pages.size() * 4);
-    pd.off_tile_agents = put(pl.tile_agents.data(), pl.tile_agents.size() * 4);
-    pd.off_call_agents = put(ca.data(), ca.size() * sizeof(CallAgent));
-    pd.off_csr_ptr = put(pl.csr_ptr.data(), pl.csr_ptr.size() * 4);
-    pd.off_csr_slots = put(pl.csr_slots.data(), pl.csr_slots.size() * 4);
-    pd.off_cta = put(pl.cta_begin.data(), pl.cta_begin.size() * 4);
-    pd.n_ctas = (int)pl.cta_begin.size() - 1;
-    pd.off_partials = align_up((int64_t)blob.size(), 256);
-    int64_t need = pd.off_partials + (int64_t)pd.n_partials * pd.partial_stride * 4;
+    int64_t need = pack_plan(pl, A, C, causal, agents, seq, g, blob, pd);
     if (need > (int64_t)scratch_bytes) {
       char msg[160];
       std::snprintf(msg, sizeof msg,
@@ -955,15 +974,17 @@ fk_status fk_pool_set_profile_event(fk_pool* p, void* event) {
 fk_status fk_check(fk_pool* p, void* stream) {
   if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
   cudaStream_t st = (cudaStream_t)stream;
-  uint32_t word[2] = {0, 0};
-  cudaError_t e = cudaMemcpyAsync(word, p->g.base + p->g.off_err, 8, cudaMemcpyDeviceToHost, st);
+  uint32_t word[3] = {0, 0, 0};
+  cudaError_t e = cudaMemcpyAsync(word, p->g.base + p->g.off_err, 12, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "fk_check");
   if (word[0] || word[1]) {
-    cudaMemsetAsync(p->g.base + p->g.off_err, 0, 8, st);
+    cudaMemsetAsync(p->g.base + p->g.off_err, 0, 12, st);
     cudaStreamSynchronize(st);
-    char msg[128];
-    std::snprintf(msg, sizeof msg, "device check fired: bounds 0x%x, waits %u", word[0], word[1]);
+    char msg[160];
+    std::snprintf(msg, sizeof msg,
+                  "device check fired: bounds 0x%x, waits %u (first: warp %u, barrier smem 0x%x)",
+                  word[0], word[1], (word[2] >> 20) & 0x7FFu, word[2] & 0xFFFFFu);
     return fail(word[1] ? FK_ERR_TIMEOUT : FK_ERR_DEVICE_CHECK, msg);
   }
   return FK_OK;

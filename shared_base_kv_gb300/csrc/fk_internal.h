@@ -68,8 +68,19 @@ struct PlanDev {
   int32_t n_partials;      // partial slots
   int32_t partial_stride;  // floats per partial slot: d + rmax_pad + 4
   int32_t n_ctas;          // persistent CTAs; CTA c runs items cta[c] .. cta[c+1]-1
+  int32_t n_mpairs;        // decode-shaped calls: (agent tile, kv head) pairs with an M
   int64_t off_items, off_row_agent, off_row_cg, off_pages, off_tile_agents,
           off_call_agents, off_csr_ptr, off_csr_slots, off_partials, off_cta;
+  int64_t off_mpairs, off_item_mpair;   // MPair[n_mpairs], int32[n_items]
+};
+
+// One (agent tile, kv head) of a decode-shaped call: the rows of its agents
+// and where its query-side RoPE matrix M (d x 4 sum-of-ranks f16, in the
+// decode kernel's shared-memory image) sits in the workspace.
+struct MPair {
+  int32_t head, agent_begin, n_agents, row_begin;
+  int32_t zcols, pad;      // columns of M (4 x the tile's padded rank sum)
+  int64_t mofs;            // byte offset from the workspace start
 };
 
 // Host launchers (fk_kernels.cu).  All return a cudaError_t as int.
@@ -91,6 +102,12 @@ int launch_attention(const PoolGeom& g, const PlanDev& p, int layer,
                      const uint16_t* q, uint16_t* out, int compressed,
                      int num_sms, void* stream, int* n_launches,
                      void* event_after_main);
+
+// Decode-shaped calls (four query rows per agent: G * C == 4) run the
+// decode kernel (fk_decode.cu); the combine is shared.
+bool decode_applies(const PoolGeom& g, const PlanDev& p);
+int launch_decode(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q,
+                  int compressed, void* stream);
 
 // Device address and size of the static scratch array that
 // fk_residual_attention_noalloc uses (looked up once per device).

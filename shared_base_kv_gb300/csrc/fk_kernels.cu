@@ -122,8 +122,6 @@ __global__ void agent_register_kernel(PoolGeom g, int agent, int r, int rp,
 
 // ============================================================ codec =====
 
-__constant__ float c_lloyd[8] = {-2.1520f, -1.3439f, -0.7560f, -0.2451f,
-                                 0.2451f,  0.7560f,  1.3439f,  2.1520f};
 
 __device__ __forceinline__ float bf16_at(const uint8_t* p) {
   return __bfloat162float(*(const __nv_bfloat16*)p);
@@ -1178,7 +1176,12 @@ static int launch_attn_t(const PoolGeom& g, const PlanDev& p, int layer, const u
     if (e != cudaSuccess) return (int)e;
     attr_done = true;
   }
-  attention_kernel<D, COMP><<<p.n_ctas, attn::kThreads, LY::TOTAL, st>>>(g, p, layer, q);
+  if (decode_applies(g, p)) {
+    int de = launch_decode(g, p, layer, q, COMP ? 1 : 0, st);
+    if (de != 0) return de;
+  } else {
+    attention_kernel<D, COMP><<<p.n_ctas, attn::kThreads, LY::TOTAL, st>>>(g, p, layer, q);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
   if (ev) {
@@ -1206,7 +1209,7 @@ int launch_attention(const PoolGeom& g, const PlanDev& p, int layer, const uint1
                      void* event_after_main) {
   cudaStream_t st = (cudaStream_t)stream;
   cudaEvent_t ev = (cudaEvent_t)event_after_main;
-  *n_launches = 2;
+  *n_launches = decode_applies(g, p) ? 3 : 2;   // (M build,) attention, combine
   if (g.d == 128) {
     return compressed ? launch_attn_t<128, true>(g, p, layer, q, out, num_sms, st, ev)
                       : launch_attn_t<128, false>(g, p, layer, q, out, num_sms, st, ev);

@@ -54,7 +54,9 @@ def test_parity_reduced(name, variant):
         assert mx <= MAX_ABS and mean <= MEAN_ABS, (name, variant, layer, mx, mean, rel)
         assert rel < 2e-2
     dw.check()
-    assert fk_last_launch_count(dw.pool.h) == 2
+    # decode-shaped calls (four query rows per agent) add the M-build grid
+    decode_shaped = (w.H_q // w.H_kv) * w.C == 4
+    assert fk_last_launch_count(dw.pool.h) == (3 if decode_shaped else 2)
 
 
 @pytest.mark.parametrize("variant", ["base", "peaked", "strong"])
