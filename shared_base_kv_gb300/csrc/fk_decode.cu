@@ -29,9 +29,10 @@
 // under programmatic dependent launch and waits for that grid only before
 // its first copy of M).
 //
-// Warp roles (352 threads): warp 0 bulk copies, warp 1 MMA issue (converged
-// warp, elect.sync), warp 2 dequantiser of the compressed pool, warps 3-6
-// and 7-10 two compute warpgroups.  Warpgroup w owns query rows 8w .. 8w+7
+// Warp roles (384 threads): warp 0 key (and M) bulk copies, warp 11 value
+// bulk copies, warp 1 MMA issue (converged warp, elect.sync), warp 2
+// dequantiser of the compressed pool, warps 3-6 and 7-10 two compute
+// warpgroups.  Warpgroup w owns query rows 8w .. 8w+7
 // (agents 2w, 2w+1): their Z reduction, online softmax, P and epilogue; it
 // also writes its half of the RoPE frequencies of each Trig tile.  Two warps of identical code per SM
 // sub-partition hide each other's latencies.  A warp reaches TMEM lanes
@@ -47,7 +48,7 @@
 namespace fk {
 namespace dec {
 
-constexpr int kThreads = 352;       // 11 warps
+constexpr int kThreads = 384;       // 12 warps
 constexpr int kRPA = 4;               // query rows per agent
 constexpr int kRows = 16;             // padded query rows of a tile (<= 4 agents)
 constexpr int kA = kMaxAgentsPerTile;
@@ -57,9 +58,11 @@ constexpr int kPChunk = 144;          // P: 8 keys x 8 rows core matrix, padded
 constexpr int kPRowGroup = 16 * kPChunk;
 constexpr int kLvChunk = 9 * 128;     // Lv^T: 8 rank groups + the ones group
 constexpr int kOnesLane = 64;
-// TMEM columns: base scores, O^T, OL^T (16 rows each), the generator's
-// per-lane rotation table, two Trig stages, two Z buffers
-constexpr uint32_t kTmS = 0, kTmOT = 16, kTmOL = 32, kTmTau = 64, kTmTrig = 128, kTmZ = 256;
+// TMEM columns: base scores (two buffers of 16 rows: 0 and 48), O^T, OL^T
+// (16 rows each), the per-lane rotation table, two Trig stages, two Z buffers
+constexpr uint32_t kTmS = 0, kTmOT = 16, kTmOL = 32, kTmS1 = 48, kTmTau = 64, kTmTrig = 128,
+                   kTmZ = 256;
+__host__ __device__ constexpr uint32_t tm_s(int b) { return b ? kTmS1 : kTmS; }
 
 template <int D, bool COMP>
 struct Layout {
@@ -91,14 +94,15 @@ struct Layout {
 
 enum {
   B_KB_FULL0, B_KB_FULL1, B_KB_EMPTY0, B_KB_EMPTY1, B_VB_FULL0, B_VB_FULL1, B_VB_EMPTY0,
-  B_VB_EMPTY1, B_LV_FULL, B_LV_EMPTY, B_M_FULL, B_M_EMPTY, B_ITEM_FULL, B_TRIG_FULL0, B_TRIG_FULL1, B_S_FULL,
-  B_S_EMPTY, B_Z_FULL0, B_Z_FULL1, B_Z_FREE0, B_Z_FREE1, B_P_FULL0, B_P_FULL1, B_PV_DONE0,
+  B_VB_EMPTY1, B_LV_FULL, B_LV_EMPTY, B_M_FULL, B_M_EMPTY, B_ITEM_FULL, B_TRIG_FULL0, B_TRIG_FULL1, B_S_FULL0,
+  B_S_FULL1, B_S_EMPTY0, B_S_EMPTY1, B_Z_FULL0, B_Z_FULL1, B_Z_FREE0, B_Z_FREE1, B_P_FULL0, B_P_FULL1, B_PV_DONE0,
   B_PV_DONE1, B_ACC_EMPTY, B_KQ_FULL, B_KQ_EMPTY, B_VC_FULL, B_VC_EMPTY, B_FINAL, B_COUNT
 };
 // Arrival counts: 8 = lane 0 of each warp of both compute warpgroups; 1 =
 // one thread, a bulk-copy transaction count or an MMA commit.
 __host__ __device__ constexpr uint32_t bar_count(int i) {
-  return (i == B_ITEM_FULL || i == B_TRIG_FULL0 || i == B_TRIG_FULL1 || i == B_S_EMPTY ||
+  return (i == B_ITEM_FULL || i == B_TRIG_FULL0 || i == B_TRIG_FULL1 || i == B_S_EMPTY0 ||
+          i == B_S_EMPTY1 ||
           i == B_Z_FREE0 || i == B_Z_FREE1 || i == B_P_FULL0 || i == B_P_FULL1 ||
           i == B_ACC_EMPTY)
              ? 8u
@@ -106,7 +110,7 @@ __host__ __device__ constexpr uint32_t bar_count(int i) {
 }
 constexpr uint64_t kEmptyMask =
     (1ull << B_KB_EMPTY0) | (1ull << B_KB_EMPTY1) | (1ull << B_VB_EMPTY0) | (1ull << B_VB_EMPTY1) |
-    (1ull << B_LV_EMPTY) | (1ull << B_M_EMPTY) | (1ull << B_S_EMPTY) | (1ull << B_Z_FREE0) | (1ull << B_Z_FREE1) |
+    (1ull << B_LV_EMPTY) | (1ull << B_M_EMPTY) | (1ull << B_S_EMPTY0) | (1ull << B_S_EMPTY1) | (1ull << B_Z_FREE0) | (1ull << B_Z_FREE1) |
     (1ull << B_ACC_EMPTY) | (1ull << B_KQ_EMPTY) | (1ull << B_VC_EMPTY);
 static_assert(B_COUNT <= 64, "one parity bit per barrier");
 
@@ -282,28 +286,70 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
   const int it_begin = cta_items[blockIdx.x], it_end = cta_items[blockIdx.x + 1];
 
   if (warp == 0) {
-    // ============================================ producer (whole warp) ====
+    // ============================================== key copies (warp 0) ====
     // every lane waits; lane 0 posts the transaction count; the lanes then
-    // split the tile's bulk copies (one page or one 8-key Lv chunk each)
+    // split the tile's bulk copies (one page each).  Keys run ahead as far as
+    // the two key stages allow, independently of the values.
     int tc = 0;
     for (int it = it_begin; it < it_end; ++it) {
       Item I;
       load_item(g, p, ws, it, I);
       const int32_t* pages = (const int32_t*)(ws + p.off_pages) + I.page_begin;
-      // the item's M (built by the preceding grid) once the previous item's
-      // Z MMAs are done with the buffer
-      {
-        const MPair mpr = ((const MPair*)(ws + p.off_mpairs))[((const int32_t*)(ws + p.off_item_mpair))[it]];
-        const uint32_t mbytes = (uint32_t)mpr.zcols * D * 2;
-        wait(B_M_EMPTY);
-        if (it == it_begin) asm volatile("griddepcontrol.wait;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_expect_tx(bar(B_M_FULL), mbytes);
-        __syncwarp();
-        for (uint32_t o = lane * 4096u; o < mbytes; o += 32u * 4096u)
-          bulk_g2s(sbase + LY::oM + o, ws + mpr.mofs + o, min(4096u, mbytes - o), bar(B_M_FULL));
+      const int tc0 = tc;
+      for (int k = 0; k < I.n_tiles; ++k) {
+        const int p0 = k * kTilePages;
+        const int np = min(kTilePages, I.n_pages - p0);
+        tc = tc0 + k;
+        if (!COMP) {
+          const int st = tc & 1;
+          wait(B_KB_EMPTY0 + st);
+          __syncwarp();
+          if (lane == 0) mbar_expect_tx(bar(B_KB_FULL0 + st), np * LY::PAGE_B);
+          __syncwarp();
+          if (lane < np && !*abort_flag) {
+            const uint8_t* src = g.base + g.off_kb + (int64_t)layer * g.kb_layer_bytes +
+                                 ((int64_t)pages[p0 + lane] * g.H_kv + I.head) * LY::PAGE_B;
+            bulk_g2s(sbase + LY::oKB + st * LY::TILE_B + lane * LY::PAGE_B, src, LY::PAGE_B,
+                     bar(B_KB_FULL0 + st));
+          }
+        } else {
+          wait(B_KQ_EMPTY);
+          __syncwarp();
+          if (lane == 0) mbar_expect_tx(bar(B_KQ_FULL), np * kPage * D);
+          __syncwarp();
+          if (lane < np && !*abort_flag) {
+            const uint8_t* src = g.base + g.off_kq +
+                                 ((((int64_t)layer * g.num_pages + pages[p0 + lane]) * g.H_kv + I.head) * kPage) * D;
+            bulk_g2s(sbase + LY::oKQ + lane * kPage * D, src, kPage * D, bar(B_KQ_FULL));
+          }
+        }
+        if (k == 0) {
+        // the item's M (built by the preceding grid) once the previous item's
+        // Z MMAs are done with the buffer; after the first key tile, which
+        // need not wait for that
+        {
+          const MPair mpr = ((const MPair*)(ws + p.off_mpairs))[((const int32_t*)(ws + p.off_item_mpair))[it]];
+          const uint32_t mbytes = (uint32_t)mpr.zcols * D * 2;
+          wait(B_M_EMPTY);
+          if (it == it_begin) asm volatile("griddepcontrol.wait;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_expect_tx(bar(B_M_FULL), mbytes);
+          __syncwarp();
+          for (uint32_t o = lane * 4096u; o < mbytes && !*abort_flag; o += 32u * 4096u)
+            bulk_g2s(sbase + LY::oM + o, ws + mpr.mofs + o, min(4096u, mbytes - o), bar(B_M_FULL));
+        }
+        }
       }
-      // values of tile k (stage vt % NVB) and the Lv^T stage
+      tc = tc0 + I.n_tiles;
+    }
+  } else if (warp == 11) {
+    // ============================================ value copies (warp 11) ====
+    // values of tile k: Vb (or the compressed codes) and the Lv^T stage
+    int tc = 0;
+    for (int it = it_begin; it < it_end; ++it) {
+      Item I;
+      load_item(g, p, ws, it, I);
+      const int32_t* pages = (const int32_t*)(ws + p.off_pages) + I.page_begin;
       auto load_values = [&](int k, int vt) {
         const int p0 = k * kTilePages;
         const int np = min(kTilePages, I.n_pages - p0);
@@ -313,7 +359,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_expect_tx(bar(B_VC_FULL), np * kPage * (3 * D / 8 + 4));
           __syncwarp();
-          if (lane < np) {
+          if (lane < np && !*abort_flag) {
             const int64_t tok = (((int64_t)layer * g.num_pages + pages[p0 + lane]) * g.H_kv + I.head) * kPage;
             bulk_g2s(sbase + LY::oVC + lane * kPage * (3 * D / 8), g.base + g.off_vc + tok * (3 * D / 8),
                      kPage * (3 * D / 8), bar(B_VC_FULL));
@@ -326,7 +372,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_expect_tx(bar(B_VB_FULL0 + st), np * LY::PAGE_B);
           __syncwarp();
-          if (lane < np) {
+          if (lane < np && !*abort_flag) {
             const uint8_t* src = g.base + g.off_vb + (int64_t)layer * g.kb_layer_bytes +
                                  ((int64_t)pages[p0 + lane] * g.H_kv + I.head) * LY::PAGE_B;
             bulk_g2s(sbase + LY::oVB + st * LY::TILE_B + lane * LY::PAGE_B, src, LY::PAGE_B,
@@ -344,7 +390,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           mbar_expect_tx(bar(B_LV_FULL), bytes);
         }
         __syncwarp();
-        for (int x = lane; x < I.n_ag * nch; x += 32) {
+        for (int x = lane; x < I.n_ag * nch && !*abort_flag; x += 32) {
           const int ax = x / nch, c = x % nch;
           const uint8_t* src = nullptr;
           int cb = 0, cl = 0;
@@ -358,40 +404,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           bulk_g2s(sbase + LY::oLV + c * kLvChunk + (cl / 8) * 128, src + c * cb, cb, bar(B_LV_FULL));
         }
       };
-      // keys of tile k, then the values of tile k - 1 (consumed one tile later);
-      // one call site each keeps the warp's loop small
-      const int tc0 = tc;
-      for (int k = 0; k <= I.n_tiles; ++k) {
-        const int p0 = k * kTilePages;
-        const int np = min(kTilePages, I.n_pages - p0);
-        tc = tc0 + k;
-        if (k == I.n_tiles) {
-        } else if (!COMP) {
-          const int st = tc & 1;
-          wait(B_KB_EMPTY0 + st);
-          __syncwarp();
-          if (lane == 0) mbar_expect_tx(bar(B_KB_FULL0 + st), np * LY::PAGE_B);
-          __syncwarp();
-          if (lane < np) {
-            const uint8_t* src = g.base + g.off_kb + (int64_t)layer * g.kb_layer_bytes +
-                                 ((int64_t)pages[p0 + lane] * g.H_kv + I.head) * LY::PAGE_B;
-            bulk_g2s(sbase + LY::oKB + st * LY::TILE_B + lane * LY::PAGE_B, src, LY::PAGE_B,
-                     bar(B_KB_FULL0 + st));
-          }
-        } else {
-          wait(B_KQ_EMPTY);
-          __syncwarp();
-          if (lane == 0) mbar_expect_tx(bar(B_KQ_FULL), np * kPage * D);
-          __syncwarp();
-          if (lane < np) {
-            const uint8_t* src = g.base + g.off_kq +
-                                 ((((int64_t)layer * g.num_pages + pages[p0 + lane]) * g.H_kv + I.head) * kPage) * D;
-            bulk_g2s(sbase + LY::oKQ + lane * kPage * D, src, kPage * D, bar(B_KQ_FULL));
-          }
-        }
-        if (k > 0) load_values(k - 1, tc0 + k - 1);
-      }
-      tc = tc0 + I.n_tiles;
+      for (int k = 0; k < I.n_tiles; ++k, ++tc) load_values(k, tc);
     }
   } else if (warp == 1) {
     // ======================================= MMA issue (converged warp) ====
@@ -413,7 +426,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         if (j == 0) wait(B_ACC_EMPTY);
         tc_fence_after();
         __syncwarp();
-        if (elect_one()) {
+        if (elect_one() && !*abort_flag) {
           const uint64_t dP = sdesc(sbase + LY::oP + pb * LY::P_B, kPChunk, kPRowGroup);
           const uint64_t dV = sdesc(sbase + LY::oVB + vs * LY::TILE_B, (D / 8) * 128, 128);
           const uint64_t dL = sdesc(sbase + LY::oLV, kLvChunk, 128);
@@ -430,7 +443,30 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         }
         __syncwarp();
       };
+      // base scores of tile k (buffer t & 1 of the two S buffers)
+      auto issue_s = [&](int t) {
+        const int kb = t & 1;
+        wait(B_S_EMPTY0 + kb);
+        wait(B_KB_FULL0 + kb);
+        tc_fence_after();
+        __syncwarp();
+        if (elect_one() && !*abort_flag) {
+          const uint64_t dK = sdesc(sbase + LY::oKB + kb * LY::TILE_B, 128, (D / 8) * 128);
+          const uint64_t dQ = sdesc(sbase + LY::oQ, 128, (D / 8) * 128);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_ss(tmem + tm_s(kb), dK + (uint64_t)(ks * 16), dQ + (uint64_t)(ks * 16), idS,
+                   ks > 0 ? 1u : 0u);
+          mma_commit(bar(B_KB_EMPTY0 + kb));
+          mma_commit(bar(B_S_FULL0 + kb));
+        }
+        __syncwarp();
+      };
+      // per tile k: Z(k), then the next tile's base scores, then the values
+      // of tile k - 1 (which wait for that tile's P), so that neither Z nor S
+      // queues behind a P the compute warpgroups have not written yet
       const int tc0 = tc;
+      issue_s(tc0);
       for (int k = 0; k <= I.n_tiles; ++k) {
         if (k == I.n_tiles) {
           if (elect_one()) mma_commit(bar(B_M_EMPTY));   // every Z MMA of the item is issued
@@ -440,21 +476,6 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         }
         tc = tc0 + k;
         const int kb = tc & 1;
-        wait(B_S_EMPTY);
-        wait(B_KB_FULL0 + kb);
-        tc_fence_after();
-        __syncwarp();
-        if (elect_one()) {
-          const uint64_t dK = sdesc(sbase + LY::oKB + kb * LY::TILE_B, 128, (D / 8) * 128);
-          const uint64_t dQ = sdesc(sbase + LY::oQ, 128, (D / 8) * 128);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            mma_ss(tmem + kTmS, dK + (uint64_t)(ks * 16), dQ + (uint64_t)(ks * 16), idS,
-                   ks > 0 ? 1u : 0u);
-          mma_commit(bar(B_KB_EMPTY0 + kb));
-          mma_commit(bar(B_S_FULL));
-        }
-        __syncwarp();
         wait(B_TRIG_FULL0 + kb);
         for (int c = 0; c < n_zc; ++c, ++zq) {
           const int zb = zq & 1;
@@ -462,7 +483,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           wait(B_Z_FREE0 + zb);
           tc_fence_after();
           __syncwarp();
-          if (elect_one()) {
+          if (elect_one() && !*abort_flag) {
             const uint32_t idZ = idesc_f16(128, ncol, 0);
             const uint64_t dM = sdesc(sbase + LY::oM + c * (kZBuf / 8) * SBO_M, 128, SBO_M);
             const uint32_t tA = tmem + kTmTrig + kb * NF;
@@ -474,81 +495,97 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           }
           __syncwarp();
         }
+        if (k + 1 < I.n_tiles) issue_s(tc + 1);
         if (k > 0) pv(k - 1, tc0 + k - 1);
       }
       tc = tc0 + I.n_tiles;
     }
+    // drain: every MMA issued must complete before tensor memory is freed,
+    // also after a timed-out wait (then no further MMA was issued)
     if (elect_one()) mma_commit(bar(B_FINAL));
     __syncwarp();
-    wait(B_FINAL);
+    mbar_wait_drain(bar(B_FINAL), 0);
   } else if (COMP && warp == 2) {
     // ====================================== dequantiser (compressed pool) ====
     const float kscale = ((const float*)(g.base + g.off_ks))[layer];
     int tc = 0;
+    // keys of tile k, then the values of tile k - 1: the same order as the
+    // bulk copies, so the keys of the next tile never wait for the value
+    // MMAs that free the single value stage
     for (int it = it_begin; it < it_end; ++it) {
       Item I;
       load_item(g, p, ws, it, I);
-      for (int k = 0; k < I.n_tiles; ++k, ++tc) {
-        const int np = min(kTilePages, I.n_pages - k * kTilePages);
-        const int kb = tc & 1, vs = tc % LY::NVB;
-        // keys: int8 [page][16][D] -> bf16 (value * scale) in the key layout
-        wait(B_KQ_FULL);
-        wait(B_KB_EMPTY0 + kb);
-        uint8_t* kdst = smem + LY::oKB + kb * LY::TILE_B;
-        for (int u = lane; u < np * kPage * (D / 8); u += 32) {
-          const int ch = u % (D / 8), row = (u / (D / 8)) % kPage, pj = u / (kPage * (D / 8));
-          const int8_t* src = (const int8_t*)(smem + LY::oKQ) + (pj * kPage + row) * D + ch * 8;
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf2((float)src[2 * e] * kscale, (float)src[2 * e + 1] * kscale);
-          *(uint4*)(kdst + pj * LY::PAGE_B + ((row / 8) * (D / 8) + ch) * 128 + (row % 8) * 16) =
-              make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) { mbar_arrive(bar(B_KB_FULL0 + kb)); mbar_arrive(bar(B_KQ_EMPTY)); }
-        // values: codes -> level * norm / D in the value layout (rotated domain)
-        wait(B_VC_FULL);
-        wait(B_VB_EMPTY0 + vs);
-        uint8_t* vdst = smem + LY::oVB + vs * LY::TILE_B;
-        for (int u = lane; u < np * 2 * (D / 8); u += 32) {
-          const int dg = u % (D / 8), tcn = (u / (D / 8)) % 2, pj = u / (2 * (D / 8));
-          float w8[8];
-          uint32_t c8[8];
-#pragma unroll
-          for (int tt = 0; tt < 8; ++tt) {
-            const int row = tcn * 8 + tt;
-            const uint8_t* cb = smem + LY::oVC + (pj * kPage + row) * (3 * D / 8);
-            const uint32_t b0 = cb[dg], b1 = cb[D / 8 + dg], b2 = cb[2 * (D / 8) + dg];
-            c8[tt] = b0 | (b1 << 8) | (b2 << 16);
-            w8[tt] = ((const float*)(smem + LY::oVN))[pj * kPage + row] * (1.0f / D);
-          }
-          uint8_t* dst = vdst + pj * LY::PAGE_B + (tcn * (D / 8) + dg) * 128;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {   // d = 8 dg + e
+      const int tc0 = tc;
+      for (int j = 0; j <= I.n_tiles; ++j) {
+        if (j < I.n_tiles) {
+          const int k = j;
+          const int np = min(kTilePages, I.n_pages - k * kTilePages);
+          const int kb = (tc0 + k) & 1;
+          // keys: int8 [page][16][D] -> bf16 (value * scale) in the key layout
+          wait(B_KQ_FULL);
+          wait(B_KB_EMPTY0 + kb);
+          uint8_t* kdst = smem + LY::oKB + kb * LY::TILE_B;
+          for (int u = lane; u < np * kPage * (D / 8); u += 32) {
+            const int ch = u % (D / 8), row = (u / (D / 8)) % kPage, pj = u / (kPage * (D / 8));
+            const int8_t* src = (const int8_t*)(smem + LY::oKQ) + (pj * kPage + row) * D + ch * 8;
             uint32_t w[4];
 #pragma unroll
-            for (int h2 = 0; h2 < 4; ++h2) {
-              float v2[2];
-#pragma unroll
-              for (int z = 0; z < 2; ++z) {
-                const uint32_t cc = c8[2 * h2 + z];
-                const uint32_t code = ((cc >> e) & 1u) | (((cc >> (8 + e)) & 1u) << 1) |
-                                      (((cc >> (16 + e)) & 1u) << 2);
-                v2[z] = c_lloyd[code] * w8[2 * h2 + z];
-              }
-              w[h2] = pack_bf2(v2[0], v2[1]);
-            }
-            *(uint4*)(dst + e * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf2((float)src[2 * e] * kscale, (float)src[2 * e + 1] * kscale);
+            *(uint4*)(kdst + pj * LY::PAGE_B + ((row / 8) * (D / 8) + ch) * 128 + (row % 8) * 16) =
+                make_uint4(w[0], w[1], w[2], w[3]);
           }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) { mbar_arrive(bar(B_KB_FULL0 + kb)); mbar_arrive(bar(B_KQ_EMPTY)); }
         }
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) { mbar_arrive(bar(B_VB_FULL0 + vs)); mbar_arrive(bar(B_VC_EMPTY)); }
+        if (j > 0) {
+          const int k = j - 1;
+          const int np = min(kTilePages, I.n_pages - k * kTilePages);
+          const int vs = (tc0 + k) % LY::NVB;
+          // values: codes -> level * norm / D in the value layout (rotated domain)
+          wait(B_VC_FULL);
+          wait(B_VB_EMPTY0 + vs);
+          uint8_t* vdst = smem + LY::oVB + vs * LY::TILE_B;
+          for (int u = lane; u < np * 2 * (D / 8); u += 32) {
+            const int dg = u % (D / 8), tcn = (u / (D / 8)) % 2, pj = u / (2 * (D / 8));
+            float w8[8];
+            uint32_t c8[8];
+#pragma unroll
+            for (int tt = 0; tt < 8; ++tt) {
+              const int row = tcn * 8 + tt;
+              const uint8_t* cb = smem + LY::oVC + (pj * kPage + row) * (3 * D / 8);
+              const uint32_t b0 = cb[dg], b1 = cb[D / 8 + dg], b2 = cb[2 * (D / 8) + dg];
+              c8[tt] = b0 | (b1 << 8) | (b2 << 16);
+              w8[tt] = ((const float*)(smem + LY::oVN))[pj * kPage + row] * (1.0f / D);
+            }
+            uint8_t* dst = vdst + pj * LY::PAGE_B + (tcn * (D / 8) + dg) * 128;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {   // d = 8 dg + e
+              uint32_t w[4];
+#pragma unroll
+              for (int h2 = 0; h2 < 4; ++h2) {
+                float v2[2];
+#pragma unroll
+                for (int z = 0; z < 2; ++z) {
+                  const uint32_t cc = c8[2 * h2 + z];
+                  const uint32_t code = ((cc >> e) & 1u) | (((cc >> (8 + e)) & 1u) << 1) |
+                                        (((cc >> (16 + e)) & 1u) << 2);
+                  v2[z] = c_lloyd[code] * w8[2 * h2 + z];
+                }
+                w[h2] = pack_bf2(v2[0], v2[1]);
+              }
+              *(uint4*)(dst + e * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) { mbar_arrive(bar(B_VB_FULL0 + vs)); mbar_arrive(bar(B_VC_EMPTY)); }
+        }
       }
+      tc = tc0 + I.n_tiles;
     }
-  } else if (warp >= 3) {
+  } else if (warp >= 3 && warp <= 10) {
     // ============================================ compute warpgroups ====
     constexpr int NFH = NF / 2;                      // RoPE frequencies per warpgroup
     const int cw = (warp - 3) >> 2;                  // warpgroup 0 or 1
@@ -595,7 +632,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_TRIG_FULL0 + b));
+      if (lane == 0) mbar_arrive_relaxed(bar(B_TRIG_FULL0 + b));
     };
     int tc = 0, zq = 0, pv_seen = 0;
     // The value MMAs of tile j signal PV_DONE[j & 1].  They are awaited
@@ -701,12 +738,12 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         const int ntok = min(kTileTok, (n_pages - k * kTilePages) * kPage);
         // base scores of rows r0 .. r0 + 7
         uint32_t sv[8];
-        wait(B_S_FULL);
+        wait(B_S_FULL0 + (tc & 1));
         tc_fence_after();
-        tmem_ld8_wait(tmem + kTmS + r0 + lane_off, sv);
+        tmem_ld8_wait(tmem + tm_s(tc & 1) + r0 + lane_off, sv);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_S_EMPTY));
+        if (lane == 0) mbar_arrive_relaxed(bar(B_S_EMPTY0 + (tc & 1)));
         // Trig of the next tile (and of this one at the item's first tile),
         // into the stage whose previous reader, Z(k - 1), this warpgroup has
         // already waited for.  The MMA warp needs Trig(k + 1) only after its
@@ -759,9 +796,8 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_Z_FREE0 + zb));
+          if (lane == 0) mbar_arrive_relaxed(bar(B_Z_FREE0 + zb));
         }
-        if (k + 1 < n_tiles) prefetch_lk(k + 1);
         // ---- online softmax (base 2); the running max of a row moves only
         // when the tile max exceeds it by more than 2^8 (then O^T, OL^T are
         // rescaled in TMEM)
@@ -805,6 +841,8 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_P_FULL0 + (tc & 1)));
+        // after the release above: that arrive need not wait for these
+        if (k + 1 < n_tiles) prefetch_lk(k + 1);
       }
       // ---- epilogue: this warpgroup's rows of the item's split partials
       pv_until(tc);
@@ -842,7 +880,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_ACC_EMPTY));
+      if (lane == 0) mbar_arrive_relaxed(bar(B_ACC_EMPTY));
     }
   }
   // ---- tear-down.  After a timed-out wait, give bulk copies still in

@@ -24,6 +24,14 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Relaxed arrive: signals without waiting for this thread's outstanding
+// memory operations.  For hand-offs of tensor memory whose reads or writes
+// the thread has already waited for (tcgen05.wait) and fenced
+// (tcgen05.fence::before_thread_sync); shared-memory data hand-offs keep
+// the release form.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                "r"(bytes)
@@ -72,6 +80,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t& parity,
   parity ^= 1u;
   if (mbar_try(bar, par)) return true;
   return mbar_wait_slow(bar, par, abort_flag, err_word);
+}
+
+// Bounded wait that ignores the abort flag: for draining work already in
+// flight (tensor-core MMAs complete on their own) before resources such as
+// tensor memory are released.  Gives up after ~1 s of clock.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity))
+    if (clock64() - t0 > 2000000000LL) return false;
+  return true;
 }
 
 // ------------------------------------------------------- bulk copies --
