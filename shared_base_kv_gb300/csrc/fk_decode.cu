@@ -59,9 +59,10 @@ constexpr int kPRowGroup = 16 * kPChunk;
 constexpr int kLvChunk = 9 * 128;     // Lv^T: 8 rank groups + the ones group
 constexpr int kOnesLane = 64;
 // TMEM columns: base scores (two buffers of 16 rows: 0 and 48), O^T, OL^T
-// (16 rows each), the per-lane rotation table, two Trig stages, two Z buffers
-constexpr uint32_t kTmS = 0, kTmOT = 16, kTmOL = 32, kTmS1 = 48, kTmTau = 64, kTmTrig = 128,
-                   kTmZ = 256;
+// (16 rows each), the Lv^T stage (A operand of the OL^T MMAs, copied from
+// shared memory), the per-lane rotation table, the Trig stage, two Z buffers
+constexpr uint32_t kTmS = 0, kTmOT = 16, kTmOL = 32, kTmS1 = 48, kTmLv = 64, kTmTau = 128,
+                   kTmTrig = 192, kTmZ = 256;
 __host__ __device__ constexpr uint32_t tm_s(int b) { return b ? kTmS1 : kTmS; }
 
 template <int D, bool COMP>
@@ -82,12 +83,12 @@ struct Layout {
   static constexpr int oVB = oKB + NKB * TILE_B;   // d = 64: the Vb^T MMA reads 1 KB past a
   static constexpr int oLV = oVB + NVB * TILE_B;   // stage; the Lv^T MMA reads 896 B past LV
   static constexpr int oQ = oLV + LV_B;            // (both land in finite data)
-  static constexpr int oP = oQ + Q_B;
-  static constexpr int oKQ = oP + 2 * P_B;
+  static constexpr int oP = oQ + Q_B;                // one P buffer (see the compute warpgroups)
+  static constexpr int oKQ = oP + P_B;
   static constexpr int oVC = oKQ + KQ_B;
   static constexpr int oVN = oVC + VC_B;
   static constexpr int oMISC = (oVN + VN_B + 127) / 128 * 128;
-  static constexpr int MISC_B = 3072;
+  static constexpr int MISC_B = 2048;
   static constexpr int TOTAL = oMISC + MISC_B;
   static_assert(Q_B >= 1024, "the Lv^T over-read must land in Q");
 };
@@ -123,7 +124,7 @@ struct Misc {
   float red[4][kRows];
   int32_t row_lim[kRows];          // key t is visible to row j iff t < row_lim[j]
   int32_t lim_min[2];              // smallest row_lim of each warpgroup's rows (0: padded rows)
-  float2 rot[2][64];               // cos, sin of t0 * theta_i of a tile (2-tile ring)
+  float2 rot[64];                  // cos, sin of t0 * theta_i of the tile being written
   unsigned long long frac[64];     // theta_i / (2 pi) as a 64-bit binary fraction
   // per compute warpgroup and 8-rank group j: owning agent (0 or 1 within the
   // warpgroup) and the address of key t's 8 ranks,
@@ -132,7 +133,7 @@ struct Misc {
   int32_t gstride[2][8];
   int32_t gagent[2][8];
 };
-static_assert(sizeof(Misc) <= 3072, "Misc must fit its smem slot");
+static_assert(sizeof(Misc) <= 2048, "Misc must fit its smem slot");
 
 struct Item {
   int head, n_rows, n_pages, lp_begin, n_ag, partial_begin, row_begin, n_tiles, page_begin,
@@ -422,23 +423,20 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         const int pb = pt & 1, vs = pt % LY::NVB;
         wait(B_P_FULL0 + pb);
         wait(B_VB_FULL0 + vs);
-        wait(B_LV_FULL);
         if (j == 0) wait(B_ACC_EMPTY);
         tc_fence_after();
         __syncwarp();
         if (elect_one() && !*abort_flag) {
-          const uint64_t dP = sdesc(sbase + LY::oP + pb * LY::P_B, kPChunk, kPRowGroup);
+          const uint64_t dP = sdesc(sbase + LY::oP, kPChunk, kPRowGroup);
           const uint64_t dV = sdesc(sbase + LY::oVB + vs * LY::TILE_B, (D / 8) * 128, 128);
-          const uint64_t dL = sdesc(sbase + LY::oLV, kLvChunk, 128);
 #pragma unroll
           for (int ks = 0; ks < kTileTok / 16; ++ks) {
             const uint32_t acc = (j == 0 && ks == 0) ? 0u : 1u;
             const uint64_t bP = dP + (uint64_t)((ks * 2 * kPChunk) >> 4);
             mma_ss(tmem + kTmOT, dV + (uint64_t)((ks * LY::PAGE_B) >> 4), bP, idS, acc);
-            mma_ss(tmem + kTmOL, dL + (uint64_t)((ks * 2 * kLvChunk) >> 4), bP, idS, acc);
+            mma_ts(tmem + kTmOL, tmem + kTmLv + 8 * ks, bP, idS, acc);
           }
           mma_commit(bar(B_VB_EMPTY0 + vs));
-          mma_commit(bar(B_LV_EMPTY));
           mma_commit(bar(B_PV_DONE0 + pb));
         }
         __syncwarp();
@@ -462,21 +460,43 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         }
         __syncwarp();
       };
-      // per tile k: Z(k), then the next tile's base scores, then the values
-      // of tile k - 1 (which wait for that tile's P), so that neither Z nor S
-      // queues behind a P the compute warpgroups have not written yet
+      // Lv^T of the next tile in order: shared-memory stage -> TMEM
+      // (tcgen05.cp, one 128-lane x 16-key block per K step).  Issued after
+      // the value MMAs that read the previous Lv^T in TMEM (tensor-core
+      // operations of a thread run in issue order); its commit frees the
+      // shared stage, so the following tile's Lv loads for a whole tile.
+      auto copy_lv = [&]() {
+        wait(B_LV_FULL);
+        tc_fence_after();
+        __syncwarp();
+        if (elect_one() && !*abort_flag) {
+          const uint64_t dL = sdesc(sbase + LY::oLV, kLvChunk, 128);
+#pragma unroll
+          for (int ks = 0; ks < kTileTok / 16; ++ks)
+            asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(tmem + kTmLv + 8 * ks),
+                         "l"(dL + (uint64_t)((ks * 2 * kLvChunk) >> 4)));
+          mma_commit(bar(B_LV_EMPTY));
+        }
+        __syncwarp();
+      };
+      // per tile k: Z(k); tile k - 1's Lv^T into TMEM and its values (they
+      // wait for that tile's P; the compute warpgroups' next P waits for
+      // them); the next tile's base scores (still a tile ahead of their use;
+      // they wait for a key tile from memory, which must not hold up the
+      // values).  Nothing ahead of Z(k + 1) waits for a load.
       const int tc0 = tc;
       issue_s(tc0);
       for (int k = 0; k <= I.n_tiles; ++k) {
         if (k == I.n_tiles) {
           if (elect_one()) mma_commit(bar(B_M_EMPTY));   // every Z MMA of the item is issued
           __syncwarp();
+          copy_lv();
           pv(k - 1, tc0 + k - 1);
           break;
         }
         tc = tc0 + k;
         const int kb = tc & 1;
-        wait(B_TRIG_FULL0 + kb);
+        wait(B_TRIG_FULL0);
         for (int c = 0; c < n_zc; ++c, ++zq) {
           const int zb = zq & 1;
           const int ncol = min(kZBuf, zcols - c * kZBuf);
@@ -486,7 +506,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           if (elect_one() && !*abort_flag) {
             const uint32_t idZ = idesc_f16(128, ncol, 0);
             const uint64_t dM = sdesc(sbase + LY::oM + c * (kZBuf / 8) * SBO_M, 128, SBO_M);
-            const uint32_t tA = tmem + kTmTrig + kb * NF;
+            const uint32_t tA = tmem + kTmTrig;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
               mma_ts(tmem + kTmZ + zb * kZBuf, tA + 8 * ks, dM + (uint64_t)(ks * 16), idZ,
@@ -495,8 +515,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           }
           __syncwarp();
         }
+        if (k > 0) {
+          copy_lv();
+          pv(k - 1, tc0 + k - 1);
+        }
         if (k + 1 < I.n_tiles) issue_s(tc + 1);
-        if (k > 0) pv(k - 1, tc0 + k - 1);
       }
       tc = tc0 + I.n_tiles;
     }
@@ -599,6 +622,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
     const int32_t* row_agent_all = (const int32_t*)(ws + p.off_row_agent);
     const int32_t* row_cg_all = (const int32_t*)(ws + p.off_row_cg);
     const CallAgent* ca = (const CallAgent*)(ws + p.off_call_agents);
+    // Trig column i holds [cos, sin]((t0 + lane) theta_i) as an f16 pair.
     // rotation of this lane's key offset tau = ln within a tile, for this
     // warpgroup's frequencies: f16 pairs kept in TMEM
 #pragma unroll 1
@@ -612,10 +636,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       tmem_st16(tmem + kTmTau + f0 + c0 + lane_off, w);
     }
     tmem_wait_st();
-    // Trig of the tile at keys t0 .. t0 + 127 into stage b: column i holds
-    // [cos, sin]((t0 + lane) theta_i) as an f16 pair
-    auto make_trig = [&](int t0, int b) {
-      if (ln < NFH) M.rot[b][f0 + ln] = rot_at(M.frac[f0 + ln], t0);
+    // Trig of a tile (keys t0 .. t0 + 127) into the Trig stage: the tile
+    // start's rotation (exact phase, one frequency per thread) composed in
+    // fp32 with this lane's offset rotation
+    auto make_trig = [&](int t0) {
+      if (ln < NFH) M.rot[f0 + ln] = rot_at(M.frac[f0 + ln], t0);
       named_bar(bar_sync, 128);
 #pragma unroll 1
       for (int c0 = 0; c0 < NFH; c0 += 16) {
@@ -623,22 +648,20 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         tmem_ld16_wait(tmem + kTmTau + f0 + c0 + lane_off, w);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float2 rb = M.rot[b][f0 + c0 + e];
+          const float2 rb = M.rot[f0 + c0 + e];
           const float2 rt = __half22float2(as_h2(w[e]));
           w[e] = pack_h2(rb.x * rt.x - rb.y * rt.y, rb.y * rt.x + rb.x * rt.y);
         }
-        tmem_st16(tmem + kTmTrig + b * NF + f0 + c0 + lane_off, w);
+        tmem_st16(tmem + kTmTrig + f0 + c0 + lane_off, w);
       }
       tmem_wait_st();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_relaxed(bar(B_TRIG_FULL0 + b));
+      named_bar(bar_sync, 128);                 // rot[] readers done before the next write
+      if (lane == 0) mbar_arrive_relaxed(bar(B_TRIG_FULL0));
     };
     int tc = 0, zq = 0, pv_seen = 0;
-    // The value MMAs of tile j signal PV_DONE[j & 1].  They are awaited
-    // lazily (P of tile j reuses the buffer of tile j - 2), so with a single
-    // barrier its phase could run two ahead of the waiter, which parity
-    // waits cannot tell from zero; alternating barriers stay within one.
+    // The value MMAs of tile j signal PV_DONE[j & 1].  Alternating barriers
+    // keep a waiter within one phase of each, which parity waits need.
     auto pv_until = [&](int n) {
       while (pv_seen < n) { wait(B_PV_DONE0 + (pv_seen & 1)); ++pv_seen; }
     };
@@ -732,6 +755,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         }
       };
       prefetch_lk(0);
+      make_trig(lp_begin * kPage);     // the item's first tile
 
       for (int k = 0; k < n_tiles; ++k, ++tc) {
         const int t0 = (lp_begin + k * kTilePages) * kPage;
@@ -744,13 +768,6 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_relaxed(bar(B_S_EMPTY0 + (tc & 1)));
-        // Trig of the next tile (and of this one at the item's first tile),
-        // into the stage whose previous reader, Z(k - 1), this warpgroup has
-        // already waited for.  The MMA warp needs Trig(k + 1) only after its
-        // value MMAs of tile k, which wait for this tile's P anyway.
-#pragma unroll 1
-        for (int kt = (k == 0 ? 0 : k + 1); kt <= k + 1 && kt < n_tiles; ++kt)
-          make_trig((lp_begin + kt * kTilePages) * kPage, (tc + kt - k) & 1);
         {
           const bool ok = lk_ok(k);
 #pragma unroll
@@ -798,6 +815,9 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_relaxed(bar(B_Z_FREE0 + zb));
         }
+        // Trig of the next tile into the single Trig stage: this warpgroup
+        // has waited for every Z MMA of this tile, the stage's only readers
+        if (k + 1 < n_tiles) make_trig(t0 + kTileTok);
         // ---- online softmax (base 2); the running max of a row moves only
         // when the tile max exceeds it by more than 2^8 (then O^T, OL^T are
         // rescaled in TMEM)
@@ -828,9 +848,9 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           raise_max(M, sv[0], sv[1], sv[2], sv[3], sv[4], sv[5], sv[6], sv[7], r0, sw, lane, ln,
                     bar_sync, k > 0, tmem + kTmOT + r0 + lane_off, tmem + kTmOL + r0 + lane_off);
         }
-        // P of this tile into buffer tc & 1 (its previous reader is PV(tc - 2))
-        pv_until(tc - 1);
-        uint8_t* prow = smem + LY::oP + (tc & 1) * LY::P_B + cw * kPRowGroup + (ln / 8) * kPChunk + (ln % 8) * 2;
+        // P of this tile into the P buffer (its previous reader is PV(tc - 1))
+        pv_until(tc);
+        uint8_t* prow = smem + LY::oP + cw * kPRowGroup + (ln / 8) * kPChunk + (ln % 8) * 2;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float m = M.m_used[r0 + j];
@@ -843,6 +863,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         if (lane == 0) mbar_arrive(bar(B_P_FULL0 + (tc & 1)));
         // after the release above: that arrive need not wait for these
         if (k + 1 < n_tiles) prefetch_lk(k + 1);
+
       }
       // ---- epilogue: this warpgroup's rows of the item's split partials
       pv_until(tc);

@@ -1111,6 +1111,8 @@ static int grid_for(int64_t work, int per_block) {
   return (int)(b < 1 ? 1 : (b > 65535 ? 65535 : b));
 }
 
+
+
 int launch_base_append(const PoolGeom& g, int layer, const int32_t* page_of_chunk, int n_chunks,
                        int pos, int n, const uint16_t* Kb, const uint16_t* Vb, void* stream) {
   PageList pl;
