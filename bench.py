@@ -31,10 +31,11 @@ METRIC = "agent decode tokens/sec and achieved HBM GB/s, 8 agents × 32K shared 
 UNIT = "agent-tokens/s"
 WORKLOAD = "llama8b_32k"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ("shared_base_kv_gb300/csrc/fk_kernels.cu",
+KERNEL_SOURCES = ("shared_base_kv_gb300/csrc/fk_decode.cu",
+                  "shared_base_kv_gb300/csrc/fk_kernels.cu",
                   "shared_base_kv_gb300/csrc/fk_device.cuh",
                   "shared_base_kv_gb300/csrc/fk_internal.h")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attention_kernel_llama8b_32k.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_llama8b_32k.txt")
 
 
 def kernel_source_hash() -> str:
