@@ -56,14 +56,18 @@ constexpr int kMaxZ = kRPA * kMaxRankSum;   // Z columns of a tile: (rank, row) 
 constexpr int kZBuf = 128;            // Z columns per TMEM buffer
 constexpr int kPChunk = 144;          // P: 8 keys x 8 rows core matrix, padded
 constexpr int kPRowGroup = 16 * kPChunk;
-constexpr int kLvChunk = 9 * 128;     // Lv^T: 8 rank groups + the ones group
+// [Lv | 1]^T stage: rank group m (8 ranks x 128 keys, 16 core matrices of
+// 8 ranks x 8 keys) at m * kLvGroup; groups 0-7 hold the tile's agents'
+// ranks in column order, group 8 the ones row (TMEM lane 64 of OL^T)
+constexpr int kLvGroup = 16 * 128;
 constexpr int kOnesLane = 64;
 // TMEM columns: base scores (two buffers of 16 rows: 0 and 48), O^T, OL^T
-// (16 rows each), the Lv^T stage (A operand of the OL^T MMAs, copied from
-// shared memory), the per-lane rotation table, the Trig stage, two Z buffers
-constexpr uint32_t kTmS = 0, kTmOT = 16, kTmOL = 32, kTmS1 = 48, kTmLv = 64, kTmTau = 128,
-                   kTmTrig = 192, kTmZ = 256;
+// (16 rows each), two Trig stages (64 and 192), the per-lane rotation
+// table, two Z buffers (one per 128-column chunk of a tile's Z)
+constexpr uint32_t kTmS = 0, kTmOT = 16, kTmOL = 32, kTmS1 = 48, kTmTrig0 = 64, kTmTau = 128,
+                   kTmTrig1 = 192, kTmZ = 256;
 __host__ __device__ constexpr uint32_t tm_s(int b) { return b ? kTmS1 : kTmS; }
+__host__ __device__ constexpr uint32_t tm_trig(int b) { return b ? kTmTrig1 : kTmTrig0; }
 
 template <int D, bool COMP>
 struct Layout {
@@ -72,7 +76,7 @@ struct Layout {
   static constexpr int NKB = 2;
   static constexpr int NVB = COMP ? 1 : 2;
   static constexpr int M_B = (kMaxZ / 8) * (D / 8) * 128;
-  static constexpr int LV_B = 16 * kLvChunk;
+  static constexpr int LV_B = 9 * kLvGroup;
   static constexpr int Q_B = kRows * D * 2;
   static constexpr int P_B = 2 * kPRowGroup;
   static constexpr int KQ_B = COMP ? kTilePages * kPage * D : 0;
@@ -80,30 +84,28 @@ struct Layout {
   static constexpr int VN_B = COMP ? kTilePages * kPage * 4 : 0;
   static constexpr int oM = 0;
   static constexpr int oKB = oM + M_B;
-  static constexpr int oVB = oKB + NKB * TILE_B;   // d = 64: the Vb^T MMA reads 1 KB past a
-  static constexpr int oLV = oVB + NVB * TILE_B;   // stage; the Lv^T MMA reads 896 B past LV
-  static constexpr int oQ = oLV + LV_B;            // (both land in finite data)
-  static constexpr int oP = oQ + Q_B;                // one P buffer (see the compute warpgroups)
-  static constexpr int oKQ = oP + P_B;
+  static constexpr int oVB = oKB + NKB * TILE_B;   // d = 64: the Vb^T MMA reads 1 KB past a stage
+  static constexpr int oLV = oVB + NVB * TILE_B;   // the OL^T MMA (M = 128) reads 16 groups
+  static constexpr int oQ = oLV + LV_B;            // from here: lanes 72-127 are never used
+  static constexpr int oP = oQ + Q_B;                // two P buffers
+  static constexpr int oKQ = oP + 2 * P_B;
   static constexpr int oVC = oKQ + KQ_B;
   static constexpr int oVN = oVC + VC_B;
   static constexpr int oMISC = (oVN + VN_B + 127) / 128 * 128;
   static constexpr int MISC_B = 2048;
-  static constexpr int TOTAL = oMISC + MISC_B;
-  static_assert(Q_B >= 1024, "the Lv^T over-read must land in Q");
+  static constexpr int TOTAL =
+      (oMISC + MISC_B > oLV + 16 * kLvGroup) ? oMISC + MISC_B : oLV + 16 * kLvGroup;
 };
 
 enum {
   B_KB_FULL0, B_KB_FULL1, B_KB_EMPTY0, B_KB_EMPTY1, B_VB_FULL0, B_VB_FULL1, B_VB_EMPTY0,
-  B_VB_EMPTY1, B_LV_FULL, B_LV_EMPTY, B_M_FULL, B_M_EMPTY, B_ITEM_FULL, B_TRIG_FULL0, B_TRIG_FULL1, B_S_FULL0,
-  B_S_FULL1, B_S_EMPTY0, B_S_EMPTY1, B_Z_FULL0, B_Z_FULL1, B_Z_FREE0, B_Z_FREE1, B_P_FULL0, B_P_FULL1, B_PV_DONE0,
+  B_VB_EMPTY1, B_LV_FULL, B_LV_EMPTY, B_M_FULL, B_M_EMPTY, B_ITEM_FULL, B_TRIG_FULL0, B_TRIG_FULL1, B_Z_FULL0, B_Z_FULL1, B_Z_FREE0, B_Z_FREE1, B_P_FULL0, B_P_FULL1, B_PV_DONE0,
   B_PV_DONE1, B_ACC_EMPTY, B_KQ_FULL, B_KQ_EMPTY, B_VC_FULL, B_VC_EMPTY, B_FINAL, B_COUNT
 };
 // Arrival counts: 8 = lane 0 of each warp of both compute warpgroups; 1 =
 // one thread, a bulk-copy transaction count or an MMA commit.
 __host__ __device__ constexpr uint32_t bar_count(int i) {
-  return (i == B_ITEM_FULL || i == B_TRIG_FULL0 || i == B_TRIG_FULL1 || i == B_S_EMPTY0 ||
-          i == B_S_EMPTY1 ||
+  return (i == B_ITEM_FULL || i == B_TRIG_FULL0 || i == B_TRIG_FULL1 ||
           i == B_Z_FREE0 || i == B_Z_FREE1 || i == B_P_FULL0 || i == B_P_FULL1 ||
           i == B_ACC_EMPTY)
              ? 8u
@@ -111,7 +113,7 @@ __host__ __device__ constexpr uint32_t bar_count(int i) {
 }
 constexpr uint64_t kEmptyMask =
     (1ull << B_KB_EMPTY0) | (1ull << B_KB_EMPTY1) | (1ull << B_VB_EMPTY0) | (1ull << B_VB_EMPTY1) |
-    (1ull << B_LV_EMPTY) | (1ull << B_M_EMPTY) | (1ull << B_S_EMPTY0) | (1ull << B_S_EMPTY1) | (1ull << B_Z_FREE0) | (1ull << B_Z_FREE1) |
+    (1ull << B_LV_EMPTY) | (1ull << B_M_EMPTY) | (1ull << B_Z_FREE0) | (1ull << B_Z_FREE1) |
     (1ull << B_ACC_EMPTY) | (1ull << B_KQ_EMPTY) | (1ull << B_VC_EMPTY);
 static_assert(B_COUNT <= 64, "one parity bit per barrier");
 
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
   for (int i = tid * 16; i < LY::TOTAL; i += kThreads * 16) *(uint4*)(smem + i) = make_uint4(0, 0, 0, 0);
   __syncthreads();
   for (int i = tid; i < 16 * 8; i += kThreads)
-    ((uint16_t*)(smem + LY::oLV + (i / 8) * kLvChunk + (kOnesLane / 8) * 128))[i % 8] = 0x3F80;
+    ((uint16_t*)(smem + LY::oLV + (kOnesLane / 8) * kLvGroup + (i / 8) * 128))[i % 8] = 0x3F80;
   if (tid < 64) M.frac[tid] = ((const unsigned long long*)(g.base + g.off_rope + 256))[tid];
   if (tid == 0) {
     for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), bar_count(i));
@@ -380,71 +382,73 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
                      bar(B_VB_FULL0 + st));
           }
         }
+        // Lv^T: one tensor copy per rank group of each agent (its Lv map,
+        // coordinates (0, 0, group, t0 / 8, layer)) into group column / 8 + j
         wait(B_LV_EMPTY);
-        const int ntok = min(kTileTok, g.tcap - t0);
-        const int nch = ntok / 8;                 // 8-key chunks
+        const int n_grp = I.sum_rp / 8;
         __syncwarp();
-        if (lane == 0) {
-          uint32_t bytes = 0;
-#pragma unroll
-          for (int a = 0; a < kA; ++a) bytes += ntok * I.rp[a] * 2;
-          mbar_expect_tx(bar(B_LV_FULL), bytes);
-        }
+        if (lane == 0) mbar_expect_tx(bar(B_LV_FULL), n_grp * kLvGroup);
         __syncwarp();
-        for (int x = lane; x < I.n_ag * nch && !*abort_flag; x += 32) {
-          const int ax = x / nch, c = x % nch;
-          const uint8_t* src = nullptr;
-          int cb = 0, cl = 0;
+        if (lane < n_grp && !*abort_flag) {
+          int pa = 0, j = 0;
 #pragma unroll
           for (int a = 0; a < kA; ++a)
-            if (a == ax) {
-              cb = I.rp[a] * 16;                 // one 8-key chunk of this agent's Lv
-              cl = I.col[a];
-              src = rc_lk(g, I, a, layer) + (int64_t)g.tcap * I.rp[a] * 2 + (int64_t)t0 * I.rp[a] * 2;
-            }
-          bulk_g2s(sbase + LY::oLV + c * kLvChunk + (cl / 8) * 128, src + c * cb, cb, bar(B_LV_FULL));
+            if (a < I.n_ag && lane >= I.col[a] / 8) { pa = I.pool_agent[a]; j = lane - I.col[a] / 8; }
+          const uint8_t* map = g.base + g.off_lvmap + 128LL * pa;
+          asm volatile(
+              "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+              " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(sbase + LY::oLV + lane * kLvGroup),
+              "l"(map), "r"(0), "r"(0), "r"(j), "r"(t0 / 8), "r"(layer), "r"(bar(B_LV_FULL))
+              : "memory");
         }
       };
       for (int k = 0; k < I.n_tiles; ++k, ++tc) load_values(k, tc);
     }
   } else if (warp == 1) {
     // ======================================= MMA issue (converged warp) ====
-    int tc = 0, zq = 0;
     const uint32_t idS = idesc_f16(128, kRows, 1);
+    int tc = 0;
     for (int it = it_begin; it < it_end; ++it) {
       Item I;
       load_item(g, p, ws, it, I);
       const int zcols = kRPA * I.sum_rp;
       const int n_zc = (zcols + kZBuf - 1) / kZBuf;
       wait(B_M_FULL);                    // the item's M
-      wait(B_ITEM_FULL);                 // its Q, row tables
+      wait(B_ITEM_FULL);                 // its Q, row tables, first Trig stages
       tc_fence_after();
+      // values of tile j (global tile pt): O^T += Vb^T P, OL^T += [Lv | 1]^T P,
+      // both A operands in shared memory
       auto pv = [&](int j, int pt) {
         const int pb = pt & 1, vs = pt % LY::NVB;
         wait(B_P_FULL0 + pb);
         wait(B_VB_FULL0 + vs);
+        wait(B_LV_FULL);
         if (j == 0) wait(B_ACC_EMPTY);
         tc_fence_after();
         __syncwarp();
         if (elect_one() && !*abort_flag) {
-          const uint64_t dP = sdesc(sbase + LY::oP, kPChunk, kPRowGroup);
+          const uint64_t dP = sdesc(sbase + LY::oP + pb * LY::P_B, kPChunk, kPRowGroup);
           const uint64_t dV = sdesc(sbase + LY::oVB + vs * LY::TILE_B, (D / 8) * 128, 128);
+          const uint64_t dL = sdesc(sbase + LY::oLV, 128, kLvGroup);
 #pragma unroll
           for (int ks = 0; ks < kTileTok / 16; ++ks) {
             const uint32_t acc = (j == 0 && ks == 0) ? 0u : 1u;
             const uint64_t bP = dP + (uint64_t)((ks * 2 * kPChunk) >> 4);
             mma_ss(tmem + kTmOT, dV + (uint64_t)((ks * LY::PAGE_B) >> 4), bP, idS, acc);
-            mma_ts(tmem + kTmOL, tmem + kTmLv + 8 * ks, bP, idS, acc);
+            mma_ss(tmem + kTmOL, dL + (uint64_t)((ks * 256) >> 4), bP, idS, acc);
           }
           mma_commit(bar(B_VB_EMPTY0 + vs));
+          mma_commit(bar(B_LV_EMPTY));
           mma_commit(bar(B_PV_DONE0 + pb));
         }
         __syncwarp();
       };
-      // base scores of tile k (buffer t & 1 of the two S buffers)
+      // base scores of global tile t into S buffer t & 1.  Its previous
+      // reader, tile t - 2, released it with Z_FREE0 (the compute warpgroups
+      // read S before the first Z chunk), which this warp has waited for.
+      // The Z_FULL commits of tile t cover these MMAs.
       auto issue_s = [&](int t) {
         const int kb = t & 1;
-        wait(B_S_EMPTY0 + kb);
         wait(B_KB_FULL0 + kb);
         tc_fence_after();
         __syncwarp();
@@ -456,71 +460,43 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
             mma_ss(tmem + tm_s(kb), dK + (uint64_t)(ks * 16), dQ + (uint64_t)(ks * 16), idS,
                    ks > 0 ? 1u : 0u);
           mma_commit(bar(B_KB_EMPTY0 + kb));
-          mma_commit(bar(B_S_FULL0 + kb));
         }
         __syncwarp();
       };
-      // Lv^T of the next tile in order: shared-memory stage -> TMEM
-      // (tcgen05.cp, one 128-lane x 16-key block per K step).  Issued after
-      // the value MMAs that read the previous Lv^T in TMEM (tensor-core
-      // operations of a thread run in issue order); its commit frees the
-      // shared stage, so the following tile's Lv loads for a whole tile.
-      auto copy_lv = [&]() {
-        wait(B_LV_FULL);
-        tc_fence_after();
-        __syncwarp();
-        if (elect_one() && !*abort_flag) {
-          const uint64_t dL = sdesc(sbase + LY::oLV, kLvChunk, 128);
-#pragma unroll
-          for (int ks = 0; ks < kTileTok / 16; ++ks)
-            asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(tmem + kTmLv + 8 * ks),
-                         "l"(dL + (uint64_t)((ks * 2 * kLvChunk) >> 4)));
-          mma_commit(bar(B_LV_EMPTY));
-        }
-        __syncwarp();
-      };
-      // per tile k: Z(k); tile k - 1's Lv^T into TMEM and its values (they
-      // wait for that tile's P; the compute warpgroups' next P waits for
-      // them); the next tile's base scores (still a tile ahead of their use;
-      // they wait for a key tile from memory, which must not hold up the
-      // values).  Nothing ahead of Z(k + 1) waits for a load.
+      // per tile k: Z(k) chunk by chunk (Trig(k) was written two tiles
+      // ahead; chunk c waits for the reads of chunk c of tile k - 1), the
+      // next tile's base scores, then the values of tile k - 1, which wait
+      // for that tile's P.  The tensor pipe holds Z(k) and S(k + 1) while
+      // the compute warpgroups finish P(k - 1).
       const int tc0 = tc;
       issue_s(tc0);
-      for (int k = 0; k <= I.n_tiles; ++k) {
-        if (k == I.n_tiles) {
-          if (elect_one()) mma_commit(bar(B_M_EMPTY));   // every Z MMA of the item is issued
-          __syncwarp();
-          copy_lv();
-          pv(k - 1, tc0 + k - 1);
-          break;
-        }
+      for (int k = 0; k < I.n_tiles; ++k) {
         tc = tc0 + k;
-        const int kb = tc & 1;
-        wait(B_TRIG_FULL0);
-        for (int c = 0; c < n_zc; ++c, ++zq) {
-          const int zb = zq & 1;
-          const int ncol = min(kZBuf, zcols - c * kZBuf);
-          wait(B_Z_FREE0 + zb);
+        const int st = tc & 1;
+        wait(B_TRIG_FULL0 + st);
+        for (int c = 0; c < n_zc; ++c) {
+          wait(B_Z_FREE0 + c);
           tc_fence_after();
           __syncwarp();
           if (elect_one() && !*abort_flag) {
+            const int ncol = min(kZBuf, zcols - c * kZBuf);
             const uint32_t idZ = idesc_f16(128, ncol, 0);
             const uint64_t dM = sdesc(sbase + LY::oM + c * (kZBuf / 8) * SBO_M, 128, SBO_M);
-            const uint32_t tA = tmem + kTmTrig;
+            const uint32_t tA = tmem + tm_trig(st);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
-              mma_ts(tmem + kTmZ + zb * kZBuf, tA + 8 * ks, dM + (uint64_t)(ks * 16), idZ,
+              mma_ts(tmem + kTmZ + c * kZBuf, tA + 8 * ks, dM + (uint64_t)(ks * 16), idZ,
                      ks > 0 ? 1u : 0u);
-            mma_commit(bar(B_Z_FULL0 + zb));
+            mma_commit(bar(B_Z_FULL0 + c));
           }
           __syncwarp();
         }
-        if (k > 0) {
-          copy_lv();
-          pv(k - 1, tc0 + k - 1);
-        }
         if (k + 1 < I.n_tiles) issue_s(tc + 1);
+        if (k > 0) pv(k - 1, tc - 1);
       }
+      if (elect_one()) mma_commit(bar(B_M_EMPTY));   // every Z MMA of the item is issued
+      __syncwarp();
+      pv(I.n_tiles - 1, tc0 + I.n_tiles - 1);
       tc = tc0 + I.n_tiles;
     }
     // drain: every MMA issued must complete before tensor memory is freed,
@@ -636,10 +612,10 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       tmem_st16(tmem + kTmTau + f0 + c0 + lane_off, w);
     }
     tmem_wait_st();
-    // Trig of a tile (keys t0 .. t0 + 127) into the Trig stage: the tile
+    // Trig of a tile (keys t0 .. t0 + 127) into Trig stage st: the tile
     // start's rotation (exact phase, one frequency per thread) composed in
     // fp32 with this lane's offset rotation
-    auto make_trig = [&](int t0) {
+    auto make_trig = [&](int t0, int st) {
       if (ln < NFH) M.rot[f0 + ln] = rot_at(M.frac[f0 + ln], t0);
       named_bar(bar_sync, 128);
 #pragma unroll 1
@@ -652,14 +628,14 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           const float2 rt = __half22float2(as_h2(w[e]));
           w[e] = pack_h2(rb.x * rt.x - rb.y * rt.y, rb.y * rt.x + rb.x * rt.y);
         }
-        tmem_st16(tmem + kTmTrig + f0 + c0 + lane_off, w);
+        tmem_st16(tmem + tm_trig(st) + f0 + c0 + lane_off, w);
       }
       tmem_wait_st();
       tc_fence_before();
       named_bar(bar_sync, 128);                 // rot[] readers done before the next write
-      if (lane == 0) mbar_arrive_relaxed(bar(B_TRIG_FULL0));
+      if (lane == 0) mbar_arrive_relaxed(bar(B_TRIG_FULL0 + st));
     };
-    int tc = 0, zq = 0, pv_seen = 0;
+    int tc = 0, pv_seen = 0;
     // The value MMAs of tile j signal PV_DONE[j & 1].  Alternating barriers
     // keep a waiter within one phase of each, which parity waits need.
     auto pv_until = [&](int n) {
@@ -668,8 +644,9 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
     for (int it = it_begin; it < it_end; ++it) {
       int n_tiles, lp_begin, n_pages, n_zc, g_lo, g_hi;
       // ---- item set-up.  Every MMA that read the previous item's Q and
-      // Trig stages has completed (this warpgroup waited for all of them),
-      // so those buffers are free without a barrier of their own.
+      // Trig stages has completed (this warpgroup waited for all of them:
+      // the Z_FULL commits of a tile cover its S MMAs), so those buffers are
+      // free without a barrier of their own.
       named_bar(bar_sync, 128);                 // this warpgroup is done with the tables
       {
         Item I;
@@ -755,19 +732,20 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         }
       };
       prefetch_lk(0);
-      make_trig(lp_begin * kPage);     // the item's first tile
+      // Trig of the item's first two tiles; tile k's Trig goes to stage
+      // (global tile) & 1 and is written two tiles ahead
+      make_trig(lp_begin * kPage, tc & 1);
+      if (n_tiles > 1) make_trig(lp_begin * kPage + kTileTok, (tc + 1) & 1);
 
       for (int k = 0; k < n_tiles; ++k, ++tc) {
         const int t0 = (lp_begin + k * kTilePages) * kPage;
         const int ntok = min(kTileTok, (n_pages - k * kTilePages) * kPage);
-        // base scores of rows r0 .. r0 + 7
+        // base scores of rows r0 .. r0 + 7: S(k) was issued before Z(k), so
+        // the first Z chunk's commit covers it
         uint32_t sv[8];
-        wait(B_S_FULL0 + (tc & 1));
+        wait(B_Z_FULL0);
         tc_fence_after();
         tmem_ld8_wait(tmem + tm_s(tc & 1) + r0 + lane_off, sv);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_relaxed(bar(B_S_EMPTY0 + (tc & 1)));
         {
           const bool ok = lk_ok(k);
 #pragma unroll
@@ -783,10 +761,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < n_zc; ++c, ++zq) {
-          const int zb = zq & 1;
-          wait(B_Z_FULL0 + zb);
-          tc_fence_after();
+        for (int c = 0; c < n_zc; ++c) {
+          if (c > 0) {
+            wait(B_Z_FULL0 + c);
+            tc_fence_after();
+          }
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int j = 4 * c + u;      // 8-rank group of these 32 columns
@@ -795,7 +774,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
               const uint32_t lw[4] = {L.x, L.y, L.z, L.w};
               float t4[kRPA] = {0.f, 0.f, 0.f, 0.f};
               uint32_t v[32];
-              tmem_ld32_wait(tmem + kTmZ + zb * kZBuf + 32 * u + lane_off, v);
+              tmem_ld32_wait(tmem + kTmZ + c * kZBuf + 32 * u + lane_off, v);
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 const float l = (e & 1) ? bf_hi(lw[e / 2]) : bf_lo(lw[e / 2]);
@@ -811,13 +790,12 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
               }
             }
           }
+          // chunk c (and, for c = 0, the S buffer) read: Z(k + 1) chunk c
+          // and S(k + 2) may overwrite them
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_relaxed(bar(B_Z_FREE0 + zb));
+          if (lane == 0) mbar_arrive_relaxed(bar(B_Z_FREE0 + c));
         }
-        // Trig of the next tile into the single Trig stage: this warpgroup
-        // has waited for every Z MMA of this tile, the stage's only readers
-        if (k + 1 < n_tiles) make_trig(t0 + kTileTok);
         // ---- online softmax (base 2); the running max of a row moves only
         // when the tile max exceeds it by more than 2^8 (then O^T, OL^T are
         // rescaled in TMEM)
@@ -848,9 +826,9 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           raise_max(M, sv[0], sv[1], sv[2], sv[3], sv[4], sv[5], sv[6], sv[7], r0, sw, lane, ln,
                     bar_sync, k > 0, tmem + kTmOT + r0 + lane_off, tmem + kTmOL + r0 + lane_off);
         }
-        // P of this tile into the P buffer (its previous reader is PV(tc - 1))
-        pv_until(tc);
-        uint8_t* prow = smem + LY::oP + cw * kPRowGroup + (ln / 8) * kPChunk + (ln % 8) * 2;
+        // P of this tile into P buffer tc & 1 (its previous reader is PV(tc - 2))
+        pv_until(tc - 1);
+        uint8_t* prow = smem + LY::oP + (tc & 1) * LY::P_B + cw * kPRowGroup + (ln / 8) * kPChunk + (ln % 8) * 2;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float m = M.m_used[r0 + j];
@@ -863,6 +841,9 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         if (lane == 0) mbar_arrive(bar(B_P_FULL0 + (tc & 1)));
         // after the release above: that arrive need not wait for these
         if (k + 1 < n_tiles) prefetch_lk(k + 1);
+        // Trig of tile k + 2 into this tile's stage, whose readers (the Z(k)
+        // MMAs) completed before Z_FULL
+        if (k + 2 < n_tiles) make_trig(t0 + 2 * kTileTok, tc & 1);
 
       }
       // ---- epilogue: this warpgroup's rows of the item's split partials

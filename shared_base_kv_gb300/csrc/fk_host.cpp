@@ -1,6 +1,7 @@
 // Host side of libforkkv: pool metadata (page reference counts and free
 // list, copy-on-write appends, agent registry, rCache arena), the work-list
 // planner, and the C ABI.  Kernels live in fk_kernels.cu.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -135,6 +136,7 @@ PoolGeom make_geom(const fk_pool_config* c) {
   g.off_agents = take((int64_t)sizeof(AgentDev) * g.max_agents);
   g.off_rope = take(4LL * 4 * 64);
   g.off_err = take(64);
+  g.off_lvmap = take(128LL * g.max_agents);
   if (g.compressed) {
     int64_t tok = (int64_t)g.L * g.num_pages * g.H_kv * kPage;
     g.off_kq = take(tok * g.d);
@@ -185,14 +187,61 @@ fk_status stage_upload(fk_pool* p, const void* src, size_t bytes, void* dst,
   return FK_OK;
 }
 
+// TMA tensor map of one agent's Lv rows, all layers.  Lv of layer l sits at
+// rc_off + l * rc_layer_bytes + tcap * rp * 2 as [tcap/8 chunks][rp/8 rank
+// groups][8 ranks][8 keys] (bf16); the map's dimensions, innermost first,
+// are (key in chunk, rank in group, rank group, chunk, layer), so a box of
+// (8, 8, 1, 16, 1) is one rank group of a 128-key tile: 16 consecutive
+// 128-byte core matrices (keys past tcap read as zeros).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)f;
+  });
+  return fn;
+}
+
+static fk_status encode_lv_map(const PoolGeom& g, const fk_pool::Agent& A, CUtensorMap* m) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return fail(FK_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  void* base = g.base + A.rc_off + (int64_t)g.tcap * A.rp * 2;
+  const cuuint64_t dims[5] = {8, 8, (cuuint64_t)(A.rp / 8), (cuuint64_t)(g.tcap / 8),
+                              (cuuint64_t)g.L};
+  const cuuint64_t strides[4] = {16, 128, (cuuint64_t)A.rp * 16,
+                                 (cuuint64_t)rc_layer_bytes(g, A.rp)};
+  const cuuint32_t box[5] = {8, 8, 1, 16, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FK_ERR_CUDA, "cuTensorMapEncodeTiled failed for an Lv map");
+  return FK_OK;
+}
+
 fk_status upload_agent(fk_pool* p, int a, cudaStream_t st) {
   const auto& A = p->agents[a];
   AgentDev dv{};
   dv.rp = A.live ? A.rp : 0;
   dv.s = A.s;
   dv.rc_off = A.rc_off;
-  return stage_upload(p, &dv, sizeof(dv),
-                      p->g.base + p->g.off_agents + (int64_t)a * sizeof(AgentDev), st);
+  fk_status r = stage_upload(p, &dv, sizeof(dv),
+                             p->g.base + p->g.off_agents + (int64_t)a * sizeof(AgentDev), st);
+  if (r != FK_OK || !A.live) return r;
+  alignas(64) CUtensorMap m;
+  r = encode_lv_map(p->g, A, &m);
+  if (r != FK_OK) return r;
+  return stage_upload(p, &m, sizeof(m), p->g.base + p->g.off_lvmap + 128LL * a, st);
 }
 
 // ----------------------------------------------------------- planner --
@@ -485,7 +534,7 @@ fk_status fk_pool_create(const fk_pool_config* cfg, void* dev_buf, size_t bytes,
   // zero the page stores (rows never appended must read as finite zeros),
   // the small tables and the compressed copy
   e = cudaMemset(p->g.base + g.off_kb, 0, 2 * g.kb_layer_bytes * g.L);
-  if (e == cudaSuccess) e = cudaMemset(p->g.base + g.off_agents, 0, g.off_err + 64 - g.off_agents);
+  if (e == cudaSuccess) e = cudaMemset(p->g.base + g.off_agents, 0, g.off_lvmap + 128LL * g.max_agents - g.off_agents);
   if (e == cudaSuccess && g.compressed)
     e = cudaMemset(p->g.base + g.off_kq, 0, g.off_kmax + 4LL * g.L - g.off_kq);
   if (e != cudaSuccess) { cudaEventDestroy(p->stage.done); delete p; return cuda_fail(e, "cudaMemset"); }

@@ -41,6 +41,7 @@ struct PoolGeom {
   float rope_base;
   int64_t off_kb, off_vb, off_bk, off_bv, off_agents, off_rope, off_err;
   int64_t off_kq, off_vc, off_vn, off_ks, off_kmax, off_meta, off_ws;
+  int64_t off_lvmap;       // per pool agent: 128-byte TMA tensor map of its Lv (all layers)
   int64_t ws_bytes, meta_bytes;
   int64_t page_bytes;      // bytes of one (page, head) bf16 block: 16*d*2
   int64_t kb_layer_bytes;  // num_pages * H_kv * page_bytes
