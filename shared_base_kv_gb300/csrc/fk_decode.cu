@@ -92,7 +92,7 @@ struct Layout {
   static constexpr int oVC = oKQ + KQ_B;
   static constexpr int oVN = oVC + VC_B;
   static constexpr int oMISC = (oVN + VN_B + 127) / 128 * 128;
-  static constexpr int MISC_B = 2048;
+  static constexpr int MISC_B = 4096;
   static constexpr int TOTAL =
       (oMISC + MISC_B > oLV + 16 * kLvGroup) ? oMISC + MISC_B : oLV + 16 * kLvGroup;
 };
@@ -126,7 +126,8 @@ struct Misc {
   float red[4][kRows];
   int32_t row_lim[kRows];          // key t is visible to row j iff t < row_lim[j]
   int32_t lim_min[2];              // smallest row_lim of each warpgroup's rows (0: padded rows)
-  float2 rot[64];                  // cos, sin of t0 * theta_i of the tile being written
+  float2 rot[8][32];               // per compute warp: cos, sin of t0 * theta_i, its
+                                   // warpgroup's frequencies, for the tile being written
   unsigned long long frac[64];     // theta_i / (2 pi) as a 64-bit binary fraction
   // per compute warpgroup and 8-rank group j: owning agent (0 or 1 within the
   // warpgroup) and the address of key t's 8 ranks,
@@ -135,7 +136,7 @@ struct Misc {
   int32_t gstride[2][8];
   int32_t gagent[2][8];
 };
-static_assert(sizeof(Misc) <= 2048, "Misc must fit its smem slot");
+static_assert(sizeof(Misc) <= 4096, "Misc must fit its smem slot");
 
 struct Item {
   int head, n_rows, n_pages, lp_begin, n_ag, partial_begin, row_begin, n_tiles, page_begin,
@@ -299,9 +300,13 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       load_item(g, p, ws, it, I);
       const int32_t* pages = (const int32_t*)(ws + p.off_pages) + I.page_begin;
       const int tc0 = tc;
+      // page id of this lane's page of the next tile, loaded a tile ahead
+      int pg = lane < min(kTilePages, I.n_pages) ? pages[lane] : 0;
       for (int k = 0; k < I.n_tiles; ++k) {
         const int p0 = k * kTilePages;
         const int np = min(kTilePages, I.n_pages - p0);
+        const int pg_k = pg;
+        if (p0 + kTilePages + lane < I.n_pages && lane < kTilePages) pg = pages[p0 + kTilePages + lane];
         tc = tc0 + k;
         if (!COMP) {
           const int st = tc & 1;
@@ -311,7 +316,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           __syncwarp();
           if (lane < np && !*abort_flag) {
             const uint8_t* src = g.base + g.off_kb + (int64_t)layer * g.kb_layer_bytes +
-                                 ((int64_t)pages[p0 + lane] * g.H_kv + I.head) * LY::PAGE_B;
+                                 ((int64_t)pg_k * g.H_kv + I.head) * LY::PAGE_B;
             bulk_g2s(sbase + LY::oKB + st * LY::TILE_B + lane * LY::PAGE_B, src, LY::PAGE_B,
                      bar(B_KB_FULL0 + st));
           }
@@ -322,7 +327,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           __syncwarp();
           if (lane < np && !*abort_flag) {
             const uint8_t* src = g.base + g.off_kq +
-                                 ((((int64_t)layer * g.num_pages + pages[p0 + lane]) * g.H_kv + I.head) * kPage) * D;
+                                 ((((int64_t)layer * g.num_pages + pg_k) * g.H_kv + I.head) * kPage) * D;
             bulk_g2s(sbase + LY::oKQ + lane * kPage * D, src, kPage * D, bar(B_KQ_FULL));
           }
         }
@@ -353,17 +358,21 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       Item I;
       load_item(g, p, ws, it, I);
       const int32_t* pages = (const int32_t*)(ws + p.off_pages) + I.page_begin;
+      // page id of this lane's page of the next tile, loaded a tile ahead
+      int pg = lane < min(kTilePages, I.n_pages) ? pages[lane] : 0;
       auto load_values = [&](int k, int vt) {
         const int p0 = k * kTilePages;
         const int np = min(kTilePages, I.n_pages - p0);
         const int t0 = (I.lp_begin + p0) * kPage;
+        const int pg_k = pg;
+        if (p0 + kTilePages + lane < I.n_pages && lane < kTilePages) pg = pages[p0 + kTilePages + lane];
         if (COMP) {
           wait(B_VC_EMPTY);
           __syncwarp();
           if (lane == 0) mbar_expect_tx(bar(B_VC_FULL), np * kPage * (3 * D / 8 + 4));
           __syncwarp();
           if (lane < np && !*abort_flag) {
-            const int64_t tok = (((int64_t)layer * g.num_pages + pages[p0 + lane]) * g.H_kv + I.head) * kPage;
+            const int64_t tok = (((int64_t)layer * g.num_pages + pg_k) * g.H_kv + I.head) * kPage;
             bulk_g2s(sbase + LY::oVC + lane * kPage * (3 * D / 8), g.base + g.off_vc + tok * (3 * D / 8),
                      kPage * (3 * D / 8), bar(B_VC_FULL));
             bulk_g2s(sbase + LY::oVN + lane * kPage * 4, g.base + g.off_vn + tok * 4, kPage * 4,
@@ -377,7 +386,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           __syncwarp();
           if (lane < np && !*abort_flag) {
             const uint8_t* src = g.base + g.off_vb + (int64_t)layer * g.kb_layer_bytes +
-                                 ((int64_t)pages[p0 + lane] * g.H_kv + I.head) * LY::PAGE_B;
+                                 ((int64_t)pg_k * g.H_kv + I.head) * LY::PAGE_B;
             bulk_g2s(sbase + LY::oVB + st * LY::TILE_B + lane * LY::PAGE_B, src, LY::PAGE_B,
                      bar(B_VB_FULL0 + st));
           }
@@ -465,9 +474,8 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       };
       // per tile k: Z(k) chunk by chunk (Trig(k) was written two tiles
       // ahead; chunk c waits for the reads of chunk c of tile k - 1), the
-      // next tile's base scores, then the values of tile k - 1, which wait
-      // for that tile's P.  The tensor pipe holds Z(k) and S(k + 1) while
-      // the compute warpgroups finish P(k - 1).
+      // values of tile k - 1, which wait for that tile's P, then the next
+      // tile's base scores, whose keys get the longest lead this way.
       const int tc0 = tc;
       issue_s(tc0);
       for (int k = 0; k < I.n_tiles; ++k) {
@@ -491,8 +499,8 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           }
           __syncwarp();
         }
-        if (k + 1 < I.n_tiles) issue_s(tc + 1);
         if (k > 0) pv(k - 1, tc - 1);
+        if (k + 1 < I.n_tiles) issue_s(tc + 1);
       }
       if (elect_one()) mma_commit(bar(B_M_EMPTY));   // every Z MMA of the item is issued
       __syncwarp();
@@ -613,18 +621,20 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
     }
     tmem_wait_st();
     // Trig of a tile (keys t0 .. t0 + 127) into Trig stage st: the tile
-    // start's rotation (exact phase, one frequency per thread) composed in
-    // fp32 with this lane's offset rotation
+    // start's rotation (exact phase; each warp computes its warpgroup's
+    // frequencies, one per lane, into its own slot, so no other warp is
+    // waited for) composed in fp32 with this lane's offset rotation
+    float2* rotw = M.rot[warp - 3];
     auto make_trig = [&](int t0, int st) {
-      if (ln < NFH) M.rot[f0 + ln] = rot_at(M.frac[f0 + ln], t0);
-      named_bar(bar_sync, 128);
+      if (lane < NFH) rotw[lane] = rot_at(M.frac[f0 + lane], t0);
+      __syncwarp();
 #pragma unroll 1
       for (int c0 = 0; c0 < NFH; c0 += 16) {
         uint32_t w[16];
         tmem_ld16_wait(tmem + kTmTau + f0 + c0 + lane_off, w);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float2 rb = M.rot[f0 + c0 + e];
+          const float2 rb = rotw[c0 + e];
           const float2 rt = __half22float2(as_h2(w[e]));
           w[e] = pack_h2(rb.x * rt.x - rb.y * rt.y, rb.y * rt.x + rb.x * rt.y);
         }
@@ -632,7 +642,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      named_bar(bar_sync, 128);                 // rot[] readers done before the next write
+      __syncwarp();                             // rotw readers done before the next write
       if (lane == 0) mbar_arrive_relaxed(bar(B_TRIG_FULL0 + st));
     };
     int tc = 0, pv_seen = 0;
@@ -715,23 +725,29 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         named_bar(bar_sync, 128);               // tables visible to the whole warpgroup
         if (lane == 0) mbar_arrive(bar(B_ITEM_FULL));
       }
-      // Lk of this thread's key: prefetched into L1 a tile ahead and loaded
-      // once the tile's base scores are read
+      // Lk of this thread's key, loaded into registers a tile ahead: the
+      // loads of tile k + 1 are issued once tile k's Z reduction has used
+      // the registers, so they arrive while this tile finishes
       uint4 lkA[4], lkB[4];            // rank groups 0-3 and 4-7 (two arrays: the chunk
                                        // select below stays a register select)
-      auto lk_ok = [&](int k) { return (lp_begin + k * kTilePages) * kPage + ln < g.tcap; };
-      auto lk_addr = [&](int k, int j) {
+      auto load_lk = [&](int k) {
         const int t = (lp_begin + k * kTilePages) * kPage + ln;
-        return (const uint4*)(M.gbase[cw][j] + (int64_t)(t / 8) * M.gstride[cw][j] + (t % 8) * 16);
-      };
-      auto prefetch_lk = [&](int k) {
-        if (lk_ok(k)) {
+        const bool ok = t < g.tcap;
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (j >= g_lo && j < g_hi) asm volatile("prefetch.global.L1 [%0];" ::"l"(lk_addr(k, j)));
+        for (int j = 0; j < 4; ++j) {
+          lkA[j] = lkB[j] = make_uint4(0, 0, 0, 0);
+          if (j >= g_lo && j < g_hi && ok)
+            lkA[j] = __ldg((const uint4*)(M.gbase[cw][j] + (int64_t)(t / 8) * M.gstride[cw][j] + (t % 8) * 16));
+          if (j + 4 >= g_lo && j + 4 < g_hi && ok)
+            lkB[j] = __ldg((const uint4*)(M.gbase[cw][j + 4] + (int64_t)(t / 8) * M.gstride[cw][j + 4] + (t % 8) * 16));
         }
       };
-      prefetch_lk(0);
+      load_lk(0);
+      // running maxima of this warpgroup's rows, kept in registers (the
+      // shared copy changes only in raise_max)
+      float mreg[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mreg[j] = -INFINITY;
       // Trig of the item's first two tiles; tile k's Trig goes to stage
       // (global tile) & 1 and is written two tiles ahead
       make_trig(lp_begin * kPage, tc & 1);
@@ -746,15 +762,6 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         wait(B_Z_FULL0);
         tc_fence_after();
         tmem_ld8_wait(tmem + tm_s(tc & 1) + r0 + lane_off, sv);
-        {
-          const bool ok = lk_ok(k);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            lkA[j] = lkB[j] = make_uint4(0, 0, 0, 0);
-            if (j >= g_lo && j < g_hi && ok) lkA[j] = __ldg(lk_addr(k, j));
-            if (j + 4 >= g_lo && j + 4 < g_hi && ok) lkB[j] = __ldg(lk_addr(k, j + 4));
-          }
-        }
         // residual scores: acc[4 la + g] = sum_k Lk[t,k] Z[t,(col + k) * 4 + g]
         // for local agent la of this warpgroup
         float acc[8];
@@ -796,6 +803,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_relaxed(bar(B_Z_FREE0 + c));
         }
+        if (k + 1 < n_tiles) load_lk(k + 1);
         // ---- online softmax (base 2); the running max of a row moves only
         // when the tile max exceeds it by more than 2^8 (then O^T, OL^T are
         // rescaled in TMEM)
@@ -806,7 +814,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           for (int j = 0; j < 8; ++j) {
             const float s = (__uint_as_float(sv[j]) + acc[j]) * scale_log2;
             sv[j] = __float_as_uint(s);
-            need |= s > M.m_used[r0 + j] + 8.f;
+            need |= s > mreg[j] + 8.f;
           }
         } else {
           const int tabs = t0 + ln;
@@ -815,7 +823,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
             const bool ok = ln < ntok && tabs < M.row_lim[r0 + j];
             const float s = ok ? (__uint_as_float(sv[j]) + acc[j]) * scale_log2 : -INFINITY;
             sv[j] = __float_as_uint(s);
-            need |= s > M.m_used[r0 + j] + 8.f;
+            need |= s > mreg[j] + 8.f;
           }
         }
         int any;
@@ -825,13 +833,15 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           if (k > 0) pv_until(tc);           // O^T, OL^T hold every earlier tile
           raise_max(M, sv[0], sv[1], sv[2], sv[3], sv[4], sv[5], sv[6], sv[7], r0, sw, lane, ln,
                     bar_sync, k > 0, tmem + kTmOT + r0 + lane_off, tmem + kTmOL + r0 + lane_off);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) mreg[j] = M.m_used[r0 + j];
         }
         // P of this tile into P buffer tc & 1 (its previous reader is PV(tc - 2))
         pv_until(tc - 1);
         uint8_t* prow = smem + LY::oP + (tc & 1) * LY::P_B + cw * kPRowGroup + (ln / 8) * kPChunk + (ln % 8) * 2;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float m = M.m_used[r0 + j];
+          const float m = mreg[j];
           const float pv = exp2f(__uint_as_float(sv[j]) - (m == -INFINITY ? 0.f : m));
           *(__nv_bfloat16*)(prow + j * 16) = __float2bfloat16_rn(pv);
         }
@@ -839,8 +849,6 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_P_FULL0 + (tc & 1)));
-        // after the release above: that arrive need not wait for these
-        if (k + 1 < n_tiles) prefetch_lk(k + 1);
         // Trig of tile k + 2 into this tile's stage, whose readers (the Z(k)
         // MMAs) completed before Z_FULL
         if (k + 2 < n_tiles) make_trig(t0 + 2 * kTileTok, tc & 1);

@@ -355,20 +355,34 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
           total_w += (int64_t)sg.len * (2 + sg.n_ag);
         }
   }
-  int64_t total_pages = 0;
-  for (auto& sg : segs) total_pages += sg.len;
-  const int n_ctas = (int)std::max<int64_t>(1, std::min<int64_t>(target_items, total_pages));
+  int64_t total_tiles = 0;
+  for (auto& sg : segs) total_tiles += (sg.len + kTilePages - 1) / kTilePages;
+  const int n_ctas = (int)std::max<int64_t>(1, std::min<int64_t>(target_items, total_tiles));
   pl.cta_begin.assign(n_ctas + 1, 0);
+  // A CTA that starts a second item pays for it (the item's set-up, its
+  // own M and a drained pipeline: about two tiles of work), so such CTAs
+  // are charged that much extra weight; pieces are cut at whole key tiles
+  // of their segment, so only a segment's last item has a partial tile.
+  auto item_cost = [&](const Seg& sg) { return (int64_t)2 * kTilePages * (2 + sg.n_ag); };
+  int64_t total_wc = total_w;
+  for (size_t i = 1; i < segs.size(); ++i) total_wc += item_cost(segs[i]);
   size_t si = 0;
   int off = 0;           // pages of segs[si] already handed out
   int64_t acc = 0;       // weight handed out so far
   for (int c = 0; c < n_ctas; ++c) {
     pl.cta_begin[c] = (int)pl.items.size();
-    const int64_t goal = total_w * (c + 1) / n_ctas;
+    const int64_t goal = total_wc * (c + 1) / n_ctas;
+    bool first = true;
     while (si < segs.size() && (acc < goal || c == n_ctas - 1)) {
       const Seg& sg = segs[si];
       const int64_t wpp = 2 + sg.n_ag;
+      if (!first) {
+        if (acc + item_cost(sg) >= goal && c != n_ctas - 1) break;
+        acc += item_cost(sg);
+      }
+      first = false;
       int64_t want = (c == n_ctas - 1) ? (sg.len - off) : (goal - acc + wpp - 1) / wpp;
+      want = (want + kTilePages - 1) / kTilePages * kTilePages;
       int take = (int)std::max<int64_t>(1, std::min<int64_t>(want, sg.len - off));
       fk_work_item it{};
       it.head = sg.head;

@@ -114,6 +114,10 @@ def test_plan_balances_pieces():
     # every head covers all 2048 pages twice (two 4-agent row tiles)
     assert set(pages_per_head.values()) == {2 * 2048}
     assert len(items) <= 152 + 16
+    # pieces are cut at whole 128-key tiles of their segment
+    assert all(it["lp_begin"] % 8 == 0 for it in items)
+    tiles = [(it["n_pages"] + 7) // 8 for it in items]
+    assert sum(tiles) == 16 * 256
 
 
 def test_plan_rejects_bad_tables():
