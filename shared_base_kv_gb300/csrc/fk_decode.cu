@@ -728,21 +728,26 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       // Lk of this thread's key, loaded into registers a tile ahead: the
       // loads of tile k + 1 are issued once tile k's Z reduction has used
       // the registers, so they arrive while this tile finishes
-      uint4 lkA[4], lkB[4];            // rank groups 0-3 and 4-7 (two arrays: the chunk
+      uint4 lkA[4] = {}, lkB[4] = {};  // rank groups 0-3 and 4-7 (two arrays: the chunk
                                        // select below stays a register select)
+      // (a lane past the rCache capacity reads the last row instead: its
+      // key is masked; registers of groups this warpgroup does not own keep
+      // stale values and are never read, so no load result is merged with a
+      // constant, which would make the issue wait for the load)
       auto load_lk = [&](int k) {
-        const int t = (lp_begin + k * kTilePages) * kPage + ln;
-        const bool ok = t < g.tcap;
+        const int t = min((lp_begin + k * kTilePages) * kPage + ln, g.tcap - 1);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          lkA[j] = lkB[j] = make_uint4(0, 0, 0, 0);
-          if (j >= g_lo && j < g_hi && ok)
+          if (j >= g_lo && j < g_hi)
             lkA[j] = __ldg((const uint4*)(M.gbase[cw][j] + (int64_t)(t / 8) * M.gstride[cw][j] + (t % 8) * 16));
-          if (j + 4 >= g_lo && j + 4 < g_hi && ok)
+          if (j + 4 >= g_lo && j + 4 < g_hi)
             lkB[j] = __ldg((const uint4*)(M.gbase[cw][j + 4] + (int64_t)(t / 8) * M.gstride[cw][j + 4] + (t % 8) * 16));
         }
       };
       load_lk(0);
+      uint32_t gmask = 0;              // bit j: rank group j belongs to this warpgroup's second agent
+#pragma unroll
+      for (int j = 0; j < 8; ++j) gmask |= (M.gagent[cw][j] == 1) ? (1u << j) : 0u;
       // running maxima of this warpgroup's rows, kept in registers (the
       // shared copy changes only in raise_max)
       float mreg[8];
@@ -788,12 +793,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
                 ffma2(t4[0], t4[1], l, l, __uint_as_float(v[e * kRPA]), __uint_as_float(v[e * kRPA + 1]));
                 ffma2(t4[2], t4[3], l, l, __uint_as_float(v[e * kRPA + 2]), __uint_as_float(v[e * kRPA + 3]));
               }
-              if (M.gagent[cw][j] == 0) {
+              const bool second = (gmask >> j) & 1u;
 #pragma unroll
-                for (int gq = 0; gq < kRPA; ++gq) acc[gq] += t4[gq];
-              } else {
-#pragma unroll
-                for (int gq = 0; gq < kRPA; ++gq) acc[kRPA + gq] += t4[gq];
+              for (int gq = 0; gq < kRPA; ++gq) {
+                acc[gq] += second ? 0.f : t4[gq];
+                acc[kRPA + gq] += second ? t4[gq] : 0.f;
               }
             }
           }
@@ -842,7 +846,10 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float m = mreg[j];
-          const float pv = exp2f(__uint_as_float(sv[j]) - (m == -INFINITY ? 0.f : m));
+          // 2^x of x <= 8 (or -inf): the hardware approximation, far finer
+          // than the bf16 rounding that follows
+          float pv;
+          asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(pv) : "f"(__uint_as_float(sv[j]) - (m == -INFINITY ? 0.f : m)));
           *(__nv_bfloat16*)(prow + j * 16) = __float2bfloat16_rn(pv);
         }
         fence_proxy_async();
