@@ -29,15 +29,16 @@
 // under programmatic dependent launch and waits for that grid only before
 // its first copy of M).
 //
-// Warp roles (384 threads): warp 0 key (and M) bulk copies, warp 11 value
-// bulk copies, warp 1 MMA issue (converged warp, elect.sync), warp 2
-// dequantiser of the compressed pool, warps 3-6 and 7-10 two compute
-// warpgroups.  Warpgroup w owns query rows 8w .. 8w+7
-// (agents 2w, 2w+1): their Z reduction, online softmax, P and epilogue; it
-// also writes its half of the RoPE frequencies of each Trig tile.  Two warps of identical code per SM
-// sub-partition hide each other's latencies.  A warp reaches TMEM lanes
-// 32 (warp % 4) .. +31, so a thread of TMEM lane 32 (warp % 4) + lane
-// handles the key (or d, or rank) of that lane.
+// Warp roles (512 threads): warp 0 key (and M) bulk copies, warp 3 value
+// copies, warp 1 MMA issue (converged warp, elect.sync), warp 2 dequantiser
+// of the compressed pool; warps 4-7 and 8-11 two compute warpgroups;
+// warps 12-15 the Trig warpgroup.  Compute warpgroup w owns query rows
+// 8w .. 8w+7 (agents 2w, 2w+1): their Z reduction, online softmax, P and
+// epilogue.  The Trig warpgroup writes each tile's Trig two tiles ahead.
+// setmaxnreg moves registers from the copy, MMA and Trig warps to the
+// compute warpgroups.  A warp reaches TMEM lanes 32 (warp % 4) .. +31, so
+// a thread of TMEM lane 32 (warp % 4) + lane handles the key (or d, or
+// rank) of that lane.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -48,7 +49,7 @@
 namespace fk {
 namespace dec {
 
-constexpr int kThreads = 384;       // 12 warps
+constexpr int kThreads = 512;       // 16 warps
 constexpr int kRPA = 4;               // query rows per agent
 constexpr int kRows = 16;             // padded query rows of a tile (<= 4 agents)
 constexpr int kA = kMaxAgentsPerTile;
@@ -102,14 +103,14 @@ enum {
   B_VB_EMPTY1, B_LV_FULL, B_LV_EMPTY, B_M_FULL, B_M_EMPTY, B_ITEM_FULL, B_TRIG_FULL0, B_TRIG_FULL1, B_Z_FULL0, B_Z_FULL1, B_Z_FREE0, B_Z_FREE1, B_P_FULL0, B_P_FULL1, B_PV_DONE0,
   B_PV_DONE1, B_ACC_EMPTY, B_KQ_FULL, B_KQ_EMPTY, B_VC_FULL, B_VC_EMPTY, B_FINAL, B_COUNT
 };
-// Arrival counts: 8 = lane 0 of each warp of both compute warpgroups; 1 =
-// one thread, a bulk-copy transaction count or an MMA commit.
+// Arrival counts: 8 = lane 0 of each warp of both compute warpgroups; 4 =
+// lane 0 of each Trig warp; 1 = one thread, a bulk-copy transaction count
+// or an MMA commit.
 __host__ __device__ constexpr uint32_t bar_count(int i) {
-  return (i == B_ITEM_FULL || i == B_TRIG_FULL0 || i == B_TRIG_FULL1 ||
-          i == B_Z_FREE0 || i == B_Z_FREE1 || i == B_P_FULL0 || i == B_P_FULL1 ||
-          i == B_ACC_EMPTY)
+  return (i == B_ITEM_FULL || i == B_Z_FREE0 || i == B_Z_FREE1 || i == B_P_FULL0 ||
+          i == B_P_FULL1 || i == B_ACC_EMPTY)
              ? 8u
-             : 1u;
+             : (i == B_TRIG_FULL0 || i == B_TRIG_FULL1) ? 4u : 1u;
 }
 constexpr uint64_t kEmptyMask =
     (1ull << B_KB_EMPTY0) | (1ull << B_KB_EMPTY1) | (1ull << B_VB_EMPTY0) | (1ull << B_VB_EMPTY1) |
@@ -126,8 +127,8 @@ struct Misc {
   float red[4][kRows];
   int32_t row_lim[kRows];          // key t is visible to row j iff t < row_lim[j]
   int32_t lim_min[2];              // smallest row_lim of each warpgroup's rows (0: padded rows)
-  float2 rot[8][32];               // per compute warp: cos, sin of t0 * theta_i, its
-                                   // warpgroup's frequencies, for the tile being written
+  float2 rot[4][64];               // per Trig warp: cos, sin of t0 * theta_i of the
+                                   // tile being written
   unsigned long long frac[64];     // theta_i / (2 pi) as a 64-bit binary fraction
   // per compute warpgroup and 8-rank group j: owning agent (0 or 1 within the
   // warpgroup) and the address of key t's 8 ranks,
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
   uint64_t ph = kEmptyMask;          // parity each role waits for, bit i for barrier i
   auto wait = [&](int i) {
     uint32_t par = (uint32_t)(ph >> i) & 1u;
-    mbar_wait(bar(i), par, abort_flag, errw);
+    mbar_wait_inl(bar(i), par, abort_flag, errw);
     ph ^= 1ull << i;
   };
   asm volatile("griddepcontrol.launch_dependents;");
@@ -289,6 +290,14 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
   const uint32_t tmem = M.tmem_base;
   const int it_begin = cta_items[blockIdx.x], it_end = cta_items[blockIdx.x + 1];
 
+  // Register split: the copy and MMA warps (warpgroup 0) and the Trig
+  // warpgroup hand registers to the two compute warpgroups; the shares add
+  // up to the launch's 512 x 128 (the dequantiser of the compressed pool
+  // keeps more in warpgroup 0).
+  constexpr int kRegCopy = COMP ? 120 : 104, kRegTrig = 88, kRegCompute = COMP ? 152 : 160;
+  static_assert(128 * kRegCopy + 128 * kRegTrig + 256 * kRegCompute <= 65536, "register split");
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCopy) : "memory");
   if (warp == 0) {
     // ============================================== key copies (warp 0) ====
     // every lane waits; lane 0 posts the transaction count; the lanes then
@@ -350,8 +359,8 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       }
       tc = tc0 + I.n_tiles;
     }
-  } else if (warp == 11) {
-    // ============================================ value copies (warp 11) ====
+  } else if (warp == 3) {
+    // ============================================= value copies (warp 3) ====
     // values of tile k: Vb (or the compressed codes) and the Lv^T stage
     int tc = 0;
     for (int it = it_begin; it < it_end; ++it) {
@@ -592,59 +601,20 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       }
       tc = tc0 + I.n_tiles;
     }
-  } else if (warp >= 3 && warp <= 10) {
-    // ============================================ compute warpgroups ====
-    constexpr int NFH = NF / 2;                      // RoPE frequencies per warpgroup
-    const int cw = (warp - 3) >> 2;                  // warpgroup 0 or 1
+  }
+  } else if (warp < 12) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegCompute) : "memory");
+    // ====================================== compute warpgroups (4-11) ====
+    const int cw = (warp - 4) >> 2;                  // warpgroup 0 or 1
     const int ln = 32 * (warp & 3) + lane;           // TMEM lane = key / d / rank
     const int sw = warp & 3;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const int bar_sync = 1 + 2 * cw, bar_or = 2 + 2 * cw;   // this warpgroup's named barriers
     const int r0 = 8 * cw;                           // first query row of this warpgroup
-    const int f0 = NFH * cw;                         // first frequency of this warpgroup
     const float scale_log2 = 1.4426950408889634f * rsqrtf((float)D);
     const int32_t* row_agent_all = (const int32_t*)(ws + p.off_row_agent);
     const int32_t* row_cg_all = (const int32_t*)(ws + p.off_row_cg);
     const CallAgent* ca = (const CallAgent*)(ws + p.off_call_agents);
-    // Trig column i holds [cos, sin]((t0 + lane) theta_i) as an f16 pair.
-    // rotation of this lane's key offset tau = ln within a tile, for this
-    // warpgroup's frequencies: f16 pairs kept in TMEM
-#pragma unroll 1
-    for (int c0 = 0; c0 < NFH; c0 += 16) {
-      uint32_t w[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float2 r = rot_at(M.frac[f0 + c0 + e], ln);
-        w[e] = pack_h2(r.x, r.y);
-      }
-      tmem_st16(tmem + kTmTau + f0 + c0 + lane_off, w);
-    }
-    tmem_wait_st();
-    // Trig of a tile (keys t0 .. t0 + 127) into Trig stage st: the tile
-    // start's rotation (exact phase; each warp computes its warpgroup's
-    // frequencies, one per lane, into its own slot, so no other warp is
-    // waited for) composed in fp32 with this lane's offset rotation
-    float2* rotw = M.rot[warp - 3];
-    auto make_trig = [&](int t0, int st) {
-      if (lane < NFH) rotw[lane] = rot_at(M.frac[f0 + lane], t0);
-      __syncwarp();
-#pragma unroll 1
-      for (int c0 = 0; c0 < NFH; c0 += 16) {
-        uint32_t w[16];
-        tmem_ld16_wait(tmem + kTmTau + f0 + c0 + lane_off, w);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float2 rb = rotw[c0 + e];
-          const float2 rt = __half22float2(as_h2(w[e]));
-          w[e] = pack_h2(rb.x * rt.x - rb.y * rt.y, rb.y * rt.x + rb.x * rt.y);
-        }
-        tmem_st16(tmem + tm_trig(st) + f0 + c0 + lane_off, w);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();                             // rotw readers done before the next write
-      if (lane == 0) mbar_arrive_relaxed(bar(B_TRIG_FULL0 + st));
-    };
     int tc = 0, pv_seen = 0;
     // The value MMAs of tile j signal PV_DONE[j & 1].  Alternating barriers
     // keep a waiter within one phase of each, which parity waits need.
@@ -753,10 +723,6 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       float mreg[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) mreg[j] = -INFINITY;
-      // Trig of the item's first two tiles; tile k's Trig goes to stage
-      // (global tile) & 1 and is written two tiles ahead
-      make_trig(lp_begin * kPage, tc & 1);
-      if (n_tiles > 1) make_trig(lp_begin * kPage + kTileTok, (tc + 1) & 1);
 
       for (int k = 0; k < n_tiles; ++k, ++tc) {
         const int t0 = (lp_begin + k * kTilePages) * kPage;
@@ -856,9 +822,6 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_P_FULL0 + (tc & 1)));
-        // Trig of tile k + 2 into this tile's stage, whose readers (the Z(k)
-        // MMAs) completed before Z_FULL
-        if (k + 2 < n_tiles) make_trig(t0 + 2 * kTileTok, tc & 1);
 
       }
       // ---- epilogue: this warpgroup's rows of the item's split partials
@@ -898,6 +861,63 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_relaxed(bar(B_ACC_EMPTY));
+    }
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegTrig) : "memory");
+    // ======================================== Trig tiles (warps 12-15) ====
+    // Trig column i of a tile holds [cos, sin]((t0 + lane) theta_i) as an
+    // f16 pair: the tile start's rotation (exact phase, computed by each
+    // warp for itself, one frequency per lane) composed in fp32 with the
+    // rotation of the lane's key offset tau, a table kept in TMEM.  Tile
+    // k's Trig goes to stage (global tile) & 1, written once the Z MMAs of
+    // tile k - 2 (the stage's last readers) have completed.
+    const int ln = 32 * (warp & 3) + lane;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+#pragma unroll 1
+    for (int c0 = 0; c0 < NF; c0 += 16) {
+      uint32_t w[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float2 r = rot_at(M.frac[c0 + e], ln);
+        w[e] = pack_h2(r.x, r.y);
+      }
+      tmem_st16(tmem + kTmTau + c0 + lane_off, w);
+    }
+    tmem_wait_st();
+    float2* rotw = M.rot[warp - 12];
+    auto make_trig = [&](int t0, int st) {
+      for (int f = lane; f < NF; f += 32) rotw[f] = rot_at(M.frac[f], t0);
+      __syncwarp();
+#pragma unroll 1
+      for (int c0 = 0; c0 < NF; c0 += 16) {
+        uint32_t w[16];
+        tmem_ld16_wait(tmem + kTmTau + c0 + lane_off, w);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float2 rb = rotw[c0 + e];
+          const float2 rt = __half22float2(as_h2(w[e]));
+          w[e] = pack_h2(rb.x * rt.x - rb.y * rt.y, rb.y * rt.x + rb.x * rt.y);
+        }
+        tmem_st16(tmem + tm_trig(st) + c0 + lane_off, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();                             // rotw readers done before the next write
+      if (lane == 0) mbar_arrive_relaxed(bar(B_TRIG_FULL0 + st));
+    };
+    int tc = 0;
+    for (int it = it_begin; it < it_end; ++it) {
+      Item I;
+      load_item(g, p, ws, it, I);
+      const int n_zc = (kRPA * I.sum_rp + kZBuf - 1) / kZBuf;
+      const int tb = I.lp_begin * kPage;
+      make_trig(tb, tc & 1);
+      if (I.n_tiles > 1) make_trig(tb + kTileTok, (tc + 1) & 1);
+      for (int k = 0; k < I.n_tiles; ++k, ++tc) {
+        for (int c = 0; c < n_zc; ++c) wait(B_Z_FULL0 + c);   // Z(k) has completed
+        tc_fence_after();
+        if (k + 2 < I.n_tiles) make_trig(tb + (k + 2) * kTileTok, tc & 1);
+      }
     }
   }
   // ---- tear-down.  After a timed-out wait, give bulk copies still in
@@ -982,6 +1002,13 @@ static int launch_decode_t(const PoolGeom& g, const PlanDev& p, int layer, const
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, COMP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL);
     if (e != cudaSuccess) return (int)e;
+    // the warps' register split (setmaxnreg) hands out exactly the block's
+    // launch registers, 512 x 128: a build with another count would leave
+    // the compute warps waiting for registers, so it is refused here
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, decode_kernel<D, COMP>);
+    if (e != cudaSuccess) return (int)e;
+    if (fa.numRegs != 128) return (int)cudaErrorInvalidConfiguration;
     attr_done = true;
   }
   constexpr int units = 8 * dec::kRPA * (D / 2);      // most units of a pair (sum of ranks 64)

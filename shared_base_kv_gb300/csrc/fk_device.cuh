@@ -59,8 +59,10 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // Only the first test is inlined at each call site; the polling loop is out
 // of line, which keeps the warp-specialised kernels' hot loops small enough
 // for the instruction cache.
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
-                                                   volatile int* abort_flag, uint32_t* err_word) {
+template <bool kInline>
+static __device__ __forceinline__ bool mbar_wait_slow_body(uint32_t bar, uint32_t parity,
+                                                           volatile int* abort_flag,
+                                                           uint32_t* err_word) {
   long long t0 = clock64();
   while (true) {
     if (*abort_flag) return false;
@@ -73,6 +75,10 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
     }
   }
 }
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                   volatile int* abort_flag, uint32_t* err_word) {
+  return mbar_wait_slow_body<false>(bar, parity, abort_flag, err_word);
+}
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t& parity,
                                           volatile int* abort_flag,
                                           uint32_t* err_word) {
@@ -80,6 +86,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t& parity,
   parity ^= 1u;
   if (mbar_try(bar, par)) return true;
   return mbar_wait_slow(bar, par, abort_flag, err_word);
+}
+// The same wait with the polling loop inlined, for kernels whose warps run
+// under different register budgets (setmaxnreg): a call from such code to
+// one out-of-line function cannot be register-allocated.  The loop is cold:
+// the first test suspends until the phase completes, so it is never fetched
+// in normal operation.
+__device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t& parity,
+                                              volatile int* abort_flag, uint32_t* err_word) {
+  const uint32_t par = parity;
+  parity ^= 1u;
+  if (mbar_try(bar, par)) return true;
+  return mbar_wait_slow_body<true>(bar, par, abort_flag, err_word);
 }
 
 // Bounded wait that ignores the abort flag: for draining work already in
