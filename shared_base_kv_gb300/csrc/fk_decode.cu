@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           const int st = tc & 1;
           wait(B_KB_EMPTY0 + st);
           __syncwarp();
-          if (lane == 0) mbar_expect_tx(bar(B_KB_FULL0 + st), np * LY::PAGE_B);
+          if (lane == 0) mbar_expect_tx_relaxed(bar(B_KB_FULL0 + st), np * LY::PAGE_B);
           __syncwarp();
           if (lane < np && !*abort_flag) {
             const uint8_t* src = g.base + g.off_kb + (int64_t)layer * g.kb_layer_bytes +
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         } else {
           wait(B_KQ_EMPTY);
           __syncwarp();
-          if (lane == 0) mbar_expect_tx(bar(B_KQ_FULL), np * kPage * D);
+          if (lane == 0) mbar_expect_tx_relaxed(bar(B_KQ_FULL), np * kPage * D);
           __syncwarp();
           if (lane < np && !*abort_flag) {
             const uint8_t* src = g.base + g.off_kq +
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           wait(B_M_EMPTY);
           if (it == it_begin) asm volatile("griddepcontrol.wait;" ::: "memory");
           __syncwarp();
-          if (lane == 0) mbar_expect_tx(bar(B_M_FULL), mbytes);
+          if (lane == 0) mbar_expect_tx_relaxed(bar(B_M_FULL), mbytes);
           __syncwarp();
           for (uint32_t o = lane * 4096u; o < mbytes && !*abort_flag; o += 32u * 4096u)
             bulk_g2s(sbase + LY::oM + o, ws + mpr.mofs + o, min(4096u, mbytes - o), bar(B_M_FULL));
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         if (COMP) {
           wait(B_VC_EMPTY);
           __syncwarp();
-          if (lane == 0) mbar_expect_tx(bar(B_VC_FULL), np * kPage * (3 * D / 8 + 4));
+          if (lane == 0) mbar_expect_tx_relaxed(bar(B_VC_FULL), np * kPage * (3 * D / 8 + 4));
           __syncwarp();
           if (lane < np && !*abort_flag) {
             const int64_t tok = (((int64_t)layer * g.num_pages + pg_k) * g.H_kv + I.head) * kPage;
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           const int st = vt % LY::NVB;
           wait(B_VB_EMPTY0 + st);
           __syncwarp();
-          if (lane == 0) mbar_expect_tx(bar(B_VB_FULL0 + st), np * LY::PAGE_B);
+          if (lane == 0) mbar_expect_tx_relaxed(bar(B_VB_FULL0 + st), np * LY::PAGE_B);
           __syncwarp();
           if (lane < np && !*abort_flag) {
             const uint8_t* src = g.base + g.off_vb + (int64_t)layer * g.kb_layer_bytes +
@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         wait(B_LV_EMPTY);
         const int n_grp = I.sum_rp / 8;
         __syncwarp();
-        if (lane == 0) mbar_expect_tx(bar(B_LV_FULL), n_grp * kLvGroup);
+        if (lane == 0) mbar_expect_tx_relaxed(bar(B_LV_FULL), n_grp * kLvGroup);
         __syncwarp();
         if (lane < n_grp && !*abort_flag) {
           int pa = 0, j = 0;
@@ -954,22 +954,38 @@ __global__ void __launch_bounds__(256) mbuild_kernel(PoolGeom g, PlanDev p, int 
   const AgentDev* ag = (const AgentDev*)(g.base + g.off_agents);
   const int32_t* row_agent = (const int32_t*)(ws + p.off_row_agent) + mp.row_begin;
   const int32_t* row_cg = (const int32_t*)(ws + p.off_row_cg) + mp.row_begin;
+  // the pair's agents and query rows, looked up once per block (the look-
+  // ups are chained loads; done per thread they would serialise)
+  __shared__ int s_pa[kA], s_rp[kA];
+  __shared__ float s_s[kA];
+  __shared__ int64_t s_qrow[kA * kRPA];
+  const int tid = threadIdx.x;
+  if (tid < mp.n_agents) {
+    const int pa_a = ca[tile_agents[mp.agent_begin + tid]].pool_agent;
+    const AgentDev dv = ag[pa_a];
+    s_pa[tid] = pa_a;
+    s_rp[tid] = dv.rp;
+    s_s[tid] = dv.s;
+  }
+  if (tid >= 32 && tid < 32 + mp.n_agents * kRPA) {
+    const int row = tid - 32;
+    const int ci = row_agent[row], cg = row_cg[row];
+    s_qrow[row] = ((int64_t)ci * p.C + cg / g.G) * g.H_q + mp.head * g.G + cg % g.G;
+  }
+  __syncthreads();
   const int u = blockIdx.x * blockDim.x + threadIdx.x;
   const int n_units = (mp.zcols / kRPA / 8) * kRPA * NF;
   if (u >= n_units) return;
   const int i = u % NF, gq = (u / NF) % kRPA, j = u / (NF * kRPA);
   // owning agent of rank group j
-  int col = 0, ai = 0, rp = 0, pa = 0;
-  float sa = 0.f;
+  int col = 0, ai = 0;
   for (int a = 0; a < mp.n_agents; ++a) {
-    const int pa_a = ca[tile_agents[mp.agent_begin + a]].pool_agent;
-    const AgentDev dv = ag[pa_a];
-    if (8 * j >= col && 8 * j < col + dv.rp) { ai = a; rp = dv.rp; pa = pa_a; sa = dv.s; break; }
-    col += dv.rp;
+    if (8 * j >= col && 8 * j < col + s_rp[a]) { ai = a; break; }
+    col += s_rp[a];
   }
-  const int row = ai * kRPA + gq;
-  const int ci = row_agent[row], cg = row_cg[row];
-  const int64_t qrow = ((int64_t)ci * p.C + cg / g.G) * g.H_q + mp.head * g.G + cg % g.G;
+  const int rp = s_rp[ai], pa = s_pa[ai];
+  const float sa = s_s[ai];
+  const int64_t qrow = s_qrow[ai * kRPA + gq];
   const __nv_bfloat16* qp = (const __nv_bfloat16*)(q + qrow * D);
   const __nv_bfloat16* bk = (const __nv_bfloat16*)(g.base + g.off_bk + (int64_t)pa * g.bk_agent_bytes) +
                             ((int64_t)layer * g.H_kv + mp.head) * (int64_t)D * g.rmax_pad;

@@ -37,6 +37,14 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                "r"(bytes)
                : "memory");
 }
+// The same without release semantics, for a producer whose only job is to
+// post the byte count of bulk copies it issues next: it publishes no
+// writes of its own, so it need not wait for its earlier loads to finish.
+__device__ __forceinline__ void mbar_expect_tx_relaxed(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
 // Test-and-wait: the thread may be suspended (up to ~1 ms) until the phase
 // completes instead of spinning, so polling warps leave issue slots to the
 // warps doing the arithmetic.

@@ -1067,16 +1067,37 @@ __global__ void __launch_bounds__(D) combine_kernel(PoolGeom g, PlanDev p, int l
   const int pa = ca[i].pool_agent;
   const AgentDev dv = ag[pa];
   const int b = ptr[row], e = ptr[row + 1];
-  float Mx = -INFINITY;
-  for (int k = b; k < e; ++k) Mx = fmaxf(Mx, part[(int64_t)slots[k] * PS]);
-  float L = 0.f, o = 0.f, ol = 0.f;
-  for (int k = b; k < e; ++k) {
+  // one pass over the splits with a running maximum (log-sum-exp merge);
+  // four splits' loads are issued before any of them is used
+  const bool has_r = d < dv.rp;
+  float Mx = -INFINITY, L = 0.f, o = 0.f, ol = 0.f;
+  auto merge = [&](float m, float l, float ov, float olv) {
+    if (m == -INFINITY) return;                // a split that saw no visible key
+    const float nm = fmaxf(Mx, m);
+    const float a = (Mx == -INFINITY) ? 0.f : exp2f(Mx - nm);
+    const float w = exp2f(m - nm);
+    L = L * a + w * l;
+    o = o * a + w * ov;
+    ol = ol * a + w * olv;
+    Mx = nm;
+  };
+  int k = b;
+  for (; k + 4 <= e; k += 4) {
+    float m[4], l[4], ov[4], olv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float* s = part + (int64_t)slots[k + j] * PS;
+      m[j] = s[0];
+      l[j] = s[1];
+      ov[j] = s[4 + d];
+      olv[j] = has_r ? s[4 + D + d] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) merge(m[j], l[j], ov[j], olv[j]);
+  }
+  for (; k < e; ++k) {
     const float* s = part + (int64_t)slots[k] * PS;
-    const float m = s[0];
-    const float w = (m == -INFINITY) ? 0.f : exp2f(m - Mx);
-    L += w * s[1];
-    o += w * s[4 + d];
-    if (d < dv.rp) ol += w * s[4 + D + d];
+    merge(s[0], s[1], s[4 + d], has_r ? s[4 + D + d] : 0.f);
   }
   if (d < kMaxRankPad) sol[d] = d < dv.rp ? ol : 0.f;
   if (COMP) {
@@ -1096,6 +1117,7 @@ __global__ void __launch_bounds__(D) combine_kernel(PoolGeom g, PlanDev p, int l
   const uint16_t* bv = (const uint16_t*)(g.base + g.off_bv + (int64_t)pa * g.bv_agent_bytes) +
                        (int64_t)layer * g.rmax_pad * g.H_kv * D + h * D + d;
   float up = 0.f;
+#pragma unroll 8
   for (int kk = 0; kk < dv.rp; ++kk) {
     uint16_t u = bv[(int64_t)kk * g.H_kv * D];
     up = fmaf(sol[kk], __bfloat162float(*(const __nv_bfloat16*)&u), up);
