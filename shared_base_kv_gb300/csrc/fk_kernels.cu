@@ -1047,13 +1047,14 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
 // summary, section 3), rotate the value sum of a compressed pool back
 // (inverse FWHT), normalise, round to bf16.
 template <int D, bool COMP>
-__global__ void __launch_bounds__(D) combine_kernel(PoolGeom g, PlanDev p, int layer,
-                                                    uint16_t* __restrict__ out) {
+__global__ void __launch_bounds__(4 * D) combine_kernel(PoolGeom g, PlanDev p, int layer,
+                                                        uint16_t* __restrict__ out) {
   // partials are written by the preceding attention grid
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float sol[kMaxRankPad];
   __shared__ float sx[D];
-  const int row = blockIdx.x, d = threadIdx.x;
+  __shared__ float qo[4][D], qol[4][kMaxRankPad], qm[4], ql[4];
+  const int row = blockIdx.x, d = threadIdx.x % D, qq = threadIdx.x / D;
   const uint8_t* ws = g.base + g.off_ws;
   const int32_t* ptr = (const int32_t*)(ws + p.off_csr_ptr);
   const int32_t* slots = (const int32_t*)(ws + p.off_csr_slots);
@@ -1067,8 +1068,9 @@ __global__ void __launch_bounds__(D) combine_kernel(PoolGeom g, PlanDev p, int l
   const int pa = ca[i].pool_agent;
   const AgentDev dv = ag[pa];
   const int b = ptr[row], e = ptr[row + 1];
-  // one pass over the splits with a running maximum (log-sum-exp merge);
-  // four splits' loads are issued before any of them is used
+  // four thread groups take every fourth split (a log-sum-exp merge with a
+  // running maximum each, all their loads issued first), then group 0
+  // merges the four
   const bool has_r = d < dv.rp;
   float Mx = -INFINITY, L = 0.f, o = 0.f, ol = 0.f;
   auto merge = [&](float m, float l, float ov, float olv) {
@@ -1081,12 +1083,12 @@ __global__ void __launch_bounds__(D) combine_kernel(PoolGeom g, PlanDev p, int l
     ol = ol * a + w * olv;
     Mx = nm;
   };
-  int k = b;
-  for (; k + 4 <= e; k += 4) {
+  int k = b + qq;
+  for (; k + 12 < e; k += 16) {
     float m[4], l[4], ov[4], olv[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float* s = part + (int64_t)slots[k + j] * PS;
+      const float* s = part + (int64_t)slots[k + 4 * j] * PS;
       m[j] = s[0];
       l[j] = s[1];
       ov[j] = s[4 + d];
@@ -1095,23 +1097,31 @@ __global__ void __launch_bounds__(D) combine_kernel(PoolGeom g, PlanDev p, int l
 #pragma unroll
     for (int j = 0; j < 4; ++j) merge(m[j], l[j], ov[j], olv[j]);
   }
-  for (; k < e; ++k) {
+  for (; k < e; k += 4) {
     const float* s = part + (int64_t)slots[k] * PS;
     merge(s[0], s[1], s[4 + d], has_r ? s[4 + D + d] : 0.f);
   }
+  qo[qq][d] = o;
+  if (d < kMaxRankPad) qol[qq][d] = ol;
+  if (d == 0) { qm[qq] = Mx; ql[qq] = L; }
+  __syncthreads();
+  if (qq != 0) return;
+  Mx = -INFINITY; L = 0.f; o = 0.f; ol = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) merge(qm[j], ql[j], qo[j][d], d < kMaxRankPad ? qol[j][d] : 0.f);
   if (d < kMaxRankPad) sol[d] = d < dv.rp ? ol : 0.f;
   if (COMP) {
     sx[d] = o;
-    __syncthreads();
+    asm volatile("bar.sync 1, %0;" ::"r"(D) : "memory");
     for (int hh = 1; hh < D; hh <<= 1) {      // unnormalised FWHT, natural order
       const float a0 = sx[d & ~hh], a1 = sx[d | hh];
-      __syncthreads();
+      asm volatile("bar.sync 1, %0;" ::"r"(D) : "memory");
       sx[d] = (d & hh) ? (a0 - a1) : (a0 + a1);
-      __syncthreads();
+      asm volatile("bar.sync 1, %0;" ::"r"(D) : "memory");
     }
     o = sx[d];
   } else {
-    __syncthreads();
+    asm volatile("bar.sync 1, %0;" ::"r"(D) : "memory");
   }
   // up-projection of the merged low-rank value sum: (sum_t p_t Lv_t) Bv
   const uint16_t* bv = (const uint16_t*)(g.base + g.off_bv + (int64_t)pa * g.bv_agent_bytes) +
@@ -1216,7 +1226,7 @@ static int launch_attn_t(const PoolGeom& g, const PlanDev& p, int layer, const u
   // for that grid inside (programmatic dependent launch)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.n_out_rows);
-  cfg.blockDim = dim3(D);
+  cfg.blockDim = dim3(4 * D);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
