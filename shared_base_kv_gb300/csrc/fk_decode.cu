@@ -940,7 +940,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
 // frequency i): two 16-byte loads of Bk (ranks 8j.. of features i and
 // i + d/2), two query elements, eight f16 pairs out.
 template <int D>
-__global__ void __launch_bounds__(256) mbuild_kernel(PoolGeom g, PlanDev p, int layer,
+__global__ void __launch_bounds__(1024) mbuild_kernel(PoolGeom g, PlanDev p, int layer,
                                                      const uint16_t* __restrict__ q) {
   using namespace dec;
   constexpr int NF = D / 2;
@@ -973,9 +973,11 @@ __global__ void __launch_bounds__(256) mbuild_kernel(PoolGeom g, PlanDev p, int 
     s_qrow[row] = ((int64_t)ci * p.C + cg / g.G) * g.H_q + mp.head * g.G + cg % g.G;
   }
   __syncthreads();
-  const int u = blockIdx.x * blockDim.x + threadIdx.x;
+  // one block per pair (few SMs busy, so most decode CTAs start at once);
+  // each thread takes units tid, tid + 1024, ...
   const int n_units = (mp.zcols / kRPA / 8) * kRPA * NF;
-  if (u >= n_units) return;
+#pragma unroll 2
+  for (int u = tid; u < n_units; u += blockDim.x) {
   const int i = u % NF, gq = (u / NF) % kRPA, j = u / (NF * kRPA);
   // owning agent of rank group j
   int col = 0, ai = 0;
@@ -1005,6 +1007,7 @@ __global__ void __launch_bounds__(256) mbuild_kernel(PoolGeom g, PlanDev p, int 
         pack_h2(x0 * bi + x1 * bh, x1 * bi - x0 * bh);
   }
 }
+  }
 
 // ============================================================ launcher ==
 
@@ -1027,8 +1030,7 @@ static int launch_decode_t(const PoolGeom& g, const PlanDev& p, int layer, const
     if (fa.numRegs != 128) return (int)cudaErrorInvalidConfiguration;
     attr_done = true;
   }
-  constexpr int units = 8 * dec::kRPA * (D / 2);      // most units of a pair (sum of ranks 64)
-  mbuild_kernel<D><<<dim3((units + 255) / 256, p.n_mpairs), 256, 0, st>>>(g, p, layer, q);
+  mbuild_kernel<D><<<dim3(1, p.n_mpairs), 1024, 0, st>>>(g, p, layer, q);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
   // programmatic dependent launch: the decode grid's set-up overlaps the M
