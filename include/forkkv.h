@@ -316,6 +316,64 @@ fk_status fk_plan_host(int A, int C, int H_q, int H_kv, int page_size,
                        int32_t* tile_agents, int cap_tile_agents,
                        int* n_tile_agents);
 
+/* ------------------------------------------------ two-tier prefix index --
+ * Host-only index above the page pool (ForkKV guide, "DualRadixTree:
+ * Two-Tier Hierarchical Cache Indexing", "Two-Tier Lookup Mechanics" and
+ * "Reference Counting and Eviction").  Tier 1 is a radix tree over prompt
+ * token prefixes at page granularity: each node owns the physical bCache
+ * page ids of its span.  Tier 2 is a set of adapter leaves per node: an
+ * adapter id bound to the owner of its residual rows for that prefix (for
+ * example the pool agent slot).  A node counts the adapter leaves at or
+ * below it; only nodes with no such leaf and no children are evicted,
+ * least recently used first.  Only whole pages of an exactly equal prefix
+ * are indexed (a page's keys and values depend on every earlier token).
+ *
+ * A node handle (int64) names the end of a cached prefix; handles stay valid
+ * until that node is evicted.  Handle 0 is the empty prefix.  The index
+ * takes over one pool reference per page passed to fk_radix_insert and gives
+ * it back through the ids that fk_radix_evict returns (release them with
+ * fk_pages_release).  Not thread-safe: one host thread per index.
+ * Errors: FK_ERR_INVALID_ARG with fk_last_error() set; nothing changes. */
+typedef struct fk_radix fk_radix;
+
+fk_status fk_radix_create(int page_size, fk_radix** out);
+void fk_radix_destroy(fk_radix* index);
+
+/* Tier-1 lookup: the longest cached page prefix of tokens[0, n_tokens).
+ * *n_matched = whole pages matched; *node = handle of that prefix's end
+ * (a node is split when the match ends inside its span).  If pages is not
+ * NULL, the matched page ids are written there (cap_pages >= *n_matched).
+ * Marks the prefix as used now. */
+fk_status fk_radix_match(fk_radix* index, const int32_t* tokens, int n_tokens, int32_t* pages,
+                         int cap_pages, int* n_matched, int64_t* node);
+
+/* Caches the whole pages of tokens[0, n_tokens): new_pages[0, n_new) are the
+ * ids of the pages after the currently cached prefix, which n_new must cover
+ * exactly (floor(n_tokens / page_size) - cached pages).  *node = handle of
+ * the prompt's last whole page. */
+fk_status fk_radix_insert(fk_radix* index, const int32_t* tokens, int n_tokens,
+                          const int32_t* new_pages, int n_new, int64_t* node);
+
+/* Tier 2 at a node: *owner = the adapter's owner, or -1 if it has no leaf
+ * (a full hit needs both tiers; base only is the partial hit). */
+fk_status fk_radix_adapter_get(fk_radix* index, int64_t node, int32_t adapter, int32_t* owner);
+/* Adds the adapter's leaf (counted by the node and all its ancestors). */
+fk_status fk_radix_adapter_attach(fk_radix* index, int64_t node, int32_t adapter, int32_t owner);
+/* Removes the leaf; *owner (if not NULL) = its owner, whose residual rows
+ * the caller reclaims at once (fk_agent_release). */
+fk_status fk_radix_adapter_detach(fk_radix* index, int64_t node, int32_t adapter, int32_t* owner);
+
+/* Evicts unreferenced leaf nodes, least recently used first, until at least
+ * want_pages page ids are written to pages_out (or no node is evictable, or
+ * the next node's pages would not fit in cap_pages); *n_out = ids written. */
+fk_status fk_radix_evict(fk_radix* index, int want_pages, int32_t* pages_out, int cap_pages,
+                         int* n_out);
+
+/* Cached nodes (not counting the empty prefix) and pages. */
+fk_status fk_radix_stats(const fk_radix* index, int64_t* n_nodes, int64_t* n_pages);
+/* Adapter leaves at or below a node. */
+fk_status fk_radix_node_ref(const fk_radix* index, int64_t node, int64_t* ref);
+
 #ifdef __cplusplus
 }
 #endif

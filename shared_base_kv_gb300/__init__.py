@@ -112,6 +112,16 @@ def lib() -> ctypes.CDLL:
             "fk_plan_host": (i32, [i32, i32, i32, i32, i32, P32, i32, P32, P32, i32, i32, i32,
                                    ctypes.POINTER(fk_work_item), i32, P32,
                                    P32, P32, i32, P32, P32, i32, P32, P32, i32, P32]),
+            "fk_radix_create": (i32, [i32, ctypes.POINTER(vp)]),
+            "fk_radix_destroy": (None, [vp]),
+            "fk_radix_match": (i32, [vp, P32, i32, P32, i32, ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_int64)]),
+            "fk_radix_insert": (i32, [vp, P32, i32, P32, i32, ctypes.POINTER(ctypes.c_int64)]),
+            "fk_radix_adapter_get": (i32, [vp, i64, ctypes.c_int32, P32]),
+            "fk_radix_adapter_attach": (i32, [vp, i64, ctypes.c_int32, ctypes.c_int32]),
+            "fk_radix_adapter_detach": (i32, [vp, i64, ctypes.c_int32, P32]),
+            "fk_radix_evict": (i32, [vp, i32, P32, i32, ctypes.POINTER(i32)]),
+            "fk_radix_stats": (i32, [vp, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
+            "fk_radix_node_ref": (i32, [vp, i64, ctypes.POINTER(ctypes.c_int64)]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -308,6 +318,76 @@ def fk_plan_host(A: int, C: int, H_q: int, H_kv: int, block_table, seq_lens, ran
                           _p32(ta), n_ta.value, ctypes.byref(n_ta)))
     its = [{f: getattr(items[i], f) for f, _ in fk_work_item._fields_} for i in range(n_it.value)]
     return its, ra[:n_rw.value], rc[:n_rw.value], pg[:n_pg.value], ta[:n_ta.value]
+
+
+# ------------------------------------------------------- two-tier index --
+
+class RadixIndex:
+    """The library's two-tier prefix index (tier 1: token prefixes to bCache
+    pages; tier 2: adapter leaves).  Argument marshalling only."""
+
+    def __init__(self, page_size: int = 16):
+        h = ctypes.c_void_p()
+        _check(lib().fk_radix_create(int(page_size), ctypes.byref(h)))
+        self.h = h
+        self.page_size = int(page_size)
+
+    def close(self) -> None:
+        if self.h:
+            lib().fk_radix_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def match(self, tokens):
+        """(pages matched, their page ids, node handle)."""
+        t = _i32(tokens)
+        cap = t.size // self.page_size
+        pages = np.zeros(max(cap, 1), np.int32)
+        n = ctypes.c_int()
+        node = ctypes.c_int64()
+        _check(lib().fk_radix_match(self.h, _p32(t), t.size, _p32(pages), cap, ctypes.byref(n),
+                                    ctypes.byref(node)))
+        return n.value, pages[:n.value].copy(), node.value
+
+    def insert(self, tokens, new_pages) -> int:
+        t, p = _i32(tokens), _i32(new_pages)
+        node = ctypes.c_int64()
+        _check(lib().fk_radix_insert(self.h, _p32(t), t.size, _p32(p), p.size, ctypes.byref(node)))
+        return node.value
+
+    def adapter_get(self, node: int, adapter: int) -> int:
+        o = ctypes.c_int32()
+        _check(lib().fk_radix_adapter_get(self.h, int(node), int(adapter), ctypes.byref(o)))
+        return o.value
+
+    def adapter_attach(self, node: int, adapter: int, owner: int) -> None:
+        _check(lib().fk_radix_adapter_attach(self.h, int(node), int(adapter), int(owner)))
+
+    def adapter_detach(self, node: int, adapter: int) -> int:
+        o = ctypes.c_int32()
+        _check(lib().fk_radix_adapter_detach(self.h, int(node), int(adapter), ctypes.byref(o)))
+        return o.value
+
+    def evict(self, want_pages: int, cap: int = 1 << 16) -> np.ndarray:
+        out = np.zeros(max(cap, 1), np.int32)
+        n = ctypes.c_int()
+        _check(lib().fk_radix_evict(self.h, int(want_pages), _p32(out), int(cap), ctypes.byref(n)))
+        return out[:n.value].copy()
+
+    def stats(self):
+        a, b = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().fk_radix_stats(self.h, ctypes.byref(a), ctypes.byref(b)))
+        return a.value, b.value
+
+    def node_ref(self, node: int) -> int:
+        r = ctypes.c_int64()
+        _check(lib().fk_radix_node_ref(self.h, int(node), ctypes.byref(r)))
+        return r.value
 
 
 # ------------------------------------------------------------ conveniences --

@@ -501,6 +501,9 @@ int64_t pack_plan(const HostPlan& pl, int A, int C, int causal, const int32_t* a
 
 // ================================================================= ABI ==
 
+// Last-error text for the other translation units of the library.
+void fk_internal_set_error(const char* msg) { g_err = msg; }
+
 extern "C" {
 
 const char* fk_last_error(void) { return g_err.c_str(); }

@@ -233,3 +233,32 @@ def test_load_compressed_round_trip():
         assert np.array_equal(gvc[1, page].transpose(1, 0, 2), vcp[i])
         assert np.array_equal(gvn[1, page].T, vn[i])
     assert pool.region(fk.FK_REGION_KS).cpu().numpy().view(np.float32)[1] == 0.25
+
+
+def test_prefix_index_drives_page_references():
+    """The two-tier index owns one reference per cached page; agents fork
+    their own.  Evicting a prefix returns its ids for release, and a page an
+    agent still holds survives the release (ForkKV guide, "Reference
+    Counting and Eviction")."""
+    pool = _pool(num_pages=8)
+    h = pool.h
+    idx = fk.RadixIndex(16)
+    doc = list(range(16 * 3 + 5))
+    m, _, _ = idx.match(doc)
+    assert m == 0
+    pages = fk.fk_pages_alloc(h, 3)                   # computed by the caller (case C)
+    node = idx.insert(doc, pages)
+    row = fk.fk_fork(h, pages)                        # one agent reads the prefix
+    idx.adapter_attach(node, adapter=1, owner=0)
+    assert [fk.fk_page_refcount(h, int(p)) for p in pages] == [2, 2, 2]
+    assert idx.evict(3).size == 0                     # the adapter depends on it
+    idx.adapter_detach(node, 1)
+    freed = idx.evict(3)
+    assert sorted(freed.tolist()) == sorted(pages.tolist())
+    fk.fk_pages_release(h, freed)
+    assert [fk.fk_page_refcount(h, int(p)) for p in pages] == [1, 1, 1]   # the agent's
+    fk.fk_pages_release(h, row)
+    assert [fk.fk_page_refcount(h, int(p)) for p in pages] == [0, 0, 0]
+    again = fk.fk_pages_alloc(h, 8)                   # every page is free again
+    assert again.size == 8
+    pool.close()
