@@ -40,6 +40,9 @@ EXPORTS = (
     "fk_pool_load_compressed", "fk_residual_attention", "fk_last_launch_count",
     "fk_check", "fk_plan_host", "fk_pool_set_profile_event", "fk_agent_rcache",
     "fk_residual_attention_noalloc",
+    "fk_radix_create", "fk_radix_destroy", "fk_radix_match", "fk_radix_insert",
+    "fk_radix_adapter_get", "fk_radix_adapter_attach", "fk_radix_adapter_detach",
+    "fk_radix_evict", "fk_radix_stats", "fk_radix_node_ref",
 )
 
 
