@@ -160,6 +160,16 @@ fk_status fk_agent_register(fk_pool* pool, int agent, int rank, float s,
                             void* stream);
 fk_status fk_agent_release(fk_pool* pool, int agent);
 
+/* Shared-A (LRAgent summary, "BaseLRShared"): register agent `agent` with
+ * its own up-projections Bk, Bv and scale s but no rCache of its own: it
+ * reads the low-rank rows of live agent `src` (same rank; with A shared by
+ * the adapters, X A is the same for all of them), so those rows are stored
+ * and streamed once.  Appends through either agent write the shared rows.
+ * The rows are reclaimed when the last agent using them is released.
+ * FK_ERR_INVALID_ARG if `agent` is taken or `src` is not live. */
+fk_status fk_agent_register_shared(fk_pool* pool, int agent, int src, float s,
+                                   const uint16_t* Bk, const uint16_t* Bv, void* stream);
+
 /* Where agent `agent`'s residual cache lives: byte offset (from the pool
  * carve-out) of its layer-0 Lk block, the bytes one layer of Lk+Lv takes
  * (Lv follows Lk after half of them), and its padded rank (rank rounded up

@@ -39,7 +39,7 @@ EXPORTS = (
     "fk_base_append", "fk_residual_append", "fk_pool_compress",
     "fk_pool_load_compressed", "fk_residual_attention", "fk_last_launch_count",
     "fk_check", "fk_plan_host", "fk_pool_set_profile_event", "fk_agent_rcache",
-    "fk_residual_attention_noalloc",
+    "fk_residual_attention_noalloc", "fk_agent_register_shared",
     "fk_radix_create", "fk_radix_destroy", "fk_radix_match", "fk_radix_insert",
     "fk_radix_adapter_get", "fk_radix_adapter_attach", "fk_radix_adapter_detach",
     "fk_radix_evict", "fk_radix_stats", "fk_radix_node_ref",
@@ -99,6 +99,7 @@ def lib() -> ctypes.CDLL:
             "fk_page_refcount": (i32, [vp, ctypes.c_int32]),
             "fk_agent_register": (i32, [vp, i32, i32, ctypes.c_float, vp, vp, vp]),
             "fk_agent_release": (i32, [vp, i32]),
+            "fk_agent_register_shared": (i32, [vp, i32, i32, ctypes.c_float, vp, vp, vp]),
             "fk_base_append": (i32, [vp, i32, P32, i32, i32, i32, vp, vp, vp]),
             "fk_residual_append": (i32, [vp, i32, i32, i32, i32, vp, vp, vp]),
             "fk_pool_compress": (i32, [vp, i32, vp]),
@@ -215,6 +216,12 @@ def fk_page_refcount(h, page_id: int) -> int:
 
 def fk_agent_register(h, agent: int, rank: int, s: float, Bk, Bv, stream=None) -> None:
     _check(lib().fk_agent_register(h, agent, rank, float(s), _dev(Bk), _dev(Bv), _stream(stream)))
+
+
+def fk_agent_register_shared(h, agent: int, src: int, s: float, Bk, Bv, stream=None) -> None:
+    """Shared-A: `agent` reads live agent `src`'s low-rank rows."""
+    _check(lib().fk_agent_register_shared(h, agent, src, float(s), _dev(Bk), _dev(Bv),
+                                          _stream(stream)))
 
 
 def fk_agent_release(h, agent: int) -> None:

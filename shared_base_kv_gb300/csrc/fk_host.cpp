@@ -67,6 +67,7 @@ struct fk_pool {
   };
   std::vector<Agent> agents;
   std::map<int64_t, int64_t> rc_free;        // offset -> bytes
+  std::map<int64_t, int> rc_users;           // rCache offset -> agents reading it (Shared-A)
   Staging stage;
   // cached work list
   bool plan_valid = false;
@@ -675,6 +676,7 @@ fk_status fk_agent_register(fk_pool* p, int agent, int rank, float s,
   if (len > need) p->rc_free[off + need] = len - need;
   auto& A = p->agents[agent];
   A.live = true; A.rank = rank; A.rp = rp; A.s = s; A.rc_off = off; A.rc_bytes = need;
+  p->rc_users[off] = 1;
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = cudaMemsetAsync(p->g.base + off, 0, need, st);
   AgentDev dv{rp, s, off};
@@ -683,9 +685,35 @@ fk_status fk_agent_register(fk_pool* p, int agent, int rank, float s,
   fk_status r2 = (e == cudaSuccess) ? upload_agent(p, agent, st) : cuda_fail(e, "agent register");
   if (r2 != FK_OK) {
     A = fk_pool::Agent{};
+    p->rc_users.erase(off);
     p->rc_free[off] = need;
     return r2;
   }
+  p->plan_valid = false;
+  return FK_OK;
+}
+
+fk_status fk_agent_register_shared(fk_pool* p, int agent, int src, float s, const uint16_t* Bk,
+                                   const uint16_t* Bv, void* stream) {
+  if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
+  if (agent < 0 || agent >= p->g.max_agents || src < 0 || src >= p->g.max_agents)
+    return fail(FK_ERR_INVALID_ARG, "agent id out of range");
+  if (p->agents[agent].live) return fail(FK_ERR_INVALID_ARG, "agent id already registered");
+  if (!p->agents[src].live) return fail(FK_ERR_INVALID_ARG, "source agent is not registered");
+  if (!Bk || !Bv) return fail(FK_ERR_INVALID_ARG, "Bk/Bv are NULL");
+  if (!std::isfinite(s)) return fail(FK_ERR_INVALID_ARG, "s must be finite");
+  const auto S = p->agents[src];
+  auto& A = p->agents[agent];
+  A.live = true; A.rank = S.rank; A.rp = S.rp; A.s = s; A.rc_off = S.rc_off; A.rc_bytes = S.rc_bytes;
+  cudaStream_t st = (cudaStream_t)stream;
+  AgentDev dv{A.rp, s, A.rc_off};
+  cudaError_t e = (cudaError_t)launch_agent_register(p->g, agent, A.rank, A.rp, dv, Bk, Bv, stream);
+  fk_status r2 = (e == cudaSuccess) ? upload_agent(p, agent, st) : cuda_fail(e, "agent register");
+  if (r2 != FK_OK) {
+    A = fk_pool::Agent{};
+    return r2;
+  }
+  ++p->rc_users[A.rc_off];
   p->plan_valid = false;
   return FK_OK;
 }
@@ -694,6 +722,15 @@ fk_status fk_agent_release(fk_pool* p, int agent) {
   if (!p || agent < 0 || agent >= p->g.max_agents || !p->agents[agent].live)
     return fail(FK_ERR_INVALID_ARG, "agent not registered");
   auto& A = p->agents[agent];
+  // rows still read by another agent (Shared-A) stay
+  auto u = p->rc_users.find(A.rc_off);
+  if (u != p->rc_users.end() && u->second > 1) {
+    --u->second;
+    A = fk_pool::Agent{};
+    p->plan_valid = false;
+    return upload_agent(p, agent, nullptr);
+  }
+  if (u != p->rc_users.end()) p->rc_users.erase(u);
   // return the range and merge neighbours
   int64_t off = A.rc_off, len = A.rc_bytes;
   auto nx = p->rc_free.lower_bound(off);

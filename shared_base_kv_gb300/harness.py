@@ -16,7 +16,7 @@ from typing import Optional
 import numpy as np
 import torch
 
-from . import (Pool, fk_agent_register, fk_base_append, fk_check, fk_fork, fk_last_launch_count,
+from . import (Pool, fk_agent_register, fk_agent_register_shared, fk_base_append, fk_check, fk_fork, fk_last_launch_count,
                fk_pages_alloc, fk_pages_release, fk_pool_compress, fk_pool_load_compressed,
                fk_residual_append, fk_residual_attention)
 
@@ -25,7 +25,7 @@ class DeviceWorkload:
     def __init__(self, w, *, layers: Optional[list] = None, device: str = "cuda",
                  compressed: Optional[str] = None, codes: Optional[dict] = None,
                  spare_pages: int = 0, workspace_bytes: int = 0,
-                 page_shuffle_seed: Optional[int] = None):
+                 page_shuffle_seed: Optional[int] = None, shared_a: bool = False):
         """``compressed``: None, ``"gpu"`` (encode with fk_pool_compress) or
         ``"codes"`` (load the per-layer codes in ``codes[layer] = (kq,
         k_scale, vcodes_packed, vnorm)``, slot-ordered host arrays)."""
@@ -33,6 +33,7 @@ class DeviceWorkload:
         self.dev = torch.device(device)
         self.layers = list(range(w.n_layers)) if layers is None else list(layers)
         self.compressed = compressed
+        self.shared_a = shared_a
         rmax = int(np.max(w.ranks))
         self.pool = Pool(n_layers=w.n_layers, n_q_heads=w.H_q, n_kv_heads=w.H_kv, head_dim=w.d,
                          num_pages=w.n_slots + spare_pages, max_agents=w.A, max_rank=rmax,
@@ -56,7 +57,12 @@ class DeviceWorkload:
             r = int(w.ranks[a])
             Bk = torch.stack([w.layer(l).bk[a] for l in range(w.n_layers)]).to(self.dev)
             Bv = torch.stack([w.layer(l).bv[a] for l in range(w.n_layers)]).to(self.dev)
-            fk_agent_register(h, a, r, w.s, Bk.contiguous(), Bv.contiguous())
+            if shared_a and a > 0:
+                # Shared-A: agents read agent 0's low-rank rows (the workload's
+                # lk/lv must then be the same for every agent)
+                fk_agent_register_shared(h, a, 0, w.s, Bk.contiguous(), Bv.contiguous())
+            else:
+                fk_agent_register(h, a, r, w.s, Bk.contiguous(), Bv.contiguous())
         for l in self.layers:
             self._load_layer(l, codes)
         # Reference counts: one per agent naming a page.
@@ -75,7 +81,7 @@ class DeviceWorkload:
             n = int(w.slot_fill[slot])
             row = np.array([self.slot_page[slot]], dtype=np.int32)
             fk_base_append(h, l, row, 0, pk[slot, :n].contiguous(), pv[slot, :n].contiguous())
-        for a in range(w.A):
+        for a in range(1 if self.shared_a else w.A):
             fk_residual_append(h, l, a, 0, ld.lk[a].to(self.dev).contiguous(),
                                ld.lv[a].to(self.dev).contiguous())
         if self.compressed == "gpu":

@@ -218,3 +218,20 @@ def test_agent_order_permutes_outputs():
                           False, False, out)
     got = out.float().cpu().numpy()
     assert np.abs(got - base[perm]).max() <= 2e-3
+
+
+def test_parity_shared_a_agents_read_one_low_rank_cache():
+    """Shared-A (LRAgent summary, "BaseLRShared"): every agent has its own B
+    but reads agent 0's low-rank rows; the oracle is given those same rows
+    for every agent."""
+    w = workloads.make_workload("llama8b_32k", prefix=1000, A=8)
+    ld = w.layer(0)
+    for a in range(1, w.A):
+        ld.lk[a] = ld.lk[0]
+        ld.lv[a] = ld.lv[0]
+    dw, out = _run(w, shared_a=True)
+    ref = oracle_out(w, 0)
+    mx, mean, rel = errors(out, ref)
+    assert mx <= MAX_ABS and mean <= MEAN_ABS, (mx, mean, rel)
+    # agents differ only through B: their outputs must differ
+    assert np.abs(out[0] - out[1]).max() > 1e-3

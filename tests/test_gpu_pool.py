@@ -262,3 +262,24 @@ def test_prefix_index_drives_page_references():
     again = fk.fk_pages_alloc(h, 8)                   # every page is free again
     assert again.size == 8
     pool.close()
+
+
+def test_shared_a_rows_live_until_the_last_reader_is_released():
+    pool = _pool(agents=4)
+    h = pool.h
+    Bk, Bv = _bf16((L, 16, H * D), 5), _bf16((L, 16, H * D), 6)
+    fk.fk_agent_register(h, 0, 16, 1.0, Bk, Bv)
+    fk.fk_agent_register_shared(h, 1, 0, 0.5, Bk, Bv)
+    off0, lb0, rp0 = fk.fk_agent_rcache(h, 0)
+    off1, lb1, rp1 = fk.fk_agent_rcache(h, 1)
+    assert (off0, lb0, rp0) == (off1, lb1, rp1)
+    with pytest.raises(fk.FKError):
+        fk.fk_agent_register_shared(h, 2, 3, 1.0, Bk, Bv)     # source not registered
+    fk.fk_agent_release(h, 0)
+    assert fk.fk_agent_rcache(h, 1)[0] == off1                # agent 1 still reads the rows
+    fk.fk_agent_register(h, 2, 16, 1.0, Bk, Bv)
+    assert fk.fk_agent_rcache(h, 2)[0] != off1                # not handed out again
+    fk.fk_agent_release(h, 1)
+    fk.fk_agent_register(h, 3, 16, 1.0, Bk, Bv)
+    assert fk.fk_agent_rcache(h, 3)[0] == off1                # reclaimed after the last reader
+    pool.close()
