@@ -200,6 +200,26 @@ fk_status fk_residual_append(fk_pool* pool, int layer, int agent, int pos,
                              int n, const uint16_t* Lk, const uint16_t* Lv,
                              void* stream);
 
+/* Low-rank prefill of agent `agent`, layer `layer`: computes Lk = X A_k and
+ * Lv = X A_v for tokens pos..pos+n-1 on the device and writes them into the
+ * agent's rCache (ForkKV guide, "Two-Tier Lookup Mechanics", case B: the
+ * base cache already holds the prefix, so only the adapter's low-rank
+ * projection of the hidden states is computed; LRAgent summary,
+ * "BaseShared").  X: dev bf16 [n][d_model] row-major, the layer's input
+ * hidden states (after its norm) of those tokens; Ak, Av: dev bf16
+ * [d_model][rank] row-major (rank = the agent's registered rank).  The
+ * product accumulates in fp32 over d_model and is rounded once to bf16
+ * (nearest even).  d_model a positive multiple of 128; X, Ak, Av 16-byte
+ * aligned; pos + n <= max_tokens.  The caller keeps ownership of X, Ak,
+ * Av, which must stay valid until the stream reaches the call.  For a
+ * Shared-A agent the rows land in the rCache it shares.
+ * FK_ERR_INVALID_ARG on a bad argument (nothing is launched); a launch
+ * failure is FK_ERR_CUDA; a kernel that timed out on a wait sets the
+ * pool's error word (fk_check) and writes no rows. */
+fk_status fk_residual_prefill(fk_pool* pool, int layer, int agent, int pos, int n,
+                              const uint16_t* X, const uint16_t* Ak, const uint16_t* Av,
+                              int d_model, void* stream);
+
 /* ---- compressed shared pool (PolyKV summary, section 2B) ---- */
 
 /* Encode layer `layer` of every live page (reference count > 0, rows that

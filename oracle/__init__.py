@@ -17,6 +17,9 @@ materialised (no blocking, fusion or reordering):
   "BaseShared").
 * ``compress`` -- int8 per-tensor keys and 3-bit FWHT + Lloyd-Max values with
   a per-vector norm (PolyKV summary, section 2B).
+* ``lowrank`` -- the residual prefill ``Lk = X A_k``, ``Lv = X A_v`` of an
+  agent over a prefix the base cache already holds (ForkKV guide, "Two-Tier
+  Lookup Mechanics", case B).
 * ``paging`` -- the sharing classes of a block table (which agents name the
   same physical page at the same logical page; ForkKV guide, "Two-Tier Lookup
   Mechanics" and "The Copy-on-Write Paradigm").
@@ -35,3 +38,4 @@ from .compress import (  # noqa: F401
     k_int8_decode, v3_encode, v3_decode, pack_planes, unpack_planes,
     compression_ratio, encode_pages, decode_pages)
 from .paging import page_classes, coverage  # noqa: F401
+from .lowrank import lowrank_projection, lora_projection  # noqa: F401

@@ -42,7 +42,7 @@ EXPORTS = (
     "fk_residual_attention_noalloc", "fk_agent_register_shared",
     "fk_radix_create", "fk_radix_destroy", "fk_radix_match", "fk_radix_insert",
     "fk_radix_adapter_get", "fk_radix_adapter_attach", "fk_radix_adapter_detach",
-    "fk_radix_evict", "fk_radix_stats", "fk_radix_node_ref",
+    "fk_radix_evict", "fk_radix_stats", "fk_radix_node_ref", "fk_residual_prefill",
 )
 
 
@@ -102,6 +102,7 @@ def lib() -> ctypes.CDLL:
             "fk_agent_register_shared": (i32, [vp, i32, i32, ctypes.c_float, vp, vp, vp]),
             "fk_base_append": (i32, [vp, i32, P32, i32, i32, i32, vp, vp, vp]),
             "fk_residual_append": (i32, [vp, i32, i32, i32, i32, vp, vp, vp]),
+            "fk_residual_prefill": (i32, [vp, i32, i32, i32, i32, vp, vp, vp, i32, vp]),
             "fk_pool_compress": (i32, [vp, i32, vp]),
             "fk_pool_load_compressed": (i32, [vp, i32, P32, i32, vp, vp, vp, ctypes.c_float, vp]),
             "fk_residual_attention": (i32, [vp, i32, vp, P32, P32, i32, P32, i32, i32, i32,
@@ -249,6 +250,14 @@ def fk_base_append(h, layer: int, block_table_row: np.ndarray, pos: int, Kb, Vb,
 def fk_residual_append(h, layer: int, agent: int, pos: int, Lk, Lv, stream=None) -> None:
     _check(lib().fk_residual_append(h, layer, agent, pos, int(Lk.shape[0]), _dev(Lk), _dev(Lv),
                                     _stream(stream)))
+
+
+def fk_residual_prefill(h, layer: int, agent: int, pos: int, X, Ak, Av, stream=None) -> None:
+    """Lk = X Ak, Lv = X Av (X: bf16 [n][d_model], Ak/Av: bf16
+    [d_model][rank]) computed on the device into the agent's rCache rows
+    pos..pos+n-1."""
+    _check(lib().fk_residual_prefill(h, layer, agent, pos, int(X.shape[0]), _dev(X), _dev(Ak),
+                                     _dev(Av), int(X.shape[1]), _stream(stream)))
 
 
 def fk_pool_compress(h, layer: int, stream=None) -> None:

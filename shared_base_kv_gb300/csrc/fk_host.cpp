@@ -845,6 +845,28 @@ fk_status fk_residual_append(fk_pool* p, int layer, int agent, int pos, int n,
   return FK_OK;
 }
 
+fk_status fk_residual_prefill(fk_pool* p, int layer, int agent, int pos, int n,
+                              const uint16_t* X, const uint16_t* Ak, const uint16_t* Av,
+                              int d_model, void* stream) {
+  if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
+  if (layer < 0 || layer >= p->g.L) return fail(FK_ERR_INVALID_ARG, "layer out of range");
+  if (agent < 0 || agent >= p->g.max_agents || !p->agents[agent].live)
+    return fail(FK_ERR_INVALID_ARG, "agent not registered");
+  if (pos < 0 || n < 0 || (int64_t)pos + n > p->cfg.max_tokens)
+    return fail(FK_ERR_INVALID_ARG, "rows out of the rCache capacity");
+  if (d_model <= 0 || d_model % 128 != 0)
+    return fail(FK_ERR_INVALID_ARG, "d_model must be a positive multiple of 128");
+  if (n == 0) return FK_OK;
+  if (!X || !Ak || !Av) return fail(FK_ERR_INVALID_ARG, "X/Ak/Av are NULL");
+  if (((uintptr_t)X | (uintptr_t)Ak | (uintptr_t)Av) % 16 != 0)
+    return fail(FK_ERR_INVALID_ARG, "X/Ak/Av must be 16-byte aligned");
+  const auto& A = p->agents[agent];
+  AgentDev dv{A.rp, A.s, A.rc_off};
+  int e = launch_residual_prefill(p->g, layer, dv, A.rank, pos, n, d_model, X, Ak, Av, stream);
+  if (e != 0) return cuda_fail((cudaError_t)e, "residual prefill kernel");
+  return FK_OK;
+}
+
 fk_status fk_pool_compress(fk_pool* p, int layer, void* stream) {
   if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
   if (!p->g.compressed) return fail(FK_ERR_INVALID_ARG, "pool has no compressed copy");

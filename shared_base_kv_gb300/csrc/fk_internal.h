@@ -91,6 +91,11 @@ int launch_base_append(const PoolGeom& g, int layer, const int32_t* page_of_chun
 int launch_residual_append(const PoolGeom& g, int layer, const AgentDev& ag,
                            int r, int pos, int n, const uint16_t* Lk,
                            const uint16_t* Lv, void* stream);
+// Lk = X A_k and Lv = X A_v of tokens pos..pos+n-1 on the tensor cores,
+// written into the agent's rCache (fk_prefill.cu).
+int launch_residual_prefill(const PoolGeom& g, int layer, const AgentDev& ag, int r, int pos,
+                            int n, int d_model, const uint16_t* X, const uint16_t* Ak,
+                            const uint16_t* Av, void* stream);
 int launch_agent_register(const PoolGeom& g, int agent, int r, int rp,
                           const AgentDev& ag, const uint16_t* Bk,
                           const uint16_t* Bv, void* stream);

@@ -102,6 +102,75 @@ def test_rope_linearity_makes_post_rope_base_shareable():
     assert np.allclose(lhs, rhs, atol=1e-12)
 
 
+# ------------------------------------------------------ low-rank prefill ----
+
+def test_lowrank_projection_brute_force_integers():
+    # small integers: every product and sum is exact, so the sums written
+    # out by hand must agree to the last bit
+    rng = _rng(21)
+    X = rng.integers(-4, 5, (3, 5)).astype(np.float64)
+    A = rng.integers(-4, 5, (5, 2)).astype(np.float64)
+    got = oracle.lowrank_projection(X, A)
+    assert got.shape == (3, 2)
+    for i in range(3):
+        for j in range(2):
+            acc = 0.0
+            for k in range(5):
+                acc += X[i, k] * A[k, j]
+            assert got[i, j] == acc
+
+
+def test_lowrank_projection_special_cases():
+    rng = _rng(22)
+    X = rng.standard_normal((6, 8))
+    assert np.array_equal(oracle.lowrank_projection(X, np.eye(8)), X)        # A = I
+    assert not oracle.lowrank_projection(X, np.zeros((8, 3))).any()          # A = 0
+    A = rng.standard_normal((8, 4))
+    perm = np.array([2, 0, 3, 1])
+    # permuting A's columns permutes the factor's columns; scaling X's rows
+    # scales the factor's rows
+    assert np.allclose(oracle.lowrank_projection(X, A[:, perm]),
+                       oracle.lowrank_projection(X, A)[:, perm], atol=1e-13)
+    dsc = np.arange(1.0, 7.0)
+    assert np.allclose(oracle.lowrank_projection(dsc[:, None] * X, A),
+                       dsc[:, None] * oracle.lowrank_projection(X, A), atol=1e-12)
+    with pytest.raises(ValueError):
+        oracle.lowrank_projection(X, A.T)                                     # transposed operand
+    # bf16 inputs are taken at their exact values
+    xb = torch.tensor(X, dtype=torch.bfloat16)
+    ab = torch.tensor(A, dtype=torch.bfloat16)
+    assert np.array_equal(oracle.lowrank_projection(xb, ab),
+                          xb.double().numpy() @ ab.double().numpy())
+
+
+def test_lowrank_factor_rebuilds_lora_keys_and_values():
+    # base cache (post-RoPE X W0 per head) + the prefill's factor X A through
+    # the oracle's residual materialisation equals the merged-weight LoRA
+    # projection X (W0 + s A B), rotated for keys (ForkKV guide, "Mathematical
+    # Decomposition of LoRA KV Activations")
+    rng = _rng(23)
+    T, dm, H_kv, d, r, s, base = 9, 16, 2, 8, 3, 0.75, 10000.0
+    X = rng.standard_normal((T, dm))
+    W0k, W0v = rng.standard_normal((dm, H_kv * d)), rng.standard_normal((dm, H_kv * d))
+    Ak, Av = rng.standard_normal((dm, r)), rng.standard_normal((dm, r))
+    Bk, Bv = rng.standard_normal((r, H_kv * d)), rng.standard_normal((r, H_kv * d))
+    pos = np.arange(T)
+    lk, lv = oracle.lowrank_projection(X, Ak), oracle.lowrank_projection(X, Av)
+    full_k = oracle.lora_projection(X, W0k, Ak, Bk, s)
+    full_v = oracle.lora_projection(X, W0v, Av, Bv, s)
+    for h in range(H_kv):
+        cols = slice(h * d, (h + 1) * d)
+        kb = oracle.rope(X @ W0k[:, cols], pos, base)
+        vb = X @ W0v[:, cols]
+        k, v = oracle.agent_kv(kb, vb, lk, lv, Bk, Bv, s, h, pos, base)
+        assert np.allclose(k, oracle.rope(full_k[:, cols], pos, base), atol=1e-10)
+        assert np.allclose(v, full_v[:, cols], atol=1e-10)
+    # the factors of the two projections are not interchangeable
+    k_swapped, _ = oracle.agent_kv(oracle.rope(X @ W0k[:, :d], pos, base), X @ W0v[:, :d],
+                                   lv, lk, Bk, Bv, s, 0, pos, base)
+    assert not np.allclose(k_swapped, oracle.rope(full_k[:, :d], pos, base), atol=1e-3)
+
+
 # ----------------------------------------------------------- attention ----
 
 def _tiny_inputs(seed, A=2, T=(5, 3), H_q=4, H_kv=2, d=8, r=(2, 3), P=4,
