@@ -6,6 +6,11 @@ bf16 base cache in 16-token pages (H_q=32, H_kv=8, d=128, rank 16), one
 decode query per agent.  A step is one ``fk_residual_attention`` call: the
 attention kernel plus the split-K combine.  Prints one JSON line.
 
+The line also carries ``prefill``: the low-rank prefill a forked agent runs
+over that shared prefix before its first decode step (``Lk = X A_k``,
+``Lv = X A_v`` over the 32,768 prefix tokens, d_model 4096, rank 16, one
+``fk_residual_prefill`` call), timed on its own with its own roofline.
+
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
 N > 1 runs one independent replica per GPU (the path has no data exchange);
@@ -36,11 +41,16 @@ KERNEL_SOURCES = ("shared_base_kv_gb300/csrc/fk_decode.cu",
                   "shared_base_kv_gb300/csrc/fk_device.cuh",
                   "shared_base_kv_gb300/csrc/fk_internal.h")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_llama8b_32k.txt")
+PREFILL_SOURCES = ("shared_base_kv_gb300/csrc/fk_prefill.cu",
+                   "shared_base_kv_gb300/csrc/fk_device.cuh",
+                   "shared_base_kv_gb300/csrc/fk_internal.h")
+PREFILL_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "prefill_kernel_llama8b_32k.txt")
+PREFILL_SHAPE = {"n": 32768, "d_model": 4096, "rank": 16}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -72,17 +82,17 @@ def measured_peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_per_launch():
+def traffic_per_launch(path=TRAFFIC_FILE, sources=KERNEL_SOURCES):
     """dram read+write bytes per launch from the committed ncu summary, if it
     was taken on the current kernel sources."""
     try:
         vals = {}
-        with open(TRAFFIC_FILE) as f:
+        with open(path) as f:
             for line in f:
                 if ":" in line:
                     k, v = line.split(":", 1)
                     vals[k.strip()] = v.strip()
-        if vals.get("kernel_source_sha256") != kernel_source_hash():
+        if vals.get("kernel_source_sha256") != kernel_source_hash(sources):
             return None
         return int(float(vals["dram_bytes_per_launch"]))
     except Exception:
@@ -215,6 +225,22 @@ def reduce_over_ranks(total_ms: float, e2e_ms: float, units: int, e2e_units: int
             e2e_units * world / (e2e_ms / 1e3), e2e_ms)
 
 
+class L2Flush:
+    """Between timed launches: write a buffer of twice the L2 size, then read
+    another one, so that L2 holds none of the next launch's inputs and the
+    write's dirty lines are written back before the launch's events start
+    (left dirty, their write-back would be charged to the next kernel)."""
+
+    def __init__(self, dev, l2_bytes: int):
+        import torch
+        self.w = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(2 * l2_bytes // 4, dtype=torch.float32, device=dev)
+
+    def zero_(self):
+        self.w.zero_()
+        self.r.sum()
+
+
 def run_gb300(args, rank: int, world: int, local_rank: int):
     import numpy as np
     import torch
@@ -235,8 +261,7 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
     stream = torch.cuda.current_stream(dev)
     h = dw.pool.h
     props = torch.cuda.get_device_properties(dev)
-    flush = torch.empty(int(2 * getattr(props, "L2_cache_size", 128 << 20)), dtype=torch.uint8,
-                        device=dev)
+    flush = L2Flush(dev, int(getattr(props, "L2_cache_size", 128 << 20)))
 
     def step():
         fk_residual_attention(h, 0, q, agents, bt, seq, False, False, out, stream)
@@ -291,6 +316,7 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
     e2e_ms = sum(e_s[k].elapsed_time(e_e[k]) for k in range(KE))
     ok = bool(torch.isfinite(out.float()).all().item())
     dw.check()
+    prefill = measure_prefill(dev, stream, flush, args.prefill_steps) if args.prefill_steps else None
     value, total_ms, e2e_value, e2e_ms = reduce_over_ranks(
         total_ms, e2e_ms, w.A * K, w.A * KE, world, dev)
     ab = algorithmic_bytes(w)
@@ -303,7 +329,8 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "flushed between steps (memset of 2x L2), outside the step's events",
+                   "l2": "flushed between steps, outside the step's events: a memset of 2x L2, "
+                         "then a read of another 2x L2 buffer (writes back the dirty lines)",
                    "step_hbm_gbs": ab["step"] / (total_ms / K / 1e3) / 1e9,
                    "step_bytes": ab["step"]},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -318,8 +345,57 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
         "gpu_launches": launches,
         "clocks": clk,
         "outputs_finite": ok,
+        "prefill": prefill,
     }
     return res
+
+
+def measure_prefill(dev, stream, flush, steps: int) -> dict:
+    """One forked agent's low-rank prefill over the shared prefix, timed
+    with CUDA events on the launching stream (L2 flushed between launches,
+    outside the events)."""
+    import torch
+    from shared_base_kv_gb300 import Pool, fk_agent_register, fk_check, fk_residual_prefill
+    n, dm, r = PREFILL_SHAPE["n"], PREFILL_SHAPE["d_model"], PREFILL_SHAPE["rank"]
+    pool = Pool(n_layers=1, n_q_heads=32, n_kv_heads=8, head_dim=128, num_pages=4,
+                max_agents=1, max_rank=r, max_tokens=n)
+    g = torch.Generator(device=dev).manual_seed(1234)
+    B = torch.zeros(1, r, 8 * 128, dtype=torch.bfloat16, device=dev)
+    fk_agent_register(pool.h, 0, r, 1.0, B, B)
+    X = torch.randn(n, dm, generator=g, device=dev).to(torch.bfloat16)
+    Ak = (torch.randn(dm, r, generator=g, device=dev) / dm ** 0.5).to(torch.bfloat16)
+    Av = (torch.randn(dm, r, generator=g, device=dev) / dm ** 0.5).to(torch.bfloat16)
+    for _ in range(3):
+        fk_residual_prefill(pool.h, 0, 0, 0, X, Ak, Av, stream)
+    torch.cuda.synchronize(dev)
+    # all launches are enqueued before one synchronize, so the host's own
+    # call overhead overlaps the flush and never sits inside the events
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        fk_residual_prefill(pool.h, 0, 0, 0, X, Ak, Av, stream)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    fk_check(pool.h, stream)
+    pool.close()
+    avg = statistics.mean(ms)
+    algo = n * dm * 2 + 2 * dm * r * 2 + 2 * n * r * 2
+    peak, peak_kind = measured_peak_hbm()
+    achieved = algo / (avg / 1e3) / 1e9
+    return {
+        "workload": f"one agent's low-rank prefill over {n} shared prefix tokens, "
+                    f"d_model {dm}, rank {r}: X [{n}, {dm}] bf16 times A_k, A_v [{dm}, {r}]",
+        "ms": avg, "launches": steps,
+        "tokens_per_s": n / (avg / 1e3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "traffic": traffic_per_launch(PREFILL_TRAFFIC_FILE, PREFILL_SOURCES),
+                     "kernel": f"lr_prefill_kernel<{r}>", "bytes_per_launch": algo,
+                     "peak_kind": f"{peak_kind} hbm_gbs"},
+    }
 
 
 def run_reference(args):
@@ -356,6 +432,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--prefill-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", type=float, default=None)
     args = ap.parse_args()

@@ -861,8 +861,21 @@ fk_status fk_residual_prefill(fk_pool* p, int layer, int agent, int pos, int n,
   if (((uintptr_t)X | (uintptr_t)Ak | (uintptr_t)Av) % 16 != 0)
     return fail(FK_ERR_INVALID_ARG, "X/Ak/Av must be 16-byte aligned");
   const auto& A = p->agents[agent];
+  // X as 128-row x 64-feature boxes in the 128-byte swizzle the MMA reads;
+  // rows past n are filled with zeros
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return fail(FK_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  alignas(64) CUtensorMap xm;
+  const cuuint64_t dims[2] = {(cuuint64_t)d_model, (cuuint64_t)n};
+  const cuuint64_t strides[1] = {(cuuint64_t)d_model * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  if (fn(&xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)X, dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return fail(FK_ERR_CUDA, "cuTensorMapEncodeTiled failed for X");
   AgentDev dv{A.rp, A.s, A.rc_off};
-  int e = launch_residual_prefill(p->g, layer, dv, A.rank, pos, n, d_model, X, Ak, Av, stream);
+  int e = launch_residual_prefill(p->g, layer, dv, A.rank, pos, n, d_model, &xm, Ak, Av, stream);
   if (e != 0) return cuda_fail((cudaError_t)e, "residual prefill kernel");
   return FK_OK;
 }

@@ -92,9 +92,10 @@ int launch_residual_append(const PoolGeom& g, int layer, const AgentDev& ag,
                            int r, int pos, int n, const uint16_t* Lk,
                            const uint16_t* Lv, void* stream);
 // Lk = X A_k and Lv = X A_v of tokens pos..pos+n-1 on the tensor cores,
-// written into the agent's rCache (fk_prefill.cu).
+// written into the agent's rCache (fk_prefill.cu).  x_map: 128-byte TMA
+// tensor map of X ([n][d_model] bf16, 64 x 128 boxes, 128-byte swizzle).
 int launch_residual_prefill(const PoolGeom& g, int layer, const AgentDev& ag, int r, int pos,
-                            int n, int d_model, const uint16_t* X, const uint16_t* Ak,
+                            int n, int d_model, const void* x_map, const uint16_t* Ak,
                             const uint16_t* Av, void* stream);
 int launch_agent_register(const PoolGeom& g, int agent, int r, int rp,
                           const AgentDev& ag, const uint16_t* Bk,

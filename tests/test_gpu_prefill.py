@@ -70,14 +70,15 @@ def _check_factor(got_u16, X, A):
     assert rel < 4e-3, rel
 
 
+@pytest.mark.parametrize("ranks", [(8, 24, 40, 64), (16, 32, 48, 56)])
 @pytest.mark.parametrize("dm", [128, 384])
-def test_prefill_matches_oracle_for_every_padded_rank(dm):
-    # ranks 8, 24, 40, 64 give padded ranks 16, 32, 48, 64: every tile width
-    # the kernel instantiates; 300 tokens = two whole 128-token tiles and a
-    # ragged tail, starting at a position that is not a multiple of 8
+def test_prefill_matches_oracle_for_every_rank(dm, ranks):
+    # every rank the kernel instantiates (padded ranks 16, 32, 48, 64, with
+    # and without padding columns); 300 tokens = two whole 128-token tiles
+    # and a ragged tail, starting at a position that is not a multiple of 8
     pool = _pool()
     pos, n, layer = 37, 300, 1
-    for agent, r in enumerate((8, 24, 40, 64)):
+    for agent, r in enumerate(ranks):
         B = torch.zeros(L, r, H * D, dtype=torch.bfloat16).cuda()
         fk.fk_agent_register(pool.h, agent, r, 1.0, B, B)
         X = _hidden(n, dm, 100 + agent)
