@@ -404,6 +404,51 @@ fk_status fk_radix_stats(const fk_radix* index, int64_t* n_nodes, int64_t* n_pag
 /* Adapter leaves at or below a node. */
 fk_status fk_radix_node_ref(const fk_radix* index, int64_t node, int64_t* ref);
 
+/* ---------------------------------------------- workflow-aware eviction --
+ * KVFlow review, "Agent Step Graph and Steps-to-Execution" and
+ * "Workflow-aware eviction".  An agent's steps-to-execution is the number of
+ * workflow steps before it runs again.  Each agent marks its fixed-prompt
+ * prefix node (and every ancestor) with that value; a node's priority is the
+ * smallest value marking it, so a prefix shared by several agents is kept
+ * while any of them runs soon.  fk_radix_evict_workflow then evicts the
+ * evictable leaf (no adapter leaf at or below it, no children) with the
+ * largest priority first: unmarked nodes (dynamic suffixes) before every
+ * marked node, equal priorities least recently used first; a parent becomes
+ * a candidate once its last child is gone.  Evicting a node leaves the marks
+ * its agents put on the ancestors (the agent still needs the shared prefix).
+ * A split copies the marks of the split node to its new prefix node. */
+
+/* One agent with steps-to-execution `step` (>= 0) whose fixed prompt ends
+ * at `node` (not the root): +1 on that step's count at node and ancestors. */
+fk_status fk_radix_priority_assign(fk_radix* index, int64_t node, int32_t step);
+/* Undoes one such assignment (FK_ERR_INVALID_ARG, and no change, if a node
+ * on the path holds no count for that step). */
+fk_status fk_radix_priority_release(fk_radix* index, int64_t node, int32_t step);
+/* Drops every assignment (before marking the next workflow step's values). */
+fk_status fk_radix_priority_clear(fk_radix* index);
+/* *priority = the node's priority, or -1 if no agent marks it. */
+fk_status fk_radix_node_priority(const fk_radix* index, int64_t node, int32_t* priority);
+/* Evicts as described above until at least want_pages page ids are written
+ * to pages_out (or nothing is evictable, or the next node's pages would not
+ * fit in cap_pages); *n_out = ids written, in eviction order. */
+fk_status fk_radix_evict_workflow(fk_radix* index, int want_pages, int32_t* pages_out,
+                                  int cap_pages, int* n_out);
+
+/* Steps-to-execution of every agent of an agent step graph.  Agent i's
+ * predecessors are preds[pred_offsets[i] .. pred_offsets[i+1]) (host, CSR,
+ * pred_offsets[0] = 0, ids in [0, n_agents)); join[i] is FK_JOIN_AND (the
+ * agent waits for all predecessors: max of their values + 1) or FK_JOIN_OR
+ * (any predecessor triggers it: min + 1); fixed[i] >= 0 gives agent i's
+ * value directly (e.g. 0 for agents that run in the current step), -1 lets
+ * it be computed.  steps[i] (host, out) = the value, or -1 if the agent
+ * never runs: no fixed value and no predecessor, an AND over a predecessor
+ * that never runs, or an OR whose predecessors all never run.
+ * FK_ERR_INVALID_ARG (steps untouched) on bad arguments or on a cycle whose
+ * agents have no fixed value. */
+enum { FK_JOIN_AND = 0, FK_JOIN_OR = 1 };
+fk_status fk_workflow_steps(int n_agents, const int32_t* pred_offsets, const int32_t* preds,
+                            const int32_t* join, const int32_t* fixed, int32_t* steps);
+
 #ifdef __cplusplus
 }
 #endif

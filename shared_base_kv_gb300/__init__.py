@@ -43,6 +43,8 @@ EXPORTS = (
     "fk_radix_create", "fk_radix_destroy", "fk_radix_match", "fk_radix_insert",
     "fk_radix_adapter_get", "fk_radix_adapter_attach", "fk_radix_adapter_detach",
     "fk_radix_evict", "fk_radix_stats", "fk_radix_node_ref", "fk_residual_prefill",
+    "fk_radix_priority_assign", "fk_radix_priority_release", "fk_radix_priority_clear",
+    "fk_radix_node_priority", "fk_radix_evict_workflow", "fk_workflow_steps",
 )
 
 
@@ -127,6 +129,12 @@ def lib() -> ctypes.CDLL:
             "fk_radix_evict": (i32, [vp, i32, P32, i32, ctypes.POINTER(i32)]),
             "fk_radix_stats": (i32, [vp, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
             "fk_radix_node_ref": (i32, [vp, i64, ctypes.POINTER(ctypes.c_int64)]),
+            "fk_radix_priority_assign": (i32, [vp, i64, i32]),
+            "fk_radix_priority_release": (i32, [vp, i64, i32]),
+            "fk_radix_priority_clear": (i32, [vp]),
+            "fk_radix_node_priority": (i32, [vp, i64, ctypes.POINTER(i32)]),
+            "fk_radix_evict_workflow": (i32, [vp, i32, P32, i32, ctypes.POINTER(i32)]),
+            "fk_workflow_steps": (i32, [i32, P32, P32, P32, P32, P32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -407,6 +415,48 @@ class RadixIndex:
         r = ctypes.c_int64()
         _check(lib().fk_radix_node_ref(self.h, int(node), ctypes.byref(r)))
         return r.value
+
+    def priority_assign(self, node: int, step: int) -> None:
+        _check(lib().fk_radix_priority_assign(self.h, int(node), int(step)))
+
+    def priority_release(self, node: int, step: int) -> None:
+        _check(lib().fk_radix_priority_release(self.h, int(node), int(step)))
+
+    def priority_clear(self) -> None:
+        _check(lib().fk_radix_priority_clear(self.h))
+
+    def node_priority(self, node: int) -> Optional[int]:
+        """The node's priority, or None if no agent marks it."""
+        p = ctypes.c_int32()
+        _check(lib().fk_radix_node_priority(self.h, int(node), ctypes.byref(p)))
+        return None if p.value < 0 else p.value
+
+    def evict_workflow(self, want_pages: int, cap: int = 1 << 16) -> np.ndarray:
+        out = np.zeros(max(cap, 1), np.int32)
+        n = ctypes.c_int()
+        _check(lib().fk_radix_evict_workflow(self.h, int(want_pages), _p32(out), int(cap),
+                                             ctypes.byref(n)))
+        return out[:n.value].copy()
+
+
+FK_JOIN_AND, FK_JOIN_OR = 0, 1
+
+
+def workflow_steps(preds, join, fixed):
+    """Steps-to-execution of every agent of an agent step graph:
+    ``preds[i]`` lists agent i's predecessors, ``join[i]`` is FK_JOIN_AND or
+    FK_JOIN_OR, ``fixed[i]`` a given value or None.  Returns a list with
+    None for agents that never run."""
+    n = len(preds)
+    off = np.zeros(n + 1, np.int32)
+    for i, p in enumerate(preds):
+        off[i + 1] = off[i] + len(p)
+    flat = _i32([int(x) for p in preds for x in p] or [0])
+    j = _i32([int(x) for x in join] or [0])
+    f = _i32([-1 if v is None else int(v) for v in fixed] or [0])
+    out = np.zeros(max(n, 1), np.int32)
+    _check(lib().fk_workflow_steps(n, _p32(off), _p32(flat), _p32(j), _p32(f), _p32(out)))
+    return [None if v < 0 else int(v) for v in out[:n]]
 
 
 # ------------------------------------------------------------ conveniences --

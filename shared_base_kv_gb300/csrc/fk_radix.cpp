@@ -17,15 +17,29 @@
 // depends on every earlier token, so only whole pages of an exactly equal
 // prefix are shared; a trailing partial page is never indexed.
 //
+// Workflow-aware eviction (KVFlow review, "Agent Step Graph and
+// Steps-to-Execution", "Workflow-aware eviction"): an agent's
+// steps-to-execution (how many workflow steps until it runs again) follows
+// from its predecessors' values, max + 1 behind a barrier (AND), min + 1
+// behind a branch (OR).  Each agent marks its fixed-prompt node and every
+// ancestor with its value; a node's priority is the smallest value that
+// marks it (a shared prefix is kept while any of its agents runs soon).
+// Eviction by priority removes the evictable leaf with the largest priority
+// first (unmarked nodes, e.g. dynamic suffixes, before all marked ones;
+// ties least recently used first) and considers a parent once its last
+// child is gone.
+//
 // The index owns one pool reference per page it holds; the caller takes
 // those references when it inserts pages and drops them (fk_pages_release)
 // for the ids that eviction returns.  Agents that use the pages hold their
 // own references (fk_fork), so evicting a page from the index never frees
 // a page an agent still reads.
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <map>
 #include <memory>
+#include <queue>
 #include <string>
 #include <vector>
 
@@ -42,6 +56,7 @@ struct Node {
   std::map<int32_t, int32_t> adapters;       // tier 2: adapter id -> rCache owner (agent slot)
   int64_t ref = 0;                           // adapter leaves at or below this node
   uint64_t last_use = 0;                     // logical clock of the last lookup through it
+  std::map<int32_t, int32_t> steps;          // steps-to-execution -> agents marking this node
 };
 
 }  // namespace
@@ -100,6 +115,7 @@ Node* split(fk_radix* r, Node* node, int k) {
   head->pages.assign(node->pages.begin(), node->pages.begin() + k);
   head->ref = node->ref;
   head->last_use = node->last_use;
+  head->steps = node->steps;   // every mark on node passed through its prefix
   std::unique_ptr<Node> own = std::move(parent->children[key]);
   parent->children.erase(key);
   node->tokens.erase(node->tokens.begin(), node->tokens.begin() + (size_t)k * P);
@@ -267,6 +283,140 @@ fk_status fk_radix_node_ref(const fk_radix* r, int64_t node, int64_t* ref) {
   auto it = r->by_id.find(node);
   if (it == r->by_id.end()) return rfail(FK_ERR_INVALID_ARG, "unknown node");
   *ref = it->second->ref;
+  return FK_OK;
+}
+
+// ------------------------------------------------- workflow priorities --
+
+fk_status fk_radix_priority_assign(fk_radix* r, int64_t node, int32_t step) {
+  if (!r || step < 0) return rfail(FK_ERR_INVALID_ARG, "NULL index or negative step");
+  auto it = r->by_id.find(node);
+  if (it == r->by_id.end() || node == 0) return rfail(FK_ERR_INVALID_ARG, "unknown node or the root");
+  for (Node* x = it->second; x && x != r->root.get(); x = x->parent) ++x->steps[step];
+  return FK_OK;
+}
+
+fk_status fk_radix_priority_release(fk_radix* r, int64_t node, int32_t step) {
+  if (!r) return rfail(FK_ERR_INVALID_ARG, "NULL index");
+  auto it = r->by_id.find(node);
+  if (it == r->by_id.end() || node == 0) return rfail(FK_ERR_INVALID_ARG, "unknown node or the root");
+  for (Node* x = it->second; x && x != r->root.get(); x = x->parent)
+    if (!x->steps.count(step)) return rfail(FK_ERR_INVALID_ARG, "no such assignment on this path");
+  for (Node* x = it->second; x && x != r->root.get(); x = x->parent)
+    if (--x->steps[step] == 0) x->steps.erase(step);
+  return FK_OK;
+}
+
+fk_status fk_radix_priority_clear(fk_radix* r) {
+  if (!r) return rfail(FK_ERR_INVALID_ARG, "NULL index");
+  for (auto& kv : r->by_id) kv.second->steps.clear();
+  return FK_OK;
+}
+
+fk_status fk_radix_node_priority(const fk_radix* r, int64_t node, int32_t* priority) {
+  if (!r || !priority) return rfail(FK_ERR_INVALID_ARG, "NULL argument");
+  auto it = r->by_id.find(node);
+  if (it == r->by_id.end()) return rfail(FK_ERR_INVALID_ARG, "unknown node");
+  *priority = it->second->steps.empty() ? -1 : it->second->steps.begin()->first;
+  return FK_OK;
+}
+
+fk_status fk_radix_evict_workflow(fk_radix* r, int want_pages, int32_t* pages_out, int cap_pages,
+                                  int* n_out) {
+  if (!r || !n_out || (!pages_out && cap_pages) || cap_pages < 0)
+    return rfail(FK_ERR_INVALID_ARG, "NULL argument or negative capacity");
+  *n_out = 0;
+  // eviction order: larger priority first (unmarked = above every step),
+  // then the least recently used
+  auto prio = [](const Node* x) -> int64_t {
+    return x->steps.empty() ? INT64_MAX : (int64_t)x->steps.begin()->first;
+  };
+  auto later = [&](const Node* a, const Node* b) {   // true: a leaves after b
+    const int64_t pa = prio(a), pb = prio(b);
+    if (pa != pb) return pa < pb;
+    return a->last_use > b->last_use;
+  };
+  std::priority_queue<Node*, std::vector<Node*>, decltype(later)> heap(later);
+  for (auto& kv : r->by_id) {
+    Node* x = kv.second;
+    if (x != r->root.get() && x->ref == 0 && x->children.empty()) heap.push(x);
+  }
+  while (*n_out < want_pages && !heap.empty()) {
+    Node* v = heap.top();
+    if (*n_out + (int)v->pages.size() > cap_pages) break;
+    heap.pop();
+    std::copy(v->pages.begin(), v->pages.end(), pages_out + *n_out);
+    *n_out += (int)v->pages.size();
+    r->n_pages -= (int64_t)v->pages.size();
+    Node* parent = v->parent;
+    r->by_id.erase(v->id);
+    parent->children.erase(page_key(v->tokens.data(), r->P));   // frees v
+    if (parent != r->root.get() && parent->ref == 0 && parent->children.empty()) heap.push(parent);
+  }
+  return FK_OK;
+}
+
+fk_status fk_workflow_steps(int n_agents, const int32_t* pred_offsets, const int32_t* preds,
+                            const int32_t* join, const int32_t* fixed, int32_t* steps) {
+  if (n_agents < 0 || (n_agents > 0 && (!pred_offsets || !join || !fixed || !steps)))
+    return rfail(FK_ERR_INVALID_ARG, "NULL argument or negative agent count");
+  if (n_agents == 0) return FK_OK;
+  if (pred_offsets[0] != 0) return rfail(FK_ERR_INVALID_ARG, "pred_offsets[0] must be 0");
+  for (int i = 0; i < n_agents; ++i) {
+    if (pred_offsets[i + 1] < pred_offsets[i]) return rfail(FK_ERR_INVALID_ARG, "pred_offsets not monotonic");
+    if (join[i] != FK_JOIN_AND && join[i] != FK_JOIN_OR) return rfail(FK_ERR_INVALID_ARG, "bad join type");
+    if (fixed[i] < -1) return rfail(FK_ERR_INVALID_ARG, "fixed values are >= 0 or -1");
+  }
+  if (pred_offsets[n_agents] > 0 && !preds) return rfail(FK_ERR_INVALID_ARG, "preds is NULL");
+  for (int e = 0; e < pred_offsets[n_agents]; ++e)
+    if (preds[e] < 0 || preds[e] >= n_agents) return rfail(FK_ERR_INVALID_ARG, "predecessor out of range");
+  // depth-first over predecessors with an explicit stack; state 0 = not
+  // visited, 1 = on the stack, 2 = done (value in out, -1 = never runs)
+  std::vector<int32_t> out(n_agents, -1);
+  std::vector<uint8_t> state(n_agents, 0);
+  for (int i = 0; i < n_agents; ++i)
+    if (fixed[i] >= 0) { out[i] = fixed[i]; state[i] = 2; }
+  std::vector<std::pair<int, int>> st;   // (agent, next predecessor index)
+  for (int s0 = 0; s0 < n_agents; ++s0) {
+    if (state[s0] == 2) continue;
+    st.push_back({s0, pred_offsets[s0]});
+    state[s0] = 1;
+    while (!st.empty()) {
+      auto& [a, e] = st.back();
+      if (e < pred_offsets[a + 1]) {
+        const int p = preds[e++];
+        if (state[p] == 1) return rfail(FK_ERR_INVALID_ARG, "cycle through agents with no fixed value");
+        if (state[p] == 0) {
+          state[p] = 1;
+          st.push_back({p, pred_offsets[p]});
+        }
+        continue;
+      }
+      // every predecessor of a is done
+      const int b = pred_offsets[a], eend = pred_offsets[a + 1];
+      int32_t v = -1;
+      if (eend > b) {
+        if (join[a] == FK_JOIN_AND) {
+          int32_t m = 0;
+          bool ok = true;
+          for (int k = b; k < eend; ++k) {
+            if (out[preds[k]] < 0) { ok = false; break; }
+            m = std::max(m, out[preds[k]]);
+          }
+          v = ok ? m + 1 : -1;
+        } else {
+          int32_t m = INT32_MAX;
+          for (int k = b; k < eend; ++k)
+            if (out[preds[k]] >= 0) m = std::min(m, out[preds[k]]);
+          v = m == INT32_MAX ? -1 : m + 1;
+        }
+      }
+      out[a] = v;
+      state[a] = 2;
+      st.pop_back();
+    }
+  }
+  std::copy(out.begin(), out.end(), steps);
   return FK_OK;
 }
 

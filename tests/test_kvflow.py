@@ -181,3 +181,117 @@ def test_scan_eviction_equals_the_heap_form():
         b = _random_tree(np.random.default_rng(seed), 12, 8)
         want = int(rng.integers(1, 30))
         assert a.evict(want) == _heap_evict(b, want)
+
+
+# ---------------------------------------------- C++ index against the oracle --
+
+import shared_base_kv_gb300 as fk  # noqa: E402
+
+P = 4
+
+
+class _Mirror:
+    """The same tree in the library's index and in the oracle model.  Nodes
+    are added as whole new spans under an existing prefix (no splits), and
+    the model replays the index's logical clock: an insert marks the root,
+    then every node on the parent's path, then the new node as used."""
+
+    def __init__(self):
+        self.r = fk.RadixIndex(P)
+        self.t = ok.PrefixTree()
+        self.clock = 0
+        self.tokens = {0: []}
+        self.path = {0: [0]}
+        self.next_page = 0
+        self.uid = 0
+
+    def add(self, parent, k):
+        toks = list(self.tokens[parent])
+        for _ in range(k):
+            self.uid += 1
+            toks += [self.uid * 1000 + i for i in range(P)]
+        pages = list(range(self.next_page, self.next_page + k))
+        self.next_page += k
+        node = self.r.insert(toks, pages)
+        for x in self.path[parent]:
+            self.clock += 1
+            self.t.last_use[x] = self.clock
+        self.clock += 1
+        self.t.add(node, parent, pages, last_use=self.clock)
+        self.tokens[node] = toks
+        self.path[node] = self.path[parent] + [node]
+        return node
+
+    def attach(self, node, adapter):
+        self.r.adapter_attach(node, adapter, 0)
+        for x in self.path[node][1:]:
+            self.t.ref[x] += 1
+
+    def assign(self, node, step):
+        self.r.priority_assign(node, step)
+        self.t.assign(node, step)
+
+
+def test_index_priorities_and_eviction_match_the_oracle():
+    rng = np.random.default_rng(41)
+    for trial in range(60):
+        m = _Mirror()
+        nodes = [0]
+        for _ in range(int(rng.integers(1, 16))):
+            nodes.append(m.add(int(rng.choice(nodes)), int(rng.integers(1, 4))))
+        live = nodes[1:]
+        for _ in range(int(rng.integers(0, 10))):
+            m.assign(int(rng.choice(live)), int(rng.integers(0, 6)))
+        for a in range(int(rng.integers(0, 3))):
+            m.attach(int(rng.choice(live)), a)
+        for x in live:
+            assert m.r.node_priority(x) == m.t.priority(x), (trial, x)
+        while True:
+            want = int(rng.integers(1, 6))
+            got = list(m.r.evict_workflow(want))
+            exp = m.t.evict(want)
+            assert got == exp, (trial, got, exp)
+            if not exp:
+                break
+        assert m.r.stats()[1] == sum(len(p) for x, p in m.t.pages.items() if x != 0)
+        m.r.close()
+
+
+def test_release_clear_and_split_keep_the_counts():
+    m = _Mirror()
+    a = m.add(0, 3)
+    b = m.add(a, 1)
+    m.assign(b, 4)
+    m.assign(b, 1)
+    assert m.r.node_priority(a) == 1
+    m.r.priority_release(b, 1)
+    assert m.r.node_priority(a) == 4 and m.r.node_priority(b) == 4
+    with pytest.raises(fk.FKError):
+        m.r.priority_release(b, 1)                 # no such assignment left
+    with pytest.raises(fk.FKError):
+        m.r.priority_assign(b, -1)
+    with pytest.raises(fk.FKError):
+        m.r.priority_assign(0, 1)                  # the root carries no mark
+    # a lookup that ends inside a's span splits it; the new prefix node
+    # carries a's marks
+    _, _, head = m.r.match(m.tokens[a][:P])
+    assert head not in (0, a) and m.r.node_priority(head) == 4
+    m.r.priority_clear()
+    assert m.r.node_priority(b) is None and m.r.node_priority(head) is None
+    m.r.close()
+
+
+def test_workflow_steps_match_the_oracle():
+    rng = np.random.default_rng(42)
+    for _ in range(300):
+        preds, join, fixed = _random_dag(rng, int(rng.integers(1, 14)))
+        assert fk.workflow_steps(preds, join, fixed) == ok.steps_to_execution(preds, join, fixed)
+    # loops broken by a fixed agent, and the errors
+    assert fk.workflow_steps([[2], [0], [1]], [AND, OR, AND], [0, None, None]) == [0, 1, 2]
+    with pytest.raises(fk.FKError):
+        fk.workflow_steps([[1], [0]], [AND, AND], [None, None])
+    with pytest.raises(fk.FKError):
+        fk.workflow_steps([[5]], [AND], [None])                  # predecessor out of range
+    with pytest.raises(fk.FKError):
+        fk.workflow_steps([[]], [2], [None])                     # join type
+    assert fk.workflow_steps([], [], []) == []
