@@ -948,31 +948,19 @@ __global__ void __launch_bounds__(1024) mbuild_kernel(PoolGeom g, PlanDev p, int
   // completion before reading M
   asm volatile("griddepcontrol.launch_dependents;");
   const uint8_t* ws = g.base + g.off_ws;
-  const MPair mp = ((const MPair*)(ws + p.off_mpairs))[blockIdx.y];
-  const int32_t* tile_agents = (const int32_t*)(ws + p.off_tile_agents);
-  const CallAgent* ca = (const CallAgent*)(ws + p.off_call_agents);
-  const AgentDev* ag = (const AgentDev*)(g.base + g.off_agents);
-  const int32_t* row_agent = (const int32_t*)(ws + p.off_row_agent) + mp.row_begin;
-  const int32_t* row_cg = (const int32_t*)(ws + p.off_row_cg) + mp.row_begin;
-  // the pair's agents and query rows, looked up once per block (the look-
-  // ups are chained loads; done per thread they would serialise)
-  __shared__ int s_pa[kA], s_rp[kA];
-  __shared__ float s_s[kA];
-  __shared__ int64_t s_qrow[kA * kRPA];
+  // the pair's record (its agents' pool ids, ranks, scales and q rows were
+  // looked up by the host), staged once per block
+  __shared__ __align__(16) MPair smp;
   const int tid = threadIdx.x;
-  if (tid < mp.n_agents) {
-    const int pa_a = ca[tile_agents[mp.agent_begin + tid]].pool_agent;
-    const AgentDev dv = ag[pa_a];
-    s_pa[tid] = pa_a;
-    s_rp[tid] = dv.rp;
-    s_s[tid] = dv.s;
-  }
-  if (tid >= 32 && tid < 32 + mp.n_agents * kRPA) {
-    const int row = tid - 32;
-    const int ci = row_agent[row], cg = row_cg[row];
-    s_qrow[row] = ((int64_t)ci * p.C + cg / g.G) * g.H_q + mp.head * g.G + cg % g.G;
-  }
+  static_assert(sizeof(MPair) % 4 == 0, "MPair is copied as words");
+  if (tid < (int)(sizeof(MPair) / 4))
+    ((uint32_t*)&smp)[tid] = ((const uint32_t*)((const MPair*)(ws + p.off_mpairs) + blockIdx.y))[tid];
   __syncthreads();
+  const MPair& mp = smp;
+  const int* s_pa = mp.pool_agent;
+  const int* s_rp = mp.rp;
+  const float* s_s = mp.s;
+  const int32_t* s_qrow = mp.qrow;
   // one block per pair (few SMs busy, so most decode CTAs start at once);
   // each thread takes units tid, tid + 1024, ...
   const int n_units = (mp.zcols / kRPA / 8) * kRPA * NF;

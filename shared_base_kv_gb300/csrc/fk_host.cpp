@@ -71,6 +71,7 @@ struct fk_pool {
   Staging stage;
   // cached work list
   bool plan_valid = false;
+  uint64_t plan_gen = 0;                     // bumped whenever agents or pages change
   std::vector<int32_t> key;                  // call inputs the plan is for
   HostPlan plan;
   PlanDev plan_dev{};
@@ -447,6 +448,25 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
   return FK_OK;
 }
 
+// The host-side lookups of each M pair (see MPair): pool agent, padded
+// rank and scale of its agents, and the q row of each query row.
+void fill_mpairs(HostPlan& pl, const fk_pool* p, const int32_t* agents, int C) {
+  const PoolGeom& g = p->g;
+  const int G = g.H_q / g.H_kv;
+  for (auto& m : pl.mpairs) {
+    for (int a = 0; a < m.n_agents; ++a) {
+      const int pa = agents[pl.tile_agents[m.agent_begin + a]];
+      m.pool_agent[a] = pa;
+      m.rp[a] = p->agents[pa].rp;
+      m.s[a] = p->agents[pa].s;
+    }
+    for (int row = 0; row < m.n_agents * 4; ++row) {
+      const int ci = pl.row_agent[m.row_begin + row], cg = pl.row_cg[m.row_begin + row];
+      m.qrow[row] = (ci * C + cg / G) * g.H_q + m.head * G + cg % G;
+    }
+  }
+}
+
 // Pack a work list into the workspace image: the plan arrays, then the
 // split partials, then the decode kernel's M matrices.  Returns the bytes of
 // workspace the call needs (blob covers the plan arrays only).
@@ -634,6 +654,7 @@ fk_status fk_pages_release(fk_pool* p, int n, const int32_t* ids) {
     if (p->refcount[kv.first] == 0) p->free_list.push_back(kv.first);
   }
   p->plan_valid = false;
+  ++p->plan_gen;
   return FK_OK;
 }
 
@@ -690,6 +711,7 @@ fk_status fk_agent_register(fk_pool* p, int agent, int rank, float s,
     return r2;
   }
   p->plan_valid = false;
+  ++p->plan_gen;
   return FK_OK;
 }
 
@@ -715,6 +737,7 @@ fk_status fk_agent_register_shared(fk_pool* p, int agent, int src, float s, cons
   }
   ++p->rc_users[A.rc_off];
   p->plan_valid = false;
+  ++p->plan_gen;
   return FK_OK;
 }
 
@@ -728,6 +751,7 @@ fk_status fk_agent_release(fk_pool* p, int agent) {
     --u->second;
     A = fk_pool::Agent{};
     p->plan_valid = false;
+    ++p->plan_gen;
     return upload_agent(p, agent, nullptr);
   }
   if (u != p->rc_users.end()) p->rc_users.erase(u);
@@ -743,6 +767,7 @@ fk_status fk_agent_release(fk_pool* p, int agent) {
   p->rc_free[off] = len;
   A = fk_pool::Agent{};
   p->plan_valid = false;
+  ++p->plan_gen;
   return upload_agent(p, agent, nullptr);
 }
 
@@ -825,6 +850,7 @@ fk_status fk_base_append(fk_pool* p, int layer, int32_t* row, int max_pages, int
     f = (uint8_t)std::max<int>(f, end);
   }
   p->plan_valid = false;
+  ++p->plan_gen;
   return FK_OK;
 }
 
@@ -995,6 +1021,7 @@ fk_status fk_residual_attention(fk_pool* p, int layer, const uint16_t* q, const 
     fk_status s = plan_build(A, C, g.H_q, g.H_kv, kPage, bt, max_pages, seq, rp.data(),
                              kMaxRows, kMaxRankSum, p->num_sms, pl);
     if (s != FK_OK) return s;
+    fill_mpairs(pl, p, agents, C);
     // pack into the workspace
     PlanDev pd{};
     std::vector<uint8_t> blob;
@@ -1049,6 +1076,7 @@ fk_status fk_residual_attention_noalloc(fk_pool* p, int layer, const uint16_t* q
   key.insert(key.end(), agents, agents + A);
   key.insert(key.end(), seq, seq + A);
   key.insert(key.end(), bt, bt + (int64_t)A * max_pages);
+  key.insert(key.end(), {(int32_t)(p->plan_gen & 0x7FFFFFFF), (int32_t)(p->plan_gen >> 31)});
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   NoallocCache& cache = g_noalloc[p->device & 63];
   if (cache.pool != p || cache.device != p->device || cache.key != key) {
@@ -1072,6 +1100,7 @@ fk_status fk_residual_attention_noalloc(fk_pool* p, int layer, const uint16_t* q
     fk_status s = plan_build(A, C, g.H_q, g.H_kv, kPage, bt, max_pages, seq, rp.data(),
                              kMaxRows, kMaxRankSum, p->num_sms, pl);
     if (s != FK_OK) return s;
+    fill_mpairs(pl, p, agents, C);
     PlanDev pd{};
     std::vector<uint8_t> blob;
     int64_t need = pack_plan(pl, A, C, causal, agents, seq, g, blob, pd);

@@ -82,6 +82,12 @@ struct MPair {
   int32_t head, agent_begin, n_agents, row_begin;
   int32_t zcols, pad;      // columns of M (4 x the tile's padded rank sum)
   int64_t mofs;            // byte offset from the workspace start
+  // looked up by the host, so that building M needs no chain of table
+  // loads: per tile agent its pool agent, padded rank and residual scale,
+  // and the q row of each of its four query rows
+  int32_t pool_agent[kMaxAgentsPerTile], rp[kMaxAgentsPerTile];
+  float s[kMaxAgentsPerTile];
+  int32_t qrow[kMaxAgentsPerTile * 4];
 };
 
 // Host launchers (fk_kernels.cu).  All return a cudaError_t as int.

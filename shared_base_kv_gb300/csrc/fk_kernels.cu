@@ -1046,14 +1046,16 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
 // (log-sum-exp in base 2), apply Bv once to the merged P Lv (LRAgent
 // summary, section 3), rotate the value sum of a compressed pool back
 // (inverse FWHT), normalise, round to bf16.
+constexpr int kCombineSlotCache = 512;   // split slots of a row staged in shared memory
+
 template <int D, bool COMP>
 __global__ void __launch_bounds__(4 * D) combine_kernel(PoolGeom g, PlanDev p, int layer,
                                                         uint16_t* __restrict__ out) {
-  // partials are written by the preceding attention grid
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float sol[kMaxRankPad];
   __shared__ float sx[D];
   __shared__ float qo[4][D], qol[4][kMaxRankPad], qm[4], ql[4];
+  __shared__ uint16_t sbv[kMaxRankPad * D];         // this row's Bv slice, [rank][D]
+  __shared__ int32_t sslot[kCombineSlotCache];
   const int row = blockIdx.x, d = threadIdx.x % D, qq = threadIdx.x / D;
   const uint8_t* ws = g.base + g.off_ws;
   const int32_t* ptr = (const int32_t*)(ws + p.off_csr_ptr);
@@ -1068,6 +1070,22 @@ __global__ void __launch_bounds__(4 * D) combine_kernel(PoolGeom g, PlanDev p, i
   const int pa = ca[i].pool_agent;
   const AgentDev dv = ag[pa];
   const int b = ptr[row], e = ptr[row + 1];
+  // The plan tables, the agent table and Bv were written before the
+  // attention grid started: stage this row's slots and Bv slice while that
+  // grid is still running (the launch is programmatic), so that only the
+  // partials are read after the wait.
+  {
+    const uint16_t* bvb = (const uint16_t*)(g.base + g.off_bv + (int64_t)pa * g.bv_agent_bytes) +
+                          (int64_t)layer * g.rmax_pad * g.H_kv * D + h * D;
+    for (int idx = threadIdx.x; idx < dv.rp * D; idx += 4 * D)
+      sbv[idx] = bvb[(int64_t)(idx / D) * g.H_kv * D + idx % D];
+    const int ns = min(e - b, kCombineSlotCache);
+    for (int j = threadIdx.x; j < ns; j += 4 * D) sslot[j] = slots[b + j];
+  }
+  __syncthreads();
+  auto slot = [&](int k) { return k - b < kCombineSlotCache ? sslot[k - b] : slots[k]; };
+  // partials are written by the preceding attention grid
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // four thread groups take every fourth split (a log-sum-exp merge with a
   // running maximum each, all their loads issued first), then group 0
   // merges the four
@@ -1088,7 +1106,7 @@ __global__ void __launch_bounds__(4 * D) combine_kernel(PoolGeom g, PlanDev p, i
     float m[4], l[4], ov[4], olv[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float* s = part + (int64_t)slots[k + 4 * j] * PS;
+      const float* s = part + (int64_t)slot(k + 4 * j) * PS;
       m[j] = s[0];
       l[j] = s[1];
       ov[j] = s[4 + d];
@@ -1098,7 +1116,7 @@ __global__ void __launch_bounds__(4 * D) combine_kernel(PoolGeom g, PlanDev p, i
     for (int j = 0; j < 4; ++j) merge(m[j], l[j], ov[j], olv[j]);
   }
   for (; k < e; k += 4) {
-    const float* s = part + (int64_t)slots[k] * PS;
+    const float* s = part + (int64_t)slot(k) * PS;
     merge(s[0], s[1], s[4 + d], has_r ? s[4 + D + d] : 0.f);
   }
   qo[qq][d] = o;
@@ -1124,12 +1142,10 @@ __global__ void __launch_bounds__(4 * D) combine_kernel(PoolGeom g, PlanDev p, i
     asm volatile("bar.sync 1, %0;" ::"r"(D) : "memory");
   }
   // up-projection of the merged low-rank value sum: (sum_t p_t Lv_t) Bv
-  const uint16_t* bv = (const uint16_t*)(g.base + g.off_bv + (int64_t)pa * g.bv_agent_bytes) +
-                       (int64_t)layer * g.rmax_pad * g.H_kv * D + h * D + d;
   float up = 0.f;
 #pragma unroll 8
   for (int kk = 0; kk < dv.rp; ++kk) {
-    uint16_t u = bv[(int64_t)kk * g.H_kv * D];
+    const uint16_t u = sbv[kk * D + d];
     up = fmaf(sol[kk], __bfloat162float(*(const __nv_bfloat16*)&u), up);
   }
   __nv_bfloat16 r = __float2bfloat16_rn((o + dv.s * up) / L);
