@@ -55,3 +55,26 @@ def test_noalloc_rejects_calls_beyond_the_array():
         _call(fk.fk_residual_attention_noalloc, dw, q)
     assert e.value.code == fk.FK_ERR_OOM
     assert "static array" in str(e.value)
+
+
+def test_noalloc_replans_after_an_agent_is_registered_again():
+    # the no-allocation entry point caches its work list, which carries the
+    # agents' ranks and residual scales; registering an agent again (here
+    # with three times the scale) must not reuse it
+    w = workloads.make_workload("llama8b_32k", "strong", prefix=1000, A=8)
+    dw = harness.DeviceWorkload(w)
+    q = dw.queries(0)
+    first = _call(fk.fk_residual_attention_noalloc, dw, q).float()
+    h = dw.pool.h
+    ld = w.layer(0)
+    Bk = torch.stack([w.layer(l).bk[0] for l in range(w.n_layers)]).cuda().contiguous()
+    Bv = torch.stack([w.layer(l).bv[0] for l in range(w.n_layers)]).cuda().contiguous()
+    fk.fk_agent_release(h, 0)
+    fk.fk_agent_register(h, 0, int(w.ranks[0]), 3.0 * w.s, Bk, Bv)
+    fk.fk_residual_append(h, 0, 0, 0, ld.lk[0].cuda().contiguous(), ld.lv[0].cuda().contiguous())
+    ref = _call(fk.fk_residual_attention, dw, q).float()
+    got = _call(fk.fk_residual_attention_noalloc, dw, q).float()
+    assert torch.equal(got, ref)
+    assert not torch.equal(got[0], first[0])          # agent 0's rows see the new scale
+    assert torch.equal(got[1:], first[1:])            # the others do not change
+    dw.check()
