@@ -311,6 +311,7 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
     torch.cuda.synchronize(dev)
     fk_pool_set_profile_event(h, None)
     main_ms = [km_s[k].elapsed_time(km_m[k]) for k in range(KM)]
+    graph = graph_step_ms(dev, stream, flush, h, q, agents, bt, seq, out, min(K, 500))
     # end to end through the public call, host buffers: H2D q, call, D2H out
     q_host = q.cpu().pin_memory()
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -330,6 +331,7 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
     ok = bool(torch.isfinite(out.float()).all().item())
     dw.check()
     prefill = measure_prefill(dev, stream, flush, args.prefill_steps) if args.prefill_steps else None
+    configs = measure_configs(dev, stream, flush) if args.all_configs else None
     value, total_ms, e2e_value, e2e_ms = reduce_over_ranks(
         total_ms, e2e_ms, w.A * K, w.A * KE, world, dev)
     ab = algorithmic_bytes(w)
@@ -346,6 +348,8 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
                          "then a read of another 2x L2 buffer (writes back the dirty lines)",
                    "kernel_timing": "roofline.kernel_ms from separate steps with an event "
                                     "between the attention kernel and the combine",
+                   "step_ms_p10_p50_p90": percentiles(step_ms),
+                   "cuda_graph": graph,
                    "step_hbm_gbs": ab["step"] / (total_ms / K / 1e3) / 1e9,
                    "step_bytes": ab["step"]},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -362,6 +366,112 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
         "outputs_finite": ok,
         "prefill": prefill,
     }
+    if configs is not None:
+        res["configs"] = configs
+    return res
+
+
+def percentiles(ms) -> list:
+    import numpy as np
+    return [float(np.percentile(ms, p)) for p in (10, 50, 90)]
+
+
+def graph_step_ms(dev, stream, flush, h, q, agents, bt, seq, out, steps: int) -> dict:
+    """The same step captured once into a CUDA graph and replayed (the call's
+    work list is cached, so the capture holds only its kernel launches)."""
+    import torch
+    from shared_base_kv_gb300 import fk_residual_attention
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fk_residual_attention(h, 0, q, agents, bt, seq, False, False, out, side)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(g, stream=side):
+            fk_residual_attention(h, 0, q, agents, bt, seq, False, False, out, side)
+        torch.cuda.synchronize(dev)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+        return {"ms_per_step": statistics.mean(ms), "ms_p10_p50_p90": percentiles(ms),
+                "steps": steps}
+    except Exception as e:                      # a capture the runtime refuses
+        return {"error": f"{type(e).__name__}: {str(e)[:200]}"}
+
+
+def measure_configs(dev, stream, flush) -> list:
+    """Absolute numbers for every workload (one fk_residual_attention call per
+    layer; the 32-layer workload's step is its 32 calls).  Median and
+    p10/p90 over L2-flushed iterations."""
+    import numpy as np
+    import torch
+    import workloads
+    from shared_base_kv_gb300 import fk_residual_attention, harness
+    res = []
+    for name, comp, iters in (("tiny", None, 200), ("llama8b_32k", None, 200),
+                              ("agents32_layers32", None, 30), ("qwen72b_chunk", None, 50),
+                              ("compressed", "gpu", 200)):
+        w = workloads.make_workload(name)
+        dw = harness.DeviceWorkload(w, device=str(dev), compressed=comp)
+        qs = [dw.queries(l) for l in range(w.n_layers)]
+        w.drop()
+        out = torch.empty_like(qs[0])
+        agents = np.arange(w.A, dtype=np.int32)
+        bt = np.ascontiguousarray(dw.block_table, dtype=np.int32)
+        seq = np.ascontiguousarray(w.seq_lens, dtype=np.int32)
+        h = dw.pool.h
+
+        def step():
+            for l in range(w.n_layers):
+                fk_residual_attention(h, l, qs[l], agents, bt, seq, w.causal, comp is not None,
+                                      out, stream)
+
+        for _ in range(3):
+            step()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(iters)]
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        dw.check()
+        ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+        p10, p50, p90 = percentiles(ms)
+        ab = algorithmic_bytes(w)
+        per_layer = ab["step"]
+        if comp is not None:     # int8 K (d B) + 3-bit V (3d/8 B) + fp32 norm per (token, head)
+            per_layer = (int(np.sum(w.slot_fill)) * w.H_kv * (w.d + 3 * w.d // 8 + 4)
+                         + ab["rcache"] + ab["q"] + ab["out"])
+        G = w.H_q // w.H_kv
+        flops = 0
+        for a in range(w.A):     # per (agent, key, kv head): recon + scores + P Vb + P Lv; up-projection per row
+            r = int(w.ranks[a])
+            flops += w.H_kv * (int(w.seq_lens[a]) * (2 * r * w.d + G * w.C * (4 * w.d + 2 * r))
+                               + G * w.C * 2 * r * w.d)
+        flops *= w.n_layers
+        res.append({"workload": name, "layers": w.n_layers, "agents": w.A, "C": w.C,
+                    "ms_p50": p50, "ms_p10": p10, "ms_p90": p90,
+                    "agent_tokens_per_s": w.A * w.C / (p50 / 1e3),
+                    "algorithmic_bytes": per_layer * w.n_layers,
+                    "gbs": per_layer * w.n_layers / (p50 / 1e3) / 1e9,
+                    "algorithmic_tflop": flops / 1e12,
+                    "tflops": flops / (p50 / 1e3) / 1e12,
+                    "compressed": comp is not None})
+        dw.pool.close()
+        del dw, qs, out
+        torch.cuda.empty_cache()
     return res
 
 
@@ -448,6 +558,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--prefill-steps", type=int, default=100)
+    ap.add_argument("--all-configs", action="store_true",
+                    help="also time every workload (tiny, llama8b_32k, agents32_layers32, "
+                         "qwen72b_chunk, compressed) and add their numbers as 'configs'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", type=float, default=None)
     args = ap.parse_args()
