@@ -183,3 +183,42 @@ def test_prefill_argument_errors():
     lk, lv, _ = _read_factors(pool, 0, 0, 200)
     assert not lk.any() and not lv.any()
     pool.close()
+
+
+@pytest.mark.parametrize("n", [1, 127, 128, 129])
+def test_prefill_runs_ending_at_the_capacity(n):
+    # a run whose last token is the rCache's last row (max_tokens = 640 =
+    # the padded capacity), one tile boundary either side of 128 tokens
+    pool = _pool(agents=1, max_rank=32, max_tokens=640)
+    r, dm = 24, 256
+    B = torch.zeros(L, r, H * D, dtype=torch.bfloat16).cuda()
+    fk.fk_agent_register(pool.h, 0, r, 1.0, B, B)
+    X, Ak, Av = _hidden(n, dm, 50 + n), _down(dm, r, 60), _down(dm, r, 61)
+    pos = 640 - n
+    fk.fk_residual_prefill(pool.h, 1, 0, pos, X.cuda(), Ak.cuda(), Av.cuda())
+    torch.cuda.synchronize()
+    fk.fk_check(pool.h)
+    lk, lv, _ = _read_factors(pool, 0, 1, 640)
+    _check_factor(lk[pos:, :r], X, Ak)
+    _check_factor(lv[pos:, :r], X, Av)
+    assert not lk[:pos].any() and not lv[:pos].any()
+    with pytest.raises(fk.FKError):                           # one row past the capacity
+        fk.fk_residual_prefill(pool.h, 1, 0, pos + 1, X.cuda(), Ak.cuda(), Av.cuda())
+    pool.close()
+
+
+def test_prefill_wide_hidden_state():
+    # d_model 8192: 64 chunks through the stage ring, rank 64 (padded rank
+    # equal to the rank: no padding columns)
+    pool = _pool(agents=1, max_rank=64, max_tokens=256)
+    r, dm, n = 64, 8192, 200
+    B = torch.zeros(L, r, H * D, dtype=torch.bfloat16).cuda()
+    fk.fk_agent_register(pool.h, 0, r, 1.0, B, B)
+    X, Ak, Av = _hidden(n, dm, 70), _down(dm, r, 71), _down(dm, r, 72)
+    fk.fk_residual_prefill(pool.h, 0, 0, 0, X.cuda(), Ak.cuda(), Av.cuda())
+    torch.cuda.synchronize()
+    fk.fk_check(pool.h)
+    lk, lv, _ = _read_factors(pool, 0, 0, 200)
+    _check_factor(lk[:, :r], X, Ak)
+    _check_factor(lv[:, :r], X, Av)
+    pool.close()
