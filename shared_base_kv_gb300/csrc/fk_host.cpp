@@ -448,6 +448,90 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
   return FK_OK;
 }
 
+// Calls the chunk kernel takes: many query rows per agent and kv head.
+bool use_chunk(const PoolGeom& g, int C, int compressed) {
+  return !compressed && g.d == 128 && (g.H_q / g.H_kv) * C >= 128;
+}
+
+// Work list of the chunk kernel (calls with >= 128 query rows per agent
+// and kv head): one item per (call agent, kv head, block of 128 of the
+// agent's G*C rows, run of whole 128-token tiles).  Units are taken in the
+// order (kv head, agent, row block), so that the agents reading one head's
+// shared pages run side by side, and cut at tile boundaries so that each of
+// at most n_ctas CTAs gets the same number of tiles.  Every item writes one
+// split partial per row; the combine lists map each output row to them.
+fk_status plan_chunk(int A, int C, int H_q, int H_kv, const int32_t* bt, int max_pages,
+                     const int32_t* seq, int n_ctas, HostPlan& out) {
+  if (A < 1 || C < 1 || H_kv < 1 || H_q % H_kv || n_ctas < 1)
+    return fail(FK_ERR_INVALID_ARG, "bad call shape");
+  const int G = H_q / H_kv, R = G * C, nb = (R + 127) / 128;
+  for (int i = 0; i < A; ++i) {
+    if (seq[i] < C) return fail(FK_ERR_INVALID_ARG, "seq_lens[i] must be >= C >= 1");
+    const int np = (seq[i] + kPage - 1) / kPage;
+    if (np > max_pages) return fail(FK_ERR_INVALID_ARG, "seq_len exceeds max_pages");
+    for (int lp = 0; lp < np; ++lp)
+      if (bt[(int64_t)i * max_pages + lp] < 0)
+        return fail(FK_ERR_INVALID_ARG, "block table names no page for a live token");
+  }
+  int64_t total = 0;
+  for (int i = 0; i < A; ++i) total += (int64_t)H_kv * nb * (((seq[i] + kPage - 1) / kPage + kTilePages - 1) / kTilePages);
+  const int64_t quota = (total + n_ctas - 1) / n_ctas;
+  HostPlan pl;
+  pl.cta_begin.push_back(0);
+  int64_t acc = 0;
+  for (int h = 0; h < H_kv; ++h)
+    for (int i = 0; i < A; ++i)
+      for (int b = 0; b < nb; ++b) {
+        const int np = (seq[i] + kPage - 1) / kPage;
+        const int tiles = (np + kTilePages - 1) / kTilePages;
+        int done = 0;
+        while (done < tiles) {
+          const int take = (int)std::min<int64_t>(tiles - done, quota - acc);
+          fk_work_item it{};
+          it.head = h;
+          it.row_begin = 128 * b;
+          it.n_rows = std::min(128, R - 128 * b);
+          it.page_begin = (int)pl.pages.size();
+          it.lp_begin = done * kTilePages;
+          it.n_pages = std::min(take * kTilePages, np - it.lp_begin);
+          it.agent_begin = i;
+          it.n_agents = 1;
+          it.partial_begin = pl.n_partials;
+          for (int j = 0; j < it.n_pages; ++j)
+            pl.pages.push_back(bt[(int64_t)i * max_pages + it.lp_begin + j]);
+          pl.n_partials += it.n_rows;
+          pl.items.push_back(it);
+          done += take;
+          acc += take;
+          if (acc == quota) {
+            pl.cta_begin.push_back((int)pl.items.size());
+            acc = 0;
+          }
+        }
+      }
+  if (acc > 0) pl.cta_begin.push_back((int)pl.items.size());
+  // combine lists: output row (i, c, hq) -> partial slots
+  const int n_out = A * C * H_q;
+  std::vector<int32_t> cnt(n_out + 1, 0);
+  auto out_row = [&](const fk_work_item& it, int r) {
+    const int ridx = it.row_begin + r, c = ridx / G, g = ridx % G;
+    return (it.agent_begin * C + c) * H_q + it.head * G + g;
+  };
+  for (auto& it : pl.items)
+    for (int r = 0; r < it.n_rows; ++r) cnt[out_row(it, r) + 1]++;
+  for (int o = 0; o < n_out; ++o) {
+    if (cnt[o + 1] == 0) return fail(FK_ERR_INVALID_ARG, "an output row has no keys");
+    cnt[o + 1] += cnt[o];
+  }
+  pl.csr_ptr = cnt;
+  pl.csr_slots.assign(cnt[n_out], 0);
+  std::vector<int32_t> pos(cnt.begin(), cnt.end() - 1);
+  for (auto& it : pl.items)
+    for (int r = 0; r < it.n_rows; ++r) pl.csr_slots[pos[out_row(it, r)]++] = it.partial_begin + r;
+  out = std::move(pl);
+  return FK_OK;
+}
+
 // The host-side lookups of each M pair (see MPair): pool agent, padded
 // rank and scale of its agents, and the q row of each query row.
 void fill_mpairs(HostPlan& pl, const fk_pool* p, const int32_t* agents, int C) {
@@ -996,7 +1080,7 @@ fk_status fk_residual_attention(fk_pool* p, int layer, const uint16_t* q, const 
   // cache key: everything the work list depends on
   std::vector<int32_t> key;
   key.reserve(8 + 2 * A + (size_t)A * max_pages);
-  key.insert(key.end(), {A, C, causal ? 1 : 0, max_pages});
+  key.insert(key.end(), {A, C, causal ? 1 : 0, max_pages, compressed ? 1 : 0});
   key.insert(key.end(), agents, agents + A);
   key.insert(key.end(), seq, seq + A);
   key.insert(key.end(), bt, bt + (int64_t)A * max_pages);
@@ -1018,14 +1102,17 @@ fk_status fk_residual_attention(fk_pool* p, int layer, const uint16_t* q, const 
       }
     }
     HostPlan pl;
-    fk_status s = plan_build(A, C, g.H_q, g.H_kv, kPage, bt, max_pages, seq, rp.data(),
-                             kMaxRows, kMaxRankSum, p->num_sms, pl);
+    const bool chunk = use_chunk(g, C, compressed);
+    fk_status s = chunk ? plan_chunk(A, C, g.H_q, g.H_kv, bt, max_pages, seq, p->num_sms, pl)
+                        : plan_build(A, C, g.H_q, g.H_kv, kPage, bt, max_pages, seq, rp.data(),
+                                     kMaxRows, kMaxRankSum, p->num_sms, pl);
     if (s != FK_OK) return s;
     fill_mpairs(pl, p, agents, C);
     // pack into the workspace
     PlanDev pd{};
     std::vector<uint8_t> blob;
     int64_t need = pack_plan(pl, A, C, causal, agents, seq, g, blob, pd);
+    pd.chunk = chunk ? 1 : 0;
     if (need > g.ws_bytes) return fail(FK_ERR_OOM, "workspace too small for this call");
     fk_status s2 = stage_upload(p, blob.data(), blob.size(), g.base + g.off_ws, st);
     if (s2 != FK_OK) return s2;
@@ -1072,7 +1159,7 @@ fk_status fk_residual_attention_noalloc(fk_pool* p, int layer, const uint16_t* q
   cudaStream_t st = (cudaStream_t)stream;
   std::vector<int32_t> key;
   key.reserve(8 + 2 * A + (size_t)A * max_pages);
-  key.insert(key.end(), {A, C, causal ? 1 : 0, max_pages});
+  key.insert(key.end(), {A, C, causal ? 1 : 0, max_pages, compressed ? 1 : 0});
   key.insert(key.end(), agents, agents + A);
   key.insert(key.end(), seq, seq + A);
   key.insert(key.end(), bt, bt + (int64_t)A * max_pages);
@@ -1097,13 +1184,16 @@ fk_status fk_residual_attention_noalloc(fk_pool* p, int layer, const uint16_t* q
       }
     }
     HostPlan pl;
-    fk_status s = plan_build(A, C, g.H_q, g.H_kv, kPage, bt, max_pages, seq, rp.data(),
-                             kMaxRows, kMaxRankSum, p->num_sms, pl);
+    const bool chunk = use_chunk(g, C, compressed);
+    fk_status s = chunk ? plan_chunk(A, C, g.H_q, g.H_kv, bt, max_pages, seq, p->num_sms, pl)
+                        : plan_build(A, C, g.H_q, g.H_kv, kPage, bt, max_pages, seq, rp.data(),
+                                     kMaxRows, kMaxRankSum, p->num_sms, pl);
     if (s != FK_OK) return s;
     fill_mpairs(pl, p, agents, C);
     PlanDev pd{};
     std::vector<uint8_t> blob;
     int64_t need = pack_plan(pl, A, C, causal, agents, seq, g, blob, pd);
+    pd.chunk = chunk ? 1 : 0;
     if (need > (int64_t)scratch_bytes) {
       char msg[160];
       std::snprintf(msg, sizeof msg,

@@ -70,6 +70,7 @@ struct PlanDev {
   int32_t partial_stride;  // floats per partial slot: d + rmax_pad + 4
   int32_t n_ctas;          // persistent CTAs; CTA c runs items cta[c] .. cta[c+1]-1
   int32_t n_mpairs;        // decode-shaped calls: (agent tile, kv head) pairs with an M
+  int32_t chunk;           // 1: the items are the chunk kernel's (fk_chunk.cu)
   int64_t off_items, off_row_agent, off_row_cg, off_pages, off_tile_agents,
           off_call_agents, off_csr_ptr, off_csr_slots, off_partials, off_cta;
   int64_t off_mpairs, off_item_mpair;   // MPair[n_mpairs], int32[n_items]
@@ -121,6 +122,12 @@ int launch_attention(const PoolGeom& g, const PlanDev& p, int layer,
 bool decode_applies(const PoolGeom& g, const PlanDev& p);
 int launch_decode(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q,
                   int compressed, void* stream);
+
+// Calls with at least 128 query rows per agent and kv head (d = 128,
+// uncompressed pool) run the chunk kernel (fk_chunk.cu); the combine is
+// shared.
+bool chunk_applies(const PoolGeom& g, const PlanDev& p);
+int launch_chunk(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q, void* stream);
 
 // Device address and size of the static scratch array that
 // fk_residual_attention_noalloc uses (looked up once per device).

@@ -1226,7 +1226,11 @@ static int launch_attn_t(const PoolGeom& g, const PlanDev& p, int layer, const u
     if (e != cudaSuccess) return (int)e;
     attr_done = true;
   }
-  if (decode_applies(g, p)) {
+  if (p.chunk) {
+    if (COMP || !chunk_applies(g, p)) return (int)cudaErrorInvalidValue;   // planner mismatch
+    int ce = launch_chunk(g, p, layer, q, st);
+    if (ce != 0) return ce;
+  } else if (decode_applies(g, p)) {
     int de = launch_decode(g, p, layer, q, COMP ? 1 : 0, st);
     if (de != 0) return de;
   } else {
