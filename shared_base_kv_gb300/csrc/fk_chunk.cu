@@ -12,17 +12,22 @@
 // the combine kernel.
 //
 // Per 128-key tile:
-//   warp 0       bulk-copies the tile's Kb and Vb pages (one 4 KB block per
-//                page) and its Lk, Lv rows (one contiguous block each);
-//   warp 1       U = Lk BkT (tcgen05, TMEM, keys x d fp32); then
-//                S = Q K_a^T (rows x keys); then O += P Vb, OL += P Lv;
+//   warp 0       bulk-copies the tile's Lk rows, Kb pages and then Vb pages
+//                and Lv rows (one 4 KB block per page, one block of rows);
+//   warp 1       S = Q K_a^T (rows x keys); U = Lk BkT of the next tile
+//                (keys x d, fp32); O += P Vb and OL += P Lv of the previous
+//                tile, with P read from TMEM;
+//   warp 2       the rotation of each tile's first key, cos and sin of
+//                t0 theta_i reduced exactly through a 64-bit fraction of a
+//                turn, one tile ahead;
 //   warps 4-7    one thread per key: K_a = Kb + s RoPE_t(U) rounded to
-//                bf16, written over the tile's Kb in shared memory;
+//                bf16, written over the tile's Kb in shared memory; the
+//                key's rotation is the tile's composed with the key's own
+//                offset rotation (kept in registers for the whole kernel);
 //   warps 8-11   one thread per row: masked online softmax of S (base 2;
 //                O and OL are rescaled in TMEM only when a row's running
-//                maximum grows by more than 2^8), P in bf16 written over
-//                the tile's consumed keys; at the end of an item, the
-//                row's split partial (m, l, O, OL).
+//                maximum grows by more than 2^8), P in bf16 into TMEM; at
+//                the end of an item, the row's split partial (m, l, O, OL).
 // Every wait is bounded: a timeout sets the pool's error word and the CTA
 // abort flag, and the CTA leaves after a grace period for copies in flight.
 #include <cuda_runtime.h>
@@ -38,7 +43,7 @@ namespace chk {
 constexpr int D = 128;
 constexpr int kThreads = 384;
 constexpr int kRMax = 64;                       // padded rank limit
-constexpr uint32_t kTmU = 0, kTmS = 128, kTmO = 256, kTmOL = 384;
+constexpr uint32_t kTmU = 0, kTmS = 128, kTmO = 256, kTmOL = 384, kTmP = 448;
 
 struct Layout {
   static constexpr int PAGE_B = kPage * D * 2;            // one (page, head) block: 4 KB
@@ -57,7 +62,7 @@ struct Layout {
   static constexpr int oQ = oLK + LR_B;
   static constexpr int oBK = oQ + Q_B;
   static constexpr int oMISC = oBK + BK_B;
-  static constexpr int MISC_B = 1024;
+  static constexpr int MISC_B = 2048;
   static constexpr int TOTAL = oMISC + MISC_B;
 };
 static_assert(Layout::TOTAL <= 232448, "shared memory over the 227 KB a CTA may use");
@@ -65,25 +70,29 @@ static_assert(Layout::TOTAL <= 232448, "shared memory over the 227 KB a CTA may 
 enum {
   B_KB_FULL0, B_KB_FULL1, B_KB_EMPTY0, B_KB_EMPTY1, B_LK_FULL, B_LK_EMPTY, B_V_FULL0, B_V_FULL1,
   B_V_EMPTY0, B_V_EMPTY1, B_BK_FULL, B_BK_EMPTY, B_Q_FULL, B_U_FULL, B_U_FREE, B_KA_READY,
-  B_S_FULL, B_S_FREE, B_P_FULL, B_PV_DONE, B_ACC_EMPTY, B_FINAL, B_COUNT
+  B_S_FULL, B_S_FREE, B_P_FULL, B_PV_DONE, B_ACC_EMPTY, B_FINAL, B_ROT_FULL0, B_ROT_FULL1,
+  B_ROT_EMPTY0, B_ROT_EMPTY1, B_COUNT
 };
 // arrivals: one lane per warp of a warpgroup, else one thread or a commit
 __host__ __device__ constexpr uint32_t bar_count(int i) {
   return (i == B_Q_FULL || i == B_U_FREE || i == B_KA_READY || i == B_S_FREE || i == B_P_FULL ||
-          i == B_ACC_EMPTY)
+          i == B_ACC_EMPTY || i == B_ROT_EMPTY0 || i == B_ROT_EMPTY1)
              ? 4u
              : 1u;
 }
 // barriers a role waits on as "empty" start one phase ahead
 constexpr uint32_t kEmptyMask = (1u << B_KB_EMPTY0) | (1u << B_KB_EMPTY1) | (1u << B_LK_EMPTY) |
                                 (1u << B_V_EMPTY0) | (1u << B_V_EMPTY1) | (1u << B_BK_EMPTY) |
-                                (1u << B_U_FREE) | (1u << B_S_FREE) | (1u << B_ACC_EMPTY);
+                                (1u << B_U_FREE) | (1u << B_S_FREE) | (1u << B_ACC_EMPTY) |
+                                (1u << B_ROT_EMPTY0) | (1u << B_ROT_EMPTY1);
 
 struct Misc {
   uint64_t bar[B_COUNT];
+  unsigned long long frac[64];   // theta_i / (2 pi) as a 64-bit binary fraction
+  float2 rot[2][64];             // (cos, sin) of t0 theta_i, a ring of two tiles
+  float theta[64];               // theta_i
   uint32_t tmem_base;
   int abort_flag;
-  unsigned long long frac[64];   // theta_i / (2 pi) as a 64-bit binary fraction
 };
 static_assert(sizeof(Misc) <= Layout::MISC_B, "Misc must fit its smem slot");
 
@@ -153,7 +162,10 @@ __global__ void __launch_bounds__(chk::kThreads, 1)
   // ---- set-up: zero smem (stale rows read by masked keys stay finite),
   // RoPE fractions, barriers, TMEM
   for (int i = tid * 16; i < LY::oMISC; i += kThreads * 16) *(uint4*)(smem + i) = make_uint4(0, 0, 0, 0);
-  if (tid < 64) M.frac[tid] = ((const unsigned long long*)(g.base + g.off_rope + 256))[tid];
+  if (tid < 64) {
+    M.theta[tid] = ((const float*)(g.base + g.off_rope))[tid];
+    M.frac[tid] = ((const unsigned long long*)(g.base + g.off_rope + 256))[tid];
+  }
   if (tid == 0) {
     for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), bar_count(i));
     M.abort_flag = 0;
@@ -183,23 +195,26 @@ __global__ void __launch_bounds__(chk::kThreads, 1)
                  g.base + g.off_bk + (int64_t)I.pool_agent * g.bk_agent_bytes +
                      ((int64_t)layer * g.H_kv + I.head) * (int64_t)D * g.rmax_pad * 2,
                  D * I.rp * 2, bar(B_BK_FULL));
-        for (int k = 0; k < I.n_tiles; ++k, ++tc) {
+        bool ok = true;
+        for (int k = 0; k < I.n_tiles && ok; ++k, ++tc) {
           const int kb = tc & 1;
           const int p0 = k * kTilePages;
           const int np = min(kTilePages, I.n_pages - p0);
           const int t0 = (I.lp_begin + p0) * kPage;
           const int nr = min(kTileTok, g.tcap - t0);          // rCache rows of the tile
-          if (!wait(B_KB_EMPTY0 + kb)) break;
+          // Lk (freed by the previous tile's U), Kb (freed by the S of two
+          // tiles back), Vb and Lv (freed by the PV of two tiles back)
+          if (!wait(B_LK_EMPTY)) { ok = false; break; }
+          mbar_expect_tx(bar(B_LK_FULL), nr * I.rp * 2);
+          bulk_g2s(sbase + LY::oLK, lk + (int64_t)t0 * I.rp * 2, nr * I.rp * 2, bar(B_LK_FULL));
+          if (!wait(B_KB_EMPTY0 + kb)) { ok = false; break; }
           mbar_expect_tx(bar(B_KB_FULL0 + kb), np * LY::PAGE_B);
           for (int j = 0; j < np; ++j)
             bulk_g2s(sbase + (kb ? LY::oKB1 : LY::oKB0) + j * LY::PAGE_B,
                      g.base + g.off_kb + (int64_t)layer * g.kb_layer_bytes +
                          ((int64_t)pages[p0 + j] * g.H_kv + I.head) * LY::PAGE_B,
                      LY::PAGE_B, bar(B_KB_FULL0 + kb));
-          if (!wait(B_LK_EMPTY)) break;
-          mbar_expect_tx(bar(B_LK_FULL), nr * I.rp * 2);
-          bulk_g2s(sbase + LY::oLK, lk + (int64_t)t0 * I.rp * 2, nr * I.rp * 2, bar(B_LK_FULL));
-          if (!wait(B_V_EMPTY0 + kb)) break;
+          if (!wait(B_V_EMPTY0 + kb)) { ok = false; break; }
           mbar_expect_tx(bar(B_V_FULL0 + kb), np * LY::PAGE_B + nr * I.rp * 2);
           for (int j = 0; j < np; ++j)
             bulk_g2s(sbase + (kb ? LY::oVB1 : LY::oVB0) + j * LY::PAGE_B,
@@ -209,6 +224,7 @@ __global__ void __launch_bounds__(chk::kThreads, 1)
           bulk_g2s(sbase + (kb ? LY::oLV1 : LY::oLV0), lv + (int64_t)t0 * I.rp * 2, nr * I.rp * 2,
                    bar(B_V_FULL0 + kb));
         }
+        if (!ok) break;
       }
     }
     __syncwarp();
@@ -224,50 +240,55 @@ __global__ void __launch_bounds__(chk::kThreads, 1)
         const uint32_t idL = idesc_f16(128, I.rp, 1);
         if (!wait(B_BK_FULL) || !wait(B_Q_FULL)) break;
         tc_fence_after();
-        bool ok = true;
-        for (int k = 0; k <= I.n_tiles && ok; ++k) {
-          if (k < I.n_tiles) {
-            const int kb = (tc + k) & 1;
-            // U = Lk BkT: keys x d, K = padded rank
-            if (!wait(B_LK_FULL) || !wait(B_U_FREE)) { ok = false; break; }
-            tc_fence_after();
-            for (int ks = 0; ks < I.rp / 16; ++ks)
-              mma_ss(t_U, sdesc(sbase + LY::oLK + ks * 256, 128, I.rp * 16),
-                     sdesc(sbase + LY::oBK + ks * 256, 128, I.rp * 16), idK, ks > 0 ? 1u : 0u);
-            mma_commit(bar(B_U_FULL));
-            mma_commit(bar(B_LK_EMPTY));
-            if (k == I.n_tiles - 1) mma_commit(bar(B_BK_EMPTY));
-            // S = Q K_a^T: rows x keys, K = d
-            if (!wait(B_KA_READY) || !wait(B_S_FREE)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t kbase = sbase + (kb ? LY::oKB1 : LY::oKB0);
+        // U = Lk BkT of tile k: keys x d, K = padded rank
+        auto issue_u = [&](int k) {
+          if (!wait(B_LK_FULL) || !wait(B_U_FREE)) return false;
+          tc_fence_after();
+          for (int ks = 0; ks < I.rp / 16; ++ks)
+            mma_ss(t_U, sdesc(sbase + LY::oLK + ks * 256, 128, I.rp * 16),
+                   sdesc(sbase + LY::oBK + ks * 256, 128, I.rp * 16), idK, ks > 0 ? 1u : 0u);
+          mma_commit(bar(B_U_FULL));
+          mma_commit(bar(B_LK_EMPTY));
+          if (k == I.n_tiles - 1) mma_commit(bar(B_BK_EMPTY));
+          return true;
+        };
+        // O += P Vb, OL += P Lv of tile j (P from TMEM, bf16 pairs)
+        auto issue_pv = [&](int j) {
+          const int kb = (tc + j) & 1;
+          if (!wait(B_P_FULL) || !wait(B_V_FULL0 + kb)) return false;
+          if (j == 0 && !wait(B_ACC_EMPTY)) return false;
+          tc_fence_after();
+          const uint32_t vbase = sbase + (kb ? LY::oVB1 : LY::oVB0);
+          const uint32_t lvbase = sbase + (kb ? LY::oLV1 : LY::oLV0);
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
-              mma_ss(t_S, sdesc(sbase + LY::oQ + ks * 256, 128, (D / 8) * 128),
-                     sdesc(kbase + ks * 256, 128, (D / 8) * 128), idK, ks > 0 ? 1u : 0u);
-            mma_commit(bar(B_S_FULL));
+          for (int ks = 0; ks < kTileTok / 16; ++ks) {
+            const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
+            mma_ts(t_O, tmem + kTmP + 8 * ks, sdesc(vbase + ks * 2 * (D / 8) * 128, (D / 8) * 128, 128),
+                   idK, acc);
+            mma_ts(t_OL, tmem + kTmP + 8 * ks, sdesc(lvbase + ks * 2 * I.rp * 16, I.rp * 16, 128), idL,
+                   acc);
           }
-          if (k >= 1) {
-            // O += P Vb, OL += P Lv for tile k - 1
-            const int j = k - 1, kb = (tc + j) & 1;
-            if (!wait(B_P_FULL) || !wait(B_V_FULL0 + kb)) { ok = false; break; }
-            if (j == 0 && !wait(B_ACC_EMPTY)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t pbase = sbase + (kb ? LY::oKB1 : LY::oKB0);
-            const uint32_t vbase = sbase + (kb ? LY::oVB1 : LY::oVB0);
-            const uint32_t lvbase = sbase + (kb ? LY::oLV1 : LY::oLV0);
+          mma_commit(bar(B_PV_DONE));
+          mma_commit(bar(B_V_EMPTY0 + kb));
+          return true;
+        };
+        bool ok = issue_u(0);
+        for (int k = 0; k < I.n_tiles && ok; ++k) {
+          const int kb = (tc + k) & 1;
+          // S = Q K_a^T: rows x keys, K = d; the stage's keys are free after it
+          if (!wait(B_KA_READY) || !wait(B_S_FREE)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kbase = sbase + (kb ? LY::oKB1 : LY::oKB0);
 #pragma unroll
-            for (int ks = 0; ks < kTileTok / 16; ++ks) {
-              const uint64_t dP = sdesc(pbase + ks * 256, 128, (kTileTok / 8) * 128);
-              const uint32_t acc = (j > 0 || ks > 0) ? 1u : 0u;
-              mma_ss(t_O, dP, sdesc(vbase + ks * 2 * (D / 8) * 128, (D / 8) * 128, 128), idK, acc);
-              mma_ss(t_OL, dP, sdesc(lvbase + ks * 2 * I.rp * 16, I.rp * 16, 128), idL, acc);
-            }
-            mma_commit(bar(B_PV_DONE));
-            mma_commit(bar(B_KB_EMPTY0 + kb));
-            mma_commit(bar(B_V_EMPTY0 + kb));
-          }
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_ss(t_S, sdesc(sbase + LY::oQ + ks * 256, 128, (D / 8) * 128),
+                   sdesc(kbase + ks * 256, 128, (D / 8) * 128), idK, ks > 0 ? 1u : 0u);
+          mma_commit(bar(B_S_FULL));
+          mma_commit(bar(B_KB_EMPTY0 + kb));
+          if (k + 1 < I.n_tiles && !issue_u(k + 1)) { ok = false; break; }
+          if (k >= 1 && !issue_pv(k - 1)) { ok = false; break; }
         }
+        if (ok) ok = issue_pv(I.n_tiles - 1);
         tc += I.n_tiles;
         if (!ok) break;
       }
@@ -277,54 +298,87 @@ __global__ void __launch_bounds__(chk::kThreads, 1)
       if (!mbar_wait_drain(bar(B_FINAL), par)) *abort_flag = 1;
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 8) {
-    // =============================================== adapted keys K_a ====
-    const int kl = tid - 128;                              // TMEM lane = key of the tile
-    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+  } else if (warp == 2) {
+    // ============================== tile-start rotations, one tile ahead ====
     int tc = 0;
     for (int it = it_begin; it < it_end && !*abort_flag; ++it) {
       Item I;
       load_item(g, p, ws, it, I);
       bool ok = true;
       for (int k = 0; k < I.n_tiles; ++k, ++tc) {
-        const int kb = tc & 1;
-        const unsigned long long t = (unsigned long long)((I.lp_begin + k * kTilePages) * kPage + kl);
+        const int b = tc & 1;
+        if (!__all_sync(0xffffffffu, wait(B_ROT_EMPTY0 + b))) { ok = false; break; }
+        const unsigned long long t0 = (unsigned long long)((I.lp_begin + k * kTilePages) * kPage);
+#pragma unroll
+        for (int z = 0; z < 2; ++z) {
+          const int i = 2 * lane + z;
+          const unsigned long long fr = t0 * M.frac[i];
+          float ang = (float)(unsigned int)(fr >> 32) * 1.4629180792671596e-09f;   // 2 pi / 2^32
+          if (ang > 3.14159265f) ang -= 6.28318531f;
+          float sn, cs;
+          sincosf(ang, &sn, &cs);
+          M.rot[b][i] = make_float2(cs, sn);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_ROT_FULL0 + b));
+      }
+      if (!ok) break;
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // =============================================== adapted keys K_a ====
+    const int kl = tid - 128;                              // TMEM lane = key of the tile
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    // the rotation by this key's offset in its tile, (cos, sin) of kl theta_i
+    // as f16 pairs, for the whole kernel
+    uint32_t tau[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      float sn, cs;
+      sincosf((float)kl * M.theta[i], &sn, &cs);
+      tau[i] = pack_h2(cs, sn);
+    }
+    int tc = 0;
+    for (int it = it_begin; it < it_end && !*abort_flag; ++it) {
+      Item I;
+      load_item(g, p, ws, it, I);
+      bool ok = true;
+      for (int k = 0; k < I.n_tiles; ++k, ++tc) {
+        const int kb = tc & 1, b = tc & 1;
         // (lanes leave together: the TMEM accesses below are warp-wide)
-        if (!__all_sync(0xffffffffu, wait(B_KB_FULL0 + kb) & wait(B_U_FULL))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait(B_ROT_FULL0 + b) & wait(B_KB_FULL0 + kb) & wait(B_U_FULL))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         uint8_t* krow = smem + (kb ? LY::oKB1 : LY::oKB0) + (kl / 8) * ((D / 8) * 128) + (kl % 8) * 16;
-#pragma unroll 1
-        for (int jq = 0; jq < 4; ++jq) {
-          // frequencies 16 jq .. 16 jq + 15: d columns i and i + 64 (rotate-half)
-          uint32_t ulo[16], uhi[16];
-          tmem_ld16(tmem + kTmU + 16 * jq + lane_off, ulo);
-          tmem_ld16(tmem + kTmU + 64 + 16 * jq + lane_off, uhi);
+#pragma unroll
+        for (int jq = 0; jq < 8; ++jq) {
+          // frequencies 8 jq .. 8 jq + 7: d columns i (chunk jq) and i + 64 (chunk 8 + jq)
+          uint32_t ulo[8], uhi[8];
+          tmem_ld8(tmem + kTmU + 8 * jq + lane_off, ulo);
+          tmem_ld8(tmem + kTmU + 64 + 8 * jq + lane_off, uhi);
           tmem_wait_ld();
-          if (jq == 3) {
+          if (jq == 7) {
             // U read: the next tile's U may be written
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_U_FREE));
           }
-          uint4 klo[2], khi[2];
-          klo[0] = *(const uint4*)(krow + (2 * jq) * 128);
-          klo[1] = *(const uint4*)(krow + (2 * jq + 1) * 128);
-          khi[0] = *(const uint4*)(krow + (8 + 2 * jq) * 128);
-          khi[1] = *(const uint4*)(krow + (8 + 2 * jq + 1) * 128);
-          uint32_t lo_w[8] = {klo[0].x, klo[0].y, klo[0].z, klo[0].w, klo[1].x, klo[1].y, klo[1].z, klo[1].w};
-          uint32_t hi_w[8] = {khi[0].x, khi[0].y, khi[0].z, khi[0].w, khi[1].x, khi[1].y, khi[1].z, khi[1].w};
+          const uint4 klo = *(const uint4*)(krow + jq * 128);
+          const uint4 khi = *(const uint4*)(krow + (8 + jq) * 128);
+          uint32_t lo_w[4] = {klo.x, klo.y, klo.z, klo.w};
+          uint32_t hi_w[4] = {khi.x, khi.y, khi.z, khi.w};
 #pragma unroll
-          for (int e2 = 0; e2 < 8; ++e2) {
+          for (int e2 = 0; e2 < 4; ++e2) {
             float klf[2], khf[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const int e = 2 * e2 + h;
-              // t * theta_i modulo 2 pi, exactly, through the 64-bit fraction
-              const unsigned long long fr = t * M.frac[16 * jq + e];
-              float ang = (float)(unsigned int)(fr >> 32) * 1.4629180792671596e-09f;   // 2 pi / 2^32
-              if (ang > 3.14159265f) ang -= 6.28318531f;
-              float sn, cs;
-              __sincosf(ang, &sn, &cs);
+              const int e = 2 * e2 + h, i = 8 * jq + e;
+              // rotation of key t0 + kl: the tile start's composed with the offset's
+              const float2 r0 = M.rot[b][i];
+              const float2 rt = __half22float2(*reinterpret_cast<const __half2*>(&tau[i]));
+              const float cs = r0.x * rt.x - r0.y * rt.y;
+              const float sn = r0.y * rt.x + r0.x * rt.y;
               const float ul = __uint_as_float(ulo[e]), uh = __uint_as_float(uhi[e]);
               const float bl = h ? bf_hi(lo_w[e2]) : bf_lo(lo_w[e2]);
               const float bh = h ? bf_hi(hi_w[e2]) : bf_lo(hi_w[e2]);
@@ -334,14 +388,15 @@ __global__ void __launch_bounds__(chk::kThreads, 1)
             lo_w[e2] = pack_bf2(klf[0], klf[1]);
             hi_w[e2] = pack_bf2(khf[0], khf[1]);
           }
-          *(uint4*)(krow + (2 * jq) * 128) = make_uint4(lo_w[0], lo_w[1], lo_w[2], lo_w[3]);
-          *(uint4*)(krow + (2 * jq + 1) * 128) = make_uint4(lo_w[4], lo_w[5], lo_w[6], lo_w[7]);
-          *(uint4*)(krow + (8 + 2 * jq) * 128) = make_uint4(hi_w[0], hi_w[1], hi_w[2], hi_w[3]);
-          *(uint4*)(krow + (8 + 2 * jq + 1) * 128) = make_uint4(hi_w[4], hi_w[5], hi_w[6], hi_w[7]);
+          *(uint4*)(krow + jq * 128) = make_uint4(lo_w[0], lo_w[1], lo_w[2], lo_w[3]);
+          *(uint4*)(krow + (8 + jq) * 128) = make_uint4(hi_w[0], hi_w[1], hi_w[2], hi_w[3]);
         }
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_KA_READY));
+        if (lane == 0) {
+          mbar_arrive(bar(B_ROT_EMPTY0 + b));
+          mbar_arrive(bar(B_KA_READY));
+        }
       }
       if (!ok) break;
     }
@@ -352,6 +407,11 @@ __global__ void __launch_bounds__(chk::kThreads, 1)
     const float scale_log2 = 1.4426950408889634f * rsqrtf((float)D);
     float* part = (float*)(ws + p.off_partials);
     const int PS = p.partial_stride;
+    auto ex2 = [](float x) {
+      float y;
+      asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+      return y;
+    };
     int tc = 0;
     for (int it = it_begin; it < it_end && !*abort_flag; ++it) {
       Item I;
@@ -377,57 +437,43 @@ __global__ void __launch_bounds__(chk::kThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
       for (int k = 0; k < I.n_tiles; ++k, ++tc) {
-        const int kb = tc & 1;
         const int t0 = (I.lp_begin + k * kTilePages) * kPage;
         const int ntok = min(kTileTok, (I.n_pages - k * kTilePages) * kPage);
         const int nvis = valid ? max(0, min(ntok, lim - t0)) : 0;   // keys 0 .. nvis-1 count
         if (!__all_sync(0xffffffffu, wait(B_S_FULL))) { ok = false; break; }
         tc_fence_after();
-        // pass 1: the tile's row maximum
+        // pass 1: the tile's row maximum (two loads in flight; the scale is
+        // positive, so it is applied to the maximum only)
+        const bool full = nvis == kTileTok;                // no key of the tile is masked
         float tmax = -INFINITY;
 #pragma unroll 1
-        for (int cb = 0; cb < kTileTok; cb += 32) {
-          uint32_t v[32];
-          tmem_ld32_wait(tmem + kTmS + cb + lane_off, v);
+        for (int cb = 0; cb < kTileTok; cb += 64) {
+          uint32_t v[64];
+          tmem_ld32(tmem + kTmS + cb + lane_off, v);
+          tmem_ld32(tmem + kTmS + cb + 32 + lane_off, v + 32);
+          tmem_wait_ld();
+          if (full) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (cb + e < nvis) tmax = fmaxf(tmax, __uint_as_float(v[e]) * scale_log2);
+            for (int e = 0; e < 64; ++e) tmax = fmaxf(tmax, __uint_as_float(v[e]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+              if (cb + e < nvis) tmax = fmaxf(tmax, __uint_as_float(v[e]));
+          }
         }
+        if (tmax != -INFINITY) tmax *= scale_log2;
         bool rescale = false;
         float alpha = 1.f;
         if (m_used == -INFINITY) {
           m_used = tmax;
         } else if (tmax > m_used + 8.f) {
-          alpha = exp2f(m_used - tmax);
+          alpha = ex2(m_used - tmax);
           m_used = tmax;
           rescale = true;
         }
-        // pass 2: P = 2^(s - m) in bf16 over the tile's consumed keys, row sums
-        float lt = 0.f;
-        uint8_t* prow = smem + (kb ? LY::oKB1 : LY::oKB0) + (r / 8) * ((kTileTok / 8) * 128) + (r % 8) * 16;
-#pragma unroll 1
-        for (int cb = 0; cb < kTileTok; cb += 32) {
-          uint32_t v[32];
-          tmem_ld32_wait(tmem + kTmS + cb + lane_off, v);
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float p0 = 0.f, p1 = 0.f;
-            if (cb + e < nvis) p0 = exp2f(__uint_as_float(v[e]) * scale_log2 - m_used);
-            if (cb + e + 1 < nvis) p1 = exp2f(__uint_as_float(v[e + 1]) * scale_log2 - m_used);
-            w[e / 2] = pack_bf2(p0, p1);
-            lt += bf_lo(w[e / 2]) + bf_hi(w[e / 2]);   // the sum of what the MMA multiplies
-          }
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8)
-            *(uint4*)(prow + (cb / 8 + c8) * 128) = make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_S_FREE));
         // every accumulation is waited for in order (the previous tile's,
-        // here); when the running maximum grew by more than 2^8, O, OL and
-        // l then shrink by alpha before this tile's P is posted
+        // here): then O, OL shrink by alpha if the maximum moved, and this
+        // tile's P replaces the previous one in TMEM
         if (k > 0) {
           if (!__all_sync(0xffffffffu, wait(B_PV_DONE))) { ok = false; break; }
           tc_fence_after();
@@ -442,14 +488,43 @@ __global__ void __launch_bounds__(chk::kThreads, 1)
               for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
               tmem_st32(tmem + col + lane_off, v);
             }
-            tmem_wait_st();
           }
         }
+        // pass 2: P = 2^(s - m) as bf16 pairs into TMEM (key 2j, 2j + 1 in
+        // column j), and the row sum (fp32, before the rounding to bf16)
+        float lt = 0.f;
+        const float nm = m_used == -INFINITY ? 0.f : -m_used;
+#pragma unroll 1
+        for (int cb = 0; cb < kTileTok; cb += 32) {
+          uint32_t v[32], w[16];
+          tmem_ld32_wait(tmem + kTmS + cb + lane_off, v);
+          if (full) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float p0 = ex2(fmaf(__uint_as_float(v[e]), scale_log2, nm));
+              const float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), scale_log2, nm));
+              w[e / 2] = pack_bf2(p0, p1);
+              lt += p0 + p1;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float p0 = (cb + e < nvis) ? ex2(fmaf(__uint_as_float(v[e]), scale_log2, nm)) : 0.f;
+              const float p1 = (cb + e + 1 < nvis) ? ex2(fmaf(__uint_as_float(v[e + 1]), scale_log2, nm)) : 0.f;
+              w[e / 2] = pack_bf2(p0, p1);
+              lt += p0 + p1;
+            }
+          }
+          tmem_st16(tmem + kTmP + cb / 2 + lane_off, w);
+        }
+        tmem_wait_st();
         l = l * alpha + lt;
-        fence_proxy_async();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_P_FULL));
+        if (lane == 0) {
+          mbar_arrive(bar(B_S_FREE));
+          mbar_arrive(bar(B_P_FULL));
+        }
       }
       if (!ok) break;
       // ---- the item's split partials, once its last accumulation completed
