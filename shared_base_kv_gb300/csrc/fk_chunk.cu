@@ -20,10 +20,12 @@
 //   warp 2       the rotation of each tile's first key, cos and sin of
 //                t0 theta_i reduced exactly through a 64-bit fraction of a
 //                turn, one tile ahead;
-//   warps 4-7    one thread per key: K_a = Kb + s RoPE_t(U) rounded to
-//                bf16, written over the tile's Kb in shared memory; the
-//                key's rotation is the tile's composed with the key's own
-//                offset rotation (kept in registers for the whole kernel);
+//   warps 4-7,   one thread per key and half of the frequencies (warps
+//   12-15        4-7 the first 32, warps 12-15 the last 32): K_a = Kb +
+//                s RoPE_t(U) rounded to bf16, written over the tile's Kb in
+//                shared memory; the key's rotation is the tile's composed
+//                with the key's own offset rotation (kept in registers for
+//                the whole kernel);
 //   warps 8-11   one thread per row: masked online softmax of S (base 2;
 //                O and OL are rescaled in TMEM only when a row's running
 //                maximum grows by more than 2^8), P in bf16 into TMEM; at
@@ -41,7 +43,7 @@ namespace fk {
 namespace chk {
 
 constexpr int D = 128;
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kRMax = 64;                       // padded rank limit
 constexpr uint32_t kTmU = 0, kTmS = 128, kTmO = 256, kTmOL = 384, kTmP = 448;
 
@@ -73,12 +75,12 @@ enum {
   B_S_FULL, B_S_FREE, B_P_FULL, B_PV_DONE, B_ACC_EMPTY, B_FINAL, B_ROT_FULL0, B_ROT_FULL1,
   B_ROT_EMPTY0, B_ROT_EMPTY1, B_COUNT
 };
-// arrivals: one lane per warp of a warpgroup, else one thread or a commit
+// arrivals: one lane per warp of one or two warpgroups, else one thread or
+// a commit
 __host__ __device__ constexpr uint32_t bar_count(int i) {
-  return (i == B_Q_FULL || i == B_U_FREE || i == B_KA_READY || i == B_S_FREE || i == B_P_FULL ||
-          i == B_ACC_EMPTY || i == B_ROT_EMPTY0 || i == B_ROT_EMPTY1)
-             ? 4u
-             : 1u;
+  return (i == B_U_FREE || i == B_KA_READY || i == B_ROT_EMPTY0 || i == B_ROT_EMPTY1)
+             ? 8u   // both key warpgroups
+             : (i == B_Q_FULL || i == B_S_FREE || i == B_P_FULL || i == B_ACC_EMPTY) ? 4u : 1u;
 }
 // barriers a role waits on as "empty" start one phase ahead
 constexpr uint32_t kEmptyMask = (1u << B_KB_EMPTY0) | (1u << B_KB_EMPTY1) | (1u << B_LK_EMPTY) |
@@ -324,17 +326,18 @@ __global__ void __launch_bounds__(chk::kThreads, 1)
       }
       if (!ok) break;
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if ((warp >= 4 && warp < 8) || warp >= 12) {
     // =============================================== adapted keys K_a ====
-    const int kl = tid - 128;                              // TMEM lane = key of the tile
+    const int kl = 32 * (warp & 3) + lane;                 // TMEM lane = key of the tile
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const int f0 = warp >= 12 ? 32 : 0;                    // this warpgroup's first frequency
     // the rotation by this key's offset in its tile, (cos, sin) of kl theta_i
     // as f16 pairs, for the whole kernel
-    uint32_t tau[64];
+    uint32_t tau[32];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
+    for (int i = 0; i < 32; ++i) {
       float sn, cs;
-      sincosf((float)kl * M.theta[i], &sn, &cs);
+      sincosf((float)kl * M.theta[f0 + i], &sn, &cs);
       tau[i] = pack_h2(cs, sn);
     }
     int tc = 0;
@@ -352,20 +355,21 @@ __global__ void __launch_bounds__(chk::kThreads, 1)
         tc_fence_after();
         uint8_t* krow = smem + (kb ? LY::oKB1 : LY::oKB0) + (kl / 8) * ((D / 8) * 128) + (kl % 8) * 16;
 #pragma unroll
-        for (int jq = 0; jq < 8; ++jq) {
-          // frequencies 8 jq .. 8 jq + 7: d columns i (chunk jq) and i + 64 (chunk 8 + jq)
+        for (int jq = 0; jq < 4; ++jq) {
+          // frequencies f0 + 8 jq .. + 7: d columns i (chunk jg) and i + 64 (chunk 8 + jg)
+          const int jg = f0 / 8 + jq;
           uint32_t ulo[8], uhi[8];
-          tmem_ld8(tmem + kTmU + 8 * jq + lane_off, ulo);
-          tmem_ld8(tmem + kTmU + 64 + 8 * jq + lane_off, uhi);
+          tmem_ld8(tmem + kTmU + 8 * jg + lane_off, ulo);
+          tmem_ld8(tmem + kTmU + 64 + 8 * jg + lane_off, uhi);
           tmem_wait_ld();
-          if (jq == 7) {
+          if (jq == 3) {
             // U read: the next tile's U may be written
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_U_FREE));
           }
-          const uint4 klo = *(const uint4*)(krow + jq * 128);
-          const uint4 khi = *(const uint4*)(krow + (8 + jq) * 128);
+          const uint4 klo = *(const uint4*)(krow + jg * 128);
+          const uint4 khi = *(const uint4*)(krow + (8 + jg) * 128);
           uint32_t lo_w[4] = {klo.x, klo.y, klo.z, klo.w};
           uint32_t hi_w[4] = {khi.x, khi.y, khi.z, khi.w};
 #pragma unroll
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(chk::kThreads, 1)
             for (int h = 0; h < 2; ++h) {
               const int e = 2 * e2 + h, i = 8 * jq + e;
               // rotation of key t0 + kl: the tile start's composed with the offset's
-              const float2 r0 = M.rot[b][i];
+              const float2 r0 = M.rot[b][f0 + i];
               const float2 rt = __half22float2(*reinterpret_cast<const __half2*>(&tau[i]));
               const float cs = r0.x * rt.x - r0.y * rt.y;
               const float sn = r0.y * rt.x + r0.x * rt.y;
@@ -388,8 +392,8 @@ __global__ void __launch_bounds__(chk::kThreads, 1)
             lo_w[e2] = pack_bf2(klf[0], klf[1]);
             hi_w[e2] = pack_bf2(khf[0], khf[1]);
           }
-          *(uint4*)(krow + jq * 128) = make_uint4(lo_w[0], lo_w[1], lo_w[2], lo_w[3]);
-          *(uint4*)(krow + (8 + jq) * 128) = make_uint4(hi_w[0], hi_w[1], hi_w[2], hi_w[3]);
+          *(uint4*)(krow + jg * 128) = make_uint4(lo_w[0], lo_w[1], lo_w[2], lo_w[3]);
+          *(uint4*)(krow + (8 + jg) * 128) = make_uint4(hi_w[0], hi_w[1], hi_w[2], hi_w[3]);
         }
         fence_proxy_async();
         __syncwarp();
