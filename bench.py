@@ -523,6 +523,46 @@ def measure_prefill(dev, stream, flush, steps: int) -> dict:
     }
 
 
+def run_chunk_small(args) -> dict:
+    """The chunk kernel's call on a reduced Qwen-72B-shaped causal chunk (16
+    agents, 16,384 shared prefix tokens + 32 private, C = 32): a case small
+    enough to profile whole (its launches hold about 1 GB)."""
+    import numpy as np
+    import torch
+    import workloads
+    from shared_base_kv_gb300 import fk_residual_attention, harness
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    flush = L2Flush(dev, int(torch.cuda.get_device_properties(dev).L2_cache_size))
+    w = workloads.make_workload("qwen72b_chunk", prefix=16384, A=16)
+    dw = harness.DeviceWorkload(w, device="cuda:0")
+    q = dw.queries(0)
+    w.drop()
+    out = torch.empty_like(q)
+    agents = np.arange(w.A, dtype=np.int32)
+    bt = np.ascontiguousarray(dw.block_table, dtype=np.int32)
+    seq = np.ascontiguousarray(w.seq_lens, dtype=np.int32)
+
+    def step():
+        fk_residual_attention(dw.pool.h, 0, q, agents, bt, seq, True, False, out, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    dw.check()
+    ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    return {"workload": "qwen72b_chunk reduced: 16 agents x (16384 + 32) tokens, C = 32 causal",
+            "ms_p10_p50_p90": percentiles(ms), "steps": args.steps}
+
+
 def run_reference(args):
     import workloads
     w = workloads.make_workload(WORKLOAD)
@@ -558,6 +598,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--prefill-steps", type=int, default=100)
+    ap.add_argument("--chunk-small", action="store_true",
+                    help="only time the chunk kernel's call on a reduced Qwen-72B-shaped chunk")
     ap.add_argument("--all-configs", action="store_true",
                     help="also time every workload (tiny, llama8b_32k, agents32_layers32, "
                          "qwen72b_chunk, compressed) and add their numbers as 'configs'")
@@ -576,6 +618,11 @@ def main():
             return
         os.environ["OMP_NUM_THREADS"] = os.environ.get("OMP_NUM_THREADS", "1")
         print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.chunk_small:
+        import __graft_entry__
+        __graft_entry__.build()
+        print(json.dumps(run_chunk_small(args)), flush=True)
         return
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
