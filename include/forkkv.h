@@ -346,6 +346,25 @@ fk_status fk_plan_host(int A, int C, int H_q, int H_kv, int page_size,
                        int32_t* tile_agents, int cap_tile_agents,
                        int* n_tile_agents);
 
+/* Work list of the chunk kernel, the path of calls with at least 128 query
+ * rows per agent and kv head (G * C >= 128, d = 128, uncompressed pool),
+ * built without a pool or GPU.  Items: head, row_begin (first of the
+ * item's rows among the agent's G*C rows, row index c * G + g), n_rows
+ * (<= 128), page_begin (into page_ids), n_pages, lp_begin (first logical
+ * page, a multiple of 8), agent_begin (the call agent), n_agents = 1,
+ * partial_begin (the item's first split-partial slot; one slot per row).
+ * CTA c runs items cta_begin[c] .. cta_begin[c+1]-1 (*n_cta entries).
+ * csr_ptr (A * C * H_q + 1 entries) and csr_slots list the partial slots
+ * of every output row (a, c, hq) in row order.  FK_ERR_OOM (with the
+ * counts set) if a capacity is too small; FK_ERR_INVALID_ARG for a bad
+ * shape or block table. */
+fk_status fk_plan_chunk_host(int A, int C, int H_q, int H_kv, const int32_t* block_table,
+                            int max_pages, const int32_t* seq_lens, int n_ctas,
+                            fk_work_item* items, int cap_items, int* n_items, int32_t* cta_begin,
+                            int cap_cta, int* n_cta, int32_t* page_ids, int cap_pages,
+                            int* n_pages, int32_t* csr_ptr, int cap_ptr, int32_t* csr_slots,
+                            int cap_slots, int* n_slots);
+
 /* ------------------------------------------------ two-tier prefix index --
  * Host-only index above the page pool (ForkKV guide, "DualRadixTree:
  * Two-Tier Hierarchical Cache Indexing", "Two-Tier Lookup Mechanics" and

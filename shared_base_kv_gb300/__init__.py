@@ -45,6 +45,7 @@ EXPORTS = (
     "fk_radix_evict", "fk_radix_stats", "fk_radix_node_ref", "fk_residual_prefill",
     "fk_radix_priority_assign", "fk_radix_priority_release", "fk_radix_priority_clear",
     "fk_radix_node_priority", "fk_radix_evict_workflow", "fk_workflow_steps",
+    "fk_plan_chunk_host",
 )
 
 
@@ -135,6 +136,10 @@ def lib() -> ctypes.CDLL:
             "fk_radix_node_priority": (i32, [vp, i64, ctypes.POINTER(i32)]),
             "fk_radix_evict_workflow": (i32, [vp, i32, P32, i32, ctypes.POINTER(i32)]),
             "fk_workflow_steps": (i32, [i32, P32, P32, P32, P32, P32]),
+            "fk_plan_chunk_host": (i32, [i32, i32, i32, i32, P32, i32, P32, i32,
+                                         ctypes.POINTER(fk_work_item), i32, ctypes.POINTER(i32), P32, i32,
+                                         ctypes.POINTER(i32), P32, i32, ctypes.POINTER(i32), P32,
+                                         i32, P32, i32, ctypes.POINTER(i32)]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -345,6 +350,31 @@ def fk_plan_host(A: int, C: int, H_q: int, H_kv: int, block_table, seq_lens, ran
                           _p32(ta), n_ta.value, ctypes.byref(n_ta)))
     its = [{f: getattr(items[i], f) for f, _ in fk_work_item._fields_} for i in range(n_it.value)]
     return its, ra[:n_rw.value], rc[:n_rw.value], pg[:n_pg.value], ta[:n_ta.value]
+
+
+def fk_plan_chunk_host(A: int, C: int, H_q: int, H_kv: int, block_table, seq_lens, n_ctas: int):
+    """The chunk kernel's work list for a call shape (host only): items,
+    CTA ranges, page ids, and the combine lists (csr_ptr, csr_slots)."""
+    bt, sl = _i32(block_table), _i32(seq_lens)
+    counts = [ctypes.c_int() for _ in range(4)]
+    L = lib()
+    args = lambda it, ni, cb, nc, pg, np_, cp, ncp, cs, ns: (
+        A, C, H_q, H_kv, _p32(bt), bt.shape[1], _p32(sl), n_ctas, it, ni, ctypes.byref(counts[0]),
+        cb, nc, ctypes.byref(counts[1]), pg, np_, ctypes.byref(counts[2]), cp, ncp, cs, ns,
+        ctypes.byref(counts[3]))
+    code = L.fk_plan_chunk_host(*args(None, 0, None, 0, None, 0, None, 0, None, 0))
+    if code not in (FK_OK, FK_ERR_OOM):
+        _check(code)
+    n_it, n_cta, n_pg, n_sl = (c.value for c in counts)
+    items = (fk_work_item * max(n_it, 1))()
+    cta = np.zeros(max(n_cta, 1), np.int32)
+    pg = np.zeros(max(n_pg, 1), np.int32)
+    ptr = np.zeros(A * C * H_q + 1, np.int32)
+    slots = np.zeros(max(n_sl, 1), np.int32)
+    _check(L.fk_plan_chunk_host(*args(items, n_it, _p32(cta), n_cta, _p32(pg), n_pg, _p32(ptr),
+                                      ptr.size, _p32(slots), n_sl)))
+    its = [{f: getattr(items[i], f) for f, _ in fk_work_item._fields_} for i in range(n_it)]
+    return its, cta[:n_cta], pg[:n_pg], ptr, slots[:n_sl]
 
 
 # ------------------------------------------------------- two-tier index --

@@ -1067,6 +1067,32 @@ fk_status fk_plan_host(int A, int C, int H_q, int H_kv, int page_size,
   return FK_OK;
 }
 
+fk_status fk_plan_chunk_host(int A, int C, int H_q, int H_kv, const int32_t* block_table,
+                            int max_pages, const int32_t* seq_lens, int n_ctas,
+                            fk_work_item* items, int cap_items, int* n_items, int32_t* cta_begin,
+                            int cap_cta, int* n_cta, int32_t* page_ids, int cap_pages,
+                            int* n_pages, int32_t* csr_ptr, int cap_ptr, int32_t* csr_slots,
+                            int cap_slots, int* n_slots) {
+  if (!block_table || !seq_lens) return fail(FK_ERR_INVALID_ARG, "NULL table");
+  HostPlan pl;
+  fk_status s = plan_chunk(A, C, H_q, H_kv, block_table, max_pages, seq_lens, n_ctas, pl);
+  if (s != FK_OK) return s;
+  if (n_items) *n_items = (int)pl.items.size();
+  if (n_cta) *n_cta = (int)pl.cta_begin.size();
+  if (n_pages) *n_pages = (int)pl.pages.size();
+  if (n_slots) *n_slots = (int)pl.csr_slots.size();
+  if ((int)pl.items.size() > cap_items || (int)pl.cta_begin.size() > cap_cta ||
+      (int)pl.pages.size() > cap_pages || (int)pl.csr_ptr.size() > cap_ptr ||
+      (int)pl.csr_slots.size() > cap_slots)
+    return fail(FK_ERR_OOM, "output capacity too small");
+  if (items) std::copy(pl.items.begin(), pl.items.end(), items);
+  if (cta_begin) std::copy(pl.cta_begin.begin(), pl.cta_begin.end(), cta_begin);
+  if (page_ids) std::copy(pl.pages.begin(), pl.pages.end(), page_ids);
+  if (csr_ptr) std::copy(pl.csr_ptr.begin(), pl.csr_ptr.end(), csr_ptr);
+  if (csr_slots) std::copy(pl.csr_slots.begin(), pl.csr_slots.end(), csr_slots);
+  return FK_OK;
+}
+
 fk_status fk_residual_attention(fk_pool* p, int layer, const uint16_t* q, const int32_t* agents,
                                 const int32_t* bt, int max_pages, const int32_t* seq, int A,
                                 int C, int causal, int compressed, uint16_t* out, void* stream) {

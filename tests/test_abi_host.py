@@ -130,3 +130,79 @@ def test_plan_rejects_bad_tables():
     seq[0] = 0
     with pytest.raises(fk.FKError):
         fk.fk_plan_host(w.A, w.C, w.H_q, w.H_kv, w.block_table, seq, w.ranks, 16)
+
+
+def _chunk_plan_checks(A, C, H_q, H_kv, seq, n_ctas, seed):
+    """The chunk kernel's work list against a brute-force account of what it
+    must cover (integer work: exact)."""
+    rng = np.random.default_rng(seed)
+    P = 16
+    max_pages = max((s + P - 1) // P for s in seq) + 2
+    bt = np.full((A, max_pages), -1, np.int32)
+    nxt = 0
+    for a in range(A):
+        n = (seq[a] + P - 1) // P
+        bt[a, :n] = rng.permutation(1000)[:n] + nxt
+        nxt += 1000
+    its, cta, pages, ptr, slots = fk.fk_plan_chunk_host(A, C, H_q, H_kv, bt, np.array(seq, np.int32),
+                                                        n_ctas)
+    G, R = H_q // H_kv, (H_q // H_kv) * C
+    nb = (R + 127) // 128
+    # every (agent, head, row block) covers its logical pages exactly once, in order
+    cover = {}
+    for it in its:
+        assert it["n_agents"] == 1 and it["lp_begin"] % 8 == 0
+        assert it["row_begin"] % 128 == 0 and it["n_rows"] == min(128, R - it["row_begin"])
+        key = (it["agent_begin"], it["head"], it["row_begin"] // 128)
+        got = list(pages[it["page_begin"]: it["page_begin"] + it["n_pages"]])
+        assert got == list(bt[it["agent_begin"], it["lp_begin"]: it["lp_begin"] + it["n_pages"]])
+        cover.setdefault(key, []).append((it["lp_begin"], it["n_pages"]))
+    assert len(cover) == A * H_kv * nb
+    for (a, h, b), runs in cover.items():
+        runs.sort()
+        pos = 0
+        for lp, n in runs:
+            assert lp == pos
+            pos += n
+        assert pos == (seq[a] + P - 1) // P
+    # CTAs: consecutive item ranges, each within the tile quota
+    tiles = [(it["n_pages"] + 7) // 8 for it in its]
+    quota = -(-sum(tiles) // n_ctas)
+    assert cta[0] == 0 and cta[-1] == len(its) and len(cta) - 1 <= n_ctas
+    assert all(cta[i] < cta[i + 1] for i in range(len(cta) - 1))
+    for i in range(len(cta) - 1):
+        assert sum(tiles[cta[i]: cta[i + 1]]) <= quota
+    # partial slots: one per (item, row), distinct, and every output row
+    # (a, c, hq) lists exactly the slots of the items holding it
+    want = {}
+    for it in its:
+        for r in range(it["n_rows"]):
+            ridx = it["row_begin"] + r
+            row = (it["agent_begin"] * C + ridx // G) * H_q + it["head"] * G + ridx % G
+            want.setdefault(row, []).append(it["partial_begin"] + r)
+    assert len(ptr) == A * C * H_q + 1 and ptr[0] == 0
+    for row in range(A * C * H_q):
+        assert sorted(slots[ptr[row]: ptr[row + 1]]) == sorted(want[row])
+    all_slots = [s for v in want.values() for s in v]
+    assert len(set(all_slots)) == len(all_slots) == slots.size
+
+
+def test_chunk_plan_covers_every_row_block_and_page_once():
+    # Qwen-72B-like: 8 query heads x 32 chunk tokens = 256 rows, 2 row blocks
+    _chunk_plan_checks(A=5, C=32, H_q=64, H_kv=8, seq=[1000, 33, 4128, 129, 2048], n_ctas=152,
+                       seed=3)
+    # rows not a multiple of 128 (G*C = 192) and few CTAs
+    _chunk_plan_checks(A=3, C=24, H_q=64, H_kv=8, seq=[300, 24, 900], n_ctas=7, seed=4)
+    # more CTAs than tiles
+    _chunk_plan_checks(A=1, C=32, H_q=32, H_kv=8, seq=[40], n_ctas=152, seed=5)
+
+
+def test_chunk_plan_rejects_bad_shapes():
+    bt = np.zeros((1, 4), np.int32)
+    with pytest.raises(fk.FKError):
+        fk.fk_plan_chunk_host(1, 32, 64, 8, bt, np.array([16], np.int32), 8)    # seq < C
+    with pytest.raises(fk.FKError):
+        fk.fk_plan_chunk_host(1, 32, 60, 8, bt, np.array([40], np.int32), 8)    # H_q % H_kv
+    bt[0, 1] = -1
+    with pytest.raises(fk.FKError):
+        fk.fk_plan_chunk_host(1, 32, 64, 8, bt, np.array([40], np.int32), 8)    # page missing
