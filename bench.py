@@ -1,5 +1,5 @@
 #!/usr/bin/env python
-"""Benchmark of one residual-attention decode step (see DESIGN.md).
+"""Benchmark of one residual-attention decode step.
 
 Workload: one Llama-3-8B-shaped layer, 8 LoRA agents sharing a 32,768-token
 bf16 base cache in 16-token pages (H_q=32, H_kv=8, d=128, rank 16), one
