@@ -48,3 +48,4 @@ def test_single_rank_needs_no_process_group():
     import bench
     v, t, ev, et = bench.reduce_over_ranks(10.0, 20.0, 8, 4, 1, torch.device("cpu"))
     assert (v, t, ev, et) == (800.0, 10.0, 200.0, 20.0)
+
