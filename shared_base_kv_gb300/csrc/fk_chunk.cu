@@ -49,7 +49,7 @@ constexpr uint32_t kTmU = 0, kTmS = 128, kTmO = 256, kTmOL = 384, kTmP = 448;
 
 struct Layout {
   static constexpr int PAGE_B = kPage * D * 2;            // one (page, head) block: 4 KB
-  static constexpr int KB_B = kTilePages * PAGE_B;        // a tile's keys, then its P
+  static constexpr int KB_B = kTilePages * PAGE_B;        // a tile's keys, rewritten in place as K_a
   static constexpr int VB_B = KB_B;
   static constexpr int LR_B = kTileTok * kRMax * 2;       // a tile's Lk or Lv rows
   static constexpr int Q_B = 128 * D * 2;
