@@ -156,12 +156,14 @@ class ClockSampler:
 
 # ------------------------------------------------------------ CPU oracle --
 
-def oracle_rate(w, budget_s: float, n_pairs_max: int = 10 ** 9, keys: int = 0):
+def oracle_rate(w, budget_s: float, n_pairs_max: int = 10 ** 9, keys: int = 0,
+                first_pair: int = 0, pair_stride: int = 1):
     """Time the CPU oracle on (agent, kv-head) pairs of the workload.
 
     Each pair is 1/H_kv of an agent's decode token.  With ``keys`` > 0 the
     agents' contexts are cut to their first ``keys`` tokens and the units
-    scaled by keys / T (cost is linear in the keys).  Returns
+    scaled by keys / T (cost is linear in the keys).  A worker of a pool
+    takes pairs first_pair, first_pair + pair_stride, ...  Returns
     (agent-tokens per second, pairs done, seconds)."""
     import numpy as np
     import oracle
@@ -176,7 +178,7 @@ def oracle_rate(w, budget_s: float, n_pairs_max: int = 10 ** 9, keys: int = 0):
         lk = [x[:keys] for x in lk]
         lv = [x[:keys] for x in lv]
         scale = float(keys) / float(w.seq_lens.max())
-    pairs = [(a, h) for a in range(w.A) for h in range(w.H_kv)]
+    pairs = [(a, h) for a in range(w.A) for h in range(w.H_kv)][first_pair::pair_stride]
     done, t0 = 0, time.perf_counter()
     while done < n_pairs_max and (time.perf_counter() - t0) < budget_s:
         a, h = pairs[done % len(pairs)]
@@ -187,26 +189,44 @@ def oracle_rate(w, budget_s: float, n_pairs_max: int = 10 ** 9, keys: int = 0):
     return done * scale / w.H_kv / dt, done, dt
 
 
-def cpu_baseline_child(budget_s: float):
+def _oracle_worker(job):
+    """One process of the CPU baseline's pool: its own copy of the workload,
+    every n-th (agent, kv-head) pair."""
+    budget_s, first, stride = job
     import workloads
     w = workloads.make_workload(WORKLOAD)
-    rate, done, dt = oracle_rate(w, budget_s)
-    print(json.dumps({"value": rate, "pairs": done, "seconds": dt}))
+    return oracle_rate(w, budget_s, first_pair=first, pair_stride=stride)
+
+
+def cpu_baseline_child(budget_s: float, workers: int):
+    """The oracle as it stands on the host's cores: one single-threaded
+    process per core, each over its share of the (agent, kv-head) pairs;
+    the job's rate is the sum of theirs."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(workers) as pool:
+        res = pool.map(_oracle_worker, [(budget_s, k, workers) for k in range(workers)])
+    print(json.dumps({"value": sum(r[0] for r in res), "pairs": sum(r[1] for r in res),
+                      "seconds": max(r[2] for r in res), "workers": workers}))
 
 
 def run_cpu_baseline(budget_s: float = 15.0) -> dict:
+    workers = max(1, min(os.cpu_count() or 1, 32))
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child",
-                        str(budget_s)], capture_output=True, text=True, env=env, timeout=600)
+                        str(budget_s), "--cpu-workers", str(workers)], capture_output=True,
+                       text=True, env=env, timeout=900)
     try:
         d = json.loads(r.stdout.strip().splitlines()[-1])
     except Exception:
-        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+        return {"value": None, "unit": UNIT, "cores": workers, "kind": "oracle",
                 "sample": f"failed: {r.stderr[-300:]}"}
-    return {"value": d["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": d["value"], "unit": UNIT, "cores": d["workers"], "kind": "oracle",
             "sample": f"{d['pairs']} (agent, kv-head) pairs of the full workload at 32,768 keys "
-                      f"in {d['seconds']:.1f} s, fp64 NumPy, 1 thread; a pair is 1/8 agent-token"}
+                      f"in {d['seconds']:.1f} s, fp64 NumPy, {d['workers']} single-threaded "
+                      f"processes (one per host core, BLAS pinned to 1 thread); a pair is 1/8 "
+                      f"agent-token"}
 
 
 # -------------------------------------------------------------- GPU arm --
@@ -605,9 +625,10 @@ def main():
                          "qwen72b_chunk, compressed) and add their numbers as 'configs'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", type=float, default=None)
+    ap.add_argument("--cpu-workers", type=int, default=1)
     args = ap.parse_args()
     if args.cpu_baseline_child is not None:
-        cpu_baseline_child(args.cpu_baseline_child)
+        cpu_baseline_child(args.cpu_baseline_child, args.cpu_workers)
         return
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
