@@ -619,7 +619,7 @@ def run_reference(args):
     w = workloads.make_workload(WORKLOAD)
     workers = max(1, min(os.cpu_count() or 1, 32))
     _, _, per_pair_1k = oracle_rate(w, 1e9, n_pairs_max=1, keys=1024)
-    budget = 150.0
+    budget = 100.0    # seconds, sized on one process; concurrent processes share memory bandwidth
     n = args.steps + args.warmup
     T = int(w.seq_lens.max())
     keys = int(max(16, min(T, T * budget / max(1e-9, n * per_pair_1k * T / 1024.0))))
