@@ -49,3 +49,40 @@ def test_single_rank_needs_no_process_group():
     v, t, ev, et = bench.reduce_over_ranks(10.0, 20.0, 8, 4, 1, torch.device("cpu"))
     assert (v, t, ev, et) == (800.0, 10.0, 200.0, 20.0)
 
+
+
+def _worker_leaves(rank, world, port, out):
+    from datetime import timedelta
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=timedelta(seconds=5))
+    import bench
+    if rank == 1:
+        # this rank leaves between steps: it never joins the step's reduction
+        out[1] = "left"
+        os._exit(0)
+    try:
+        bench.reduce_over_ranks(40.0, 60.0, units=800, e2e_units=400, world=world,
+                                device=torch.device("cpu"))
+        out[0] = "completed"
+    except Exception as e:                          # the collective ends with an error
+        out[0] = f"error: {type(e).__name__}"
+    os._exit(0)
+
+
+def test_a_rank_that_leaves_ends_the_reduction_with_an_error():
+    # the surviving rank learns of it through its next collective, which
+    # fails (closed connection or the short process-group timeout) instead
+    # of waiting forever
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        ctx = mp.spawn(_worker_leaves, args=(2, port, out), nprocs=2, join=False)
+        for _ in range(120):
+            if ctx.join(timeout=1):
+                break
+        else:
+            for p in ctx.processes:
+                p.kill()
+            pytest.fail("the surviving rank did not return")
+        assert out[1] == "left"
+        assert out[0].startswith("error")
