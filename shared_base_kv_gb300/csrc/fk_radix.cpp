@@ -150,6 +150,36 @@ Node* walk(fk_radix* r, const int32_t* tok, int np, int* matched, int* in_node, 
   return node;
 }
 
+// Evicts leaves (no children, no adapter leaf at or below) in the order a
+// heap with comparator `later` (true: a leaves after b) gives, until
+// want_pages page ids are written or nothing is evictable or the next
+// node's pages would not fit in cap_pages.  A parent joins the heap once its
+// last child is gone.  Keys do not change while it runs, so the order is the
+// same as picking the first node of that order among the current leaves
+// each time.
+template <class Later>
+void evict_leaves(fk_radix* r, int want_pages, int32_t* pages_out, int cap_pages, int* n_out,
+                  Later later) {
+  *n_out = 0;
+  std::priority_queue<Node*, std::vector<Node*>, Later> heap(later);
+  for (auto& kv : r->by_id) {
+    Node* x = kv.second;
+    if (x != r->root.get() && x->ref == 0 && x->children.empty()) heap.push(x);
+  }
+  while (*n_out < want_pages && !heap.empty()) {
+    Node* v = heap.top();
+    if (*n_out + (int)v->pages.size() > cap_pages) break;
+    heap.pop();
+    std::copy(v->pages.begin(), v->pages.end(), pages_out + *n_out);
+    *n_out += (int)v->pages.size();
+    r->n_pages -= (int64_t)v->pages.size();
+    Node* parent = v->parent;
+    r->by_id.erase(v->id);
+    parent->children.erase(page_key(v->tokens.data(), r->P));   // frees v
+    if (parent != r->root.get() && parent->ref == 0 && parent->children.empty()) heap.push(parent);
+  }
+}
+
 }  // namespace
 
 // ================================================================= ABI ==
@@ -250,24 +280,9 @@ fk_status fk_radix_evict(fk_radix* r, int want_pages, int32_t* pages_out, int ca
                          int* n_out) {
   if (!r || !n_out || (!pages_out && cap_pages) || cap_pages < 0)
     return rfail(FK_ERR_INVALID_ARG, "NULL argument or negative capacity");
-  *n_out = 0;
-  while (*n_out < want_pages) {
-    // least recently used node that no adapter depends on and that has no
-    // children (its pages end a cached prefix)
-    Node* v = nullptr;
-    for (auto& kv : r->by_id) {
-      Node* x = kv.second;
-      if (x == r->root.get() || x->ref != 0 || !x->children.empty()) continue;
-      if (!v || x->last_use < v->last_use) v = x;
-    }
-    if (!v || *n_out + (int)v->pages.size() > cap_pages) break;
-    std::copy(v->pages.begin(), v->pages.end(), pages_out + *n_out);
-    *n_out += (int)v->pages.size();
-    r->n_pages -= (int64_t)v->pages.size();
-    Node* parent = v->parent;
-    r->by_id.erase(v->id);
-    parent->children.erase(page_key(v->tokens.data(), r->P));   // frees v
-  }
+  // least recently used first
+  evict_leaves(r, want_pages, pages_out, cap_pages, n_out,
+               [](const Node* a, const Node* b) { return a->last_use > b->last_use; });
   return FK_OK;
 }
 
@@ -325,34 +340,16 @@ fk_status fk_radix_evict_workflow(fk_radix* r, int want_pages, int32_t* pages_ou
                                   int* n_out) {
   if (!r || !n_out || (!pages_out && cap_pages) || cap_pages < 0)
     return rfail(FK_ERR_INVALID_ARG, "NULL argument or negative capacity");
-  *n_out = 0;
-  // eviction order: larger priority first (unmarked = above every step),
-  // then the least recently used
+  // larger priority first (unmarked = above every step), then the least
+  // recently used
   auto prio = [](const Node* x) -> int64_t {
     return x->steps.empty() ? INT64_MAX : (int64_t)x->steps.begin()->first;
   };
-  auto later = [&](const Node* a, const Node* b) {   // true: a leaves after b
+  evict_leaves(r, want_pages, pages_out, cap_pages, n_out, [&](const Node* a, const Node* b) {
     const int64_t pa = prio(a), pb = prio(b);
     if (pa != pb) return pa < pb;
     return a->last_use > b->last_use;
-  };
-  std::priority_queue<Node*, std::vector<Node*>, decltype(later)> heap(later);
-  for (auto& kv : r->by_id) {
-    Node* x = kv.second;
-    if (x != r->root.get() && x->ref == 0 && x->children.empty()) heap.push(x);
-  }
-  while (*n_out < want_pages && !heap.empty()) {
-    Node* v = heap.top();
-    if (*n_out + (int)v->pages.size() > cap_pages) break;
-    heap.pop();
-    std::copy(v->pages.begin(), v->pages.end(), pages_out + *n_out);
-    *n_out += (int)v->pages.size();
-    r->n_pages -= (int64_t)v->pages.size();
-    Node* parent = v->parent;
-    r->by_id.erase(v->id);
-    parent->children.erase(page_key(v->tokens.data(), r->P));   // frees v
-    if (parent != r->root.get() && parent->ref == 0 && parent->children.empty()) heap.push(parent);
-  }
+  });
   return FK_OK;
 }
 
