@@ -177,3 +177,23 @@ def test_bad_arguments_are_rejected():
         r.adapter_detach(node, 3)
     with pytest.raises(fk.FKError):
         fk.RadixIndex(0)
+
+
+def test_eviction_scales_to_many_prefixes():
+    # 20,000 cached prefixes under 100 shared heads, then everything evicted:
+    # the heap over the current leaves keeps this well under a second
+    import time
+    r = fk.RadixIndex(P)
+    page = 0
+    for h in range(100):
+        r.insert(toks(10000 + h), [page])
+        page += 1
+        for j in range(199):
+            r.insert(toks(10000 + h, 20000 + j), [page])
+            page += 1
+    assert r.stats() == (20000, 20000)
+    t0 = time.perf_counter()
+    freed = r.evict(10 ** 6, cap=10 ** 6)
+    dt = time.perf_counter() - t0
+    assert sorted(freed) == list(range(20000)) and r.stats() == (0, 0)
+    assert dt < 2.0, dt
