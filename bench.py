@@ -351,7 +351,7 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
     ok = bool(torch.isfinite(out.float()).all().item())
     dw.check()
     prefill = measure_prefill(dev, stream, flush, args.prefill_steps) if args.prefill_steps else None
-    configs = measure_configs(dev, stream, flush) if args.all_configs else None
+    configs = measure_configs(dev, stream, flush) if (world == 1 and not args.no_configs) else None
     value, total_ms, e2e_value, e2e_ms = reduce_over_ranks(
         total_ms, e2e_ms, w.A * K, w.A * KE, world, dev)
     ab = algorithmic_bytes(w)
@@ -374,7 +374,8 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
                    "step_bytes": ab["step"]},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic_per_launch(),
-                     "kernel": "mbuild_kernel<128> + decode_kernel<128,false>",
+                     "kernel": ("decode8_kernel" if os.environ.get("FORKKV_DECODE_SLOTS") == "8"
+                                else "mbuild_kernel<128> + decode_kernel<128,false>"),
                      "kernel_ms": statistics.mean(main_ms),
                      "bytes_per_launch": ab["kernel"],
                      "peak_kind": f"{peak_kind} hbm_gbs"},
@@ -662,9 +663,10 @@ def main():
     ap.add_argument("--prefill-steps", type=int, default=100)
     ap.add_argument("--chunk-small", action="store_true",
                     help="only time the chunk kernel's call on a reduced Qwen-72B-shaped chunk")
-    ap.add_argument("--all-configs", action="store_true",
-                    help="also time every workload (tiny, llama8b_32k, agents32_layers32, "
-                         "qwen72b_chunk, compressed) and add their numbers as 'configs'")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing every workload (tiny, llama8b_32k, agents32_layers32, "
+                         "qwen72b_chunk, compressed), whose numbers the default run adds "
+                         "as 'configs' (at N=1)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", type=float, default=None)
     ap.add_argument("--cpu-workers", type=int, default=1)

@@ -79,7 +79,10 @@ typedef struct fk_pool_config {
 
 typedef struct fk_pool fk_pool;
 
-/* Message of the last failed call on this thread ("" if none). */
+/* Message of the last failed call on this thread ("" if none).  Library
+ * plumbing: the pages define no error reporting; the convention is this
+ * header's (see "Conventions shared by every call" above).  The pointer is
+ * owned by the library and valid until the thread's next call. */
 const char* fk_last_error(void);
 
 /* Library version string. */
@@ -87,15 +90,34 @@ const char* fk_version(void);
 
 /* Bytes of device memory the pool needs for `cfg` (0 and FK_ERR_* message
  * via fk_last_error if cfg is invalid).  The caller allocates them (e.g.
- * with torch) and hands them to fk_pool_create. */
+ * with torch) and hands them to fk_pool_create.  The carve-out holds the
+ * two physically separate tiers of the ForkKV guide, "The Disaggregated
+ * Memory Layout": the paged bCache (num_pages x n_layers x H_kv pages of
+ * Kb and Vb) and the rCache arena (per agent, rank-r rows X A_k, X A_v of
+ * max_tokens tokens per layer), plus each agent's Bk, Bv and the
+ * workspace.  Host only; no device call. */
 size_t fk_pool_bytes(const fk_pool_config* cfg);
 
 /* Create a pool over the caller's device carve-out `dev_buf` (dev, 256-byte
  * aligned, >= fk_pool_bytes(cfg) bytes).  The buffer's contents need not be
  * initialised.  Host metadata (page free list and reference counts, agent
- * table) lives in the returned handle.  Uses the current CUDA device. */
+ * table) lives in the returned handle.  Uses the current CUDA device.  The
+ * pool is the ForkKV guide's "DisaggregatedKVCache" ("Complete End-to-End
+ * Implementation", item 2: it manages the physical bCache and rCache
+ * memory pools) with the tiers of "The Disaggregated Memory Layout".
+ * FK_ERR_INVALID_ARG on a bad config, a NULL or misaligned buffer, or too
+ * few bytes (*out is then untouched); FK_ERR_CUDA if a device call fails.
+ * Environment (read here, fixed for the pool's life):
+ * FORKKV_DECODE_SLOTS=8 plans decode-shaped calls with d = 128 on the
+ * uncompressed pool in tiles of eight agents (every base page read once
+ * per kv head) instead of four. */
 fk_status fk_pool_create(const fk_pool_config* cfg, void* dev_buf,
                          size_t bytes, fk_pool** out);
+/* Free the handle and its host metadata (NULL: FK_ERR_INVALID_ARG).  The
+ * caller must have synchronised every stream with work on the pool; the
+ * carve-out stays the caller's to free.  Library plumbing (the pages
+ * describe no teardown beyond reclaiming an agent's rCache, "Reference
+ * Counting and Eviction"). */
 fk_status fk_pool_destroy(fk_pool* pool);
 
 /* Byte offset and size of a region of the pool carve-out, for reading the
@@ -149,7 +171,10 @@ int fk_page_refcount(const fk_pool* pool, int32_t page_id);
 /* ---- agents ---- */
 
 /* Register agent `agent` with rank `rank` (multiple of 8, <= max_rank) and
- * residual scale `s` (alpha/r of the adapter), copying its up-projections
+ * residual scale `s` (alpha/r of the adapter: ForkKV guide, "Mathematical
+ * Decomposition of LoRA KV Activations", Delta K = (alpha/r) X A_k B_k and
+ * likewise for V; the rCache keeps the factored X A, "The Disaggregated
+ * Memory Layout", item 2), copying its up-projections
  * Bk, Bv (dev bf16 [n_layers][rank][H_kv*d]) into the pool and reserving
  * its rCache (n_layers x max_tokens x rank for Lk and for Lv).
  * FK_ERR_INVALID_ARG if the id is taken; FK_ERR_OOM if the rCache arena is
@@ -180,7 +205,10 @@ fk_status fk_agent_rcache(const fk_pool* pool, int agent, size_t* lk_offset,
 /* ---- appends ---- */
 
 /* Write base keys/values of tokens pos..pos+n-1 of one sequence into layer
- * `layer` of the pages named by `block_table_row` (host, max_pages
+ * `layer` of the bCache (ForkKV guide, "The Disaggregated Memory Layout",
+ * item 1: base states, computed once, shared and immutable once shared;
+ * "The Copy-on-Write Paradigm": a writer gets a private copy) pages named
+ * by `block_table_row` (host, max_pages
  * entries, logical page -> page id, -1 = none).  Kb, Vb: dev bf16
  * [n][H_kv][d], post-RoPE.  Missing pages (-1) are allocated and written
  * into the row.  A named page whose reference count is above 1 is shared:
@@ -195,7 +223,10 @@ fk_status fk_base_append(fk_pool* pool, int layer, int32_t* block_table_row,
 
 /* Write residual rows of tokens pos..pos+n-1 of agent `agent`, layer
  * `layer`: Lk, Lv dev bf16 [n][rank] (Lk = X A_k, Lv = X A_v of those
- * tokens).  pos + n <= max_tokens. */
+ * tokens: the factored rank-r activations the rCache stores, ForkKV guide,
+ * "The Disaggregated Memory Layout", item 2).  pos + n <= max_tokens.
+ * FK_ERR_INVALID_ARG for an agent that is not live or rows out of range
+ * (nothing is launched); FK_ERR_CUDA if the copy kernel fails to launch. */
 fk_status fk_residual_append(fk_pool* pool, int layer, int agent, int pos,
                              int n, const uint16_t* Lk, const uint16_t* Lv,
                              void* stream);
@@ -287,10 +318,16 @@ fk_status fk_residual_attention(fk_pool* pool, int layer, const uint16_t* q,
  * whose work list and partials need more than FK_NOALLOC_SCRATCH_BYTES
  * fail with FK_ERR_OOM and a message giving the size needed.  The first
  * call on a device looks up the array's device address (set-up done once
- * per device), so make that first call before any stream capture.  All
- * calls share the one array, which keeps the last call's contents; calls
- * whose kernels overlap on the GPU (other streams, other pools) race on it
- * and must be ordered by the caller. */
+ * per device), so make that first call before any stream capture.  A call
+ * whose work list differs from the last one on the device (other inputs,
+ * another pool, agents registered or pages changed since) uploads it with
+ * a copy from host memory the library keeps, which stream capture does
+ * not take: make such calls outside capture; repeat calls with unchanged
+ * inputs on the same pool enqueue only the kernels.  All calls share the
+ * one array, which keeps the last call's contents; calls whose kernels
+ * overlap on the GPU (other streams, other pools) race on it and must be
+ * ordered by the caller.  FK_ERR_INVALID_ARG if the current CUDA device is
+ * not the pool's (the array is per device). */
 #define FK_NOALLOC_SCRATCH_BYTES (16u << 20)
 fk_status fk_residual_attention_noalloc(fk_pool* pool, int layer,
                                         const uint16_t* q,

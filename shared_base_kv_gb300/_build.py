@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libforkkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["fk_host.cpp", "fk_kernels.cu", "fk_decode.cu", "fk_radix.cpp", "fk_prefill.cu", "fk_chunk.cu"]
+SOURCES = ["fk_host.cpp", "fk_kernels.cu", "fk_decode.cu", "fk_decode8.cu", "fk_radix.cpp", "fk_prefill.cu",
+           "fk_chunk.cu"]
 
 
 def _nvcc() -> str:

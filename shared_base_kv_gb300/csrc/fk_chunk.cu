@@ -38,6 +38,7 @@
 
 #include "fk_device.cuh"
 #include "fk_internal.h"
+#include "fk_once.h"
 
 namespace fk {
 namespace chk {
@@ -578,13 +579,12 @@ __global__ void __launch_bounds__(chk::kThreads, 1)
 bool chunk_applies(const PoolGeom& g, const PlanDev& p) { return p.chunk != 0 && g.d == chk::D; }
 
 int launch_chunk(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q, void* stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         chk::Layout::TOTAL);
-    if (e != cudaSuccess) return (int)e;
-    attr_done = true;
-  }
+  static PerDeviceOnce once;
+  const int se = once.run([] {
+    return (int)cudaFuncSetAttribute(chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     chk::Layout::TOTAL);
+  });
+  if (se != 0) return se;
   chunk_kernel<<<p.n_ctas, chk::kThreads, chk::Layout::TOTAL, (cudaStream_t)stream>>>(g, p, layer, q);
   return (int)cudaGetLastError();
 }

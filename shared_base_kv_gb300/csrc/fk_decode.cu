@@ -45,6 +45,7 @@
 
 #include "fk_device.cuh"
 #include "fk_internal.h"
+#include "fk_once.h"
 
 namespace fk {
 namespace dec {
@@ -1004,8 +1005,8 @@ static int launch_decode_t(const PoolGeom& g, const PlanDev& p, int layer, const
                            cudaStream_t st) {
   using LY = dec::Layout<D, COMP>;
   static_assert(LY::TOTAL <= 232448, "shared memory over the 227 KB a CTA may use");
-  static bool attr_done = false;
-  if (!attr_done) {
+  static PerDeviceOnce once;
+  const int se = once.run([] {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, COMP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL);
     if (e != cudaSuccess) return (int)e;
@@ -1015,9 +1016,9 @@ static int launch_decode_t(const PoolGeom& g, const PlanDev& p, int layer, const
     cudaFuncAttributes fa{};
     e = cudaFuncGetAttributes(&fa, decode_kernel<D, COMP>);
     if (e != cudaSuccess) return (int)e;
-    if (fa.numRegs != 128) return (int)cudaErrorInvalidConfiguration;
-    attr_done = true;
-  }
+    return fa.numRegs == 128 ? 0 : (int)cudaErrorInvalidConfiguration;
+  });
+  if (se != 0) return se;
   mbuild_kernel<D><<<dim3(1, p.n_mpairs), 1024, 0, st>>>(g, p, layer, q);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;

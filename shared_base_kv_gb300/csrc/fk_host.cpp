@@ -5,8 +5,10 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -54,8 +56,13 @@ struct Staging {
 struct fk_pool {
   fk_pool_config cfg;
   PoolGeom g;
+  uint64_t uid = 0;                          // unique per pool of the process (never reused)
   int device = 0;
   int num_sms = 0;
+  // decode-shaped calls with d = 128 on the uncompressed pool: tiles of
+  // eight agent slots (FORKKV_DECODE_SLOTS=8 at pool creation) instead of
+  // four agents
+  bool slots8 = false;
   std::vector<int32_t> refcount;             // per page
   std::vector<int32_t> free_list;            // stack of free page ids
   std::vector<uint8_t> fill;                 // [L][num_pages] tokens held
@@ -248,10 +255,14 @@ fk_status upload_agent(fk_pool* p, int a, cudaStream_t st) {
 
 // ----------------------------------------------------------- planner --
 
+// slots8: the eight-slot tiles of the decode kernel for decode-shaped calls
+// (fk_decode8.cu): two halves of at most four agents and 64 padded ranks
+// each, agent slot s holding tile rows 4 s .. 4 s + 3; empty slots are -1
+// in tile_agents and their rows -1 in row_agent (no output row reads them).
 fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
                      int max_pages, const int32_t* seq, const int32_t* rpad,
                      int max_rows, int max_rank_sum, int target_items,
-                     HostPlan& out) {
+                     HostPlan& out, bool slots8 = false) {
   if (A < 1 || C < 1) return fail(FK_ERR_INVALID_ARG, "A and C must be >= 1");
   if (H_kv < 1 || H_q % H_kv) return fail(FK_ERR_INVALID_ARG, "bad head counts");
   if (!bt || !seq || !rpad) return fail(FK_ERR_INVALID_ARG, "NULL table");
@@ -279,7 +290,8 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
   std::map<std::vector<int32_t>, std::vector<std::pair<int32_t, int32_t>>> sets;
   for (auto& kv : cls) sets[kv.second].push_back(kv.first);
   // 3. tiles of every set, and page runs
-  struct Tile { std::vector<int32_t> agents; std::vector<std::pair<int32_t,int32_t>> rows; int rank_sum; };
+  if (slots8 && G * C != 4) return fail(FK_ERR_INVALID_ARG, "eight-slot tiles need four rows per agent");
+  struct Tile { std::vector<int32_t> agents; std::vector<std::pair<int32_t,int32_t>> rows; int rank_sum; int n_real = 0; };
   struct SetWork { std::vector<Tile> tiles; std::vector<std::vector<std::pair<int32_t,int32_t>>> runs; };
   std::vector<SetWork> work;
   int64_t total_units = 0;
@@ -294,7 +306,37 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
       for (int k = 0; k < n_agents; ++k) tot += (k * rpa + rpa - 1) / 16 - (k * rpa) / 16 + 1;
       return tot;
     };
-    for (int32_t a : kv.first) {
+    if (slots8) {
+      // fill half 0, then half 1; an agent that does not fit the current
+      // half opens the next one (or a new tile)
+      int half = 0, nh[2] = {0, 0}, rh[2] = {0, 0};
+      std::vector<int32_t> slot(kDecodeSlots, -1);
+      auto emit = [&]() {
+        if (nh[0] + nh[1] == 0) return;
+        Tile t{{}, {}, rh[0] + rh[1], nh[0] + nh[1]};
+        for (int s2 = 0; s2 < kDecodeSlots; ++s2) {
+          t.agents.push_back(slot[s2]);
+          for (int g2 = 0; g2 < rpa; ++g2) t.rows.push_back({slot[s2], slot[s2] >= 0 ? g2 : 0});
+        }
+        sw.tiles.push_back(t);
+        half = 0; nh[0] = nh[1] = 0; rh[0] = rh[1] = 0;
+        std::fill(slot.begin(), slot.end(), -1);
+      };
+      for (int32_t a : kv.first) {
+        while (true) {
+          if (nh[half] < kDecodeSlots / 2 && rh[half] + rpad[a] <= kDecodeHalfRank) {
+            slot[(kDecodeSlots / 2) * half + nh[half]] = a;
+            ++nh[half];
+            rh[half] += rpad[a];
+            break;
+          }
+          if (half == 0) { half = 1; continue; }
+          emit();
+        }
+      }
+      emit();
+    }
+    for (int32_t a : (slots8 ? std::vector<int32_t>{} : kv.first)) {
       if (rpa <= max_rows) {
         if ((int)cur.rows.size() + rpa > max_rows || cur.rank_sum + rpad[a] > max_rank_sum ||
             (int)cur.agents.size() >= kMaxAgentsPerTile ||
@@ -302,17 +344,18 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
           flush();
         cur.agents.push_back(a);
         cur.rank_sum += rpad[a];
+        ++cur.n_real;
         for (int cg = 0; cg < rpa; ++cg) cur.rows.push_back({a, cg});
       } else {
         flush();
         for (int c0 = 0; c0 < rpa; c0 += max_rows) {
-          Tile t{{a}, {}, rpad[a]};
+          Tile t{{a}, {}, rpad[a], 1};
           for (int cg = c0; cg < std::min(rpa, c0 + max_rows); ++cg) t.rows.push_back({a, cg});
           sw.tiles.push_back(t);
         }
       }
     }
-    flush();
+    if (!slots8) flush();
     const auto& pg = kv.second;   // sorted by logical page
     size_t s0 = 0;
     for (size_t k = 1; k <= pg.size(); ++k) {
@@ -331,7 +374,7 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
   // several items run back to back by the same CTA.
   (void)total_units;
   HostPlan pl;
-  struct Seg { int tile_row0, tile_ag0, n_rows, n_ag, rank_sum, head, page0, lp0, len; };
+  struct Seg { int tile_row0, tile_ag0, n_rows, n_ag, rank_sum, head, page0, lp0, len, n_real; };
   std::vector<Seg> segs;
   int64_t total_w = 0;
   for (auto& sw : work) {
@@ -352,62 +395,102 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
         for (size_t ri = 0; ri < sw.runs.size(); ++ri) {
           Seg sg{tile_row0[ti], tile_ag0[ti], (int)sw.tiles[ti].rows.size(),
                  (int)sw.tiles[ti].agents.size(), sw.tiles[ti].rank_sum, h, run_page0[ri],
-                 sw.runs[ri][0].first, (int)sw.runs[ri].size()};
+                 sw.runs[ri][0].first, (int)sw.runs[ri].size(), sw.tiles[ti].n_real};
           segs.push_back(sg);
-          total_w += (int64_t)sg.len * (2 + sg.n_ag);
+          total_w += (int64_t)sg.len * (2 + sg.n_real);
         }
   }
   int64_t total_tiles = 0;
   for (auto& sg : segs) total_tiles += (sg.len + kTilePages - 1) / kTilePages;
   const int n_ctas = (int)std::max<int64_t>(1, std::min<int64_t>(target_items, total_tiles));
-  pl.cta_begin.assign(n_ctas + 1, 0);
-  // A CTA that starts a second item pays for it (the item's set-up, its
-  // own M and a drained pipeline: about two tiles of work), so such CTAs
-  // are charged that much extra weight; pieces are cut at whole key tiles
-  // of their segment, so only a segment's last item has a partial tile.
-  auto item_cost = [&](const Seg& sg) { return (int64_t)2 * kTilePages * (2 + sg.n_ag); };
-  int64_t total_wc = total_w;
-  for (size_t i = 1; i < segs.size(); ++i) total_wc += item_cost(segs[i]);
-  size_t si = 0;
-  int off = 0;           // pages of segs[si] already handed out
-  int64_t acc = 0;       // weight handed out so far
-  for (int c = 0; c < n_ctas; ++c) {
-    pl.cta_begin[c] = (int)pl.items.size();
-    const int64_t goal = total_wc * (c + 1) / n_ctas;
-    bool first = true;
-    while (si < segs.size() && (acc < goal || c == n_ctas - 1)) {
-      const Seg& sg = segs[si];
-      const int64_t wpp = 2 + sg.n_ag;
-      if (!first) {
-        if (acc + item_cost(sg) >= goal && c != n_ctas - 1) break;
-        acc += item_cost(sg);
+  auto push_item = [&](const Seg& sg, int off, int take) {
+    fk_work_item it{};
+    it.head = sg.head;
+    it.row_begin = sg.tile_row0;
+    it.n_rows = sg.n_rows;
+    it.page_begin = sg.page0 + off;
+    it.n_pages = take;
+    it.lp_begin = sg.lp0 + off;
+    it.agent_begin = sg.tile_ag0;
+    it.n_agents = sg.n_ag;
+    it.partial_begin = pl.n_partials;
+    it.sum_rank = sg.rank_sum;
+    pl.n_partials += it.n_rows;
+    pl.items.push_back(it);
+  };
+  if (slots8 && (int64_t)segs.size() <= n_ctas) {
+    // One item per CTA: every segment gets a share of the CTAs in
+    // proportion to its tiles (at least one, at most one per tile), the
+    // largest remainders first, and is cut into that many runs of whole
+    // tiles of nearly equal length.  Each CTA then builds one M.
+    const int ns = (int)segs.size();
+    std::vector<int64_t> tiles(ns);
+    std::vector<int> share(ns, 1);
+    for (int i = 0; i < ns; ++i) tiles[i] = (segs[i].len + kTilePages - 1) / kTilePages;
+    int used = ns;
+    while (used < n_ctas) {
+      int best = -1;
+      double best_load = 0.0;
+      for (int i = 0; i < ns; ++i) {
+        if (share[i] >= tiles[i]) continue;
+        const double load = (double)tiles[i] / share[i];
+        if (best < 0 || load > best_load) { best = i; best_load = load; }
       }
-      first = false;
-      int64_t want = (c == n_ctas - 1) ? (sg.len - off) : (goal - acc + wpp - 1) / wpp;
-      want = (want + kTilePages - 1) / kTilePages * kTilePages;
-      int take = (int)std::max<int64_t>(1, std::min<int64_t>(want, sg.len - off));
-      fk_work_item it{};
-      it.head = sg.head;
-      it.row_begin = sg.tile_row0;
-      it.n_rows = sg.n_rows;
-      it.page_begin = sg.page0 + off;
-      it.n_pages = take;
-      it.lp_begin = sg.lp0 + off;
-      it.agent_begin = sg.tile_ag0;
-      it.n_agents = sg.n_ag;
-      it.partial_begin = pl.n_partials;
-      it.sum_rank = sg.rank_sum;
-      pl.n_partials += it.n_rows;
-      pl.items.push_back(it);
-      acc += take * wpp;
-      off += take;
-      if (off == sg.len) { ++si; off = 0; }
+      if (best < 0) break;
+      ++share[best];
+      ++used;
     }
+    pl.cta_begin.clear();
+    for (int i = 0; i < ns; ++i) {
+      const Seg& sg = segs[i];
+      for (int c = 0; c < share[i]; ++c) {
+        const int64_t t0 = tiles[i] * c / share[i], t1 = tiles[i] * (c + 1) / share[i];
+        const int off = (int)(t0 * kTilePages);
+        const int take = (int)std::min<int64_t>(t1 * kTilePages, sg.len) - off;
+        pl.cta_begin.push_back((int)pl.items.size());
+        push_item(sg, off, take);
+      }
+    }
+    pl.cta_begin.push_back((int)pl.items.size());
+  } else {
+    pl.cta_begin.assign(n_ctas + 1, 0);
+    // A CTA that starts a second item pays for it (the item's set-up, its
+    // own M and a drained pipeline: about two tiles of work), so such CTAs
+    // are charged that much extra weight; pieces are cut at whole key tiles
+    // of their segment, so only a segment's last item has a partial tile.
+    auto item_cost = [&](const Seg& sg) { return (int64_t)2 * kTilePages * (2 + sg.n_real); };
+    int64_t total_wc = total_w;
+    for (size_t i = 1; i < segs.size(); ++i) total_wc += item_cost(segs[i]);
+    size_t si = 0;
+    int off = 0;           // pages of segs[si] already handed out
+    int64_t acc = 0;       // weight handed out so far
+    for (int c = 0; c < n_ctas; ++c) {
+      pl.cta_begin[c] = (int)pl.items.size();
+      const int64_t goal = total_wc * (c + 1) / n_ctas;
+      bool first = true;
+      while (si < segs.size() && (acc < goal || c == n_ctas - 1)) {
+        const Seg& sg = segs[si];
+        const int64_t wpp = 2 + sg.n_real;
+        if (!first) {
+          if (acc + item_cost(sg) >= goal && c != n_ctas - 1) break;
+          acc += item_cost(sg);
+        }
+        first = false;
+        int64_t want = (c == n_ctas - 1) ? (sg.len - off) : (goal - acc + wpp - 1) / wpp;
+        want = (want + kTilePages - 1) / kTilePages * kTilePages;
+        int take = (int)std::max<int64_t>(1, std::min<int64_t>(want, sg.len - off));
+        push_item(sg, off, take);
+        acc += take * wpp;
+        off += take;
+        if (off == sg.len) { ++si; off = 0; }
+      }
+    }
+    pl.cta_begin[n_ctas] = (int)pl.items.size();
   }
-  pl.cta_begin[n_ctas] = (int)pl.items.size();
-  // 4b. decode-shaped calls: one query-side RoPE matrix per (agent tile,
-  // kv head), shared by the items that split that tile's pages
-  if (rpa == 4) {
+  // 4b. decode-shaped calls of the four-agent decode kernel: one
+  // query-side RoPE matrix per (agent tile, kv head), shared by the items
+  // that split that tile's pages (the eight-slot kernel builds its own)
+  if (rpa == 4 && !slots8) {
     std::map<std::pair<int32_t, int32_t>, int32_t> idx;
     for (auto& it : pl.items) {
       auto key = std::make_pair(it.agent_begin, it.head);
@@ -433,8 +516,10 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
     int c = cg / G, g = cg % G;
     return (a * C + c) * H_q + it.head * G + g;
   };
+  auto real = [&](const fk_work_item& it, int j) { return pl.row_agent[it.row_begin + j] >= 0; };
   for (auto& it : pl.items)
-    for (int j = 0; j < it.n_rows; ++j) cnt[out_row(it, j) + 1]++;
+    for (int j = 0; j < it.n_rows; ++j)
+      if (real(it, j)) cnt[out_row(it, j) + 1]++;
   for (int r = 0; r < n_out; ++r) {
     if (cnt[r + 1] == 0) return fail(FK_ERR_INVALID_ARG, "an output row has no keys");
     cnt[r + 1] += cnt[r];
@@ -443,7 +528,8 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
   pl.csr_slots.assign(cnt[n_out], 0);
   std::vector<int32_t> pos(cnt.begin(), cnt.end() - 1);
   for (auto& it : pl.items)
-    for (int j = 0; j < it.n_rows; ++j) pl.csr_slots[pos[out_row(it, j)]++] = it.partial_begin + j;
+    for (int j = 0; j < it.n_rows; ++j)
+      if (real(it, j)) pl.csr_slots[pos[out_row(it, j)]++] = it.partial_begin + j;
   out = std::move(pl);
   return FK_OK;
 }
@@ -602,6 +688,50 @@ int64_t pack_plan(const HostPlan& pl, int A, int C, int causal, const int32_t* a
   return need;
 }
 
+// Which kernel a call runs, and its work list packed for the workspace:
+// calls with many rows per agent and kv head take the chunk kernel;
+// decode-shaped calls (four rows per agent) with d = 128 on the
+// uncompressed pool take the eight-slot decode kernel when the pool was
+// created with it; the rest the four-agent decode kernel or the general
+// kernel.
+fk_status build_call_plan(const fk_pool* p, const int32_t* agents, const int32_t* bt, int max_pages,
+                          const int32_t* seq, const int32_t* rp, int A, int C, int causal,
+                          int compressed, HostPlan& pl, std::vector<uint8_t>& blob, PlanDev& pd,
+                          int64_t& need) {
+  const PoolGeom& g = p->g;
+  const bool chunk = use_chunk(g, C, compressed);
+  const bool dec8 = p->slots8 && !chunk && !compressed && g.d == 128 && g.G * C == 4;
+  fk_status s = chunk ? plan_chunk(A, C, g.H_q, g.H_kv, bt, max_pages, seq, p->num_sms, pl)
+              : dec8  ? plan_build(A, C, g.H_q, g.H_kv, kPage, bt, max_pages, seq, rp,
+                                   4 * kDecodeSlots, 2 * kDecodeHalfRank, p->num_sms, pl, true)
+                      : plan_build(A, C, g.H_q, g.H_kv, kPage, bt, max_pages, seq, rp, kMaxRows,
+                                   kMaxRankSum, p->num_sms, pl);
+  if (s != FK_OK) return s;
+  fill_mpairs(pl, p, agents, C);
+  need = pack_plan(pl, A, C, causal, agents, seq, g, blob, pd);
+  pd.chunk = chunk ? 1 : 0;
+  pd.slots8 = dec8 ? 1 : 0;
+  return FK_OK;
+}
+
+}  // namespace
+
+// Work list of fk_residual_attention_noalloc, kept apart from the pool's own
+// cache: the static scratch is shared by every pool of the process, one
+// entry per device.  Entries are keyed by the pool's uid, which no later
+// pool reuses (a new pool may get a freed pool's address), and a destroyed
+// pool's entries are cleared.  The uploaded blob stays here: its host
+// memory outlives the copy.
+namespace {
+struct NoallocCache {
+  uint64_t pool_uid = 0;
+  std::vector<int32_t> key;
+  std::vector<uint8_t> blob;
+  PlanDev pd{};
+};
+NoallocCache g_noalloc[kMaxDevices];
+std::mutex g_noalloc_mu;
+std::atomic<uint64_t> g_next_pool_uid{1};
 }  // namespace
 
 // ================================================================= ABI ==
@@ -637,11 +767,16 @@ fk_status fk_pool_create(const fk_pool_config* cfg, void* dev_buf, size_t bytes,
     return fail(FK_ERR_INVALID_ARG, "dev_buf is not device memory");
   }
   fk_pool* p = new fk_pool();
+  p->uid = g_next_pool_uid.fetch_add(1);
   p->cfg = *cfg;
   p->g = g;
   p->g.base = (uint8_t*)dev_buf;
   cudaGetDevice(&p->device);
   cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+  {
+    const char* ds = std::getenv("FORKKV_DECODE_SLOTS");
+    p->slots8 = ds != nullptr && std::strcmp(ds, "8") == 0;
+  }
   p->refcount.assign(g.num_pages, 0);
   p->free_list.reserve(g.num_pages);
   for (int i = g.num_pages - 1; i >= 0; --i) p->free_list.push_back(i);
@@ -680,6 +815,11 @@ fk_status fk_pool_create(const fk_pool_config* cfg, void* dev_buf, size_t bytes,
 
 fk_status fk_pool_destroy(fk_pool* p) {
   if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    for (NoallocCache& c : g_noalloc)
+      if (c.pool_uid == p->uid) c = NoallocCache();
+  }
   if (p->stage.pending) cudaEventSynchronize(p->stage.done);
   if (p->stage.host) cudaFreeHost(p->stage.host);
   if (p->stage.done) cudaEventDestroy(p->stage.done);
@@ -1128,17 +1268,12 @@ fk_status fk_residual_attention(fk_pool* p, int layer, const uint16_t* q, const 
       }
     }
     HostPlan pl;
-    const bool chunk = use_chunk(g, C, compressed);
-    fk_status s = chunk ? plan_chunk(A, C, g.H_q, g.H_kv, bt, max_pages, seq, p->num_sms, pl)
-                        : plan_build(A, C, g.H_q, g.H_kv, kPage, bt, max_pages, seq, rp.data(),
-                                     kMaxRows, kMaxRankSum, p->num_sms, pl);
-    if (s != FK_OK) return s;
-    fill_mpairs(pl, p, agents, C);
-    // pack into the workspace
     PlanDev pd{};
     std::vector<uint8_t> blob;
-    int64_t need = pack_plan(pl, A, C, causal, agents, seq, g, blob, pd);
-    pd.chunk = chunk ? 1 : 0;
+    int64_t need = 0;
+    fk_status s = build_call_plan(p, agents, bt, max_pages, seq, rp.data(), A, C, causal, compressed,
+                                  pl, blob, pd, need);
+    if (s != FK_OK) return s;
     if (need > g.ws_bytes) return fail(FK_ERR_OOM, "workspace too small for this call");
     fk_status s2 = stage_upload(p, blob.data(), blob.size(), g.base + g.off_ws, st);
     if (s2 != FK_OK) return s2;
@@ -1155,19 +1290,6 @@ fk_status fk_residual_attention(fk_pool* p, int layer, const uint16_t* q, const 
   return FK_OK;
 }
 
-// Work list of fk_residual_attention_noalloc, kept apart from the pool's own
-// cache: the static scratch is shared by every pool of the process.
-namespace {
-struct NoallocCache {
-  const fk_pool* pool = nullptr;
-  int device = -1;
-  std::vector<int32_t> key;
-  PlanDev pd{};
-};
-NoallocCache g_noalloc[64];
-std::mutex g_noalloc_mu;
-}  // namespace
-
 fk_status fk_residual_attention_noalloc(fk_pool* p, int layer, const uint16_t* q,
                                         const int32_t* agents, const int32_t* bt, int max_pages,
                                         const int32_t* seq, int A, int C, int causal,
@@ -1178,6 +1300,10 @@ fk_status fk_residual_attention_noalloc(fk_pool* p, int layer, const uint16_t* q
   if (!q || !out || !agents || !bt || !seq) return fail(FK_ERR_INVALID_ARG, "NULL argument");
   if (A < 1 || C < 1 || max_pages < 1) return fail(FK_ERR_INVALID_ARG, "A, C, max_pages must be >= 1");
   if (compressed && !g.compressed) return fail(FK_ERR_INVALID_ARG, "pool has no compressed copy");
+  int cur_dev = -1;
+  if (cudaGetDevice(&cur_dev) != cudaSuccess || cur_dev != p->device)
+    return fail(FK_ERR_INVALID_ARG, "the current CUDA device is not the pool's");
+  if (p->device < 0 || p->device >= kMaxDevices) return fail(FK_ERR_INVALID_ARG, "device id out of range");
   void* scratch = nullptr;
   size_t scratch_bytes = 0;
   int ce = noalloc_scratch(&scratch, &scratch_bytes);
@@ -1191,9 +1317,9 @@ fk_status fk_residual_attention_noalloc(fk_pool* p, int layer, const uint16_t* q
   key.insert(key.end(), bt, bt + (int64_t)A * max_pages);
   key.insert(key.end(), {(int32_t)(p->plan_gen & 0x7FFFFFFF), (int32_t)(p->plan_gen >> 31)});
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  NoallocCache& cache = g_noalloc[p->device & 63];
-  if (cache.pool != p || cache.device != p->device || cache.key != key) {
-    cache.pool = nullptr;
+  NoallocCache& cache = g_noalloc[p->device];
+  if (cache.pool_uid != p->uid || cache.key != key) {
+    cache.pool_uid = 0;
     std::vector<int32_t> rp(A), seen(g.max_agents, 0);
     for (int i = 0; i < A; ++i) {
       int a = agents[i];
@@ -1210,16 +1336,12 @@ fk_status fk_residual_attention_noalloc(fk_pool* p, int layer, const uint16_t* q
       }
     }
     HostPlan pl;
-    const bool chunk = use_chunk(g, C, compressed);
-    fk_status s = chunk ? plan_chunk(A, C, g.H_q, g.H_kv, bt, max_pages, seq, p->num_sms, pl)
-                        : plan_build(A, C, g.H_q, g.H_kv, kPage, bt, max_pages, seq, rp.data(),
-                                     kMaxRows, kMaxRankSum, p->num_sms, pl);
-    if (s != FK_OK) return s;
-    fill_mpairs(pl, p, agents, C);
     PlanDev pd{};
     std::vector<uint8_t> blob;
-    int64_t need = pack_plan(pl, A, C, causal, agents, seq, g, blob, pd);
-    pd.chunk = chunk ? 1 : 0;
+    int64_t need = 0;
+    fk_status s = build_call_plan(p, agents, bt, max_pages, seq, rp.data(), A, C, causal, compressed,
+                                  pl, blob, pd, need);
+    if (s != FK_OK) return s;
     if (need > (int64_t)scratch_bytes) {
       char msg[160];
       std::snprintf(msg, sizeof msg,
@@ -1227,11 +1349,12 @@ fk_status fk_residual_attention_noalloc(fk_pool* p, int layer, const uint16_t* q
                     (long long)need, scratch_bytes);
       return fail(FK_ERR_OOM, msg);
     }
-    // pageable source: the copy is staged before the call returns
-    cudaError_t e = cudaMemcpyAsync(scratch, blob.data(), blob.size(), cudaMemcpyHostToDevice, st);
+    // pageable source, kept in the cache entry until the next upload
+    cache.blob = std::move(blob);
+    cudaError_t e = cudaMemcpyAsync(scratch, cache.blob.data(), cache.blob.size(),
+                                    cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_fail(e, "work list upload");
-    cache.pool = p;
-    cache.device = p->device;
+    cache.pool_uid = p->uid;
     cache.key = std::move(key);
     cache.pd = pd;
   }

@@ -22,6 +22,12 @@ constexpr int kMaxRankSum = 64;    // sum of padded ranks of one work tile
 constexpr int kMaxAgentsPerTile = 4;
 constexpr int kMaxRowGroups = 4;   // 16-row query groups the agents of a tile touch
 constexpr int kMaxRankPad = 64;
+// Decode-shaped calls with d = 128 on an uncompressed pool run in tiles of
+// up to eight agent slots (four query rows each): two halves of four slots,
+// each half holding at most 64 padded ranks (fk_decode8.cu).
+constexpr int kDecodeSlots = 8;
+constexpr int kDecodeHalfRank = 64;
+constexpr int kMaxDevices = 64;    // devices a process may drive (per-device set-up tables)
 
 FK_HD inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 FK_HD inline int rank_pad(int r) { return (r + 15) / 16 * 16; }
@@ -71,6 +77,9 @@ struct PlanDev {
   int32_t n_ctas;          // persistent CTAs; CTA c runs items cta[c] .. cta[c+1]-1
   int32_t n_mpairs;        // decode-shaped calls: (agent tile, kv head) pairs with an M
   int32_t chunk;           // 1: the items are the chunk kernel's (fk_chunk.cu)
+  int32_t slots8;          // 1: eight-slot decode tiles (fk_decode8.cu); tile_agents holds
+                           // kDecodeSlots entries per tile (-1: empty slot), rows 4 per slot
+                           // (row_agent -1: a padded row)
   int64_t off_items, off_row_agent, off_row_cg, off_pages, off_tile_agents,
           off_call_agents, off_csr_ptr, off_csr_slots, off_partials, off_cta;
   int64_t off_mpairs, off_item_mpair;   // MPair[n_mpairs], int32[n_items]
@@ -122,6 +131,12 @@ int launch_attention(const PoolGeom& g, const PlanDev& p, int layer,
 bool decode_applies(const PoolGeom& g, const PlanDev& p);
 int launch_decode(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q,
                   int compressed, void* stream);
+
+// Decode-shaped calls planned in eight-slot tiles (d = 128, uncompressed
+// pool) run the eight-agent decode kernel (fk_decode8.cu); the combine is
+// shared.
+bool decode8_applies(const PoolGeom& g, const PlanDev& p);
+int launch_decode8(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q, void* stream);
 
 // Calls with at least 128 query rows per agent and kv head (d = 128,
 // uncompressed pool) run the chunk kernel (fk_chunk.cu); the combine is

@@ -12,10 +12,9 @@
 
 #include "fk_device.cuh"
 #include "fk_internal.h"
+#include "fk_once.h"
 
 namespace fk {
-
-constexpr int kMaxDevices = 64;
 
 __device__ __forceinline__ uint32_t* err_word(const PoolGeom& g) {
   return (uint32_t*)(g.base + g.off_err);
@@ -1219,17 +1218,20 @@ template <int D, bool COMP>
 static int launch_attn_t(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q,
                          uint16_t* out, int num_sms, cudaStream_t st, cudaEvent_t ev) {
   using LY = attn::Layout<D, COMP>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(attention_kernel<D, COMP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL);
-    if (e != cudaSuccess) return (int)e;
-    attr_done = true;
-  }
+  static PerDeviceOnce once;
+  const int se = once.run([] {
+    return (int)cudaFuncSetAttribute(attention_kernel<D, COMP>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, LY::TOTAL);
+  });
+  if (se != 0) return se;
   if (p.chunk) {
     if (COMP || !chunk_applies(g, p)) return (int)cudaErrorInvalidValue;   // planner mismatch
     int ce = launch_chunk(g, p, layer, q, st);
     if (ce != 0) return ce;
+  } else if (p.slots8) {
+    if (COMP || !decode8_applies(g, p)) return (int)cudaErrorInvalidValue;  // planner mismatch
+    int de = launch_decode8(g, p, layer, q, st);
+    if (de != 0) return de;
   } else if (decode_applies(g, p)) {
     int de = launch_decode(g, p, layer, q, COMP ? 1 : 0, st);
     if (de != 0) return de;
@@ -1263,7 +1265,7 @@ int launch_attention(const PoolGeom& g, const PlanDev& p, int layer, const uint1
                      void* event_after_main) {
   cudaStream_t st = (cudaStream_t)stream;
   cudaEvent_t ev = (cudaEvent_t)event_after_main;
-  *n_launches = decode_applies(g, p) ? 3 : 2;   // (M build,) attention, combine
+  *n_launches = (!p.slots8 && !p.chunk && decode_applies(g, p)) ? 3 : 2;   // (M build,) attention, combine
   if (g.d == 128) {
     return compressed ? launch_attn_t<128, true>(g, p, layer, q, out, num_sms, st, ev)
                       : launch_attn_t<128, false>(g, p, layer, q, out, num_sms, st, ev);

@@ -35,6 +35,7 @@
 
 #include "fk_device.cuh"
 #include "fk_internal.h"
+#include "fk_once.h"
 
 namespace fk {
 namespace pre {
@@ -306,13 +307,12 @@ static int launch_prefill_t(const CUtensorMap& xmap, const PoolGeom& g, uint8_t*
                             int pos, int n, int d_model, const uint16_t* Ak, const uint16_t* Av,
                             cudaStream_t st) {
   using LY = pre::Layout<R>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(lr_prefill_kernel<R>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, LY::BYTES);
-    if (e != cudaSuccess) return (int)e;
-    attr_done = true;
-  }
+  static PerDeviceOnce once;
+  const int se = once.run([] {
+    return (int)cudaFuncSetAttribute(lr_prefill_kernel<R>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, LY::BYTES);
+  });
+  if (se != 0) return se;
   const int grid = (n + pre::kTile - 1) / pre::kTile;
   lr_prefill_kernel<R><<<grid, pre::kThreads, LY::BYTES, st>>>(xmap, g, lk, lv, pos, n, d_model,
                                                                 Ak, Av);

@@ -32,10 +32,12 @@ def _call(fn, dw, q):
 @pytest.mark.parametrize("name,kw", [
     ("llama8b_32k", dict(prefix=1000, A=8)),
     ("agents32_layers32", dict(prefix=200, suffix=(0, 40), A=9, n_layers=1)),
+    ("qwen72b_chunk", dict(prefix=300, A=3)),          # the chunk kernel's work list
+    ("compressed", dict(prefix=500, A=6)),             # the compressed pool
 ])
 def test_noalloc_matches_pool_workspace_call(name, kw):
     w = workloads.make_workload(name, "strong", **kw)
-    dw = harness.DeviceWorkload(w)
+    dw = harness.DeviceWorkload(w, compressed="gpu" if name == "compressed" else None)
     q = dw.queries(0)
     ref = _call(fk.fk_residual_attention, dw, q).float()
     for _ in range(2):                      # two calls in a row share the array
@@ -78,3 +80,23 @@ def test_noalloc_replans_after_an_agent_is_registered_again():
     assert not torch.equal(got[0], first[0])          # agent 0's rows see the new scale
     assert torch.equal(got[1:], first[1:])            # the others do not change
     dw.check()
+
+
+def test_noalloc_does_not_reuse_a_destroyed_pools_work_list():
+    # two pools in a row with the same call inputs (agents, block table,
+    # sequence lengths) but other ranks: the second pool may get the first
+    # one's address, and its work list (tiles formed by rank) differs
+    kw = dict(prefix=200, suffix=(0, 40), A=9, n_layers=1)
+    w1 = workloads.make_workload("agents32_layers32", "strong", **kw)
+    dw1 = harness.DeviceWorkload(w1)
+    _call(fk.fk_residual_attention_noalloc, dw1, dw1.queries(0))
+    dw1.pool.close()
+    del dw1
+    w2 = workloads.make_workload("agents32_layers32", "strong", ranks=(64,), **kw)
+    assert np.array_equal(w1.seq_lens, w2.seq_lens)
+    dw2 = harness.DeviceWorkload(w2)
+    q = dw2.queries(0)
+    ref = _call(fk.fk_residual_attention, dw2, q)
+    got = _call(fk.fk_residual_attention_noalloc, dw2, q)
+    assert torch.equal(got, ref)
+    dw2.check()
