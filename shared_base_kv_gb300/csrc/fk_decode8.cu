@@ -25,14 +25,16 @@
 //   warp 1       MMA issue (converged warp, elect.sync)
 //   warps 4-7    compute warpgroup 0: agent slots 0-3 (rows 0-15)
 //   warps 8-11   compute warpgroup 1: agent slots 4-7 (rows 16-31)
-//   warps 12-15  Trig warpgroup: Trig of each tile and the tile's Lv^T
-//                into tensor memory
+//   warps 12-15  Trig warpgroup: Trig of each tile (from the pool's table of
+//                per-position rotations) and the tile's Lv^T into tensor
+//                memory
 // The compute and Trig warpgroups build M in shared memory at the start of
 // every work item.  A warp reaches TMEM lanes 32 (warp % 4) .. + 31, so the
 // thread of TMEM lane 32 (warp % 4) + lane handles the key (or d, or rank
 // slot) of that lane.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
@@ -56,15 +58,17 @@ constexpr int kMaxZ = kRPA * 8 * kMaxGroups;   // 512 Z columns: (rank, row) pai
 
 // TMEM columns: base scores S (32 rows), O^T (d lanes x 32 rows), OL^T
 // (rank lanes x 32 rows), Lv^T (rank lanes x 128 keys as bf16 pairs), Trig
-// (key lanes x 64 f16 pairs), and per compute warpgroup two Z buffers of 64
-// columns (a chunk of two 8-rank groups each).
+// (key lanes x 64 f16 pairs), and one Z buffer of 128 columns per compute
+// warpgroup (a chunk of four 8-rank groups).  A tensor-core accumulator
+// that changes from one MMA run to the next costs time (measured on GB300:
+// N = 64 MMAs of eight-deep runs into rotating buffers ran at 61 cycles
+// each against 35 into one buffer), so Z runs in as few, as wide chunks as
+// tensor memory holds.
 constexpr uint32_t kTmS = 0, kTmO = 32, kTmOL = 64, kTmLv = 96, kTmTrig = 160, kTmZ = 224;
-constexpr int kZChunkGroups = 2;
+constexpr int kZChunkGroups = 4;
 constexpr uint32_t kZBufCols = 32 * kZChunkGroups;
-__host__ __device__ constexpr uint32_t tm_z(int wg, int b) {
-  return kTmZ + kZBufCols * (uint32_t)(2 * wg + b);
-}
-static_assert(kTmZ + 4 * kZBufCols <= 512, "TMEM map");
+__host__ __device__ constexpr uint32_t tm_z(int wg) { return kTmZ + kZBufCols * (uint32_t)wg; }
+static_assert(kTmZ + 2 * kZBufCols <= 512, "TMEM map");
 
 // Shared memory.  M: K-major core matrices of 8 Z columns x 8 features
 // (f16, features 2i / 2i + 1 the cos / sin parts of frequency i).  Kb and
@@ -91,13 +95,13 @@ static_assert(TOTAL <= 232448, "shared memory over the 227 KB a CTA may use");
 
 enum {
   B_KB_FULL, B_KB_EMPTY, B_VB_FULL, B_VB_EMPTY, B_LV_FULL, B_LV_EMPTY, B_Q_FULL, B_M_FULL,
-  B_TRIG_FULL, B_TRIG_EMPTY, B_S_FULL, B_S_FREE, B_ZF00, B_ZF01, B_ZF10, B_ZF11, B_ZE00, B_ZE01,
-  B_ZE10, B_ZE11, B_P_FULL0, B_P_FULL1, B_PV_DONE0, B_PV_DONE1, B_ACC_EMPTY, B_FINAL, B_COUNT
+  B_TRIG_FULL, B_TRIG_EMPTY, B_S_FULL, B_S_FREE, B_ZF0, B_ZF1, B_ZE0, B_ZE1,
+  B_P_FULL0, B_P_FULL1, B_PV_DONE0, B_PV_DONE1, B_ACC_EMPTY, B_FINAL, B_COUNT
 };
-// Z buffer b of compute warpgroup w: full (MMA commit) and free (the
+// Z buffer of compute warpgroup w: full (MMA commit) and free (the
 // warpgroup's four warps).
-__host__ __device__ constexpr int b_zf(int w, int b) { return B_ZF00 + 2 * w + b; }
-__host__ __device__ constexpr int b_ze(int w, int b) { return B_ZE00 + 2 * w + b; }
+__host__ __device__ constexpr int b_zf(int w) { return B_ZF0 + w; }
+__host__ __device__ constexpr int b_ze(int w) { return B_ZE0 + w; }
 // Arrival counts: 8 = lane 0 of each compute warp; 12 = compute and Trig
 // warps; 4 = lane 0 of each warp of one warpgroup; 1 = a transaction count
 // or an MMA commit.
@@ -105,14 +109,13 @@ __host__ __device__ constexpr uint32_t bar_count(int i) {
   return (i == B_S_FREE || i == B_P_FULL0 || i == B_P_FULL1 || i == B_ACC_EMPTY || i == B_Q_FULL)
              ? 8u
          : (i == B_M_FULL) ? 12u
-         : (i == B_TRIG_FULL || i == B_LV_FULL || (i >= B_ZE00 && i <= B_ZE11)) ? 4u
+         : (i == B_TRIG_FULL || i == B_LV_FULL || i == B_ZE0 || i == B_ZE1) ? 4u
                                                                                : 1u;
 }
 // Barriers whose first wait must pass at once (a free buffer).
 constexpr uint64_t kEmptyMask = (1ull << B_KB_EMPTY) | (1ull << B_VB_EMPTY) |
-                                (1ull << B_LV_EMPTY) | (1ull << B_ZE00) | (1ull << B_ZE01) |
-                                (1ull << B_ZE10) | (1ull << B_ZE11) | (1ull << B_S_FREE) |
-                                (1ull << B_ACC_EMPTY);
+                                (1ull << B_LV_EMPTY) | (1ull << B_ZE0) | (1ull << B_ZE1) |
+                                (1ull << B_S_FREE) | (1ull << B_ACC_EMPTY);
 static_assert(B_COUNT <= 64, "one parity bit per barrier");
 
 struct Misc {
@@ -132,7 +135,6 @@ struct Misc {
   int32_t srp[kSlots], scol[kSlots], spa[kSlots];
   float ss[kSlots];
   int64_t src[kSlots];
-  unsigned long long frac[NF];       // theta_i / (2 pi) as a 64-bit binary fraction
   // per compute warpgroup and local 8-rank group: address of key t's 8
   // ranks is gbase + (t / 8) * gstride + (t % 8) * 16; gslot = slot - 4 cw
   const uint8_t* gbase[2][kWGGroups];
@@ -207,6 +209,18 @@ __device__ __forceinline__ uint32_t opaque_zero() {
   uint32_t z;
   asm volatile("mov.u32 %0, 0;" : "=r"(z));
   return z;
+}
+
+// A 16-byte read-only global load that stays where it is written: as
+// volatile asm it is neither repeated at its point of use nor moved past
+// the (volatile) tensor-memory waits around it, so its latency is spent
+// while the warp does other work.
+__device__ __forceinline__ uint4 ldg_pinned(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr));
+  return v;
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -289,26 +303,26 @@ __device__ __forceinline__ void reduce_group(const uint4 lkv, const uint32_t (&v
   }
 }
 
-// Trig of one tile in registers: out[i] is the f16 pair
-// [cos, sin]((t0 + key) th_i) of this thread's key, from the exact phase of
-// every element (no table).  Composed while the previous tile's Z MMAs still
-// read the Trig columns; only the store waits for them.
-__device__ __forceinline__ void compose_trig(const Misc& M, int t, uint32_t (&out)[NF]) {
+// Trig row of key t (the f16 pairs [cos, sin](t th_i), i < 64) from the
+// pool's table into registers: loaded a tile ahead, while the previous
+// tile's Z MMAs still read the Trig columns; only the store waits for them.
+__device__ __forceinline__ void load_trig(const uint8_t* table, int t, uint4 (&w)[NF / 4]) {
+  const uint8_t* row = table + (int64_t)t * (NF * 4);
 #pragma unroll
-  for (int i = 0; i < NF; ++i) {
-    const float2 r = rot_at(M.frac[i], t);
-    out[i] = pack_h2(r.x, r.y);
-  }
+  for (int j = 0; j < NF / 4; ++j) w[j] = ldg_pinned(row + 16 * j);
 }
 
-__device__ __forceinline__ void store_trig(const uint32_t (&w)[NF], uint32_t taddr) {
-  uint32_t a[16], b[16], c[16], d[16];
+__device__ __forceinline__ void store_trig(const uint4 (&w)[NF / 4], uint32_t taddr) {
 #pragma unroll
-  for (int e = 0; e < 16; ++e) { a[e] = w[e]; b[e] = w[16 + e]; c[e] = w[32 + e]; d[e] = w[48 + e]; }
-  tmem_st16(taddr, a);
-  tmem_st16(taddr + 16, b);
-  tmem_st16(taddr + 32, c);
-  tmem_st16(taddr + 48, d);
+  for (int q = 0; q < 4; ++q) {
+    uint32_t a[16];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      a[4 * e] = w[4 * q + e].x; a[4 * e + 1] = w[4 * q + e].y;
+      a[4 * e + 2] = w[4 * q + e].z; a[4 * e + 3] = w[4 * q + e].w;
+    }
+    tmem_st16(taddr + 16 * q, a);
+  }
 }
 
 }  // namespace d8
@@ -378,7 +392,6 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
   for (int i = oKB + tid * 16; i < oQ; i += kThreads * 16) *(uint4*)(smem + i) = make_uint4(0, 0, 0, 0);
   for (int i = oMISC + tid * 16; i < TOTAL; i += kThreads * 16) *(uint4*)(smem + i) = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  if (tid < NF) M.frac[tid] = ((const unsigned long long*)(g.base + g.off_rope + 256))[tid];
   if (tid == 0) {
     for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), bar_count(i));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -393,8 +406,12 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
 
   // Register split: the copy and MMA warpgroup hands registers to the
   // compute and Trig warpgroups; the shares add up to the launch's 512 x 128.
-  constexpr int kRegLow = 72, kRegCompute = 152, kRegTrig = 136;
+  // setmaxnreg.inc may only raise a warp's count and .dec only lower it
+  // (the other direction is an illegal instruction), so each warpgroup's
+  // direction follows from its share against the launch's 128.
+  constexpr int kRegLow = 72, kRegCompute = 160, kRegTrig = 120;
   static_assert(128 * kRegLow + 256 * kRegCompute + 128 * kRegTrig == 65536, "register split");
+  static_assert(kRegLow < 128 && kRegCompute > 128, "the copy/MMA warpgroup gives, the compute warpgroups take");
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegLow) : "memory");
     if (warp == 0 || warp == 3) {
@@ -413,6 +430,19 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
         const int32_t* pages = (const int32_t*)(ws + p.off_pages) + w.page_begin;
         // page id of this lane's page of the next tile, loaded a tile ahead
         int pg = lane < min(kTilePages, n_pages) ? pages[lane] : 0;
+        // the key warp also prefetches the item's rCache rows into L2 a tile
+        // ahead of the compute warps' Lk loads and the Trig warps' Lv loads:
+        // lane s < 8 the Lk rows of slot s, lane 8 + s its Lv rows (one
+        // contiguous block of rp x 256 bytes per 128-key tile)
+        const uint8_t* pf = nullptr;
+        int pf_rp = 0;
+        const int t_item = w.lp_begin * kPage;
+        auto prefetch_tile = [&](int k) {
+          if (pf == nullptr || k >= n_tiles) return;
+          const int t0 = t_item + k * kTileTok;
+          const int nt = min(kTileTok, g.tcap - t0);
+          if (nt > 0) bulk_prefetch_l2(pf + (int64_t)(t0 / 8) * pf_rp * 16, (uint32_t)((nt / 8) * pf_rp * 16));
+        };
         for (int k = 0; k < n_tiles; ++k) {
           const int p0 = k * kTilePages;
           const int np = min(kTilePages, n_pages - p0);
@@ -425,13 +455,27 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
           if (lane < np && !*abort_flag)
             bulk_g2s(dst0 + lane * PAGE_B, region + ((int64_t)pg_k * g.H_kv + head) * PAGE_B, PAGE_B,
                      bar(b_full));
+          if (keys) {
+            if (k == 0 && lane < 2 * kSlots) {
+              // (looked up once the first copies are on their way)
+              const int ci = ((const int32_t*)(ws + p.off_tile_agents))[w.agent_begin + (lane & 7)];
+              if (ci >= 0) {
+                const int pa = ((const CallAgent*)(ws + p.off_call_agents))[ci].pool_agent;
+                const AgentDev dv = ((const AgentDev*)(g.base + g.off_agents))[pa];
+                pf_rp = dv.rp;
+                pf = g.base + dv.rc_off + (int64_t)layer * rc_layer_bytes(g, dv.rp) +
+                     (lane >= kSlots ? (int64_t)g.tcap * dv.rp * 2 : 0);
+              }
+              prefetch_tile(0);
+            }
+            prefetch_tile(k + 1);
+          }
         }
       }
     } else if (warp == 1) {
       // ======================================= MMA issue (converged warp) ====
       const uint32_t id32 = idesc_f16(128, kRows, 1);
       int tc = 0;                      // tiles issued (all items), selects the P buffer
-      int zc[2] = {0, 0};              // Z chunks issued per compute warpgroup (all items)
       for (int it = it_begin; it < it_end; ++it) {
         const fk_work_item& wi = ((const fk_work_item*)(ws + p.off_items))[it];
         const int n_tiles = (wi.n_pages + kTilePages - 1) / kTilePages;
@@ -455,7 +499,9 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
         };
         // values of the item's tile j (global tile pt): O^T += Vb^T P (both
         // operands in shared memory), OL^T += Lv^T P (Lv^T in TMEM); P, Vb
-        // and Lv^T are ready
+        // and Lv^T are ready.  The two alternate, so that the shared-memory
+        // and the tensor-memory operand reads overlap (measured faster than
+        // running each accumulator's MMAs back to back).
         auto pv = [&](int j, int pt) {
           const int pb = pt & 1;
           tc_fence_after();
@@ -482,9 +528,9 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
         const int ng0 = M.half_groups[0], ng1 = M.half_groups[1];
         const int nc0 = (ng0 + kZChunkGroups - 1) / kZChunkGroups;
         const int nc1 = (ng1 + kZChunkGroups - 1) / kZChunkGroups;
-        // Z chunk m of warpgroup w: its 8-rank groups 2 m, 2 m + 1 into
-        // buffer b (the MMA warp has seen that buffer free)
-        auto issue_z = [&](int w, int m, int b) {
+        // Z chunk m of warpgroup w: its 8-rank groups 4 m .. 4 m + 3 into
+        // the warpgroup's buffer (the MMA warp has seen it free)
+        auto issue_z = [&](int w, int m) {
           tc_fence_after();
           __syncwarp();
           if (elect_one() && !*abort_flag) {
@@ -493,25 +539,46 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
             const uint32_t idZ = idesc_f16(128, 32 * ng, 0);
             const uint64_t dM = sdesc(sbase + opaque_zero() + oM + g0 * 4 * (D / 8) * 128, 128, (D / 8) * 128);
             const uint32_t tA = tmem + kTmTrig;
-            const uint32_t tD = tmem + tm_z(w, b);
+            const uint32_t tD = tmem + tm_z(w);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
               mma_ts(tD, tA + 8 * ks, dM + (uint64_t)(ks * 16), idZ, ks > 0 ? 1u : 0u);
-            mma_commit(bar(b_zf(w, b)));
+            mma_commit(bar(b_zf(w)));
           }
           __syncwarp();
         };
-        // Issue order per tile k, the order in which the inputs become
-        // ready: the values of tile k - 1 (P(k - 1) comes with the compute
-        // warps' softmax, Lv^T and Vb a tile earlier), the base scores of
-        // tile k + 1 (so that the key stage refills a tile ahead), then the
-        // Z chunks of tile k, the two warpgroups' chunks interleaved so that
-        // both read at once, once Trig(k) is written.
+        // Issue order per tile k: the first Z chunk of each warpgroup (the
+        // buffers were freed before the compute warps' softmax of tile
+        // k - 1, so these run during it), the base scores of tile k + 1 (S
+        // is free once the compute warps start tile k; the key stage
+        // refills a tile ahead), the rest of Z(k) as the compute warps free
+        // the buffers, then the values of tile k - 1, which run while the
+        // compute warps read the last chunk and do their softmax (nothing
+        // waits for them before tile k + 1).  The two warpgroups' chunks
+        // alternate, so one warpgroup reads its chunk while the other's is
+        // computed.
+        auto z_chunks = [&](int m0, int m1) {
+          for (int m = m0; m < m1; ++m) {
+            if (m < nc0) { wait(b_ze(0)); issue_z(0, m); }
+            if (m < nc1) { wait(b_ze(1)); issue_z(1, m); }
+          }
+        };
+        const int ncm = max(nc0, nc1), nearly = min(1, ncm);
         wait(B_KB_FULL);
         wait(B_S_FREE);
         issue_s();
         wait(B_M_FULL);
         for (int k = 0; k < n_tiles; ++k) {
+          wait(B_TRIG_FULL);
+          z_chunks(0, nearly);
+          if (k + 1 < n_tiles) {
+            wait(B_KB_FULL);
+            wait(B_S_FREE);
+            issue_s();
+          }
+          z_chunks(nearly, ncm);
+          if (elect_one()) mma_commit(bar(B_TRIG_EMPTY));   // every Z of the tile issued
+          __syncwarp();
           if (k > 0) {
             wait(B_P_FULL0 + ((tc0 + k - 1) & 1));
             wait(B_VB_FULL);
@@ -519,18 +586,6 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
             if (k == 1) wait(B_ACC_EMPTY);
             pv(k - 1, tc0 + k - 1);
           }
-          if (k + 1 < n_tiles) {
-            wait(B_KB_FULL);
-            wait(B_S_FREE);
-            issue_s();
-          }
-          wait(B_TRIG_FULL);
-          for (int m = 0; m < max(nc0, nc1); ++m) {
-            if (m < nc0) { wait(b_ze(0, zc[0] & 1)); issue_z(0, m, zc[0] & 1); ++zc[0]; }
-            if (m < nc1) { wait(b_ze(1, zc[1] & 1)); issue_z(1, m, zc[1] & 1); ++zc[1]; }
-          }
-          if (elect_one()) mma_commit(bar(B_TRIG_EMPTY));   // every Z of the tile issued
-          __syncwarp();
         }
         wait(B_P_FULL0 + ((tc0 + n_tiles - 1) & 1));
         wait(B_VB_FULL);
@@ -559,7 +614,6 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
     const int32_t* row_cg_all = (const int32_t*)(ws + p.off_row_cg);
     const CallAgent* ca = (const CallAgent*)(ws + p.off_call_agents);
     int tc = 0, pv_seen = 0;
-    int zc = 0;                      // Z chunks of this warpgroup read (all items)
     // The value MMAs of tile j signal PV_DONE[j & 1].  Alternating barriers
     // keep a waiter within one phase of each, which parity waits need.
     auto pv_until = [&](int n) {
@@ -668,7 +722,7 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
 #pragma unroll
         for (int jl = 0; jl < kWGGroups; ++jl)
           if (g_lo + jl < g_hi)
-            lk[jl] = __ldg((const uint4*)(M.gbase[cw][jl] + (int64_t)(t / 8) * M.gstride[cw][jl] + (t % 8) * 16));
+            lk[jl] = ldg_pinned(M.gbase[cw][jl] + (int64_t)(t / 8) * M.gstride[cw][jl] + (t % 8) * 16);
       }
       // OL^T lane ln: rank orr of the slot os whose columns hold ln (that
       // slot's rows take it in the epilogue)
@@ -698,26 +752,24 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
         if (lane == 0) mbar_arrive_relaxed(bar(B_S_FREE));
         // residual scores: acc[4 s + g] += sum_e Lk[t, 8 j + e] Z[t, 4 (8 j + e) + g]
         // for the 8-rank groups j of local slot s.  This warpgroup's chunk m
-        // holds its local groups 2 m and 2 m + 1.
+        // holds its local groups 4 m .. 4 m + 3.
         float acc[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) acc[j] = 0.f;
 #pragma unroll
         for (int jl = 0; jl < kWGGroups; ++jl) {
           if (g_lo + jl < g_hi) {
-            const int b = zc & 1;
-            if ((jl & 1) == 0) {
-              wait(b_zf(cw, b));
+            if (jl % kZChunkGroups == 0) {
+              wait(b_zf(cw));
               tc_fence_after();
             }
             uint32_t v[32];
-            tmem_ld32_wait(tmem + tm_z(cw, b) + 32 * (jl & 1) + lane_off, v);
+            tmem_ld32_wait(tmem + tm_z(cw) + 32 * (jl % kZChunkGroups) + lane_off, v);
             // chunk read: the MMA may overwrite the buffer
-            if ((jl & 1) == 1 || g_lo + jl + 1 >= g_hi) {
+            if (jl % kZChunkGroups == kZChunkGroups - 1 || g_lo + jl + 1 >= g_hi) {
               tc_fence_before();
               __syncwarp();
-              if (lane == 0) mbar_arrive_relaxed(bar(b_ze(cw, b)));
-              ++zc;
+              if (lane == 0) mbar_arrive_relaxed(bar(b_ze(cw)));
             }
             reduce_group(lk[jl], v, (gsl >> (4 * jl)) & 3u, acc);
           }
@@ -729,7 +781,7 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
 #pragma unroll
           for (int jl = 0; jl < kWGGroups; ++jl)
             if (g_lo + jl < g_hi)
-              lk[jl] = __ldg((const uint4*)(M.gbase[cw][jl] + (int64_t)(tn / 8) * M.gstride[cw][jl] + (tn % 8) * 16));
+              lk[jl] = ldg_pinned(M.gbase[cw][jl] + (int64_t)(tn / 8) * M.gstride[cw][jl] + (tn % 8) * 16);
         }
         // ---- online softmax (base 2); the running max of a row moves only
         // when the tile max exceeds it by more than 2^8 (then O^T, OL^T and
@@ -850,21 +902,25 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
       if (lane == 0) mbar_arrive_relaxed(bar(B_ACC_EMPTY));
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegTrig) : "memory");
+    if constexpr (kRegTrig > 128)
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegTrig) : "memory");
+    else if constexpr (kRegTrig < 128)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegTrig) : "memory");
     // ======================================== Trig and Lv^T (warps 12-15) ====
     // Trig column i of a tile holds [cos, sin]((t0 + lane) theta_i) as an
-    // f16 pair, from the exact phase of each element.  Tile k + 1's Trig is
-    // composed in registers while Z(k) runs and stored once Z(k) has
-    // completed.  Lv^T: lane = rank slot of the tile; 16 loads of 8 keys
-    // each, stored as bf16 key pairs once the value MMAs of the previous
-    // tile have completed.
+    // f16 pair, copied from the pool's table of per-position rotations.
+    // Tile k + 1's Trig is loaded into registers a tile ahead and stored
+    // once Z(k) has completed.  Lv^T: lane = rank slot of the tile; 16 loads
+    // of 8 keys each, stored as bf16 key pairs once the value MMAs of the
+    // previous tile have completed.
+    const uint8_t* trig_table = g.base + g.off_trig;
     const int ln = 32 * (warp & 3) + lane;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     int zdone = 0;                    // tiles whose Z MMAs are known complete
     auto z_until = [&](int n) {
       while (zdone < n) { wait(B_TRIG_EMPTY); ++zdone; }
     };
-    // (no closure refers to the composed Trig: an array captured by
+    // (no closure refers to the loaded Trig: an array captured by
     // reference stays in local memory)
     auto trig_full = [&]() {
       tmem_wait_st();
@@ -911,23 +967,22 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
         tc_fence_after();
         tmem_st32(tmem + kTmLv + 32 * hh + lane_off, w);
       };
-      {
-        uint32_t w[NF];
-        compose_trig(M, tb + ln, w);
-        store_trig(w, tmem + kTmTrig + lane_off);
-        trig_full();
-      }
+      // (keys past the capacity are masked; they read the last row)
+      uint4 tw[NF / 4];
+      load_trig(trig_table, min(tb + ln, g.tcap - 1), tw);
+      store_trig(tw, tmem + kTmTrig + lane_off);
+      trig_full();
+      if (n_tiles > 1) load_trig(trig_table, min(tb + kTileTok + ln, g.tcap - 1), tw);
       for (int k = 0; k < n_tiles; ++k) {
-        // Trig of tile k + 1, composed while Z(k) runs and stored once it
-        // has completed, then Lv^T of tile k (free once the value MMAs of
-        // tile k - 1 have completed)
+        // Trig of tile k + 1 (loaded a tile ahead), stored once Z(k) has
+        // completed; then the load of tile k + 2's, and Lv^T of tile k (free
+        // once the value MMAs of tile k - 1 have completed)
         if (k + 1 < n_tiles) {
-          uint32_t w[NF];
-          compose_trig(M, tb + (k + 1) * kTileTok + ln, w);
           z_until(tc + k + 1);
           tc_fence_after();
-          store_trig(w, tmem + kTmTrig + lane_off);
+          store_trig(tw, tmem + kTmTrig + lane_off);
           trig_full();
+          if (k + 2 < n_tiles) load_trig(trig_table, min(tb + (k + 2) * kTileTok + ln, g.tcap - 1), tw);
         }
         lv_half(k, 0);
         lv_half(k, 1);
@@ -950,6 +1005,29 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
     while (clock64() - t0 < 20000000LL) { }
   }
   if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ============================================================ RoPE table ==
+
+// [cos, sin](t theta_i) as f16 pairs for t < tcap, i < 64: one thread per
+// element, from the exact phase (the same rotation the oracle rounds).
+__global__ void trig_table_kernel(PoolGeom g) {
+  const int64_t n = (int64_t)g.tcap * d8::NF;
+  const unsigned long long* frac = (const unsigned long long*)(g.base + g.off_rope + 256);
+  uint32_t* table = (uint32_t*)(g.base + g.off_trig);
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(e / d8::NF), i = (int)(e % d8::NF);
+    const float2 r = d8::rot_at(frac[i], t);
+    table[e] = pack_h2(r.x, r.y);
+  }
+}
+
+int launch_trig_table(const PoolGeom& g) {
+  if (g.off_trig < 0 || g.d != d8::D) return (int)cudaErrorInvalidValue;
+  const int64_t n = (int64_t)g.tcap * d8::NF;
+  const int grid = (int)std::min<int64_t>((n + 255) / 256, 4096);
+  trig_table_kernel<<<grid, 256>>>(g);
+  return (int)cudaGetLastError();
 }
 
 // ============================================================ launcher ==

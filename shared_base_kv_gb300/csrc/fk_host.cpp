@@ -146,6 +146,8 @@ PoolGeom make_geom(const fk_pool_config* c) {
   g.off_rope = take(4LL * 4 * 64);
   g.off_err = take(64);
   g.off_lvmap = take(128LL * g.max_agents);
+  // the eight-slot decode kernel reads each key's RoPE rotations from here
+  g.off_trig = g.d == 128 ? take((int64_t)g.tcap * (g.d / 2) * 4) : -1;
   if (g.compressed) {
     int64_t tok = (int64_t)g.L * g.num_pages * g.H_kv * kPage;
     g.off_kq = take(tok * g.d);
@@ -809,6 +811,13 @@ fk_status fk_pool_create(const fk_pool_config* cfg, void* dev_buf, size_t bytes,
   }
   e = cudaMemcpy(p->g.base + g.off_rope, rope.data(), rope.size(), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) { cudaEventDestroy(p->stage.done); delete p; return cuda_fail(e, "cudaMemcpy"); }
+  // per-position rotations (from the fractions above), complete before the
+  // call returns
+  if (g.off_trig >= 0) {
+    e = (cudaError_t)launch_trig_table(p->g);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
+    if (e != cudaSuccess) { cudaEventDestroy(p->stage.done); delete p; return cuda_fail(e, "RoPE table"); }
+  }
   *out = p;
   return FK_OK;
 }

@@ -48,6 +48,7 @@ struct PoolGeom {
   int64_t off_kb, off_vb, off_bk, off_bv, off_agents, off_rope, off_err;
   int64_t off_kq, off_vc, off_vn, off_ks, off_kmax, off_meta, off_ws;
   int64_t off_lvmap;       // per pool agent: 128-byte TMA tensor map of its Lv (all layers)
+  int64_t off_trig;        // d = 128: [tcap][d/2] f16 pairs (cos, sin)(t theta_i); else -1
   int64_t ws_bytes, meta_bytes;
   int64_t page_bytes;      // bytes of one (page, head) bf16 block: 16*d*2
   int64_t kb_layer_bytes;  // num_pages * H_kv * page_bytes
@@ -131,6 +132,10 @@ int launch_attention(const PoolGeom& g, const PlanDev& p, int layer,
 bool decode_applies(const PoolGeom& g, const PlanDev& p);
 int launch_decode(const PoolGeom& g, const PlanDev& p, int layer, const uint16_t* q,
                   int compressed, void* stream);
+
+// Fills the pool's RoPE table of [cos, sin](t theta_i) for t < tcap (d = 128)
+// on the legacy default stream (fk_decode8.cu).
+int launch_trig_table(const PoolGeom& g);
 
 // Decode-shaped calls planned in eight-slot tiles (d = 128, uncompressed
 // pool) run the eight-agent decode kernel (fk_decode8.cu); the combine is
