@@ -82,8 +82,12 @@ struct Layout {
   static constexpr int Q_B = kRows * D * 2;
   static constexpr int P_B = 2 * kPRowGroup;
   static constexpr int KQ_B = COMP ? kTilePages * kPage * D : 0;
-  static constexpr int VC_B = COMP ? kTilePages * kPage * (3 * D / 8) : 0;
-  static constexpr int VN_B = COMP ? kTilePages * kPage * 4 : 0;
+  // compressed values: two stages of codes and norms, so that the value
+  // warp copies tile k + 1's while it expands tile k's
+  static constexpr int VCS_B = kTilePages * kPage * (3 * D / 8);
+  static constexpr int VNS_B = kTilePages * kPage * 4;
+  static constexpr int VC_B = COMP ? 2 * VCS_B : 0;
+  static constexpr int VN_B = COMP ? 2 * VNS_B : 0;
   static constexpr int oM = 0;
   static constexpr int oKB = oM + M_B;
   static constexpr int oVB = oKB + NKB * TILE_B;   // d = 64: the Vb^T MMA reads 1 KB past a stage
@@ -102,7 +106,8 @@ struct Layout {
 enum {
   B_KB_FULL0, B_KB_FULL1, B_KB_EMPTY0, B_KB_EMPTY1, B_VB_FULL0, B_VB_FULL1, B_VB_EMPTY0,
   B_VB_EMPTY1, B_LV_FULL, B_LV_EMPTY, B_M_FULL, B_M_EMPTY, B_ITEM_FULL, B_TRIG_FULL0, B_TRIG_FULL1, B_Z_FULL0, B_Z_FULL1, B_Z_FREE0, B_Z_FREE1, B_P_FULL0, B_P_FULL1, B_PV_DONE0,
-  B_PV_DONE1, B_ACC_EMPTY, B_KQ_FULL, B_KQ_EMPTY, B_VC_FULL, B_VC_EMPTY, B_FINAL, B_COUNT
+  B_PV_DONE1, B_ACC_EMPTY, B_KQ_FULL, B_KQ_EMPTY, B_VC_FULL0, B_VC_FULL1, B_VC_EMPTY0, B_VC_EMPTY1,
+  B_FINAL, B_COUNT
 };
 // Arrival counts: 8 = lane 0 of each warp of both compute warpgroups; 4 =
 // lane 0 of each Trig warp; 1 = one thread, a bulk-copy transaction count
@@ -113,10 +118,16 @@ __host__ __device__ constexpr uint32_t bar_count(int i) {
              ? 8u
              : (i == B_TRIG_FULL0 || i == B_TRIG_FULL1) ? 4u : 1u;
 }
+// compressed pool: the value stage is filled by two warps (0 and 3), each
+// expanding half of a tile's code units
+template <bool COMP>
+__host__ __device__ constexpr uint32_t bar_count_t(int i) {
+  return (COMP && (i == B_VB_FULL0 || i == B_VB_FULL1)) ? 2u : bar_count(i);
+}
 constexpr uint64_t kEmptyMask =
     (1ull << B_KB_EMPTY0) | (1ull << B_KB_EMPTY1) | (1ull << B_VB_EMPTY0) | (1ull << B_VB_EMPTY1) |
     (1ull << B_LV_EMPTY) | (1ull << B_M_EMPTY) | (1ull << B_Z_FREE0) | (1ull << B_Z_FREE1) |
-    (1ull << B_ACC_EMPTY) | (1ull << B_KQ_EMPTY) | (1ull << B_VC_EMPTY);
+    (1ull << B_ACC_EMPTY) | (1ull << B_KQ_EMPTY) | (1ull << B_VC_EMPTY0) | (1ull << B_VC_EMPTY1);
 static_assert(B_COUNT <= 64, "one parity bit per barrier");
 
 struct Misc {
@@ -137,6 +148,10 @@ struct Misc {
   const uint8_t* gbase[2][8];
   int32_t gstride[2][8];
   int32_t gagent[2][8];
+  // the dequantiser's copy of the 3-bit value codebook: lanes index it with
+  // their own codes, which a constant-memory table would serve one address
+  // at a time
+  float lloyd[8];
 };
 static_assert(sizeof(Misc) <= 4096, "Misc must fit its smem slot");
 
@@ -279,8 +294,9 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
   for (int i = tid; i < 16 * 8; i += kThreads)
     ((uint16_t*)(smem + LY::oLV + (kOnesLane / 8) * kLvGroup + (i / 8) * 128))[i % 8] = 0x3F80;
   if (tid < 64) M.frac[tid] = ((const unsigned long long*)(g.base + g.off_rope + 256))[tid];
+  if (COMP && tid < 8) M.lloyd[tid] = c_lloyd[tid];
   if (tid == 0) {
-    for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), bar_count(i));
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), bar_count_t<COMP>(i));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) tmem_alloc(smem_u32(&M.tmem_base), 512);
@@ -297,6 +313,63 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
   // keeps more in warpgroup 0).
   constexpr int kRegCopy = COMP ? 120 : 104, kRegTrig = 88, kRegCompute = COMP ? 152 : 160;
   static_assert(128 * kRegCopy + 128 * kRegTrig + 256 * kRegCompute <= 65536, "register split");
+  // Compressed pool: half `half` of global tile vt's code units (np pages)
+  // -> level * norm / D in the value layout (rotated domain).  A unit is
+  // (page, 8-token chunk, 8-d group): three code bytes per token, one per
+  // bit plane.  Warp 0 expands half 0 and frees the code stage; warp 3 (the
+  // stage's copier, which reads it in program order) expands half 1.  Both
+  // arrive on the value stage's full barrier (count 2).
+  auto expand_values = [&](int np, int vt, int half) {
+    const int cst = vt & 1;
+    wait(B_VC_FULL0 + cst);
+    wait(B_VB_EMPTY0);
+    uint8_t* vdst = smem + LY::oVB;
+    const uint8_t* vc = smem + LY::oVC + cst * LY::VCS_B;
+    const float* vn = (const float*)(smem + LY::oVN + cst * LY::VNS_B);
+    const uint8_t* book = (const uint8_t*)M.lloyd;
+    for (int u = lane + 32 * half; u < np * 2 * (D / 8); u += 64) {
+      const int dg = u % (D / 8), tcn = (u / (D / 8)) % 2, pj = u / (2 * (D / 8));
+      float w8[8];
+      uint32_t c8[8];
+#pragma unroll
+      for (int tt = 0; tt < 8; ++tt) {
+        const int row = tcn * 8 + tt;
+        const uint8_t* cb = vc + (pj * kPage + row) * (3 * D / 8);
+        const uint32_t b0 = cb[dg], b1 = cb[D / 8 + dg], b2 = cb[2 * (D / 8) + dg];
+        // bit e of the planes at bits e + 2, e + 11, e + 20: shifted right
+        // by e, e + 8, e + 16 and masked, a code's bits give its byte
+        // offset (4 x code) into the codebook
+        c8[tt] = (b0 << 2) | (b1 << 11) | (b2 << 20);
+        w8[tt] = vn[pj * kPage + row] * (1.0f / D);
+      }
+      uint8_t* dst = vdst + pj * LY::PAGE_B + (tcn * (D / 8) + dg) * 128;
+      // each lane writes the 8 rows of its core in its own rotation, so that
+      // the lanes of one store hit different banks
+#pragma unroll
+      for (int s8 = 0; s8 < 8; ++s8) {
+        const int e = (s8 + lane) & 7;   // d = 8 dg + e
+        uint32_t w[4];
+#pragma unroll
+        for (int h2 = 0; h2 < 4; ++h2) {
+          float v2[2];
+#pragma unroll
+          for (int z = 0; z < 2; ++z) {
+            const uint32_t cc = c8[2 * h2 + z];
+            const uint32_t off = ((cc >> e) & 4u) | ((cc >> (8 + e)) & 8u) | ((cc >> (16 + e)) & 16u);
+            v2[z] = *(const float*)(book + off) * w8[2 * h2 + z];
+          }
+          w[h2] = pack_bf2(v2[0], v2[1]);
+        }
+        *(uint4*)(dst + e * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(bar(B_VB_FULL0));
+      if (half == 0) mbar_arrive(bar(B_VC_EMPTY0 + cst));
+    }
+  };
   if (warp < 4) {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCopy) : "memory");
   if (warp == 0) {
@@ -357,7 +430,10 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
             bulk_g2s(sbase + LY::oM + o, ws + mpr.mofs + o, min(4096u, mbytes - o), bar(B_M_FULL));
         }
         }
+        // compressed pool: half of the previous tile's values
+        if (COMP && k > 0) expand_values(min(kTilePages, I.n_pages - (k - 1) * kTilePages), tc - 1, 0);
       }
+      if (COMP) expand_values(min(kTilePages, I.n_pages - (I.n_tiles - 1) * kTilePages), tc0 + I.n_tiles - 1, 0);
       tc = tc0 + I.n_tiles;
     }
   } else if (warp == 3) {
@@ -377,17 +453,24 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         const int pg_k = pg;
         if (p0 + kTilePages + lane < I.n_pages && lane < kTilePages) pg = pages[p0 + kTilePages + lane];
         if (COMP) {
-          wait(B_VC_EMPTY);
+          // codes and norms into stage vt & 1 (this warp expanded its
+          // previous contents, tile vt - 2, before the proxy fence that ends
+          // that expansion)
+          const int cst = vt & 1;
+          wait(B_VC_EMPTY0 + cst);   // warp 0 has expanded its half of tile vt - 2
           __syncwarp();
-          if (lane == 0) mbar_expect_tx_relaxed(bar(B_VC_FULL), np * kPage * (3 * D / 8 + 4));
+          if (lane == 0) mbar_expect_tx_relaxed(bar(B_VC_FULL0 + cst), np * kPage * (3 * D / 8 + 4));
           __syncwarp();
           if (lane < np && !*abort_flag) {
             const int64_t tok = (((int64_t)layer * g.num_pages + pg_k) * g.H_kv + I.head) * kPage;
-            bulk_g2s(sbase + LY::oVC + lane * kPage * (3 * D / 8), g.base + g.off_vc + tok * (3 * D / 8),
-                     kPage * (3 * D / 8), bar(B_VC_FULL));
-            bulk_g2s(sbase + LY::oVN + lane * kPage * 4, g.base + g.off_vn + tok * 4, kPage * 4,
-                     bar(B_VC_FULL));
+            bulk_g2s(sbase + LY::oVC + cst * LY::VCS_B + lane * kPage * (3 * D / 8),
+                     g.base + g.off_vc + tok * (3 * D / 8), kPage * (3 * D / 8), bar(B_VC_FULL0 + cst));
+            bulk_g2s(sbase + LY::oVN + cst * LY::VNS_B + lane * kPage * 4, g.base + g.off_vn + tok * 4,
+                     kPage * 4, bar(B_VC_FULL0 + cst));
           }
+          // then the previous tile's values are expanded, before the Lv^T
+          // copy below waits for the value MMAs that consume them
+          if (k > 0) expand_values(min(kTilePages, I.n_pages - (k - 1) * kTilePages), vt - 1, 1);
         } else {
           const int st = vt % LY::NVB;
           wait(B_VB_EMPTY0 + st);
@@ -422,6 +505,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         }
       };
       for (int k = 0; k < I.n_tiles; ++k, ++tc) load_values(k, tc);
+      if (COMP) expand_values(min(kTilePages, I.n_pages - (I.n_tiles - 1) * kTilePages), tc - 1, 1);
     }
   } else if (warp == 1) {
     // ======================================= MMA issue (converged warp) ====
@@ -526,15 +610,13 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
     // ====================================== dequantiser (compressed pool) ====
     const float kscale = ((const float*)(g.base + g.off_ks))[layer];
     int tc = 0;
-    // keys of tile k, then the values of tile k - 1: the same order as the
-    // bulk copies, so the keys of the next tile never wait for the value
-    // MMAs that free the single value stage
+    // keys only: the value warp expands the values
     for (int it = it_begin; it < it_end; ++it) {
       Item I;
       load_item(g, p, ws, it, I);
       const int tc0 = tc;
-      for (int j = 0; j <= I.n_tiles; ++j) {
-        if (j < I.n_tiles) {
+      for (int j = 0; j < I.n_tiles; ++j) {
+        {
           const int k = j;
           const int np = min(kTilePages, I.n_pages - k * kTilePages);
           const int kb = (tc0 + k) & 1;
@@ -542,62 +624,26 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           wait(B_KQ_FULL);
           wait(B_KB_EMPTY0 + kb);
           uint8_t* kdst = smem + LY::oKB + kb * LY::TILE_B;
+          // lanes take the 8 rows of a core matrix first, so that a warp's
+          // 16-byte stores fill whole 128-byte cores (no bank conflicts)
           for (int u = lane; u < np * kPage * (D / 8); u += 32) {
-            const int ch = u % (D / 8), row = (u / (D / 8)) % kPage, pj = u / (kPage * (D / 8));
-            const int8_t* src = (const int8_t*)(smem + LY::oKQ) + (pj * kPage + row) * D + ch * 8;
+            const int ch = (u / 8) % (D / 8), row = (u % 8) + 8 * ((u / (8 * (D / 8))) % 2),
+                      pj = u / (kPage * (D / 8));
+            // eight int8 keys in one 8-byte load
+            const uint2 kw = *(const uint2*)(smem + LY::oKQ + (pj * kPage + row) * D + ch * 8);
             uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf2((float)src[2 * e] * kscale, (float)src[2 * e + 1] * kscale);
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t src = e < 2 ? kw.x : kw.y;
+              const int sh = 16 * (e & 1);
+              w[e] = pack_bf2((float)(int8_t)(src >> sh) * kscale, (float)(int8_t)(src >> (sh + 8)) * kscale);
+            }
             *(uint4*)(kdst + pj * LY::PAGE_B + ((row / 8) * (D / 8) + ch) * 128 + (row % 8) * 16) =
                 make_uint4(w[0], w[1], w[2], w[3]);
           }
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) { mbar_arrive(bar(B_KB_FULL0 + kb)); mbar_arrive(bar(B_KQ_EMPTY)); }
-        }
-        if (j > 0) {
-          const int k = j - 1;
-          const int np = min(kTilePages, I.n_pages - k * kTilePages);
-          const int vs = (tc0 + k) % LY::NVB;
-          // values: codes -> level * norm / D in the value layout (rotated domain)
-          wait(B_VC_FULL);
-          wait(B_VB_EMPTY0 + vs);
-          uint8_t* vdst = smem + LY::oVB + vs * LY::TILE_B;
-          for (int u = lane; u < np * 2 * (D / 8); u += 32) {
-            const int dg = u % (D / 8), tcn = (u / (D / 8)) % 2, pj = u / (2 * (D / 8));
-            float w8[8];
-            uint32_t c8[8];
-#pragma unroll
-            for (int tt = 0; tt < 8; ++tt) {
-              const int row = tcn * 8 + tt;
-              const uint8_t* cb = smem + LY::oVC + (pj * kPage + row) * (3 * D / 8);
-              const uint32_t b0 = cb[dg], b1 = cb[D / 8 + dg], b2 = cb[2 * (D / 8) + dg];
-              c8[tt] = b0 | (b1 << 8) | (b2 << 16);
-              w8[tt] = ((const float*)(smem + LY::oVN))[pj * kPage + row] * (1.0f / D);
-            }
-            uint8_t* dst = vdst + pj * LY::PAGE_B + (tcn * (D / 8) + dg) * 128;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {   // d = 8 dg + e
-              uint32_t w[4];
-#pragma unroll
-              for (int h2 = 0; h2 < 4; ++h2) {
-                float v2[2];
-#pragma unroll
-                for (int z = 0; z < 2; ++z) {
-                  const uint32_t cc = c8[2 * h2 + z];
-                  const uint32_t code = ((cc >> e) & 1u) | (((cc >> (8 + e)) & 1u) << 1) |
-                                        (((cc >> (16 + e)) & 1u) << 2);
-                  v2[z] = c_lloyd[code] * w8[2 * h2 + z];
-                }
-                w[h2] = pack_bf2(v2[0], v2[1]);
-              }
-              *(uint4*)(dst + e * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) { mbar_arrive(bar(B_VB_FULL0 + vs)); mbar_arrive(bar(B_VC_EMPTY)); }
         }
       }
       tc = tc0 + I.n_tiles;
