@@ -348,6 +348,18 @@ int fk_last_launch_count(const fk_pool* pool);
  * caller. */
 fk_status fk_pool_set_profile_event(fk_pool* pool, void* event);
 
+/* Failure-detection test hook.  While `on` is nonzero, every later
+ * fk_residual_attention call on the pool that runs the four-agent decode
+ * kernel (decode-shaped calls, see fk_residual_attention) makes that
+ * kernel's key-copy warp also wait on a barrier that nothing completes.
+ * The wait gives up after its bound (about 2 s of GPU clock), the CTA takes
+ * the same abort path as any timed-out wait (no further copy or MMA is
+ * issued, MMAs in flight are drained, copies in flight get a grace period)
+ * and the next fk_check returns FK_ERR_TIMEOUT.  The output of such a call
+ * is undefined.  No GPU fault, trap or hang is involved; the pool and the
+ * context stay usable.  Off by default.  Host only. */
+fk_status fk_pool_set_test_stall(fk_pool* pool, int on);
+
 /* Synchronise `stream` and read the pool's device error word: FK_OK, or
  * FK_ERR_DEVICE_CHECK if a kernel's bounds check fired since the last
  * fk_check (the word is then cleared). */

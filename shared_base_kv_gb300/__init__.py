@@ -38,7 +38,8 @@ EXPORTS = (
     "fk_fork", "fk_page_refcount", "fk_agent_register", "fk_agent_release",
     "fk_base_append", "fk_residual_append", "fk_pool_compress",
     "fk_pool_load_compressed", "fk_residual_attention", "fk_last_launch_count",
-    "fk_check", "fk_plan_host", "fk_pool_set_profile_event", "fk_agent_rcache",
+    "fk_check", "fk_plan_host", "fk_pool_set_profile_event", "fk_pool_set_test_stall",
+    "fk_agent_rcache",
     "fk_residual_attention_noalloc", "fk_agent_register_shared",
     "fk_radix_create", "fk_radix_destroy", "fk_radix_match", "fk_radix_insert",
     "fk_radix_adapter_get", "fk_radix_adapter_attach", "fk_radix_adapter_detach",
@@ -115,6 +116,7 @@ def lib() -> ctypes.CDLL:
             "fk_last_launch_count": (i32, [vp]),
             "fk_check": (i32, [vp, vp]),
             "fk_pool_set_profile_event": (i32, [vp, vp]),
+            "fk_pool_set_test_stall": (i32, [vp, i32]),
             "fk_agent_rcache": (i32, [vp, i32, ctypes.POINTER(ctypes.c_size_t),
                                       ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(i32)]),
             "fk_plan_host": (i32, [i32, i32, i32, i32, i32, P32, i32, P32, P32, i32, i32, i32,
@@ -322,6 +324,11 @@ def fk_pool_set_profile_event(h, event) -> None:
     """``event``: a torch.cuda.Event (recorded after the main kernel) or None."""
     ptr = None if event is None else event.cuda_event
     _check(lib().fk_pool_set_profile_event(h, ptr))
+
+
+def fk_pool_set_test_stall(h, on: bool) -> None:
+    """Failure-detection test hook (see include/forkkv.h)."""
+    _check(lib().fk_pool_set_test_stall(h, 1 if on else 0))
 
 
 def fk_check(h, stream=None) -> None:

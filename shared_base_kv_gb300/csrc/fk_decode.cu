@@ -107,7 +107,9 @@ enum {
   B_KB_FULL0, B_KB_FULL1, B_KB_EMPTY0, B_KB_EMPTY1, B_VB_FULL0, B_VB_FULL1, B_VB_EMPTY0,
   B_VB_EMPTY1, B_LV_FULL, B_LV_EMPTY, B_M_FULL, B_M_EMPTY, B_ITEM_FULL, B_TRIG_FULL0, B_TRIG_FULL1, B_Z_FULL0, B_Z_FULL1, B_Z_FREE0, B_Z_FREE1, B_P_FULL0, B_P_FULL1, B_PV_DONE0,
   B_PV_DONE1, B_ACC_EMPTY, B_KQ_FULL, B_KQ_EMPTY, B_VC_FULL0, B_VC_FULL1, B_VC_EMPTY0, B_VC_EMPTY1,
-  B_FINAL, B_COUNT
+  B_FINAL,
+  B_STALL,   // never completed: the target of the failure-detection test's wait
+  B_COUNT
 };
 // Arrival counts: 8 = lane 0 of each warp of both compute warpgroups; 4 =
 // lane 0 of each Trig warp; 1 = one thread, a bulk-copy transaction count
@@ -282,8 +284,9 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
   uint64_t ph = kEmptyMask;          // parity each role waits for, bit i for barrier i
   auto wait = [&](int i) {
     uint32_t par = (uint32_t)(ph >> i) & 1u;
-    mbar_wait_inl(bar(i), par, abort_flag, errw);
+    const bool ok = mbar_wait_inl(bar(i), par, abort_flag, errw);
     ph ^= 1ull << i;
+    return ok;
   };
   asm volatile("griddepcontrol.launch_dependents;");
 
@@ -377,6 +380,9 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
     // every lane waits; lane 0 posts the transaction count; the lanes then
     // split the tile's bulk copies (one page each).  Keys run ahead as far as
     // the two key stages allow, independently of the values.
+    // (failure-detection test: a wait that gives up, so that the whole CTA
+    // takes its abort path and the call reports the timeout)
+    if (p.stall_probe) wait(B_STALL);
     int tc = 0;
     for (int it = it_begin; it < it_end; ++it) {
       Item I;
@@ -395,7 +401,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           const int st = tc & 1;
           wait(B_KB_EMPTY0 + st);
           __syncwarp();
-          if (lane == 0) mbar_expect_tx_relaxed(bar(B_KB_FULL0 + st), np * LY::PAGE_B);
+          if (lane == 0 && !*abort_flag) mbar_expect_tx_relaxed(bar(B_KB_FULL0 + st), np * LY::PAGE_B);
           __syncwarp();
           if (lane < np && !*abort_flag) {
             const uint8_t* src = g.base + g.off_kb + (int64_t)layer * g.kb_layer_bytes +
@@ -406,7 +412,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         } else {
           wait(B_KQ_EMPTY);
           __syncwarp();
-          if (lane == 0) mbar_expect_tx_relaxed(bar(B_KQ_FULL), np * kPage * D);
+          if (lane == 0 && !*abort_flag) mbar_expect_tx_relaxed(bar(B_KQ_FULL), np * kPage * D);
           __syncwarp();
           if (lane < np && !*abort_flag) {
             const uint8_t* src = g.base + g.off_kq +
@@ -424,7 +430,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           wait(B_M_EMPTY);
           if (it == it_begin) asm volatile("griddepcontrol.wait;" ::: "memory");
           __syncwarp();
-          if (lane == 0) mbar_expect_tx_relaxed(bar(B_M_FULL), mbytes);
+          if (lane == 0 && !*abort_flag) mbar_expect_tx_relaxed(bar(B_M_FULL), mbytes);
           __syncwarp();
           for (uint32_t o = lane * 4096u; o < mbytes && !*abort_flag; o += 32u * 4096u)
             bulk_g2s(sbase + LY::oM + o, ws + mpr.mofs + o, min(4096u, mbytes - o), bar(B_M_FULL));
@@ -459,7 +465,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           const int cst = vt & 1;
           wait(B_VC_EMPTY0 + cst);   // warp 0 has expanded its half of tile vt - 2
           __syncwarp();
-          if (lane == 0) mbar_expect_tx_relaxed(bar(B_VC_FULL0 + cst), np * kPage * (3 * D / 8 + 4));
+          if (lane == 0 && !*abort_flag) mbar_expect_tx_relaxed(bar(B_VC_FULL0 + cst), np * kPage * (3 * D / 8 + 4));
           __syncwarp();
           if (lane < np && !*abort_flag) {
             const int64_t tok = (((int64_t)layer * g.num_pages + pg_k) * g.H_kv + I.head) * kPage;
@@ -475,7 +481,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           const int st = vt % LY::NVB;
           wait(B_VB_EMPTY0 + st);
           __syncwarp();
-          if (lane == 0) mbar_expect_tx_relaxed(bar(B_VB_FULL0 + st), np * LY::PAGE_B);
+          if (lane == 0 && !*abort_flag) mbar_expect_tx_relaxed(bar(B_VB_FULL0 + st), np * LY::PAGE_B);
           __syncwarp();
           if (lane < np && !*abort_flag) {
             const uint8_t* src = g.base + g.off_vb + (int64_t)layer * g.kb_layer_bytes +
@@ -489,7 +495,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         wait(B_LV_EMPTY);
         const int n_grp = I.sum_rp / 8;
         __syncwarp();
-        if (lane == 0) mbar_expect_tx_relaxed(bar(B_LV_FULL), n_grp * kLvGroup);
+        if (lane == 0 && !*abort_flag) mbar_expect_tx_relaxed(bar(B_LV_FULL), n_grp * kLvGroup);
         __syncwarp();
         if (lane < n_grp && !*abort_flag) {
           int pa = 0, j = 0;

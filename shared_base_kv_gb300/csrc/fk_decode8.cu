@@ -381,8 +381,9 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
   uint64_t ph = kEmptyMask;          // parity each role waits for, bit i for barrier i
   auto wait = [&](int i) {
     uint32_t par = (uint32_t)(ph >> i) & 1u;
-    mbar_wait_inl(bar(i), par, abort_flag, errw);
+    const bool ok = mbar_wait_inl(bar(i), par, abort_flag, errw);
     ph ^= 1ull << i;
+    return ok;
   };
 
   // ---- set-up: zero the page stages (rows past a ragged tile stay
@@ -450,7 +451,7 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
           if (p0 + kTilePages + lane < n_pages && lane < kTilePages) pg = pages[p0 + kTilePages + lane];
           wait(b_empty);
           __syncwarp();
-          if (lane == 0) mbar_expect_tx_relaxed(bar(b_full), np * PAGE_B);
+          if (lane == 0 && !*abort_flag) mbar_expect_tx_relaxed(bar(b_full), np * PAGE_B);
           __syncwarp();
           if (lane < np && !*abort_flag)
             bulk_g2s(dst0 + lane * PAGE_B, region + ((int64_t)pg_k * g.H_kv + head) * PAGE_B, PAGE_B,

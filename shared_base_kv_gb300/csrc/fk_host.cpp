@@ -63,6 +63,7 @@ struct fk_pool {
   // eight agent slots (FORKKV_DECODE_SLOTS=8 at pool creation) instead of
   // four agents
   bool slots8 = false;
+  bool stall_probe = false;                  // failure-detection test hook (fk_pool_set_test_stall)
   std::vector<int32_t> refcount;             // per page
   std::vector<int32_t> free_list;            // stack of free page ids
   std::vector<uint8_t> fill;                 // [L][num_pages] tokens held
@@ -1292,7 +1293,9 @@ fk_status fk_residual_attention(fk_pool* p, int layer, const uint16_t* q, const 
     p->plan_valid = true;
   }
   int launches = 0;
-  int e = launch_attention(g, p->plan_dev, layer, q, out, compressed ? 1 : 0, p->num_sms,
+  PlanDev pd_call = p->plan_dev;
+  pd_call.stall_probe = p->stall_probe ? 1 : 0;
+  int e = launch_attention(g, pd_call, layer, q, out, compressed ? 1 : 0, p->num_sms,
                            stream, &launches, p->profile_event);
   if (e != 0) return cuda_fail((cudaError_t)e, "attention kernels");
   p->last_launches = launches;
@@ -1371,7 +1374,9 @@ fk_status fk_residual_attention_noalloc(fk_pool* p, int layer, const uint16_t* q
   g2.off_ws = (int64_t)((uint8_t*)scratch - g.base);
   g2.ws_bytes = (int64_t)scratch_bytes;
   int launches = 0;
-  int e = launch_attention(g2, cache.pd, layer, q, out, compressed ? 1 : 0, p->num_sms, stream,
+  PlanDev pd_call = cache.pd;
+  pd_call.stall_probe = p->stall_probe ? 1 : 0;
+  int e = launch_attention(g2, pd_call, layer, q, out, compressed ? 1 : 0, p->num_sms, stream,
                            &launches, nullptr);
   if (e != 0) return cuda_fail((cudaError_t)e, "attention kernels");
   p->last_launches = launches;
@@ -1379,6 +1384,12 @@ fk_status fk_residual_attention_noalloc(fk_pool* p, int layer, const uint16_t* q
 }
 
 int fk_last_launch_count(const fk_pool* p) { return p ? p->last_launches : 0; }
+
+fk_status fk_pool_set_test_stall(fk_pool* p, int on) {
+  if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");
+  p->stall_probe = on != 0;
+  return FK_OK;
+}
 
 fk_status fk_pool_set_profile_event(fk_pool* p, void* event) {
   if (!p) return fail(FK_ERR_INVALID_ARG, "pool is NULL");

@@ -81,6 +81,8 @@ struct PlanDev {
   int32_t slots8;          // 1: eight-slot decode tiles (fk_decode8.cu); tile_agents holds
                            // kDecodeSlots entries per tile (-1: empty slot), rows 4 per slot
                            // (row_agent -1: a padded row)
+  int32_t stall_probe;     // failure-detection test: the four-agent decode kernel's key
+                           // warp also waits on a barrier nothing completes (set per call)
   int64_t off_items, off_row_agent, off_row_cg, off_pages, off_tile_agents,
           off_call_agents, off_csr_ptr, off_csr_slots, off_partials, off_cta;
   int64_t off_mpairs, off_item_mpair;   // MPair[n_mpairs], int32[n_items]

@@ -525,9 +525,14 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
   uint32_t ph = kEmptyMask;
   auto wait = [&](int i) {
     uint32_t par = (ph >> i) & 1u;
-    mbar_wait(bar(i), par, abort_flag, errw);
+    const bool ok = mbar_wait(bar(i), par, abort_flag, errw);
     ph ^= 1u << i;
+    return ok;
   };
+  // the producer posts a transaction count and copies only after a wait
+  // that succeeded while the CTA carries on: after a given-up wait the
+  // stage's previous phase may still be pending
+  auto go = [&](int i) { return wait(i) && !*abort_flag; };
   // the dependent combine grid may be scheduled now; it waits for this
   // grid's completion before reading the partials
   asm volatile("griddepcontrol.launch_dependents;");
@@ -574,8 +579,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
       ItemInfo I;
       load_item(g, p, ws, it, I);
       const int32_t* pages = (const int32_t*)(ws + p.off_pages) + I.page_begin;
-      wait(B_BK_EMPTY);
-      {
+      if (go(B_BK_EMPTY)) {
         uint32_t bytes = 0;
 #pragma unroll
         for (int a = 0; a < kA; ++a) bytes += D * I.rp[a] * 2;
@@ -593,8 +597,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
         const int p0 = k * kTilePages;
         const int np = min(kTilePages, I.n_pages - p0);
         const int t0 = (I.lp_begin + p0) * kPage;
-        if (COMP) {
-          wait(B_VC_EMPTY);
+        if (COMP && go(B_VC_EMPTY)) {
           mbar_expect_tx(bar(B_VC_FULL), np * kPage * (3 * D / 8 + 4));
           for (int j = 0; j < np; ++j) {
             int pg = pages[p0 + j];
@@ -605,7 +608,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
                      bar(B_VC_FULL));
           }
         }
-        wait(B_VL_EMPTY);
+        if (!go(B_VL_EMPTY)) return;
         const int ntok = min(kTileTok, g.tcap - t0);
         uint32_t bytes = COMP ? 0 : np * LY::PAGE_B;
 #pragma unroll
@@ -633,7 +636,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
         const int np = min(kTilePages, I.n_pages - p0);
         const int t0 = (I.lp_begin + p0) * kPage;
         if (!COMP) {
-          wait(B_KB_EMPTY);
+          if (go(B_KB_EMPTY)) {
           mbar_expect_tx(bar(B_KB_FULL), np * LY::PAGE_B);
           for (int j = 0; j < np; ++j) {
             int pg = pages[p0 + j];
@@ -641,8 +644,8 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
                                  ((int64_t)pg * g.H_kv + I.head) * LY::PAGE_B;
             bulk_g2s(sbase + LY::oKB + j * LY::PAGE_B, src, LY::PAGE_B, bar(B_KB_FULL));
           }
-        } else {
-          wait(B_KQ_EMPTY);
+          }
+        } else if (go(B_KQ_EMPTY)) {
           mbar_expect_tx(bar(B_KQ_FULL), np * kPage * D);
           for (int j = 0; j < np; ++j) {
             int pg = pages[p0 + j];
@@ -653,7 +656,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
         }
         {
           const int b = COMP ? 0 : (tile_ctr & 1);
-          wait(B_LK_EMPTY0 + b);
+          if (go(B_LK_EMPTY0 + b)) {
           const int ntok = min(kTileTok, g.tcap - t0);
           uint32_t bytes = 0;
 #pragma unroll
@@ -665,6 +668,7 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
               bulk_g2s(sbase + (b ? LY::oLK1 : LY::oLK0) + I.col[a] * kTileTok * 2,
                        rc_lk(g, I, a, layer) + (int64_t)t0 * I.rp[a] * 2, ntok * I.rp[a] * 2,
                        bar(B_LK_FULL0 + b));
+          }
         }
         if (k > 0) load_values(k - 1);
       }
@@ -751,8 +755,10 @@ __global__ void __launch_bounds__(attn::kThreads, 1)
       mma_commit(bar(B_Q_EMPTY));
       mma_commit(bar(B_BK_EMPTY));
     }
+    // every MMA issued completes before tensor memory is freed, also after
+    // a given-up wait (the drain ignores the abort flag)
     mma_commit(bar(B_FINAL));
-    wait(B_FINAL);
+    mbar_wait_drain(bar(B_FINAL), (ph >> B_FINAL) & 1u);
   } else if (warp == 2) {
     // =========================== tile-start rotations, one tile ahead ====
     // Exact t0 * theta_i reduced modulo 2 pi with a 64-bit binary fraction,

@@ -153,6 +153,43 @@ def test_parity_full_tiny_stress_both():
     assert mx <= MAX_ABS and mean <= MEAN_ABS
 
 
+# ------------------------------------------------------- general kernel --
+# Calls that are neither decode-shaped (G * C == 4) nor chunk-shaped
+# (G * C >= 128 with d = 128 on the uncompressed pool) run the general
+# attention kernel: a GQA group of eight, two query rows per agent, the
+# compressed pool with C = 2, and d = 64 with 128 rows per agent and head.
+GENERAL = {
+    "gqa8_decode": dict(name="llama8b_32k", kw=dict(prefix=700, A=5, heads=(64, 8, 128))),
+    "c2_gqa4": dict(name="llama8b_32k", kw=dict(prefix=500, suffix=(0, 40), A=4, C=2)),
+    "c2_causal_gqa8": dict(name="qwen72b_chunk", kw=dict(prefix=300, A=3, C=2)),
+    "d64_c32": dict(name="tiny", kw=dict(prefix=200, A=3, C=32)),
+}
+
+
+@pytest.mark.parametrize("variant", ["base", "peaked", "strong"])
+@pytest.mark.parametrize("case", list(GENERAL))
+def test_parity_general_kernel(case, variant):
+    spec = GENERAL[case]
+    w = workloads.make_workload(spec["name"], variant, **spec["kw"])
+    G = w.H_q // w.H_kv
+    assert G * w.C != 4 and (G * w.C < 128 or w.d != 128)    # the general kernel's shapes
+    dw, out = _run(w)
+    mx, mean, rel = errors(out, oracle_out(w, 0))
+    assert mx <= MAX_ABS and mean <= MEAN_ABS, (case, variant, mx, mean, rel)
+    assert fk_last_launch_count(dw.pool.h) == 2             # attention kernel + combine
+
+
+@pytest.mark.parametrize("variant", ["base", "peaked", "strong"])
+def test_parity_general_kernel_compressed_c2(variant):
+    w = workloads.make_workload("compressed", variant, prefix=500, A=5, C=2)
+    kq, ks, vc, vn = oracle_codes(w, 0)
+    dw, out = _run(w, compressed="codes", codes={0: (kq, ks, oracle.pack_planes(vc), vn)})
+    kh, vh = oracle.decode_pages(kq, ks, vc, vn)
+    ref = oracle_out(w, 0, pages_k=kh, pages_v=vh)
+    mx, mean, rel = errors(out, ref)
+    assert mx <= MAX_ABS_COMPRESSED and mean <= MEAN_ABS, (variant, mx, mean, rel)
+
+
 # ------------------------------------------------------------ edge cases --
 
 def test_single_key_and_short_sequences(slots):

@@ -398,6 +398,31 @@ def test_int8_keys_within_half_step():
     assert oc.k_int8_scale(np.zeros(5)) == np.float32(1.0)
 
 
+def test_encode_pages_scale_over_filled_rows_only():
+    # PolyKV summary, section 2B: one key scale per tensor, max|K| / 127.  The
+    # layer's key tensor is the filled rows of its pages; rows past a page's
+    # fill (and empty pages) hold no token and must neither set the scale
+    # nor carry codes.
+    rng = _rng(41)
+    n, P, H, d = 3, 16, 2, 128
+    pk = rng.uniform(-1.0, 1.0, (n, P, H, d))
+    pv = rng.standard_normal((n, P, H, d))
+    fill = np.array([16, 5, 0])
+    pk[0, 3, 1, 7] = -3.0                  # the largest filled magnitude
+    pk[1, 5:] = 1000.0                     # past page 1's fill
+    pk[2] = -1000.0                        # an empty page
+    kq, scale, codes, norms = oc.encode_pages(pk, pv, fill)
+    assert scale == np.float32(3.0 / 127.0)
+    assert kq[0, 3, 1, 7] == -127
+    live = np.arange(P)[None, :] < fill[:, None]
+    assert not np.any(kq[~live]) and not np.any(codes[~live]) and not np.any(norms[~live])
+    # a filled row keeps its own codes: |K / scale| rounds to within half a
+    # step, and each value row's norm is its length
+    dec = kq[live].astype(np.float64) * float(scale)
+    assert np.abs(dec - pk[live]).max() <= float(scale) / 2 * (1 + 1e-6)
+    assert np.allclose(norms[live], np.linalg.norm(pv[live], axis=-1), rtol=1e-6)
+
+
 def test_int8_round_half_even():
     scale = np.float32(0.5)
     k = np.array([0.25, 0.75, -0.25, 1.25])          # K/scale = .5, 1.5, -.5, 2.5

@@ -150,11 +150,13 @@ def make_workload(name: str, variant: str = "base", *,
                   n_layers: Optional[int] = None,
                   ranks: Optional[tuple] = None,
                   C: Optional[int] = None,
-                  seed: Optional[int] = None) -> Workload:
+                  seed: Optional[int] = None,
+                  heads: Optional[tuple] = None) -> Workload:
     """Build the page tables of workload ``name`` (see ``CONFIGS``).
 
     Keyword overrides shrink a workload for tests (same shapes per token,
-    fewer tokens / agents / layers).  ``variant`` selects the stress inputs:
+    fewer tokens / agents / layers); ``heads`` = (H_q, H_kv, d) changes the
+    head shapes (calls that other attention kernels serve).  ``variant`` selects the stress inputs:
     ``peaked`` doubles q and plants, per agent, keys aligned with that
     agent's queries; ``strong`` draws the LoRA up-projections with std 0.5 so
     the residual is as large as the base.
@@ -169,6 +171,8 @@ def make_workload(name: str, variant: str = "base", *,
                      ("seed", seed)):
         if val is not None:
             cfg[key] = val
+    if heads is not None:               # (H_q, H_kv, d): other head shapes
+        cfg["H_q"], cfg["H_kv"], cfg["d"] = (int(x) for x in heads)
     P = PAGE
     A_ = int(cfg["A"])
     g = _gen(cfg["seed"])
