@@ -36,11 +36,17 @@ METRIC = "agent decode tokens/sec and achieved HBM GB/s, 8 agents × 32K shared 
 UNIT = "agent-tokens/s"
 WORKLOAD = "llama8b_32k"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ("shared_base_kv_gb300/csrc/fk_decode.cu",
                   "shared_base_kv_gb300/csrc/fk_kernels.cu",
                   "shared_base_kv_gb300/csrc/fk_device.cuh",
                   "shared_base_kv_gb300/csrc/fk_internal.h")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_llama8b_32k.txt")
+KERNEL8_SOURCES = ("shared_base_kv_gb300/csrc/fk_decode8.cu",
+                   "shared_base_kv_gb300/csrc/fk_kernels.cu",
+                   "shared_base_kv_gb300/csrc/fk_device.cuh",
+                   "shared_base_kv_gb300/csrc/fk_internal.h")
+TRAFFIC8_FILE = os.path.join(ROOT, "profiles", "decode8_kernel_llama8b_32k.txt")
 PREFILL_SOURCES = ("shared_base_kv_gb300/csrc/fk_prefill.cu",
                    "shared_base_kv_gb300/csrc/fk_device.cuh",
                    "shared_base_kv_gb300/csrc/fk_internal.h")
@@ -80,6 +86,15 @@ def measured_peak_hbm():
         return v, "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_peak_bf16():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def traffic_per_launch(path=TRAFFIC_FILE, sources=KERNEL_SOURCES):
@@ -355,6 +370,7 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
     value, total_ms, e2e_value, e2e_ms = reduce_over_ranks(
         total_ms, e2e_ms, w.A * K, w.A * KE, world, dev)
     ab = algorithmic_bytes(w)
+    slots8 = os.environ.get("FORKKV_DECODE_SLOTS") == "8"
     main_avg_s = statistics.mean(main_ms) / 1e3
     peak, peak_kind = measured_peak_hbm()
     achieved = ab["kernel"] / main_avg_s / 1e9
@@ -373,8 +389,10 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
                    "step_hbm_gbs": ab["step"] / (total_ms / K / 1e3) / 1e9,
                    "step_bytes": ab["step"]},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic_per_launch(),
-                     "kernel": ("decode8_kernel" if os.environ.get("FORKKV_DECODE_SLOTS") == "8"
+                     "frac": achieved / peak,
+                     "traffic": (traffic_per_launch(TRAFFIC8_FILE, KERNEL8_SOURCES) if slots8
+                                 else traffic_per_launch()),
+                     "kernel": ("decode8_kernel" if slots8
                                 else "mbuild_kernel<128> + decode_kernel<128,false>"),
                      "kernel_ms": statistics.mean(main_ms),
                      "bytes_per_launch": ab["kernel"],
@@ -482,14 +500,36 @@ def measure_configs(dev, stream, flush) -> list:
             flops += w.H_kv * (int(w.seq_lens[a]) * (2 * r * w.d + G * w.C * (4 * w.d + 2 * r))
                                + G * w.C * 2 * r * w.d)
         flops *= w.n_layers
+        gbs = per_layer * w.n_layers / (p50 / 1e3) / 1e9
+        tflops = flops / (p50 / 1e3) / 1e12
+        G = w.H_q // w.H_kv
+        if G * w.C >= 128 and w.d == 128 and comp is None:
+            kernel, bound = "chunk_kernel", "tensor"
+        elif G * w.C == 4:
+            eight = os.environ.get("FORKKV_DECODE_SLOTS") == "8" and w.d == 128 and comp is None
+            kernel = "decode8_kernel" if eight else f"mbuild_kernel<{w.d}> + decode_kernel<{w.d},{int(comp is not None)}>"
+            bound = "hbm"
+        else:
+            kernel, bound = f"attention_kernel<{w.d},{int(comp is not None)}>", "hbm"
+        if bound == "tensor":
+            pk, pkind = measured_peak_bf16()
+            roof = {"bound": "tensor", "achieved": tflops, "peak": pk, "unit": "TFLOP/s",
+                    "frac": tflops / pk, "peak_kind": f"{pkind} bf16_tflops (burst)"}
+        else:
+            pk, pkind = measured_peak_hbm()
+            roof = {"bound": "hbm", "achieved": gbs, "peak": pk, "unit": "GB/s",
+                    "frac": gbs / pk, "peak_kind": f"{pkind} hbm_gbs"}
+        roof["kernel"] = kernel + " + combine_kernel"
+        roof["timed"] = "whole step (every launch of the call), median"
         res.append({"workload": name, "layers": w.n_layers, "agents": w.A, "C": w.C,
                     "ms_p50": p50, "ms_p10": p10, "ms_p90": p90,
                     "agent_tokens_per_s": w.A * w.C / (p50 / 1e3),
                     "algorithmic_bytes": per_layer * w.n_layers,
-                    "gbs": per_layer * w.n_layers / (p50 / 1e3) / 1e9,
+                    "gbs": gbs,
                     "algorithmic_tflop": flops / 1e12,
-                    "tflops": flops / (p50 / 1e3) / 1e12,
-                    "compressed": comp is not None})
+                    "tflops": tflops,
+                    "compressed": comp is not None,
+                    "roofline": roof})
         dw.pool.close()
         del dw, qs, out
         torch.cuda.empty_cache()

@@ -116,3 +116,31 @@ class DeviceWorkload:
 
     def last_launches(self) -> int:
         return fk_last_launch_count(self.pool.h)
+
+
+def main(argv=None) -> int:
+    """Run one workload's attention call a few times on cuda:0 (for profilers):
+    ``python -m shared_base_kv_gb300.harness compressed --calls 4``."""
+    import argparse
+    import os
+    import sys
+    ap = argparse.ArgumentParser()
+    ap.add_argument("workload")
+    ap.add_argument("--calls", type=int, default=4)
+    args = ap.parse_args(argv)
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import workloads
+    w = workloads.make_workload(args.workload)
+    dw = DeviceWorkload(w, compressed="gpu" if w.compressed else None)
+    q = dw.queries(0)
+    out = torch.empty_like(q)
+    for _ in range(args.calls):
+        dw.attention(0, q, out)
+    torch.cuda.synchronize()
+    dw.check()
+    print(f"{args.workload}: {args.calls} calls, {dw.last_launches()} launches each")
+    return 0
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())
