@@ -457,11 +457,21 @@ def measure_configs(dev, stream, flush) -> list:
     import workloads
     from shared_base_kv_gb300 import fk_residual_attention, harness
     res = []
-    for name, comp, iters in (("tiny", None, 200), ("llama8b_32k", None, 200),
-                              ("agents32_layers32", None, 30), ("qwen72b_chunk", None, 50),
-                              ("compressed", "gpu", 200)):
+    # the last line is the headline workload with Shared-A agents (LRAgent
+    # summary, "BaseLRShared"): all eight read agent 0's low-rank rows, so
+    # the rCache bytes count once
+    for name, comp, iters, shared in (("tiny", None, 200, False), ("llama8b_32k", None, 200, False),
+                                      ("agents32_layers32", None, 30, False),
+                                      ("qwen72b_chunk", None, 50, False),
+                                      ("compressed", "gpu", 200, False),
+                                      ("llama8b_32k", None, 200, True)):
         w = workloads.make_workload(name)
-        dw = harness.DeviceWorkload(w, device=str(dev), compressed=comp)
+        if shared:
+            for l in range(w.n_layers):
+                ld = w.layer(l)
+                for a in range(1, w.A):
+                    ld.lk[a], ld.lv[a] = ld.lk[0], ld.lv[0]
+        dw = harness.DeviceWorkload(w, device=str(dev), compressed=comp, shared_a=shared)
         qs = [dw.queries(l) for l in range(w.n_layers)]
         w.drop()
         out = torch.empty_like(qs[0])
@@ -490,6 +500,8 @@ def measure_configs(dev, stream, flush) -> list:
         p10, p50, p90 = percentiles(ms)
         ab = algorithmic_bytes(w)
         per_layer = ab["step"]
+        if shared:                 # one low-rank cache for all agents
+            per_layer -= ab["rcache"] - int(w.seq_lens[0]) * int(w.ranks[0]) * 2 * 2
         if comp is not None:     # int8 K (d B) + 3-bit V (3d/8 B) + fp32 norm per (token, head)
             per_layer = (int(np.sum(w.slot_fill)) * w.H_kv * (w.d + 3 * w.d // 8 + 4)
                          + ab["rcache"] + ab["q"] + ab["out"])
@@ -521,7 +533,8 @@ def measure_configs(dev, stream, flush) -> list:
                     "frac": gbs / pk, "peak_kind": f"{pkind} hbm_gbs"}
         roof["kernel"] = kernel + " + combine_kernel"
         roof["timed"] = "whole step (every launch of the call), median"
-        res.append({"workload": name, "layers": w.n_layers, "agents": w.A, "C": w.C,
+        res.append({"workload": name + (" shared_a" if shared else ""), "layers": w.n_layers,
+                    "agents": w.A, "C": w.C,
                     "ms_p50": p50, "ms_p10": p10, "ms_p90": p90,
                     "agent_tokens_per_s": w.A * w.C / (p50 / 1e3),
                     "algorithmic_bytes": per_layer * w.n_layers,

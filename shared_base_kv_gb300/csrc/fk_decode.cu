@@ -161,6 +161,10 @@ struct Item {
   int head, n_rows, n_pages, lp_begin, n_ag, partial_begin, row_begin, n_tiles, page_begin,
       sum_rp;
   int rp[kA], col[kA], pool_agent[kA];
+  // Lv^T stage columns: agents that read the same residual rows (Shared-A:
+  // LRAgent summary, "BaseLRShared") share one block, copied once, and one
+  // OL^T rank block serves all of their rows; lv_rp = the stage's ranks
+  int lvcol[kA], lv_rp;
   float s[kA];
   int64_t rc_off[kA];
 };
@@ -195,6 +199,20 @@ __device__ __forceinline__ void load_item(const PoolGeom& g, const PlanDev& p, c
     }
   }
   I.sum_rp = col;
+  int lvc = 0;
+#pragma unroll
+  for (int a = 0; a < kA; ++a) {
+    int share = -1;
+#pragma unroll
+    for (int b = 0; b < a; ++b)
+      if (share < 0 && a < I.n_ag && I.rc_off[b] == I.rc_off[a]) share = b;
+    I.lvcol[a] = lvc;
+#pragma unroll
+    for (int b = 0; b < a; ++b)
+      if (b == share) I.lvcol[a] = I.lvcol[b];
+    if (a < I.n_ag && share < 0) lvc += I.rp[a];
+  }
+  I.lv_rp = lvc;
 }
 
 __device__ __forceinline__ const uint8_t* rc_lk(const PoolGeom& g, const Item& I, int a, int layer) {
@@ -490,10 +508,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
                      bar(B_VB_FULL0 + st));
           }
         }
-        // Lv^T: one tensor copy per rank group of each agent (its Lv map,
-        // coordinates (0, 0, group, t0 / 8, layer)) into group column / 8 + j
+        // Lv^T: one tensor copy per rank group of each distinct rCache block
+        // (its agent's Lv map, coordinates (0, 0, group, t0 / 8, layer)) into
+        // group lvcol / 8 + j
         wait(B_LV_EMPTY);
-        const int n_grp = I.sum_rp / 8;
+        const int n_grp = I.lv_rp / 8;
         __syncwarp();
         if (lane == 0 && !*abort_flag) mbar_expect_tx_relaxed(bar(B_LV_FULL), n_grp * kLvGroup);
         __syncwarp();
@@ -501,7 +520,10 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           int pa = 0, j = 0;
 #pragma unroll
           for (int a = 0; a < kA; ++a)
-            if (a < I.n_ag && lane >= I.col[a] / 8) { pa = I.pool_agent[a]; j = lane - I.col[a] / 8; }
+            if (a < I.n_ag && lane >= I.lvcol[a] / 8 && lane < (I.lvcol[a] + I.rp[a]) / 8) {
+              pa = I.pool_agent[a];
+              j = lane - I.lvcol[a] / 8;
+            }
           const uint8_t* map = g.base + g.off_lvmap + 128LL * pa;
           asm volatile(
               "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -893,20 +915,20 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           for (int e = 0; e < 8; ++e)
             if (r0 + e < n_rows) part[(int64_t)(I.partial_begin + r0 + e) * PS + 4 + ln] = __uint_as_float(raw[e]);
         }
-        // OL^T lane ln: rank ln - col of the agent whose columns hold ln
-        // (that agent's rows take it), or the row sums on the ones lane
-        int oa = -1, orr = 0;
-#pragma unroll
-        for (int a = 0; a < kA; ++a)
-          if (a < n_ag && ln >= I.col[a] && ln < I.col[a] + I.rp[a]) { oa = a; orr = ln - I.col[a]; }
+        // OL^T lane ln: for each row, rank ln - lvcol of the row's agent if
+        // its Lv block holds ln (a shared block serves every agent reading
+        // it), or the row sums on the ones lane
         tmem_ld8_wait(tmem + kTmOL + r0 + lane_off, raw);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int row = r0 + e;
+          // the row's agent, 2 cw + e / 4, as an unrolled select
+          const int la = cw ? I.lvcol[2 + e / 4] : I.lvcol[e / 4];
+          const int lr = cw ? I.rp[2 + e / 4] : I.rp[e / 4];
           if (row < n_rows) {
             float* dst = part + (int64_t)(I.partial_begin + row) * PS;
             if (ln == kOnesLane) dst[1] = __uint_as_float(raw[e]);
-            if (oa >= 0 && row / kRPA == oa) dst[4 + D + orr] = __uint_as_float(raw[e]);
+            if (row / kRPA < n_ag && ln >= la && ln < la + lr) dst[4 + D + ln - la] = __uint_as_float(raw[e]);
           }
         }
         if (ln < 8 && r0 + ln < n_rows) part[(int64_t)(I.partial_begin + r0 + ln) * PS] = M.m_used[r0 + ln];

@@ -28,12 +28,18 @@ class DeviceWorkload:
                  page_shuffle_seed: Optional[int] = None, shared_a: bool = False):
         """``compressed``: None, ``"gpu"`` (encode with fk_pool_compress) or
         ``"codes"`` (load the per-layer codes in ``codes[layer] = (kq,
-        k_scale, vcodes_packed, vnorm)``, slot-ordered host arrays)."""
+        k_scale, vcodes_packed, vnorm)``, slot-ordered host arrays).
+        ``shared_a``: True (every agent but 0 reads agent 0's low-rank rows)
+        or a dict {agent: source agent} (Shared-A registration)."""
         self.w = w
         self.dev = torch.device(device)
         self.layers = list(range(w.n_layers)) if layers is None else list(layers)
         self.compressed = compressed
-        self.shared_a = shared_a
+        if shared_a is True:
+            self.share_src = {a: 0 for a in range(1, w.A)}
+        else:
+            self.share_src = dict(shared_a or {})
+        self.shared_a = bool(self.share_src)
         rmax = int(np.max(w.ranks))
         self.pool = Pool(n_layers=w.n_layers, n_q_heads=w.H_q, n_kv_heads=w.H_kv, head_dim=w.d,
                          num_pages=w.n_slots + spare_pages, max_agents=w.A, max_rank=rmax,
@@ -57,10 +63,11 @@ class DeviceWorkload:
             r = int(w.ranks[a])
             Bk = torch.stack([w.layer(l).bk[a] for l in range(w.n_layers)]).to(self.dev)
             Bv = torch.stack([w.layer(l).bv[a] for l in range(w.n_layers)]).to(self.dev)
-            if shared_a and a > 0:
-                # Shared-A: agents read agent 0's low-rank rows (the workload's
-                # lk/lv must then be the same for every agent)
-                fk_agent_register_shared(h, a, 0, w.s, Bk.contiguous(), Bv.contiguous())
+            if a in self.share_src:
+                # Shared-A: the agent reads its source agent's low-rank rows
+                # (the workload's lk/lv must then be the same for both)
+                fk_agent_register_shared(h, a, self.share_src[a], w.s, Bk.contiguous(),
+                                         Bv.contiguous())
             else:
                 fk_agent_register(h, a, r, w.s, Bk.contiguous(), Bv.contiguous())
         for l in self.layers:
@@ -81,7 +88,9 @@ class DeviceWorkload:
             n = int(w.slot_fill[slot])
             row = np.array([self.slot_page[slot]], dtype=np.int32)
             fk_base_append(h, l, row, 0, pk[slot, :n].contiguous(), pv[slot, :n].contiguous())
-        for a in range(1 if self.shared_a else w.A):
+        for a in range(w.A):
+            if a in self.share_src:
+                continue
             fk_residual_append(h, l, a, 0, ld.lk[a].to(self.dev).contiguous(),
                                ld.lv[a].to(self.dev).contiguous())
         if self.compressed == "gpu":

@@ -298,6 +298,22 @@ def test_agent_order_across_tiles_permutes_outputs():
     assert np.abs(got - base[perm]).max() <= 2e-3
 
 
+def test_parity_shared_a_mixed_tiles(slots):
+    """Shared-A agents next to agents with rows of their own in one tile: 2
+    and 3 read the rows of 0 and 1 (same tile), 5 reads 0's from the other
+    tile.  The four-agent kernel copies each shared block once."""
+    w = workloads.make_workload("llama8b_32k", "strong", prefix=700, suffix=(0, 0), A=6)
+    share = {2: 0, 3: 1, 5: 0}
+    ld = w.layer(0)
+    for a, src in share.items():
+        ld.lk[a] = ld.lk[src]
+        ld.lv[a] = ld.lv[src]
+    dw, out = _run(w, shared_a=share)
+    mx, mean, rel = errors(out, oracle_out(w, 0))
+    assert mx <= MAX_ABS and mean <= MEAN_ABS, (mx, mean, rel)
+    assert np.abs(out[0] - out[2]).max() > 1e-3          # same rows, other B
+
+
 def test_parity_shared_a_agents_read_one_low_rank_cache():
     """Shared-A (LRAgent summary, "BaseLRShared"): every agent has its own B
     but reads agent 0's low-rank rows; the oracle is given those same rows
