@@ -20,7 +20,8 @@
 // applied once per row in the combine.  Row sums of P are warp reductions.
 //
 // Warp roles (512 threads):
-//   warp 0       bulk copies of key pages (one stage)
+//   warp 0       bulk copies of key pages (one stage); L2 prefetch of the
+//                item's Lk and Lv rows a tile ahead
 //   warp 3       bulk copies of value pages (one stage)
 //   warp 1       MMA issue (converged warp, elect.sync)
 //   warps 4-7    compute warpgroup 0: agent slots 0-3 (rows 0-15)
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(d8::kThreads, 1)
   };
 
   // ---- set-up: zero the page stages (rows past a ragged tile stay
-  // finite) and the misc block, RoPE fractions, barriers, TMEM.
+  // finite) and the misc block, barriers, TMEM.
   // (M, Q and P are written in full before they are read; the page stages
   // keep stale but finite rows past a ragged last tile)
   for (int i = oKB + tid * 16; i < oQ; i += kThreads * 16) *(uint4*)(smem + i) = make_uint4(0, 0, 0, 0);
