@@ -395,6 +395,23 @@ fk_status fk_plan_host(int A, int C, int H_q, int H_kv, int page_size,
                        int32_t* tile_agents, int cap_tile_agents,
                        int* n_tile_agents);
 
+/* The work list of a decode-shaped call (four query rows per agent: G * C
+ * == 4) in eight-slot tiles, as the eight-slot decode kernel runs it (pools
+ * created with FORKKV_DECODE_SLOTS=8).  Same arguments and outputs as
+ * fk_plan_host, with fixed tile limits: tile_agents holds 8 entries per
+ * tile (-1: an empty slot); slot s owns the tile's rows 4 s .. 4 s + 3
+ * (row_agent -1 on an empty slot's rows); each half of a tile (slots 0-3,
+ * 4-7) holds at most 64 padded ranks.  FK_ERR_INVALID_ARG unless G * C ==
+ * 4.  Host only. */
+fk_status fk_plan_host_slots8(int A, int C, int H_q, int H_kv, int page_size,
+                              const int32_t* block_table, int max_pages,
+                              const int32_t* seq_lens, const int32_t* ranks,
+                              int target_items, fk_work_item* items, int cap_items,
+                              int* n_items, int32_t* row_agent, int32_t* row_cg,
+                              int cap_rows, int* n_rows, int32_t* page_ids,
+                              int cap_pages, int* n_pages, int32_t* tile_agents,
+                              int cap_tile_agents, int* n_tile_agents);
+
 /* Work list of the chunk kernel, the path of calls with at least 128 query
  * rows per agent and kv head (G * C >= 128, d = 128, uncompressed pool),
  * built without a pool or GPU.  Items: head, row_begin (first of the

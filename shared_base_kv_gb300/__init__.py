@@ -38,7 +38,8 @@ EXPORTS = (
     "fk_fork", "fk_page_refcount", "fk_agent_register", "fk_agent_release",
     "fk_base_append", "fk_residual_append", "fk_pool_compress",
     "fk_pool_load_compressed", "fk_residual_attention", "fk_last_launch_count",
-    "fk_check", "fk_plan_host", "fk_pool_set_profile_event", "fk_pool_set_test_stall",
+    "fk_check", "fk_plan_host", "fk_plan_host_slots8", "fk_pool_set_profile_event",
+    "fk_pool_set_test_stall",
     "fk_agent_rcache",
     "fk_residual_attention_noalloc", "fk_agent_register_shared",
     "fk_radix_create", "fk_radix_destroy", "fk_radix_match", "fk_radix_insert",
@@ -122,6 +123,9 @@ def lib() -> ctypes.CDLL:
             "fk_plan_host": (i32, [i32, i32, i32, i32, i32, P32, i32, P32, P32, i32, i32, i32,
                                    ctypes.POINTER(fk_work_item), i32, P32,
                                    P32, P32, i32, P32, P32, i32, P32, P32, i32, P32]),
+            "fk_plan_host_slots8": (i32, [i32, i32, i32, i32, i32, P32, i32, P32, P32, i32,
+                                          ctypes.POINTER(fk_work_item), i32, P32,
+                                          P32, P32, i32, P32, P32, i32, P32, P32, i32, P32]),
             "fk_radix_create": (i32, [i32, ctypes.POINTER(vp)]),
             "fk_radix_destroy": (None, [vp]),
             "fk_radix_match": (i32, [vp, P32, i32, P32, i32, ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_int64)]),
@@ -355,6 +359,29 @@ def fk_plan_host(A: int, C: int, H_q: int, H_kv: int, block_table, seq_lens, ran
                           ctypes.byref(n_it), _p32(ra), _p32(rc), n_rw.value,
                           ctypes.byref(n_rw), _p32(pg), n_pg.value, ctypes.byref(n_pg),
                           _p32(ta), n_ta.value, ctypes.byref(n_ta)))
+    its = [{f: getattr(items[i], f) for f, _ in fk_work_item._fields_} for i in range(n_it.value)]
+    return its, ra[:n_rw.value], rc[:n_rw.value], pg[:n_pg.value], ta[:n_ta.value]
+
+
+def fk_plan_host_slots8(A: int, C: int, H_q: int, H_kv: int, block_table, seq_lens, ranks,
+                        target_items: int):
+    """The eight-slot decode kernel's work list for a call shape (host only)."""
+    bt, sl, rk = _i32(block_table), _i32(seq_lens), _i32(ranks)
+    n_it, n_rw, n_pg, n_ta = (ctypes.c_int() for _ in range(4))
+    L = lib()
+    code = L.fk_plan_host_slots8(A, C, H_q, H_kv, 16, _p32(bt), bt.shape[1], _p32(sl), _p32(rk),
+                                 target_items, None, 0, ctypes.byref(n_it), None, None, 0,
+                                 ctypes.byref(n_rw), None, 0, ctypes.byref(n_pg), None, 0,
+                                 ctypes.byref(n_ta))
+    if code not in (FK_OK, FK_ERR_OOM):
+        _check(code)
+    items = (fk_work_item * max(n_it.value, 1))()
+    ra, rc = np.zeros(max(n_rw.value, 1), np.int32), np.zeros(max(n_rw.value, 1), np.int32)
+    pg, ta = np.zeros(max(n_pg.value, 1), np.int32), np.zeros(max(n_ta.value, 1), np.int32)
+    _check(L.fk_plan_host_slots8(A, C, H_q, H_kv, 16, _p32(bt), bt.shape[1], _p32(sl), _p32(rk),
+                                 target_items, items, n_it.value, ctypes.byref(n_it), _p32(ra),
+                                 _p32(rc), n_rw.value, ctypes.byref(n_rw), _p32(pg), n_pg.value,
+                                 ctypes.byref(n_pg), _p32(ta), n_ta.value, ctypes.byref(n_ta)))
     its = [{f: getattr(items[i], f) for f, _ in fk_work_item._fields_} for i in range(n_it.value)]
     return its, ra[:n_rw.value], rc[:n_rw.value], pg[:n_pg.value], ta[:n_ta.value]
 

@@ -1217,6 +1217,36 @@ fk_status fk_plan_host(int A, int C, int H_q, int H_kv, int page_size,
   return FK_OK;
 }
 
+fk_status fk_plan_host_slots8(int A, int C, int H_q, int H_kv, int page_size,
+                              const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                              const int32_t* ranks, int target_items, fk_work_item* items,
+                              int cap_items, int* n_items, int32_t* row_agent, int32_t* row_cg,
+                              int cap_rows, int* n_rows, int32_t* page_ids, int cap_pages,
+                              int* n_pages, int32_t* tile_agents, int cap_tile_agents,
+                              int* n_tile_agents) {
+  if (page_size != kPage) return fail(FK_ERR_UNSUPPORTED, "page_size must be 16");
+  if (!ranks) return fail(FK_ERR_INVALID_ARG, "ranks is NULL");
+  std::vector<int32_t> rp(A > 0 ? A : 0);
+  for (int i = 0; i < A; ++i) rp[i] = rank_pad(ranks[i]);
+  HostPlan pl;
+  fk_status s = plan_build(A, C, H_q, H_kv, page_size, block_table, max_pages, seq_lens,
+                           rp.data(), 4 * kDecodeSlots, 2 * kDecodeHalfRank, target_items, pl, true);
+  if (s != FK_OK) return s;
+  if (n_items) *n_items = (int)pl.items.size();
+  if (n_rows) *n_rows = (int)pl.row_agent.size();
+  if (n_pages) *n_pages = (int)pl.pages.size();
+  if (n_tile_agents) *n_tile_agents = (int)pl.tile_agents.size();
+  if ((int)pl.items.size() > cap_items || (int)pl.row_agent.size() > cap_rows ||
+      (int)pl.pages.size() > cap_pages || (int)pl.tile_agents.size() > cap_tile_agents)
+    return fail(FK_ERR_OOM, "output capacity too small");
+  if (items) std::copy(pl.items.begin(), pl.items.end(), items);
+  if (row_agent) std::copy(pl.row_agent.begin(), pl.row_agent.end(), row_agent);
+  if (row_cg) std::copy(pl.row_cg.begin(), pl.row_cg.end(), row_cg);
+  if (page_ids) std::copy(pl.pages.begin(), pl.pages.end(), page_ids);
+  if (tile_agents) std::copy(pl.tile_agents.begin(), pl.tile_agents.end(), tile_agents);
+  return FK_OK;
+}
+
 fk_status fk_plan_chunk_host(int A, int C, int H_q, int H_kv, const int32_t* block_table,
                             int max_pages, const int32_t* seq_lens, int n_ctas,
                             fk_work_item* items, int cap_items, int* n_items, int32_t* cta_begin,

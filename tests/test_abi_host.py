@@ -23,7 +23,7 @@ def built():
 def declared_symbols():
     text = open(os.path.join(ROOT, "include", "forkkv.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(fk_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(fk_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_library_exports_every_declared_symbol():
@@ -103,6 +103,62 @@ def test_plan_covers_sharing_classes_exactly_once(name, kw):
         expect = {(a, lp, ph, cg) for a, lp, ph in cov for cg in range(G * w.C)}
         assert set(seen) == expect
         assert all(v == 1 for v in seen.values())
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("llama8b_32k", dict(prefix=900, A=8)),
+    ("llama8b_32k", dict(prefix=300, A=19)),                       # ragged last tile, 3 tiles
+    ("agents32_layers32", dict(prefix=200, suffix=(0, 40), A=13, n_layers=1)),   # mixed ranks
+])
+def test_plan_slots8_covers_sharing_classes_exactly_once(name, kw):
+    w = workloads.make_workload(name, **kw)
+    items, row_agent, row_cg, pages, tile_agents = fk.fk_plan_host_slots8(
+        w.A, w.C, w.H_q, w.H_kv, w.block_table, w.seq_lens, w.ranks, 152)
+    cov = oracle.coverage(w.block_table, w.seq_lens, w.P)
+    classes = {(lp, ph): set(ag) for lp, ph, ag in oracle.page_classes(w.block_table, w.seq_lens, w.P)}
+    for h in range(w.H_kv):
+        seen = {}
+        for it in items:
+            if it["head"] != h:
+                continue
+            slots = [int(a) for a in tile_agents[it["agent_begin"]: it["agent_begin"] + 8]]
+            assert it["n_agents"] == 8 and it["n_rows"] == 32
+            for half in (slots[:4], slots[4:]):
+                real = [a for a in half if a >= 0]
+                assert sum(((int(w.ranks[a]) + 15) // 16) * 16 for a in real) <= 64
+            rows = list(zip(row_agent[it["row_begin"]: it["row_begin"] + 32],
+                            row_cg[it["row_begin"]: it["row_begin"] + 32]))
+            for r, (a, cg) in enumerate(rows):            # slot s owns rows 4 s .. 4 s + 3
+                assert int(a) == slots[r // 4]
+                if a >= 0:
+                    assert int(cg) == r % 4
+            for k in range(it["n_pages"]):
+                lp = it["lp_begin"] + k
+                ph = int(pages[it["page_begin"] + k])
+                assert set(a for a in slots if a >= 0) <= classes[(lp, ph)]
+                for a, cg in rows:
+                    if a >= 0:
+                        key = (int(a), lp, ph, int(cg))
+                        seen[key] = seen.get(key, 0) + 1
+        expect = {(a, lp, ph, cg) for a, lp, ph in cov for cg in range(4)}
+        assert set(seen) == expect
+        assert all(v == 1 for v in seen.values())
+
+
+def test_plan_slots8_reads_each_shared_page_once_per_head():
+    # eight agents over one prefix fill one tile: every (page, head) is in
+    # exactly one item's page run
+    w = workloads.make_workload("llama8b_32k", prefix=4096, A=8)
+    items, *_ = fk.fk_plan_host_slots8(w.A, w.C, w.H_q, w.H_kv, w.block_table, w.seq_lens,
+                                       w.ranks, 152)
+    per_head = {}
+    for it in items:
+        per_head[it["head"]] = per_head.get(it["head"], 0) + it["n_pages"]
+    assert set(per_head.values()) == {4096 // 16}
+    with pytest.raises(fk.FKError):                      # only four rows per agent
+        w2 = workloads.make_workload("qwen72b_chunk", prefix=64, A=2)
+        fk.fk_plan_host_slots8(w2.A, w2.C, w2.H_q, w2.H_kv, w2.block_table, w2.seq_lens,
+                               w2.ranks, 152)
 
 
 def test_plan_balances_pieces():

@@ -100,3 +100,17 @@ def test_noalloc_does_not_reuse_a_destroyed_pools_work_list():
     got = _call(fk.fk_residual_attention_noalloc, dw2, q)
     assert torch.equal(got, ref)
     dw2.check()
+
+
+def test_noalloc_eight_slot_tiles(monkeypatch):
+    # a pool planned in eight-slot tiles: the same static array carries that
+    # kernel's work list
+    monkeypatch.setenv("FORKKV_DECODE_SLOTS", "8")
+    w = workloads.make_workload("llama8b_32k", "strong", prefix=1000, A=8)
+    dw = harness.DeviceWorkload(w)
+    q = dw.queries(0)
+    ref = _call(fk.fk_residual_attention, dw, q)
+    got = _call(fk.fk_residual_attention_noalloc, dw, q)
+    assert torch.equal(got, ref)
+    assert fk.fk_last_launch_count(dw.pool.h) == 2        # eight-slot kernel + combine
+    dw.check()
