@@ -65,6 +65,24 @@ def test_pool_bytes_accounts_for_every_region():
     assert n < (page_bytes + rc + comp + (1 << 20)) * 1.5
 
 
+def test_pool_bytes_hold_the_rope_table_for_d128():
+    # d = 128 pools also hold [cos, sin](t theta_i) as f16 pairs for every
+    # position of the rCache capacity (rounded up to 128 tokens): 256 bytes
+    # per position; d = 64 pools hold none
+    def nbytes(d, max_tokens):
+        return fk.fk_pool_bytes(fk.fk_pool_config(1, 8, 2, d, 16, 16, 2, 16, max_tokens, 0,
+                                                  1 << 20, 10000.0, 0))
+    for d in (64, 128):
+        grow = nbytes(d, 4096) - nbytes(d, 4096 - 127)     # same capacity: 4096
+        assert grow == 0
+    # 128 more positions: the rCache arena grows by the same amount for both
+    # head sizes, the table by 128 x 256 bytes for d = 128 only (regions are
+    # 256-byte aligned, so the table adds exactly that)
+    extra64 = nbytes(64, 4096 + 128) - nbytes(64, 4096)
+    extra128 = nbytes(128, 4096 + 128) - nbytes(128, 4096)
+    assert extra128 - extra64 == 128 * 256
+
+
 def _plan(w, target=152):
     return fk.fk_plan_host(w.A, w.C, w.H_q, w.H_kv, w.block_table, w.seq_lens, w.ranks, target)
 
