@@ -379,7 +379,7 @@ def run_gb300(args, rank: int, world: int, local_rank: int):
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "parallelism": f"replicas x{world}",
                    "l2": "flushed between steps, outside the step's events: a memset of 2x L2, "
                          "then a read of another 2x L2 buffer (writes back the dirty lines)",
                    "kernel_timing": "roofline.kernel_ms from separate steps with an event "
@@ -695,7 +695,9 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
         "config": {"workload": workload_desc(w),
-                   "parallelism": f"host CPU, {workers} single-threaded processes"},
+                   # the job being compared (the GPU arm's config); where it ran
+                   # is in cpu_baseline
+                   "parallelism": f"replicas x{int(os.environ.get('WORLD_SIZE', '1'))}"},
         "cpu_baseline": {"value": rate, "unit": UNIT, "kind": "oracle", "cores": workers,
                          "sample": f"each step: the fp64 oracle on {workers} (agent, kv-head) "
                                    f"pairs in parallel, one per process, over the first {keys} "
