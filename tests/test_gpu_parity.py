@@ -209,6 +209,27 @@ def test_single_key_and_short_sequences(slots):
     assert mx <= MAX_ABS and mean <= MEAN_ABS
 
 
+@pytest.mark.parametrize("ranks,A", [((64,), 1), ((8,), 8), ((64, 8), 5)])
+def test_decode_tile_shapes(slots, ranks, A):
+    # one rank-64 agent (an eight-slot tile with an empty half), eight
+    # rank-8 agents (one Z chunk per warpgroup), and a rank mix that leaves
+    # slots empty
+    w = workloads.make_workload("llama8b_32k", "strong", prefix=450, A=A, ranks=ranks)
+    dw, out = _run(w)
+    mx, mean, _ = errors(out, oracle_out(w, 0))
+    assert mx <= MAX_ABS and mean <= MEAN_ABS, (ranks, A, mx, mean)
+
+
+@pytest.mark.parametrize("ranks", [(8, 64), (16,)])
+def test_chunk_kernel_ranks(ranks):
+    # the chunk kernel with padded ranks below its 64-rank stage (rank 8 and
+    # 16 agents next to rank 64 ones)
+    w = workloads.make_workload("qwen72b_chunk", "strong", prefix=250, A=3, ranks=ranks)
+    dw, out = _run(w)
+    mx, mean, _ = errors(out, oracle_out(w, 0))
+    assert mx <= MAX_ABS and mean <= MEAN_ABS, (ranks, mx, mean)
+
+
 def test_causal_chunk_covering_whole_sequence():
     w = workloads.make_workload("qwen72b_chunk", prefix=0, A=2)     # T == C == 32
     assert list(w.seq_lens) == [32, 32]
