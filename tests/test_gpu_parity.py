@@ -230,6 +230,28 @@ def test_chunk_kernel_ranks(ranks):
     assert mx <= MAX_ABS and mean <= MEAN_ABS, (ranks, mx, mean)
 
 
+@pytest.mark.parametrize("name,heads", [("qwen72b_chunk", (16, 8, 128)), ("qwen72b_chunk", (4, 2, 64))])
+def test_causal_decode_shaped_two_tokens(slots, name, heads):
+    # G = 2 query heads per kv head and C = 2 causal chunk tokens: four rows
+    # per agent (the decode kernels), each with its own causal limit
+    w = workloads.make_workload(name, "peaked", prefix=300, A=5, C=2, heads=heads)
+    assert w.causal and (w.H_q // w.H_kv) * w.C == 4
+    dw, out = _run(w)
+    mx, mean, _ = errors(out, oracle_out(w, 0))
+    assert mx <= MAX_ABS and mean <= MEAN_ABS, (heads, mx, mean)
+
+
+def test_compressed_pool_with_private_pages():
+    # partial shared page forked per agent, private suffix pages: unfilled
+    # rows carry no codes and are masked
+    w = workloads.make_workload("compressed", "strong", prefix=300, suffix=(0, 40), A=6)
+    kq, ks, vc, vn = oracle_codes(w, 0)
+    dw, out = _run(w, compressed="codes", codes={0: (kq, ks, oracle.pack_planes(vc), vn)})
+    kh, vh = oracle.decode_pages(kq, ks, vc, vn)
+    mx, mean, rel = errors(out, oracle_out(w, 0, pages_k=kh, pages_v=vh))
+    assert mx <= MAX_ABS_COMPRESSED and mean <= MEAN_ABS, (mx, mean, rel)
+
+
 def test_causal_chunk_covering_whole_sequence():
     w = workloads.make_workload("qwen72b_chunk", prefix=0, A=2)     # T == C == 32
     assert list(w.seq_lens) == [32, 32]
