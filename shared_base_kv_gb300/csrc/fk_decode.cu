@@ -158,8 +158,7 @@ struct Misc {
 static_assert(sizeof(Misc) <= 4096, "Misc must fit its smem slot");
 
 struct Item {
-  int head, n_rows, n_pages, lp_begin, n_ag, partial_begin, row_begin, n_tiles, page_begin,
-      sum_rp;
+  int head, n_rows, n_pages, lp_begin, n_ag, partial_begin, n_tiles, page_begin, sum_rp, next;
   int rp[kA], col[kA], pool_agent[kA];
   // Lv^T stage columns: agents that read the same residual rows (Shared-A:
   // LRAgent summary, "BaseLRShared") share one block, copied once, and one
@@ -169,50 +168,34 @@ struct Item {
   int64_t rc_off[kA];
 };
 
-__device__ __forceinline__ void load_item(const PoolGeom& g, const PlanDev& p, const uint8_t* ws,
-                                          int it, Item& I) {
-  const fk_work_item& w = ((const fk_work_item*)(ws + p.off_items))[it];
-  const int32_t* tile_agents = (const int32_t*)(ws + p.off_tile_agents);
-  const CallAgent* ca = (const CallAgent*)(ws + p.off_call_agents);
-  const AgentDev* ag = (const AgentDev*)(g.base + g.off_agents);
+// Work item `it` of this call (records 0 .. gridDim.x - 1 are the CTAs'
+// first items; `next` chains the rest), looked up by the host.
+__device__ __forceinline__ const DecItem* ditem(const PlanDev& p, const uint8_t* ws, int it) {
+  return (const DecItem*)(ws + p.off_ditems) + it;
+}
+
+__device__ __forceinline__ void load_item(const PlanDev& p, const uint8_t* ws, int it, Item& I) {
+  const DecItem& w = *ditem(p, ws, it);
   I.head = w.head;
   I.n_rows = w.n_rows;
   I.n_pages = w.n_pages;
   I.lp_begin = w.lp_begin;
-  I.n_ag = w.n_agents;
+  I.n_ag = w.n_ag;
   I.partial_begin = w.partial_begin;
-  I.row_begin = w.row_begin;
   I.page_begin = w.page_begin;
+  I.sum_rp = w.sum_rp;
+  I.next = w.next;
+  I.lv_rp = w.lv_rp;
   I.n_tiles = (w.n_pages + kTilePages - 1) / kTilePages;
-  int col = 0;
 #pragma unroll
   for (int a = 0; a < kA; ++a) {
-    I.rp[a] = 0; I.col[a] = col; I.pool_agent[a] = 0; I.s[a] = 0.f; I.rc_off[a] = 0;
-    if (a < I.n_ag) {
-      const int pa = ca[tile_agents[w.agent_begin + a]].pool_agent;
-      const AgentDev dv = ag[pa];
-      I.pool_agent[a] = pa;
-      I.rp[a] = dv.rp;
-      I.s[a] = dv.s;
-      I.rc_off[a] = dv.rc_off;
-      col += dv.rp;
-    }
+    I.rp[a] = w.rp[a];
+    I.col[a] = w.col[a];
+    I.pool_agent[a] = w.pool_agent[a];
+    I.lvcol[a] = w.lvcol[a];
+    I.s[a] = w.s[a];
+    I.rc_off[a] = w.rc_off[a];
   }
-  I.sum_rp = col;
-  int lvc = 0;
-#pragma unroll
-  for (int a = 0; a < kA; ++a) {
-    int share = -1;
-#pragma unroll
-    for (int b = 0; b < a; ++b)
-      if (share < 0 && a < I.n_ag && I.rc_off[b] == I.rc_off[a]) share = b;
-    I.lvcol[a] = lvc;
-#pragma unroll
-    for (int b = 0; b < a; ++b)
-      if (b == share) I.lvcol[a] = I.lvcol[b];
-    if (a < I.n_ag && share < 0) lvc += I.rp[a];
-  }
-  I.lv_rp = lvc;
 }
 
 __device__ __forceinline__ const uint8_t* rc_lk(const PoolGeom& g, const Item& I, int a, int layer) {
@@ -294,7 +277,6 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
   Misc& M = *reinterpret_cast<Misc*>(smem + LY::oMISC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint8_t* ws = g.base + g.off_ws;
-  const int32_t* cta_items = (const int32_t*)(ws + p.off_cta);
   uint32_t* errw = err_word(g);
   volatile int* abort_flag = &M.abort_flag;
   const uint32_t sbase = smem_u32(smem);
@@ -326,7 +308,6 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = M.tmem_base;
-  const int it_begin = cta_items[blockIdx.x], it_end = cta_items[blockIdx.x + 1];
 
   // Register split: the copy and MMA warps (warpgroup 0) and the Trig
   // warpgroup hand registers to the two compute warpgroups; the shares add
@@ -402,13 +383,16 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
     // takes its abort path and the call reports the timeout)
     if (p.stall_probe) wait(B_STALL);
     int tc = 0;
-    for (int it = it_begin; it < it_end; ++it) {
+    for (int it = (int)blockIdx.x, nxt; it >= 0; it = nxt) {
       Item I;
-      load_item(g, p, ws, it, I);
+      load_item(p, ws, it, I);
+      if (I.n_pages == 0) break;   // a CTA without work
+      nxt = I.next;
       const int32_t* pages = (const int32_t*)(ws + p.off_pages) + I.page_begin;
       const int tc0 = tc;
       // page id of this lane's page of the next tile, loaded a tile ahead
-      int pg = lane < min(kTilePages, I.n_pages) ? pages[lane] : 0;
+      // (the first tile's come with the item)
+      int pg = lane < kTilePages ? ditem(p, ws, it)->first_pages[lane] : 0;
       for (int k = 0; k < I.n_tiles; ++k) {
         const int p0 = k * kTilePages;
         const int np = min(kTilePages, I.n_pages - p0);
@@ -443,15 +427,16 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         // Z MMAs are done with the buffer; after the first key tile, which
         // need not wait for that
         {
-          const MPair mpr = ((const MPair*)(ws + p.off_mpairs))[((const int32_t*)(ws + p.off_item_mpair))[it]];
-          const uint32_t mbytes = (uint32_t)mpr.zcols * D * 2;
+          const DecItem* rec = ditem(p, ws, it);
+          const uint32_t mbytes = (uint32_t)rec->mbytes;
+          const uint8_t* msrc = ws + rec->mofs;
           wait(B_M_EMPTY);
-          if (it == it_begin) asm volatile("griddepcontrol.wait;" ::: "memory");
+          if (it == (int)blockIdx.x) asm volatile("griddepcontrol.wait;" ::: "memory");
           __syncwarp();
           if (lane == 0 && !*abort_flag) mbar_expect_tx_relaxed(bar(B_M_FULL), mbytes);
           __syncwarp();
           for (uint32_t o = lane * 4096u; o < mbytes && !*abort_flag; o += 32u * 4096u)
-            bulk_g2s(sbase + LY::oM + o, ws + mpr.mofs + o, min(4096u, mbytes - o), bar(B_M_FULL));
+            bulk_g2s(sbase + LY::oM + o, msrc + o, min(4096u, mbytes - o), bar(B_M_FULL));
         }
         }
         // compressed pool: half of the previous tile's values
@@ -464,12 +449,15 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
     // ============================================= value copies (warp 3) ====
     // values of tile k: Vb (or the compressed codes) and the Lv^T stage
     int tc = 0;
-    for (int it = it_begin; it < it_end; ++it) {
+    for (int it = (int)blockIdx.x, nxt; it >= 0; it = nxt) {
       Item I;
-      load_item(g, p, ws, it, I);
+      load_item(p, ws, it, I);
+      if (I.n_pages == 0) break;   // a CTA without work
+      nxt = I.next;
       const int32_t* pages = (const int32_t*)(ws + p.off_pages) + I.page_begin;
       // page id of this lane's page of the next tile, loaded a tile ahead
-      int pg = lane < min(kTilePages, I.n_pages) ? pages[lane] : 0;
+      // (the first tile's come with the item)
+      int pg = lane < kTilePages ? ditem(p, ws, it)->first_pages[lane] : 0;
       auto load_values = [&](int k, int vt) {
         const int p0 = k * kTilePages;
         const int np = min(kTilePages, I.n_pages - p0);
@@ -539,9 +527,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
     // ======================================= MMA issue (converged warp) ====
     const uint32_t idS = idesc_f16(128, kRows, 1);
     int tc = 0;
-    for (int it = it_begin; it < it_end; ++it) {
+    for (int it = (int)blockIdx.x, nxt; it >= 0; it = nxt) {
       Item I;
-      load_item(g, p, ws, it, I);
+      load_item(p, ws, it, I);
+      if (I.n_pages == 0) break;   // a CTA without work
+      nxt = I.next;
       const int zcols = kRPA * I.sum_rp;
       const int n_zc = (zcols + kZBuf - 1) / kZBuf;
       wait(B_M_FULL);                    // the item's M
@@ -639,9 +629,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
     const float kscale = ((const float*)(g.base + g.off_ks))[layer];
     int tc = 0;
     // keys only: the value warp expands the values
-    for (int it = it_begin; it < it_end; ++it) {
+    for (int it = (int)blockIdx.x, nxt; it >= 0; it = nxt) {
       Item I;
-      load_item(g, p, ws, it, I);
+      load_item(p, ws, it, I);
+      if (I.n_pages == 0) break;   // a CTA without work
+      nxt = I.next;
       const int tc0 = tc;
       for (int j = 0; j < I.n_tiles; ++j) {
         {
@@ -687,16 +679,13 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
     const int bar_sync = 1 + 2 * cw, bar_or = 2 + 2 * cw;   // this warpgroup's named barriers
     const int r0 = 8 * cw;                           // first query row of this warpgroup
     const float scale_log2 = 1.4426950408889634f * rsqrtf((float)D);
-    const int32_t* row_agent_all = (const int32_t*)(ws + p.off_row_agent);
-    const int32_t* row_cg_all = (const int32_t*)(ws + p.off_row_cg);
-    const CallAgent* ca = (const CallAgent*)(ws + p.off_call_agents);
     int tc = 0, pv_seen = 0;
     // The value MMAs of tile j signal PV_DONE[j & 1].  Alternating barriers
     // keep a waiter within one phase of each, which parity waits need.
     auto pv_until = [&](int n) {
       while (pv_seen < n) { wait(B_PV_DONE0 + (pv_seen & 1)); ++pv_seen; }
     };
-    for (int it = it_begin; it < it_end; ++it) {
+    for (int it = (int)blockIdx.x, nxt; it >= 0; it = nxt) {
       int n_tiles, lp_begin, n_pages, n_zc, g_lo, g_hi;
       // ---- item set-up.  Every MMA that read the previous item's Q and
       // Trig stages has completed (this warpgroup waited for all of them:
@@ -705,7 +694,10 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       named_bar(bar_sync, 128);                 // this warpgroup is done with the tables
       {
         Item I;
-        load_item(g, p, ws, it, I);
+        load_item(p, ws, it, I);
+        if (I.n_pages == 0) break;              // a CTA without work
+        nxt = I.next;
+        const DecItem* rec = ditem(p, ws, it);
         const int n_rows = I.n_rows, n_ag = I.n_ag;
         n_tiles = I.n_tiles;
         lp_begin = I.lp_begin;
@@ -716,28 +708,13 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         const int c_lo = cw ? I.col[2] : I.col[0], c_hi = cw ? I.sum_rp : I.col[2];
         g_lo = c_lo / 8;
         g_hi = c_hi / 8;
-        const int32_t* row_agent = row_agent_all + I.row_begin;
-        const int32_t* row_cg = row_cg_all + I.row_begin;
         // rows: limits and running maxima
         if (ln < 8) {
           const int j = r0 + ln;
           M.m_used[j] = -INFINITY;
-          int lim = 0;
-          if (j < n_rows) {
-            const int T = ca[row_agent[j]].seq_len;
-            lim = p.causal ? min(T, T - p.C + row_cg[j] / g.G + 1) : T;
-          }
-          M.row_lim[j] = lim;
+          M.row_lim[j] = rec->row_lim[j];
         }
-        if (ln == 0) {
-          int mn = 0x7fffffff;
-          for (int j = r0; j < r0 + 8; ++j) {
-            if (j >= n_rows) { mn = 0; break; }     // padded rows must stay masked
-            const int T = ca[row_agent[j]].seq_len;
-            mn = min(mn, p.causal ? min(T, T - p.C + row_cg[j] / g.G + 1) : T);
-          }
-          M.lim_min[cw] = mn;
-        }
+        if (ln == 0) M.lim_min[cw] = rec->lim_min[cw];
         // Lk group tables of this warpgroup's agents
         if (ln < 8) {
           const int j = ln;
@@ -759,11 +736,8 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         for (int u = ln; u < 8 * (D / 8); u += 128) {
           const int row = r0 + u / (D / 8), ch = u % (D / 8);
           uint4 v = make_uint4(0, 0, 0, 0);
-          if (row < n_rows) {
-            const int ci = row_agent[row], cg = row_cg[row];
-            const int64_t qrow = ((int64_t)ci * p.C + cg / g.G) * g.H_q + I.head * g.G + cg % g.G;
-            v = *(const uint4*)(q + qrow * D + ch * 8);
-          }
+          const int qrow = row < n_rows ? rec->qrow[row] : -1;
+          if (qrow >= 0) v = *(const uint4*)(q + (int64_t)qrow * D + ch * 8);
           *(uint4*)(smem + LY::oQ + ((row / 8) * (D / 8) + ch) * 128 + (row % 8) * 16) = v;
         }
         fence_proxy_async();
@@ -904,7 +878,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       tc_fence_after();
       {
         Item I;
-        load_item(g, p, ws, it, I);
+        load_item(p, ws, it, I);
         const int n_rows = I.n_rows, n_ag = I.n_ag;
         float* part = (float*)(ws + p.off_partials);
         const int PS = p.partial_stride;
@@ -981,9 +955,11 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
       if (lane == 0) mbar_arrive_relaxed(bar(B_TRIG_FULL0 + st));
     };
     int tc = 0;
-    for (int it = it_begin; it < it_end; ++it) {
+    for (int it = (int)blockIdx.x, nxt; it >= 0; it = nxt) {
       Item I;
-      load_item(g, p, ws, it, I);
+      load_item(p, ws, it, I);
+      if (I.n_pages == 0) break;   // a CTA without work
+      nxt = I.next;
       const int n_zc = (kRPA * I.sum_rp + kZBuf - 1) / kZBuf;
       const int tb = I.lp_begin * kPage;
       make_trig(tb, tc & 1);

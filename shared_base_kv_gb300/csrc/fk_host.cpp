@@ -38,8 +38,8 @@ struct HostPlan {
   std::vector<int32_t> csr_ptr, csr_slots;
   std::vector<int32_t> cta_begin;   // items [cta_begin[c], cta_begin[c+1]) run on CTA c
   int n_partials = 0;
-  std::vector<MPair> mpairs;        // decode-shaped calls only (4 query rows per agent)
-  std::vector<int32_t> item_mpair;
+  std::vector<MPair> mpairs;        // four-agent decode calls: one M per (agent tile, kv head)
+  std::vector<int32_t> item_mpair;  // per item: its M pair
 };
 
 // Pinned host staging buffer for small host->device uploads.  A new upload
@@ -640,12 +640,89 @@ void fill_mpairs(HostPlan& pl, const fk_pool* p, const int32_t* agents, int C) {
   }
 }
 
+// The four-agent decode kernel's item records (see DecItem): the lookups
+// of each item's agents, rows and first pages, in CTA order.
+std::vector<DecItem> make_ditems(const HostPlan& pl, const fk_pool* p, const int32_t* agents,
+                                 const int32_t* seq, int C, int causal) {
+  const PoolGeom& g = p->g;
+  const int G = g.H_q / g.H_kv;
+  auto rec = [&](int it) {
+    const fk_work_item& w = pl.items[it];
+    DecItem d{};
+    d.head = w.head;
+    d.n_rows = w.n_rows;
+    d.n_pages = w.n_pages;
+    d.lp_begin = w.lp_begin;
+    d.n_ag = w.n_agents;
+    d.partial_begin = w.partial_begin;
+    d.page_begin = w.page_begin;
+    d.next = -1;
+    d.pad = it;              // item index until pack_plan places the M matrices
+    int col = 0, lvc = 0;
+    for (int a = 0; a < kMaxAgentsPerTile; ++a) {
+      d.col[a] = col;
+      d.qrow[4 * a] = d.qrow[4 * a + 1] = d.qrow[4 * a + 2] = d.qrow[4 * a + 3] = -1;
+      if (a >= w.n_agents) continue;
+      const int pa = agents[pl.tile_agents[w.agent_begin + a]];
+      d.pool_agent[a] = pa;
+      d.rp[a] = p->agents[pa].rp;
+      d.s[a] = p->agents[pa].s;
+      d.rc_off[a] = p->agents[pa].rc_off;
+      col += d.rp[a];
+      // Shared-A: an agent reading the same residual rows as an earlier one
+      // uses that agent's block of the Lv^T stage
+      int share = -1;
+      for (int b = 0; b < a && share < 0; ++b)
+        if (d.rc_off[b] == d.rc_off[a]) share = b;
+      d.lvcol[a] = share >= 0 ? d.lvcol[share] : lvc;
+      if (share < 0) lvc += d.rp[a];
+    }
+    d.sum_rp = col;
+    d.lv_rp = lvc;
+    for (int j = 0; j < 4 * kMaxAgentsPerTile; ++j) {
+      d.row_lim[j] = 0;
+      if (j >= w.n_rows) continue;
+      const int ci = pl.row_agent[w.row_begin + j], cg = pl.row_cg[w.row_begin + j];
+      if (ci < 0) continue;
+      d.qrow[j] = (ci * C + cg / G) * g.H_q + w.head * G + cg % G;
+      const int T = seq[ci];
+      d.row_lim[j] = causal ? std::min(T, T - C + cg / G + 1) : T;
+    }
+    for (int h = 0; h < 2; ++h) {
+      int mn = 0x7fffffff;
+      for (int j = 8 * h; j < 8 * h + 8; ++j) mn = std::min(mn, j < w.n_rows ? d.row_lim[j] : 0);
+      d.lim_min[h] = mn;
+    }
+    for (int k = 0; k < kTilePages; ++k)
+      d.first_pages[k] = k < w.n_pages ? pl.pages[w.page_begin + k] : 0;
+    return d;
+  };
+  const int n_ctas = (int)pl.cta_begin.size() - 1;
+  std::vector<DecItem> out(n_ctas);
+  for (int c = 0; c < n_ctas; ++c) {
+    const int b = pl.cta_begin[c], e = pl.cta_begin[c + 1];
+    if (b == e) {
+      out[c] = DecItem{};
+      out[c].next = -1;
+      continue;
+    }
+    out[c] = rec(b);
+    int prev = c;
+    for (int it = b + 1; it < e; ++it) {
+      out[prev].next = (int)out.size();
+      prev = (int)out.size();
+      out.push_back(rec(it));
+    }
+  }
+  return out;
+}
+
 // Pack a work list into the workspace image: the plan arrays, then the
-// split partials, then the decode kernel's M matrices.  Returns the bytes of
-// workspace the call needs (blob covers the plan arrays only).
+// split partials, then the four-agent decode kernel's M matrices.  Returns
+// the bytes of workspace the call needs (blob covers the plan arrays only).
 int64_t pack_plan(const HostPlan& pl, int A, int C, int causal, const int32_t* agents,
-                  const int32_t* seq, const PoolGeom& g, std::vector<uint8_t>& blob,
-                  PlanDev& pd) {
+                  const int32_t* seq, const PoolGeom& g, const std::vector<DecItem>& ditems,
+                  std::vector<uint8_t>& blob, PlanDev& pd) {
   pd = PlanDev{};
   pd.n_items = (int)pl.items.size();
   pd.n_rows = (int)pl.row_agent.size();
@@ -675,11 +752,13 @@ int64_t pack_plan(const HostPlan& pl, int A, int C, int causal, const int32_t* a
   pd.off_cta = put(pl.cta_begin.data(), pl.cta_begin.size() * 4);
   pd.n_ctas = (int)pl.cta_begin.size() - 1;
   // M offsets are known only once the partials are placed: reserve the
-  // pair table, fill it below
+  // pair table and the item records, fill them in below
   std::vector<MPair> mp = pl.mpairs;
+  std::vector<DecItem> di = ditems;
   pd.n_mpairs = (int)mp.size();
   pd.off_mpairs = put(mp.data(), mp.size() * sizeof(MPair));
-  pd.off_item_mpair = put(pl.item_mpair.data(), pl.item_mpair.size() * 4);
+  pd.n_ditems = (int)di.size();
+  pd.off_ditems = put(di.data(), di.size() * sizeof(DecItem));
   pd.off_partials = align_up((int64_t)blob.size(), 256);
   int64_t need = pd.off_partials + (int64_t)pd.n_partials * pd.partial_stride * 4;
   need = align_up(need, 1024);
@@ -688,6 +767,14 @@ int64_t pack_plan(const HostPlan& pl, int A, int C, int causal, const int32_t* a
     need += align_up((int64_t)m.zcols * g.d * 2, 1024);
   }
   if (!mp.empty()) std::memcpy(blob.data() + pd.off_mpairs, mp.data(), mp.size() * sizeof(MPair));
+  for (auto& d : di) {
+    if (d.n_pages == 0) continue;
+    const MPair& m = mp[pl.item_mpair[d.pad]];
+    d.mofs = m.mofs;
+    d.mbytes = m.zcols * g.d * 2;
+    d.pad = 0;
+  }
+  if (!di.empty()) std::memcpy(blob.data() + pd.off_ditems, di.data(), di.size() * sizeof(DecItem));
   return need;
 }
 
@@ -710,8 +797,13 @@ fk_status build_call_plan(const fk_pool* p, const int32_t* agents, const int32_t
                       : plan_build(A, C, g.H_q, g.H_kv, kPage, bt, max_pages, seq, rp, kMaxRows,
                                    kMaxRankSum, p->num_sms, pl);
   if (s != FK_OK) return s;
-  fill_mpairs(pl, p, agents, C);
-  need = pack_plan(pl, A, C, causal, agents, seq, g, blob, pd);
+  // the four-agent decode kernel reads its items as flat records
+  std::vector<DecItem> ditems;
+  if (!chunk && !dec8 && g.G * C == 4 && (g.d == 64 || g.d == 128)) {
+    fill_mpairs(pl, p, agents, C);
+    ditems = make_ditems(pl, p, agents, seq, C, causal);
+  }
+  need = pack_plan(pl, A, C, causal, agents, seq, g, ditems, blob, pd);
   pd.chunk = chunk ? 1 : 0;
   pd.slots8 = dec8 ? 1 : 0;
   return FK_OK;

@@ -77,6 +77,7 @@ struct PlanDev {
   int32_t partial_stride;  // floats per partial slot: d + rmax_pad + 4
   int32_t n_ctas;          // persistent CTAs; CTA c runs items cta[c] .. cta[c+1]-1
   int32_t n_mpairs;        // decode-shaped calls: (agent tile, kv head) pairs with an M
+  int32_t n_ditems;        // four-agent decode calls: DecItem records (0 otherwise)
   int32_t chunk;           // 1: the items are the chunk kernel's (fk_chunk.cu)
   int32_t slots8;          // 1: eight-slot decode tiles (fk_decode8.cu); tile_agents holds
                            // kDecodeSlots entries per tile (-1: empty slot), rows 4 per slot
@@ -85,19 +86,41 @@ struct PlanDev {
                            // warp also waits on a barrier nothing completes (set per call)
   int64_t off_items, off_row_agent, off_row_cg, off_pages, off_tile_agents,
           off_call_agents, off_csr_ptr, off_csr_slots, off_partials, off_cta;
-  int64_t off_mpairs, off_item_mpair;   // MPair[n_mpairs], int32[n_items]
+  int64_t off_mpairs;      // MPair[n_mpairs]
+  int64_t off_ditems;      // DecItem[n_ditems]
 };
 
-// One (agent tile, kv head) of a decode-shaped call: the rows of its agents
-// and where its query-side RoPE matrix M (d x 4 sum-of-ranks f16, in the
-// decode kernel's shared-memory image) sits in the workspace.
+// One work item of the four-agent decode kernel (fk_decode.cu) with every
+// table lookup done by the host, so that the kernel starts an item with a
+// single read.  Records 0 .. n_ctas - 1 are the CTAs' first items (a CTA
+// without work has n_pages = 0); `next` chains a CTA's further items
+// (-1: none).
+struct DecItem {
+  int32_t head, n_rows, n_pages, lp_begin, n_ag, partial_begin, page_begin, sum_rp;
+  int32_t lv_rp;           // ranks of the Lv^T stage (agents reading the same rows share one block)
+  int32_t next;
+  int32_t lim_min[2];      // per half of the rows (8 rows): fewest keys any of them sees (0: padded row)
+  int32_t rp[kMaxAgentsPerTile], col[kMaxAgentsPerTile], pool_agent[kMaxAgentsPerTile];
+  int32_t lvcol[kMaxAgentsPerTile];   // first rank of the agent's block in the Lv^T stage
+  float s[kMaxAgentsPerTile];
+  int64_t rc_off[kMaxAgentsPerTile];
+  int32_t qrow[4 * kMaxAgentsPerTile];     // q row of each query row (-1: padded row)
+  int32_t row_lim[4 * kMaxAgentsPerTile];  // keys each query row sees (0: padded row)
+  int32_t first_pages[kTilePages];         // page ids of the item's first 128-key tile
+  int64_t mofs;            // the item's M (see MPair): byte offset from the workspace start
+  int32_t mbytes, pad;
+};
+static_assert(sizeof(DecItem) % 16 == 0, "DecItem is read in 16-byte words");
+
+// One (agent tile, kv head) of a four-agent decode call: the rows of its
+// agents and where its query-side RoPE matrix M (d x 4 sum-of-ranks f16, in
+// the decode kernel's shared-memory image) sits in the workspace.  The
+// host looks up each agent's pool id, padded rank and residual scale and
+// each query row's q row, so that building M needs no chain of table loads.
 struct MPair {
   int32_t head, agent_begin, n_agents, row_begin;
   int32_t zcols, pad;      // columns of M (4 x the tile's padded rank sum)
   int64_t mofs;            // byte offset from the workspace start
-  // looked up by the host, so that building M needs no chain of table
-  // loads: per tile agent its pool agent, padded rank and residual scale,
-  // and the q row of each of its four query rows
   int32_t pool_agent[kMaxAgentsPerTile], rp[kMaxAgentsPerTile];
   float s[kMaxAgentsPerTile];
   int32_t qrow[kMaxAgentsPerTile * 4];
