@@ -371,13 +371,31 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
     work.push_back(std::move(sw));
   }
   // 4. emit items.  Segments = (tile, head, page run) in set / tile / head /
-  // run order; their pages, weighted by the per-page work (base + one unit
-  // per agent), are cut into `target_items` contiguous pieces of equal
-  // weight, one per CTA.  A piece that crosses segment boundaries becomes
-  // several items run back to back by the same CTA.
+  // run order; their pages, weighted by the per-page work, are cut into
+  // `target_items` contiguous pieces of equal weight, one per CTA.  A piece
+  // that crosses segment boundaries becomes several items run back to back
+  // by the same CTA.
+  //
+  // Per-page weight: the four-agent decode kernel's 128-key tile costs
+  // about the same whatever its agents (its per-tile chain, not the
+  // per-agent work, sets the pace; measured on GB300): about 1.9 us with at
+  // most 32 padded ranks (one 128-column Z chunk), 2.25 us with more, and
+  // 2.6 us when one compute warpgroup owns all eight rank groups (a rank-64
+  // agent alone, say): weights 5, 6 and 7.  For the other kernels the work
+  // grows with the agents (base + one unit per agent).  A segment's last,
+  // partial tile costs as much as a full one and is weighed as one.
+  auto tile_wpp = [&](const Tile& t) -> int {
+    if (rpa == 4 && !slots8) {
+      int h0 = 0, h1 = 0;
+      for (size_t k = 0; k < t.agents.size(); ++k) (k < 2 ? h0 : h1) += rpad[t.agents[k]];
+      return std::max(h0, h1) >= 64 ? 7 : (h0 + h1 <= 32 ? 5 : 6);
+    }
+    return 2 + t.n_real;
+  };
+  auto full_tiles = [](int64_t pages) { return (pages + kTilePages - 1) / kTilePages * kTilePages; };
   (void)total_units;
   HostPlan pl;
-  struct Seg { int tile_row0, tile_ag0, n_rows, n_ag, rank_sum, head, page0, lp0, len, n_real; };
+  struct Seg { int tile_row0, tile_ag0, n_rows, n_ag, rank_sum, head, page0, lp0, len, wpp; };
   std::vector<Seg> segs;
   int64_t total_w = 0;
   for (auto& sw : work) {
@@ -398,9 +416,9 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
         for (size_t ri = 0; ri < sw.runs.size(); ++ri) {
           Seg sg{tile_row0[ti], tile_ag0[ti], (int)sw.tiles[ti].rows.size(),
                  (int)sw.tiles[ti].agents.size(), sw.tiles[ti].rank_sum, h, run_page0[ri],
-                 sw.runs[ri][0].first, (int)sw.runs[ri].size(), sw.tiles[ti].n_real};
+                 sw.runs[ri][0].first, (int)sw.runs[ri].size(), tile_wpp(sw.tiles[ti])};
           segs.push_back(sg);
-          total_w += (int64_t)sg.len * (2 + sg.n_real);
+          total_w += full_tiles(sg.len) * sg.wpp;
         }
   }
   int64_t total_tiles = 0;
@@ -461,7 +479,7 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
     // own M and a drained pipeline: about two tiles of work), so such CTAs
     // are charged that much extra weight; pieces are cut at whole key tiles
     // of their segment, so only a segment's last item has a partial tile.
-    auto item_cost = [&](const Seg& sg) { return (int64_t)2 * kTilePages * (2 + sg.n_real); };
+    auto item_cost = [&](const Seg& sg) { return (int64_t)2 * kTilePages * sg.wpp; };
     int64_t total_wc = total_w;
     for (size_t i = 1; i < segs.size(); ++i) total_wc += item_cost(segs[i]);
     size_t si = 0;
@@ -473,7 +491,7 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
       bool first = true;
       while (si < segs.size() && (acc < goal || c == n_ctas - 1)) {
         const Seg& sg = segs[si];
-        const int64_t wpp = 2 + sg.n_real;
+        const int64_t wpp = sg.wpp;
         if (!first) {
           if (acc + item_cost(sg) >= goal && c != n_ctas - 1) break;
           acc += item_cost(sg);
@@ -483,7 +501,7 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
         want = (want + kTilePages - 1) / kTilePages * kTilePages;
         int take = (int)std::max<int64_t>(1, std::min<int64_t>(want, sg.len - off));
         push_item(sg, off, take);
-        acc += take * wpp;
+        acc += full_tiles(take) * wpp;
         off += take;
         if (off == sg.len) { ++si; off = 0; }
       }
