@@ -339,12 +339,35 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
       }
       emit();
     }
-    for (int32_t a : (slots8 ? std::vector<int32_t>{} : kv.first)) {
-      if (rpa <= max_rows) {
-        if ((int)cur.rows.size() + rpa > max_rows || cur.rank_sum + rpad[a] > max_rank_sum ||
-            (int)cur.agents.size() >= kMaxAgentsPerTile ||
-            groups_with((int)cur.agents.size() + 1) > kMaxRowGroups)
-          flush();
+    // Four-agent decode tiles (four rows per agent): a tile's 128-key step
+    // costs about the same whatever its agents, so the set's agents are
+    // packed into as few tiles as the rank budget allows (largest rank
+    // first, each into the first tile with room), and each tile's agents
+    // are then ordered so that its two halves (agents 0-1 and 2-3, one
+    // compute warpgroup each) carry ranks as even as possible.  Agents of
+    // equal rank keep their call order.
+    const bool pack = rpa == 4 && !slots8;
+    std::vector<int32_t> order(kv.first.begin(), kv.first.end());
+    if (pack)
+      std::stable_sort(order.begin(), order.end(),
+                       [&](int32_t x, int32_t y) { return rpad[x] > rpad[y]; });
+    auto fits = [&](const Tile& t, int32_t a) {
+      return (int)t.rows.size() + rpa <= max_rows && t.rank_sum + rpad[a] <= max_rank_sum &&
+             (int)t.agents.size() < kMaxAgentsPerTile &&
+             groups_with((int)t.agents.size() + 1) <= kMaxRowGroups;
+    };
+    std::vector<Tile> packed;
+    for (int32_t a : (slots8 ? std::vector<int32_t>{} : order)) {
+      if (pack) {
+        size_t ti = 0;
+        while (ti < packed.size() && !fits(packed[ti], a)) ++ti;
+        if (ti == packed.size()) packed.push_back(Tile{{}, {}, 0});
+        Tile& t = packed[ti];
+        t.agents.push_back(a);
+        t.rank_sum += rpad[a];
+        ++t.n_real;
+      } else if (rpa <= max_rows) {
+        if (!fits(cur, a)) flush();
         cur.agents.push_back(a);
         cur.rank_sum += rpad[a];
         ++cur.n_real;
@@ -359,6 +382,25 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
       }
     }
     if (!slots8) flush();
+    for (Tile& t : packed) {
+      // the slot order with the most even halves (the first such order in
+      // lexicographic order of positions, so equal ranks keep call order)
+      std::vector<int> perm(t.agents.size()), best;
+      for (size_t k = 0; k < perm.size(); ++k) perm[k] = (int)k;
+      int best_max = 1 << 30;
+      do {
+        int h[2] = {0, 0};
+        for (size_t k = 0; k < perm.size(); ++k) h[k < 2 ? 0 : 1] += rpad[t.agents[perm[k]]];
+        if (std::max(h[0], h[1]) < best_max) { best_max = std::max(h[0], h[1]); best = perm; }
+      } while (std::next_permutation(perm.begin(), perm.end()));
+      std::vector<int32_t> ag(t.agents.size());
+      for (size_t k = 0; k < perm.size(); ++k) ag[k] = t.agents[best[k]];
+      t.agents = ag;
+      t.rows.clear();
+      for (int32_t a : t.agents)
+        for (int cg = 0; cg < rpa; ++cg) t.rows.push_back({a, cg});
+      sw.tiles.push_back(t);
+    }
     const auto& pg = kv.second;   // sorted by logical page
     size_t s0 = 0;
     for (size_t k = 1; k <= pg.size(); ++k) {
