@@ -194,6 +194,40 @@ def test_plan_balances_pieces():
     assert sum(tiles) == 16 * 256
 
 
+def _prefix_tiles(w):
+    """Agent tiles (call-local agent indices in slot order) of the items
+    that cover the shared prefix."""
+    items, row_agent, row_cg, pages, tile_agents = _plan(w)
+    tiles = set()
+    for it in items:
+        if it["lp_begin"] == 0:
+            tiles.add(tuple(int(a) for a in tile_agents[it["agent_begin"]: it["agent_begin"] + it["n_agents"]]))
+    return tiles
+
+
+def test_plan_packs_decode_tiles_largest_rank_first():
+    # eight agents over one prefix, ranks 32 16 64 16 32 64 16 16: packed
+    # largest first into the first tile with room, four tiles (cutting in
+    # call order would close one at every rank-64 agent: five tiles)
+    w = workloads.make_workload("llama8b_32k", prefix=512, A=8)
+    w.ranks = np.array([32, 16, 64, 16, 32, 64, 16, 16], dtype=np.int32)
+    assert _prefix_tiles(w) == {(2,), (5,), (0, 4), (1, 3, 6, 7)}
+
+
+def test_plan_balances_tile_halves():
+    # one tile of ranks 32, 16, 16: the rank-32 agent takes the second half
+    # (slot 2) so that both compute warpgroups hold 32 ranks
+    w = workloads.make_workload("llama8b_32k", prefix=512, A=3)
+    w.ranks = np.array([32, 16, 16], dtype=np.int32)
+    assert _prefix_tiles(w) == {(1, 2, 0)}
+
+
+def test_plan_keeps_call_order_for_equal_ranks():
+    w = workloads.make_workload("llama8b_32k", prefix=512, A=8)
+    w.ranks = np.full(8, 16, dtype=np.int32)
+    assert _prefix_tiles(w) == {(0, 1, 2, 3), (4, 5, 6, 7)}
+
+
 def test_plan_rejects_bad_tables():
     w = workloads.make_workload("tiny")
     bt = w.block_table.copy()
