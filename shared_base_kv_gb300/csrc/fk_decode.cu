@@ -687,6 +687,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
     };
     for (int it = (int)blockIdx.x, nxt; it >= 0; it = nxt) {
       int n_tiles, lp_begin, n_pages, n_zc, g_lo, g_hi;
+      bool split;
       // ---- item set-up.  Every MMA that read the previous item's Q and
       // Trig stages has completed (this warpgroup waited for all of them:
       // the Z_FULL commits of a tile cover its S MMAs), so those buffers are
@@ -708,6 +709,15 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
         const int c_lo = cw ? I.col[2] : I.col[0], c_hi = cw ? I.sum_rp : I.col[2];
         g_lo = c_lo / 8;
         g_hi = c_hi / 8;
+        // split item: every row is warpgroup 0's (one or two agents), and
+        // warpgroup 1 takes the upper half of the rank groups; it hands its
+        // sums for warpgroup 0's rows over each tile
+        split = rec->split != 0;
+        if (split) {
+          const int G = I.sum_rp / 8, gm = (G + 1) / 2;
+          g_lo = cw ? gm : 0;
+          g_hi = cw ? G : gm;
+        }
         // rows: limits and running maxima
         if (ln < 8) {
           const int j = r0 + ln;
@@ -722,7 +732,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
 #pragma unroll
           for (int a = 1; a < kA; ++a)
             if (a < n_ag && 8 * j >= I.col[a]) aj = a;
-          M.gagent[cw][j] = aj - 2 * cw;
+          M.gagent[cw][j] = aj - (split ? 0 : 2 * cw);
           M.gbase[cw][j] = nullptr;
           M.gstride[cw][j] = 0;
 #pragma unroll
@@ -821,6 +831,29 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_relaxed(bar(B_Z_FREE0 + c));
+        }
+        if (split) {
+          // warpgroup 1's sums of warpgroup 0's rows, handed over through
+          // the S columns of warpgroup 1's own rows (padded in a split
+          // item, and already read): warp w and warp w + 4 reach the same
+          // TMEM lanes.  The buffer's next S comes after both warpgroups
+          // have released this tile's first Z chunk.
+          const uint32_t xcol = tmem + tm_s(tc & 1) + 8 + lane_off;
+          uint32_t xw[8];
+          if (cw == 1) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) xw[j] = __float_as_uint(acc[j]);
+            tmem_st8(xcol, xw);
+            tmem_wait_st();
+            tc_fence_before();
+            named_bar_arrive(6, 256);
+          } else {
+            named_bar(6, 256);
+            tc_fence_after();
+            tmem_ld8_wait(xcol, xw);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] += __uint_as_float(xw[j]);
+          }
         }
         if (k + 1 < n_tiles) load_lk(k + 1);
         // ---- online softmax (base 2); the running max of a row moves only

@@ -421,16 +421,17 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
   // Per-page weight: the four-agent decode kernel's 128-key tile costs
   // about the same whatever its agents (its per-tile chain, not the
   // per-agent work, sets the pace; measured on GB300): about 1.9 us with at
-  // most 32 padded ranks (one 128-column Z chunk), 2.25 us with more, and
-  // 2.6 us when one compute warpgroup owns all eight rank groups (a rank-64
-  // agent alone, say): weights 5, 6 and 7.  For the other kernels the work
+  // most 32 padded ranks (one 128-column Z chunk) and 2.25 us with more:
+  // weights 5 and 6.  (Tiles of one or two agents with 48 or more ranks
+  // share their rank groups between both compute warpgroups; see the
+  // decode kernel.)  For the other kernels the work
   // grows with the agents (base + one unit per agent).  A segment's last,
   // partial tile costs as much as a full one and is weighed as one.
   auto tile_wpp = [&](const Tile& t) -> int {
     if (rpa == 4 && !slots8) {
       int h0 = 0, h1 = 0;
       for (size_t k = 0; k < t.agents.size(); ++k) (k < 2 ? h0 : h1) += rpad[t.agents[k]];
-      return std::max(h0, h1) >= 64 ? 7 : (h0 + h1 <= 32 ? 5 : 6);
+      return h0 + h1 <= 32 ? 5 : 6;
     }
     return 2 + t.n_real;
   };
@@ -717,7 +718,7 @@ std::vector<DecItem> make_ditems(const HostPlan& pl, const fk_pool* p, const int
     d.partial_begin = w.partial_begin;
     d.page_begin = w.page_begin;
     d.next = -1;
-    d.pad = it;              // item index until pack_plan places the M matrices
+    d.mbytes = it;           // item index until pack_plan places the M matrices
     int col = 0, lvc = 0;
     for (int a = 0; a < kMaxAgentsPerTile; ++a) {
       d.col[a] = col;
@@ -739,6 +740,9 @@ std::vector<DecItem> make_ditems(const HostPlan& pl, const fk_pool* p, const int
     }
     d.sum_rp = col;
     d.lv_rp = lvc;
+    // at most two agents leave the second compute warpgroup without rows;
+    // with six or more rank groups it takes half of them
+    d.split = (w.n_agents <= 2 && col >= 48) ? 1 : 0;
     for (int j = 0; j < 4 * kMaxAgentsPerTile; ++j) {
       d.row_lim[j] = 0;
       if (j >= w.n_rows) continue;
@@ -829,10 +833,9 @@ int64_t pack_plan(const HostPlan& pl, int A, int C, int causal, const int32_t* a
   if (!mp.empty()) std::memcpy(blob.data() + pd.off_mpairs, mp.data(), mp.size() * sizeof(MPair));
   for (auto& d : di) {
     if (d.n_pages == 0) continue;
-    const MPair& m = mp[pl.item_mpair[d.pad]];
+    const MPair& m = mp[pl.item_mpair[d.mbytes]];
     d.mofs = m.mofs;
     d.mbytes = m.zcols * g.d * 2;
-    d.pad = 0;
   }
   if (!di.empty()) std::memcpy(blob.data() + pd.off_ditems, di.data(), di.size() * sizeof(DecItem));
   return need;

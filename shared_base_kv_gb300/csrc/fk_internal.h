@@ -108,7 +108,9 @@ struct DecItem {
   int32_t row_lim[4 * kMaxAgentsPerTile];  // keys each query row sees (0: padded row)
   int32_t first_pages[kTilePages];         // page ids of the item's first 128-key tile
   int64_t mofs;            // the item's M (see MPair): byte offset from the workspace start
-  int32_t mbytes, pad;
+  int32_t mbytes;
+  int32_t split;           // 1: the agents' rows all sit in the first half (at most two
+                           // agents) and their rank groups are shared by both halves
 };
 static_assert(sizeof(DecItem) % 16 == 0, "DecItem is read in 16-byte words");
 
