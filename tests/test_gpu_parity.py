@@ -220,6 +220,22 @@ def test_decode_tile_shapes(slots, ranks, A):
     assert mx <= MAX_ABS and mean <= MEAN_ABS, (ranks, A, mx, mean)
 
 
+@pytest.mark.parametrize("name,ranks,A", [
+    ("llama8b_32k", (32,), 2),     # two rank-32 agents: one tile, both in its first half
+    ("llama8b_32k", (64,), 3),     # three rank-64 agents, each alone in its tile
+    ("tiny", (64,), 2),            # d = 64
+])
+def test_split_items(slots, name, ranks, A):
+    # tiles of one or two agents with 48 or more ranks: the second compute
+    # warpgroup of the four-agent decode kernel takes half of the rank groups
+    # and hands its sums over through tensor memory
+    w = workloads.make_workload(name, "strong", prefix=700, A=A, ranks=ranks)
+    assert all(int(r) == ranks[0] for r in w.ranks)
+    dw, out = _run(w)
+    mx, mean, rel = errors(out, oracle_out(w, 0))
+    assert mx <= MAX_ABS and mean <= MEAN_ABS and rel < 2e-2, (name, ranks, A, mx, mean, rel)
+
+
 @pytest.mark.parametrize("ranks", [(8, 64), (16,)])
 def test_chunk_kernel_ranks(ranks):
     # the chunk kernel with padded ranks below its 64-rank stage (rank 8 and
