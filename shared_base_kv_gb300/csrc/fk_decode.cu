@@ -837,7 +837,10 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
           // the S columns of warpgroup 1's own rows (padded in a split
           // item, and already read): warp w and warp w + 4 reach the same
           // TMEM lanes.  The buffer's next S comes after both warpgroups
-          // have released this tile's first Z chunk.
+          // have released this tile's first Z chunk.  Both warpgroups wait
+          // at the barrier, so each of its phases is one tile's hand-off
+          // (with an arrive-only producer a phase could also complete on
+          // two of the producer's arrivals).
           const uint32_t xcol = tmem + tm_s(tc & 1) + 8 + lane_off;
           uint32_t xw[8];
           if (cw == 1) {
@@ -846,7 +849,7 @@ __global__ void __launch_bounds__(dec::kThreads, 1)
             tmem_st8(xcol, xw);
             tmem_wait_st();
             tc_fence_before();
-            named_bar_arrive(6, 256);
+            named_bar(6, 256);
           } else {
             named_bar(6, 256);
             tc_fence_after();

@@ -312,11 +312,6 @@ __device__ __forceinline__ bool elect_one() {
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
-// Arrival at a named barrier without waiting (the producer side of a
-// bar.arrive / bar.sync hand-off).
-__device__ __forceinline__ void named_bar_arrive(int id, int n) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
