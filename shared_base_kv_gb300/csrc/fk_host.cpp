@@ -352,7 +352,7 @@ fk_status plan_build(int A, int C, int H_q, int H_kv, int P, const int32_t* bt,
       std::stable_sort(order.begin(), order.end(),
                        [&](int32_t x, int32_t y) { return rpad[x] > rpad[y]; });
     auto fits = [&](const Tile& t, int32_t a) {
-      return (int)t.rows.size() + rpa <= max_rows && t.rank_sum + rpad[a] <= max_rank_sum &&
+      return ((int)t.agents.size() + 1) * rpa <= max_rows && t.rank_sum + rpad[a] <= max_rank_sum &&
              (int)t.agents.size() < kMaxAgentsPerTile &&
              groups_with((int)t.agents.size() + 1) <= kMaxRowGroups;
     };
