@@ -28,3 +28,40 @@ def test_chunk_workload_flops():
     per_head = T * (2 * r * d + G * C * (4 * d + 2 * r)) + G * C * 2 * r * d
     assert int(w.seq_lens[0]) == T
     assert 16 * 8 * per_head == 1513103556608
+
+
+def _profile_values(path):
+    vals = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    return vals
+
+
+@pytest.mark.parametrize("path,sources,alg", [
+    (bench.TRAFFIC_FILE, bench.KERNEL_SOURCES, 151060480),
+    (bench.TRAFFIC8_FILE, bench.KERNEL8_SOURCES, 151060480),
+    (bench.PREFILL_TRAFFIC_FILE, bench.PREFILL_SOURCES, 270794752),
+])
+def test_profile_summaries_feed_roofline_traffic(path, sources, alg):
+    # each committed ncu summary names the source hash it was taken on, its
+    # DRAM bytes per launch and the algorithmic bytes of the same launch
+    vals = _profile_values(path)
+    assert int(vals["algorithmic_bytes_per_launch"]) == alg
+    traffic = int(vals["dram_bytes_per_launch"])
+    # measured traffic can only exceed the algorithmic bytes (re-reads,
+    # write-backs), and not by much for these kernels
+    assert alg <= traffic <= 1.25 * alg
+    # the bench reports it only while the sources hash to the recorded value
+    got = bench.traffic_per_launch(path, sources)
+    assert got in (None, traffic)
+    assert (got == traffic) == (vals["kernel_source_sha256"] == bench.kernel_source_hash(sources))
+    assert bench.traffic_per_launch(path, ("workloads.py",)) is None
+
+
+def test_headline_algorithmic_bytes_per_launch():
+    # the decode launch moves the step's bytes except the bf16 output, which
+    # the combine writes
+    ab = bench.algorithmic_bytes(workloads.make_workload("llama8b_32k"))
+    assert ab["step"] - ab["out"] == 151060480
